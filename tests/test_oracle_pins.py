@@ -1,0 +1,413 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test names what it pins: brute-force sums on tiny inputs, exact rational
+arithmetic, closed-form probes, the hand-derived schedule fixture, invariants
+the pages fix (own chunk last / first, decomposed equals collective) and a
+brute-force search over schedules. A few tests plant a mistake in the oracle
+(monkeypatched, on the CPU) and check that a pin catches it.
+"""
+import itertools
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import flashoverlap_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _ints(rng, shape):
+    return rng.integers(-4, 5, size=shape).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Brute force: explicit sums of products in pure Python (tiny inputs).
+# --------------------------------------------------------------------------
+
+def _bf_gemm_rs(X, W):
+    R = len(X)
+    M, K = X[0].shape
+    N = W[0].shape[1]
+    rows = M // R
+    out = []
+    for d in range(R):
+        y = [[0 for _ in range(N)] for _ in range(rows)]
+        for i in range(rows):
+            for j in range(N):
+                acc = 0
+                for r in range(R):
+                    for k in range(K):
+                        acc += int(X[r][d * rows + i][k]) * int(W[r][k][j])
+                y[i][j] = acc
+        out.append(np.array(y, dtype=np.float64))
+    return out
+
+
+@pytest.mark.parametrize("R,M,K,N", [(1, 3, 4, 5), (2, 4, 3, 2), (3, 6, 5, 4), (4, 8, 2, 3)])
+def test_gemm_rs_matches_brute_force(R, M, K, N):
+    rng = np.random.default_rng(R * 100 + M)
+    X = [_ints(rng, (M, K)) for _ in range(R)]
+    W = [_ints(rng, (K, N)) for _ in range(R)]
+    got = oracle.gemm_rs(X, W)
+    ref = _bf_gemm_rs(X, W)
+    for d in range(R):
+        assert np.array_equal(got[d], ref[d])
+
+
+@pytest.mark.parametrize("R,M,K,N", [(1, 2, 3, 4), (2, 4, 3, 5), (3, 6, 2, 3)])
+def test_ag_gemm_matches_brute_force(R, M, K, N):
+    rng = np.random.default_rng(7 + R)
+    X = [_ints(rng, (M // R, K)) for _ in range(R)]
+    W = [_ints(rng, (K, N)) for _ in range(R)]
+    Y, G = oracle.ag_gemm(X, W)
+    rows = M // R
+    for r in range(R):
+        for g in range(M):
+            src, i = divmod(g, rows)
+            for j in range(N):
+                want = sum(int(X[src][i][k]) * int(W[r][k][j]) for k in range(K))
+                assert Y[r][g, j] == want
+    for g in range(M):
+        src, i = divmod(g, rows)
+        assert np.array_equal(G[g], X[src][i])
+
+
+@pytest.mark.parametrize("R,T,M,N", [(1, 3, 2, 4), (2, 3, 4, 2), (4, 2, 8, 3)])
+def test_dp_grad_rs_matches_brute_force(R, T, M, N):
+    rng = np.random.default_rng(11 + R)
+    X = [_ints(rng, (T, M)) for _ in range(R)]
+    dY = [_ints(rng, (T, N)) for _ in range(R)]
+    got = oracle.dp_grad_rs(X, dY)
+    rows = M // R
+    for d in range(R):
+        for i in range(rows):
+            for j in range(N):
+                want = sum(int(X[r][t][d * rows + i]) * int(dY[r][t][j])
+                           for r in range(R) for t in range(T))
+                assert got[d][i, j] == want
+
+
+def test_sampled_rows_equal_full():
+    rng = np.random.default_rng(5)
+    R, M, K, N = 4, 16, 6, 5
+    X = [_ints(rng, (M, K)) for _ in range(R)]
+    W = [_ints(rng, (K, N)) for _ in range(R)]
+    full = oracle.gemm_rs(X, W)
+    for d in range(R):
+        assert np.array_equal(oracle.gemm_rs_rows(X, W, d, [0, 3, 1]), full[d][[0, 3, 1]])
+    Xa = [_ints(rng, (M // R, K)) for _ in range(R)]
+    Y, _ = oracle.ag_gemm(Xa, W)
+    for r in range(R):
+        assert np.array_equal(oracle.ag_gemm_rows(Xa, W, r, [0, 5, 15]), Y[r][[0, 5, 15]])
+    Xd = [_ints(rng, (K, M)) for _ in range(R)]
+    dY = [_ints(rng, (K, N)) for _ in range(R)]
+    D = oracle.dp_grad_rs(Xd, dY)
+    for d in range(R):
+        assert np.array_equal(oracle.dp_grad_rs_rows(Xd, dY, d, [2, 0]), D[d][[2, 0]])
+
+
+# --------------------------------------------------------------------------
+# Exact rational arithmetic: the fp64 oracle is within fp64 rounding of the
+# exact value for non-integer inputs.
+# --------------------------------------------------------------------------
+
+def test_gemm_rs_within_fp64_rounding_of_exact():
+    rng = np.random.default_rng(3)
+    R, M, K, N = 2, 4, 7, 3
+    X = [rng.standard_normal((M, K)) for _ in range(R)]
+    W = [rng.standard_normal((K, N)) * 0.02 for _ in range(R)]
+    got = oracle.gemm_rs(X, W)
+    rows = M // R
+    for d in range(R):
+        for i in range(rows):
+            for j in range(N):
+                exact = sum(Fraction(float(X[r][d * rows + i, k])) * Fraction(float(W[r][k, j]))
+                            for r in range(R) for k in range(K))
+                mag = sum(abs(Fraction(float(X[r][d * rows + i, k])) * Fraction(float(W[r][k, j])))
+                          for r in range(R) for k in range(K))
+                assert abs(Fraction(got[d][i, j]) - exact) <= mag * Fraction(2 * R * K, 2 ** 52)
+
+
+# --------------------------------------------------------------------------
+# Closed-form probes.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
+def test_ag_identity_weight_returns_gather_in_rank_order(R):
+    rows, K = 3, 5
+    X = [np.arange(rows * K, dtype=np.float64).reshape(rows, K) + 100 * r for r in range(R)]
+    W = [np.eye(K) for _ in range(R)]
+    Y, G = oracle.ag_gemm(X, W)
+    for r in range(R):
+        for q in range(R):
+            assert np.array_equal(Y[r][q * rows:(q + 1) * rows], X[q])
+            assert np.array_equal(G[q * rows:(q + 1) * rows], X[q])
+
+
+def _pow2_probe(R, M, K, N):
+    """X_r = 2^r * E with E one-hot per row (row i -> column i mod K),
+    W_r[k, j] = k + 1. Then Y_d[i, j] = (2^R - 1) * (((d*M/R + i) mod K) + 1)."""
+    X, W = [], []
+    for r in range(R):
+        E = np.zeros((M, K))
+        E[np.arange(M), np.arange(M) % K] = 1.0
+        X.append((2.0 ** r) * E)
+        W.append(np.repeat((np.arange(K, dtype=np.float64) + 1)[:, None], N, axis=1))
+    rows = M // R
+    want = [np.repeat(((((d * rows + np.arange(rows)) % K) + 1) * (2 ** R - 1))[:, None], N, axis=1)
+            .astype(np.float64) for d in range(R)]
+    return X, W, want
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 5, 8])
+def test_power_of_two_probe_each_contribution_exactly_once(R):
+    X, W, want = _pow2_probe(R, 4 * R, 7, 3)
+    for f in (oracle.gemm_rs, oracle.simulate_gemm_rs,
+              lambda x, w: oracle.simulate_gemm_rs(x, w, ring=True)):
+        got = f(X, W)
+        for d in range(R):
+            assert np.array_equal(got[d], want[d])
+
+
+def test_planted_dropped_contribution_is_caught(monkeypatch):
+    real = O.reduce_scatter_rows
+
+    def dropped(P):
+        return real([np.zeros_like(P[0])] + list(P[1:]))   # rank 0's partial lost
+
+    monkeypatch.setattr(O, "reduce_scatter_rows", dropped)
+    X, W, want = _pow2_probe(3, 12, 5, 2)
+    got = O.gemm_rs(X, W)
+    assert not all(np.array_equal(got[d], want[d]) for d in range(3))
+
+
+def test_planted_wrong_row_block_is_caught(monkeypatch):
+    real = O.reduce_scatter_rows
+
+    def rotated(P):
+        out = real(P)
+        return out[1:] + out[:1]
+
+    monkeypatch.setattr(O, "reduce_scatter_rows", rotated)
+    X, W, want = _pow2_probe(4, 16, 5, 2)
+    got = O.gemm_rs(X, W)
+    assert not all(np.array_equal(got[d], want[d]) for d in range(4))
+
+
+def test_planted_transposed_operand_is_caught():
+    rng = np.random.default_rng(9)
+    X = [_ints(rng, (4, 4)) for _ in range(2)]
+    W = [_ints(rng, (4, 4)) for _ in range(2)]
+    ref = _bf_gemm_rs(X, W)
+    wrong = O.reduce_scatter_rows([X[r] @ W[r].T for r in range(2)])
+    assert not all(np.array_equal(wrong[d], ref[d]) for d in range(2))
+
+
+# --------------------------------------------------------------------------
+# Decomposed == collective (integer mode: bit-equal).
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 6, 8])
+def test_decomposed_rs_equals_collective(R):
+    rng = np.random.default_rng(R)
+    M, K, N = 2 * R, 5, 3
+    X = [_ints(rng, (M, K)) for _ in range(R)]
+    W = [_ints(rng, (K, N)) for _ in range(R)]
+    ref = oracle.gemm_rs(X, W)
+    for ring in (False, True):
+        got = oracle.simulate_gemm_rs(X, W, ring=ring)
+        for d in range(R):
+            assert np.array_equal(got[d], ref[d])
+    got = oracle.simulate_gemm_rs(X, W, schedule=oracle.sliced_schedule(R))
+    for d in range(R):
+        assert np.array_equal(got[d], ref[d])
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
+def test_decomposed_ag_equals_collective(R):
+    rng = np.random.default_rng(20 + R)
+    rows, K, N = 2, 4, 3
+    X = [_ints(rng, (rows, K)) for _ in range(R)]
+    W = [_ints(rng, (K, N)) for _ in range(R)]
+    ref, G = oracle.ag_gemm(X, W)
+    got, Gr = oracle.simulate_ag_gemm(X, W)
+    for r in range(R):
+        assert np.array_equal(got[r], ref[r])
+        assert np.array_equal(Gr[r], G)
+
+
+@pytest.mark.parametrize("R", [1, 2, 4, 8])
+def test_decomposed_dp_grad_equals_collective(R):
+    rng = np.random.default_rng(40 + R)
+    T, M, N = 3, 2 * R, 3
+    X = [_ints(rng, (T, M)) for _ in range(R)]
+    dY = [_ints(rng, (T, N)) for _ in range(R)]
+    ref = oracle.dp_grad_rs(X, dY)
+    got = oracle.simulate_dp_grad_rs(X, dY)
+    for d in range(R):
+        assert np.array_equal(got[d], ref[d])
+
+
+def test_ag_simulator_rejects_use_before_arrival():
+    R = 3
+    X = [np.ones((1, 2)) for _ in range(R)]
+    W = [np.ones((2, 1)) for _ in range(R)]
+    bad = oracle.ag_schedule(R).copy()
+    bad[:, [1, 2]] = bad[:, [2, 1]]          # consume the 2-hop shard first
+    with pytest.raises(AssertionError):
+        oracle.simulate_ag_gemm(X, W, schedule=bad)
+
+
+def test_ring_rs_rejects_schedule_without_own_last():
+    R = 3
+    X = [np.ones((3, 2)) for _ in range(R)]
+    W = [np.ones((2, 1)) for _ in range(R)]
+    with pytest.raises(AssertionError):
+        oracle.simulate_gemm_rs(X, W, schedule=oracle.sliced_schedule(R), ring=True)
+
+
+# --------------------------------------------------------------------------
+# Schedules: the hand-derived fixture and the invariants the pages fix.
+# --------------------------------------------------------------------------
+
+def _read_golden_schedule():
+    rs, ag = {}, {}
+    with open(os.path.join(GOLDEN, "schedule_r4.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, vals = line.split(":")
+            op, r = head.split()
+            (rs if op == "rs" else ag)[int(r)] = [int(v) for v in vals.split()]
+    return rs, ag
+
+
+def test_schedules_match_hand_derived_fixture():
+    rs, ag = _read_golden_schedule()
+    assert oracle.rs_schedule(4).tolist() == [rs[r] for r in range(4)]
+    assert oracle.ag_schedule(4).tolist() == [ag[r] for r in range(4)]
+
+
+@pytest.mark.parametrize("R", list(range(1, 17)))
+def test_schedule_invariants(R):
+    rs = oracle.rs_schedule(R)
+    ag = oracle.ag_schedule(R)
+    for r in range(R):
+        assert sorted(rs[r].tolist()) == list(range(R))       # (i) permutation
+        assert sorted(ag[r].tolist()) == list(range(R))
+        assert rs[r, R - 1] == r                               # (ii) own chunk last
+        assert ag[r, 0] == r                                   #      own shard first
+    for s in range(R):
+        assert sorted(rs[:, s].tolist()) == list(range(R))    # (iii) bijection per step
+        assert sorted(ag[:, s].tolist()) == list(range(R))
+    tr = oracle.rs_transfers(R)
+    assert len(tr) == R * (R - 1)                              # (v)
+    assert all(step < R - 1 for (_, _, _, step) in tr)        # no send at the last step
+    assert len(set((d, c, s) for (_, d, c, s) in tr)) == len(tr)
+    ring = oracle.rs_transfers(R, ring=True)
+    assert len(ring) == R * (R - 1)
+    agt = oracle.ag_transfers(R)
+    assert len(agt) == R * (R - 1)
+    for (src, dst, shard, s) in agt:                           # ring forwarding feeds step s+1
+        assert ag[dst, s + 1] == shard
+
+
+@pytest.mark.parametrize("R", [2, 3, 4, 5])
+def test_dependency_graph_is_acyclic_and_respects_order(R):
+    edges = oracle.rs_dependency_edges(R)
+    nodes = {(r, s) for r in range(R) for s in range(R)}
+    indeg = {n: 0 for n in nodes}
+    for a, b in edges:
+        indeg[b] += 1
+    ready = [n for n in nodes if indeg[n] == 0]
+    seen = 0
+    adj = {n: [] for n in nodes}
+    for a, b in edges:
+        adj[a].append(b)
+    while ready:
+        n = ready.pop()
+        seen += 1
+        for m in adj[n]:
+            indeg[m] -= 1
+            if indeg[m] == 0:
+                ready.append(m)
+    assert seen == len(nodes)
+    for (a, b) in edges:
+        if a[0] != b[0]:
+            assert b[1] > a[1] or b[1] == R - 1                # consumer later in its own order
+
+
+# --------------------------------------------------------------------------
+# Brute force over per-rank orders under the cost model.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R", [2, 3, 4])
+@pytest.mark.parametrize("tx", [0.3, 0.6, 0.9, 1.0])
+def test_rank_adaptive_is_optimal_and_tail_free(R, tx):
+    tc = 1.0
+    ends, last_sends = oracle.brute_force_rs(R, tc, tx)
+    ra = oracle.rs_makespan(oracle.rs_schedule(R), tc, tx)
+    assert ra == pytest.approx(R * tc)
+    assert ends.min() == pytest.approx(R * tc)
+    if R > 1:
+        assert np.all(ends[last_sends] >= R * tc + tx - 1e-12)
+    sl = oracle.rs_makespan(oracle.sliced_schedule(R), tc, tx)
+    if R > 1:
+        assert sl >= R * tc + tx - 1e-12
+
+
+def test_own_last_alone_is_not_enough_when_transfers_collide():
+    # Two ranks sending to one owner in the same step serialise: with
+    # t_x > t_c / 2 such an order is slower although every own chunk is last.
+    R, tc, tx = 3, 1.0, 0.9
+    orders = np.array([[1, 2, 0], [2, 0, 1], [1, 0, 2]])   # ranks 0 and 2 both send chunk 1 first
+    assert all(orders[r, R - 1] == r for r in range(R))
+    assert oracle.rs_makespan(orders, tc, tx) > R * tc
+
+
+def test_vectorised_brute_force_matches_scalar_model():
+    R = 3
+    perms = list(itertools.permutations(range(R)))
+    ends, _ = oracle.brute_force_rs(R, 1.0, 0.7)
+    rng = np.random.default_rng(0)
+    combos = list(itertools.product(range(len(perms)), repeat=R))
+    for i in rng.choice(len(combos), 40, replace=False):
+        orders = np.array([perms[q] for q in combos[i]])
+        assert ends[i] == pytest.approx(oracle.rs_makespan(orders, 1.0, 0.7))
+
+
+# --------------------------------------------------------------------------
+# Output precision and error measures.
+# --------------------------------------------------------------------------
+
+def test_round_bf16_known_values():
+    one = 1.0
+    ulp = 2.0 ** -7
+    assert oracle.round_bf16(np.array([one + ulp / 2]))[0] == one                 # tie -> even
+    assert oracle.round_bf16(np.array([one + 1.5 * ulp]))[0] == one + 2 * ulp     # tie -> even
+    assert oracle.round_bf16(np.array([one + 0.51 * ulp]))[0] == one + ulp
+    assert oracle.round_bf16(np.array([-3.0]))[0] == -3.0
+    assert oracle.round_bf16(np.array([0.0]))[0] == 0.0
+
+
+def test_round_bf16_matches_torch_cast_on_fp32_values():
+    g = torch.Generator().manual_seed(0)
+    x = torch.randn(100000, generator=g) * 37.0
+    want = x.to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_bf16(x.to(torch.float64).numpy())
+    assert np.array_equal(got, want)
+
+
+def test_rel_errors_simple_cases():
+    ref = np.array([1.0, -2.0, 0.0, 4.0])
+    fro, mx, clamped = oracle.rel_errors(ref, ref)
+    assert fro == 0.0 and mx == 0.0 and clamped == 1
+    got = ref + np.array([0.1, 0.0, 0.0, 0.0])
+    fro, mx, _ = oracle.rel_errors(got, ref)
+    assert fro == pytest.approx(0.1 / np.sqrt(21.0))
+    assert mx == pytest.approx(0.1)
