@@ -1,0 +1,433 @@
+// C ABI of libflashoverlap.so: argument checks, TMA descriptor encoding,
+// launches of the persistent chunk-GEMM kernel and of the two auxiliary
+// kernels used by the unfused baselines, and the device status query.
+#include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "fo_internal.h"
+#include "fo_kernel.cuh"
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+struct DevInfo {
+  int sms = 0;
+  bool sm103 = false;
+};
+
+// Per-device properties, queried once per device.
+fo_status device_info(DevInfo* out) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  static bool have[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (!have[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FO_ERR_CUDA;
+    }
+    cache[dev].sms = sms;
+    cache[dev].sm103 = (major == 10 && minor == 3);
+    have[dev] = true;
+  }
+  *out = cache[dev];
+  return FO_OK;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool enc2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+           uint64_t row_bytes, uint32_t box_in, uint32_t box_out) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_in, box_out};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool enc3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+           uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1) {
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+enum CallKind { KIND_NONE = 0, KIND_RS = 1, KIND_DP = 2, KIND_AG = 3, KIND_PART = 4 };
+
+// Returns the cached parameter block when the same call kind is made with
+// the same pointers again, else nullptr.
+fo::FoParams* cached_params(fo_plan_t p, int kind, const void* const* a, const void* const* b,
+                            const void* const* d) {
+  if (!p->param_cache || p->param_cache_kind != kind) return nullptr;
+  for (int r = 0; r < p->R; ++r)
+    if (p->param_cache_key[r] != a[r] || p->param_cache_key[FO_MAX_R + r] != b[r] ||
+        p->param_cache_key[2 * FO_MAX_R + r] != d[r])
+      return nullptr;
+  return static_cast<fo::FoParams*>(p->param_cache);
+}
+
+fo::FoParams* fresh_params(fo_plan_t p) {
+  if (!p->param_cache) {
+    void* mem = nullptr;
+    if (posix_memalign(&mem, 128, sizeof(fo::FoParams))) return nullptr;
+    p->param_cache = mem;
+  }
+  p->param_cache_kind = KIND_NONE;
+  memset(p->param_cache, 0, sizeof(fo::FoParams));
+  return static_cast<fo::FoParams*>(p->param_cache);
+}
+
+void remember(fo_plan_t p, int kind, const void* const* a, const void* const* b, const void* const* d) {
+  for (int r = 0; r < p->R; ++r) {
+    p->param_cache_key[r] = a[r];
+    p->param_cache_key[FO_MAX_R + r] = b[r];
+    p->param_cache_key[2 * FO_MAX_R + r] = d[r];
+  }
+  p->param_cache_kind = kind;
+}
+
+void fill_common(fo_plan_t p, fo::FoParams* k, void* ws) {
+  memcpy(k->table, p->table, sizeof(k->table));
+  memcpy(k->ord, p->ord, sizeof(k->ord));
+  k->R = p->R;
+  k->tiles_m = p->tiles_m;
+  k->tiles_n = p->tiles_n;
+  k->num_kb = p->num_kb;
+  k->rows_per_chunk = (int32_t)p->rows_per_chunk;
+  k->deterministic = p->d.deterministic ? 1 : 0;
+  k->fault_inject = p->d.fault_inject;
+  k->counters = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + p->ws_counters_off);
+  k->status = static_cast<int32_t*>(ws);
+  k->timeout_ns = p->d.timeout_ns;
+}
+
+fo_status check_ptrs(int R, const void* const* a) {
+  if (!a) return FO_ERR_INVALID_ARG;
+  for (int r = 0; r < R; ++r) {
+    if (!a[r]) return FO_ERR_INVALID_ARG;
+    if (!aligned16(a[r])) return FO_ERR_ALIGN;
+  }
+  return FO_OK;
+}
+
+// Encode the operand maps of a GEMM-RS / DP-grad-RS / pure-control call.
+fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A, const void* const* B,
+                        void* const* D, void* ws, fo::FoParams** out) {
+  const int kind = partial ? KIND_PART : (dp ? KIND_DP : KIND_RS);
+  fo::FoParams* k = cached_params(p, kind, A, B, (const void* const*)D);
+  if (k) {
+    fill_common(p, k, ws);
+    *out = k;
+    return FO_OK;
+  }
+  k = fresh_params(p);
+  if (!k) return FO_ERR_INVALID_ARG;
+  const int R = p->R;
+  const uint64_t M = (uint64_t)p->d.M, N = (uint64_t)p->d.N, rpc = (uint64_t)p->rows_per_chunk;
+  const uint64_t kr = (uint64_t)p->k_red;
+  const int es = p->elem_bytes;
+  const CUtensorMapDataType dt = es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const uint32_t bk = FO_BK_BYTES / es;
+  bool ok = true;
+  for (int r = 0; r < R && ok; ++r) {
+    if (!dp) {
+      ok &= enc2d(&k->tmA[r], dt, A[r], kr, M, kr * es, bk, FO_BM);
+      if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, B[r], N, kr, N * es, bk, bk);
+      else ok &= enc2d(&k->tmB[r], dt, B[r], kr, N, kr * es, bk, FO_BN);
+    } else {
+      ok &= enc2d(&k->tmA[r], dt, A[r], M, kr, M * es, bk, bk);
+      ok &= enc2d(&k->tmB[r], dt, B[r], N, kr, N * es, bk, bk);
+    }
+    if (partial) ok &= enc3d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D[r], N, rpc, R, N * 4, rpc * N * 4, 32, 32);
+    else ok &= enc2d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D[r], N, rpc, N * 4, 32, 32);
+  }
+  if (!ok) return FO_ERR_CUDA;
+  remember(p, kind, A, B, (const void* const*)D);
+  fill_common(p, k, ws);
+  *out = k;
+  return FO_OK;
+}
+
+fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* ws,
+                   fo::FoParams** out) {
+  fo::FoParams* k = cached_params(p, KIND_AG, X, W, (const void* const*)Y);
+  if (k) {
+    fill_common(p, k, ws);
+    *out = k;
+    return FO_OK;
+  }
+  k = fresh_params(p);
+  if (!k) return FO_ERR_INVALID_ARG;
+  const int R = p->R;
+  const uint64_t K = (uint64_t)p->d.K, nr = (uint64_t)p->n_out, rpc = (uint64_t)p->rows_per_chunk;
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok = true;
+  for (int r = 0; r < R && ok; ++r) {
+    ok &= enc2d(&k->tmA[r], dt, X[r], K, rpc, K * 2, 64, FO_BM);
+    if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, W[r], nr, K, nr * 2, 64, 64);
+    else ok &= enc2d(&k->tmB[r], dt, W[r], K, nr, K * 2, 64, FO_BN);
+    ok &= enc3d(&k->tmD[r], dt, Y[r], nr, rpc, R, nr * 2, rpc * nr * 2, 64, 32);
+  }
+  if (!ok) return FO_ERR_CUDA;
+  remember(p, KIND_AG, X, W, (const void* const*)Y);
+  fill_common(p, k, ws);
+  *out = k;
+  return FO_OK;
+}
+
+fo_status preflight(fo_plan_t p, DevInfo* di) {
+  if (!load_encode()) return FO_ERR_CUDA;
+  fo_status st = device_info(di);
+  if (st != FO_OK) return st;
+  if (!di->sm103) return FO_ERR_UNSUPPORTED;
+  (void)p;
+  return FO_OK;
+}
+
+fo_status run_chunk_gemm(fo_plan_t p, int variant, const fo::FoParams* k, const DevInfo& di, cudaStream_t s) {
+  const int total = p->R * p->R * p->tiles_m * p->tiles_n;
+  const int grid = total < di.sms ? total : di.sms;
+  cudaError_t e = fo_launch_variant(variant, *k, grid, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  p->last_launches = 1;
+  return FO_OK;
+}
+
+// ---------------------------------------------------------------- aux kernels
+
+struct PtrArray {
+  const void* p[FO_MAX_R];
+};
+struct MutPtrArray {
+  void* p[FO_MAX_R];
+};
+
+// Y_d = sum_r P_r[rows of d]: one float4 of one shard per thread and loop trip.
+__global__ void reduce_scatter_f32_kernel(PtrArray P, MutPtrArray Y, int R, int64_t shard_vec4) {
+  const int64_t total = shard_vec4 * R;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int d = (int)(i / shard_vec4);
+    const int64_t j = i - (int64_t)d * shard_vec4;
+    float4 acc = reinterpret_cast<const float4*>(P.p[0])[(int64_t)d * shard_vec4 + j];
+    for (int r = 1; r < R; ++r) {
+      const float4 v = reinterpret_cast<const float4*>(P.p[r])[(int64_t)d * shard_vec4 + j];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    reinterpret_cast<float4*>(Y.p[d])[j] = acc;
+  }
+}
+
+// G_r[rows of src] = X_src for every (r, src): 16-byte copies.
+__global__ void all_gather_copy_kernel(PtrArray X, MutPtrArray G, int R, int64_t shard_vec16) {
+  const int64_t total = shard_vec16 * R * R;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t pair = i / shard_vec16;
+    const int64_t j = i - pair * shard_vec16;
+    const int r = (int)(pair / R), src = (int)(pair - (int64_t)r * R);
+    const int4 v = reinterpret_cast<const int4*>(X.p[src])[j];
+    reinterpret_cast<int4*>(G.p[r])[(int64_t)src * shard_vec16 + j] = v;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+fo_status fo_workspace_init(fo_plan_t p, void* ws, fo_stream_t stream) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(ws, 0, p->ws_bytes, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  return FO_OK;
+}
+
+fo_status fo_gemm_rs(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* ws,
+                     fo_stream_t stream) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (p->d.op != FO_OP_GEMM_RS) return FO_ERR_INVALID_ARG;
+  fo_status st;
+  if ((st = check_ptrs(p->R, X)) || (st = check_ptrs(p->R, W)) || (st = check_ptrs(p->R, (const void* const*)Y)))
+    return st;
+  if (!aligned16(ws)) return FO_ERR_ALIGN;
+  DevInfo di;
+  if ((st = preflight(p, &di))) return st;
+  fo::FoParams* k = nullptr;
+  if ((st = build_rs_like(p, false, false, X, W, Y, ws, &k))) return st;
+  int v = p->elem_bytes == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
+  return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
+}
+
+fo_status fo_dp_grad_rs(fo_plan_t p, const void* const* X, const void* const* dY, void* const* dW, void* ws,
+                        fo_stream_t stream) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (p->d.op != FO_OP_DP_GRAD_RS) return FO_ERR_INVALID_ARG;
+  fo_status st;
+  if ((st = check_ptrs(p->R, X)) || (st = check_ptrs(p->R, dY)) || (st = check_ptrs(p->R, (const void* const*)dW)))
+    return st;
+  if (!aligned16(ws)) return FO_ERR_ALIGN;
+  DevInfo di;
+  if ((st = preflight(p, &di))) return st;
+  fo::FoParams* k = nullptr;
+  if ((st = build_rs_like(p, true, false, X, dY, dW, ws, &k))) return st;
+  return run_chunk_gemm(p, FO_V_DP_BF16, k, di, (cudaStream_t)stream);
+}
+
+fo_status fo_ag_gemm(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* const* G,
+                     void* ws, fo_stream_t stream) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (p->d.op != FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
+  if (p->d.ag_transport != FO_AG_PEER_READ) return FO_ERR_UNSUPPORTED;
+  if (G) return FO_ERR_UNSUPPORTED;
+  fo_status st;
+  if ((st = check_ptrs(p->R, X)) || (st = check_ptrs(p->R, W)) || (st = check_ptrs(p->R, (const void* const*)Y)))
+    return st;
+  if (!aligned16(ws)) return FO_ERR_ALIGN;
+  DevInfo di;
+  if ((st = preflight(p, &di))) return st;
+  fo::FoParams* k = nullptr;
+  if ((st = build_ag(p, X, W, Y, ws, &k))) return st;
+  int v = p->d.w_layout == FO_W_KN ? FO_V_AG_BF16_KN : FO_V_AG_BF16_NK;
+  return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
+}
+
+fo_status fo_gemm_partials(fo_plan_t p, const void* const* A, const void* const* B, void* const* P, void* ws,
+                           fo_stream_t stream) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (p->d.op == FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
+  fo_status st;
+  if ((st = check_ptrs(p->R, A)) || (st = check_ptrs(p->R, B)) || (st = check_ptrs(p->R, (const void* const*)P)))
+    return st;
+  DevInfo di;
+  if ((st = preflight(p, &di))) return st;
+  const bool dp = p->d.op == FO_OP_DP_GRAD_RS;
+  fo::FoParams* k = nullptr;
+  if ((st = build_rs_like(p, dp, true, A, B, P, ws, &k))) return st;
+  int v = dp ? FO_V_PART_DP
+             : (p->elem_bytes == 4 ? FO_V_PART_TF32_NK
+                                   : (p->d.w_layout == FO_W_KN ? FO_V_PART_BF16_KN : FO_V_PART_BF16_NK));
+  return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
+}
+
+fo_status fo_reduce_scatter_f32(fo_plan_t p, const void* const* P, void* const* Y, fo_stream_t stream) {
+  if (!p) return FO_ERR_INVALID_ARG;
+  if (p->d.op == FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
+  fo_status st;
+  if ((st = check_ptrs(p->R, P)) || (st = check_ptrs(p->R, (const void* const*)Y))) return st;
+  if (p->n_out % 4) return FO_ERR_ALIGN;
+  DevInfo di;
+  if ((st = device_info(&di))) return st;
+  PtrArray pa = {};
+  MutPtrArray ya = {};
+  for (int r = 0; r < p->R; ++r) {
+    pa.p[r] = P[r];
+    ya.p[r] = Y[r];
+  }
+  const int64_t shard_vec4 = p->rows_per_chunk * p->n_out / 4;
+  reduce_scatter_f32_kernel<<<di.sms * 4, 256, 0, (cudaStream_t)stream>>>(pa, ya, p->R, shard_vec4);
+  if (cudaGetLastError() != cudaSuccess) return FO_ERR_CUDA;
+  p->last_launches = 1;
+  return FO_OK;
+}
+
+fo_status fo_all_gather_copy(fo_plan_t p, const void* const* X, void* const* G, fo_stream_t stream) {
+  if (!p) return FO_ERR_INVALID_ARG;
+  if (p->d.op != FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
+  fo_status st;
+  if ((st = check_ptrs(p->R, X)) || (st = check_ptrs(p->R, (const void* const*)G))) return st;
+  DevInfo di;
+  if ((st = device_info(&di))) return st;
+  PtrArray xa = {};
+  MutPtrArray ga = {};
+  for (int r = 0; r < p->R; ++r) {
+    xa.p[r] = X[r];
+    ga.p[r] = G[r];
+  }
+  const int64_t shard_vec16 = p->rows_per_chunk * p->d.K * 2 / 16;
+  all_gather_copy_kernel<<<di.sms * 4, 256, 0, (cudaStream_t)stream>>>(xa, ga, p->R, shard_vec16);
+  if (cudaGetLastError() != cudaSuccess) return FO_ERR_CUDA;
+  p->last_launches = 1;
+  return FO_OK;
+}
+
+fo_status fo_status_query(fo_plan_t p, void* ws, fo_stream_t stream, int32_t info[4]) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  int32_t h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  if (info) memcpy(info, h, sizeof(h));
+  if (h[0] != 0) {
+    if (cudaMemset(ws, 0, p->ws_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return FO_ERR_CUDA;
+    }
+    return (fo_status)h[0];
+  }
+  return FO_OK;
+}
+
+}  // extern "C"
+
+cudaError_t fo_launch_rs(int v, const fo::FoParams& p, int grid, cudaStream_t s);
+cudaError_t fo_launch_dp(int v, const fo::FoParams& p, int grid, cudaStream_t s);
+cudaError_t fo_launch_ag(int v, const fo::FoParams& p, int grid, cudaStream_t s);
+cudaError_t fo_launch_part(int v, const fo::FoParams& p, int grid, cudaStream_t s);
+
+cudaError_t fo_launch_variant(int v, const fo::FoParams& p, int grid, cudaStream_t s) {
+  switch (v) {
+    case FO_V_RS_BF16_KN:
+    case FO_V_RS_BF16_NK:
+    case FO_V_RS_TF32_NK: return fo_launch_rs(v, p, grid, s);
+    case FO_V_DP_BF16:
+    case FO_V_PART_DP: return fo_launch_dp(v, p, grid, s);
+    case FO_V_AG_BF16_KN:
+    case FO_V_AG_BF16_NK: return fo_launch_ag(v, p, grid, s);
+    case FO_V_PART_BF16_KN:
+    case FO_V_PART_BF16_NK:
+    case FO_V_PART_TF32_NK: return fo_launch_part(v, p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}

@@ -1,0 +1,61 @@
+// Internal declarations shared by the host-side translation units of
+// libflashoverlap.so. Not part of the public ABI (see include/flashoverlap.h).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "flashoverlap.h"
+
+#define FO_MAX_R 16
+
+// Tile shape of the chunk GEMM: one CTA owns a 128 x 256 fp32 accumulator in
+// tensor memory; a pipeline stage holds 128 bytes of the reduction dimension
+// (64 bf16 or 32 fp32 elements) of both operands.
+#define FO_BM 128
+#define FO_BN 256
+#define FO_BK_BYTES 128
+
+struct fo_transfer { int32_t src, dst, chunk, step; };
+struct fo_edge { int32_t ra, sa, rb, sb; };
+
+struct fo_plan_s {
+  fo_plan_desc d;
+  int R;
+  // table[r][s]: chunk (RS/DP: owner of the partial) or source shard (AG)
+  // handled by rank r at step s.
+  int32_t table[FO_MAX_R][FO_MAX_R];
+  // ord[r][s]: how many partials of the same chunk come before (r, s) in
+  // (step, rank) order; 0 = the first partial, which stores instead of adds.
+  int32_t ord[FO_MAX_R][FO_MAX_R];
+  std::vector<fo_transfer> transfers;
+  std::vector<fo_edge> edges;
+
+  // Derived sizes of one chunk task.
+  int64_t rows_per_chunk;  // M / R: rows of one chunk of the output (RS/DP) or of one shard (AG)
+  int64_t k_red;           // reduction length of one task
+  int64_t n_out;           // output columns of one task
+  int elem_bytes;          // 2 (bf16) or 4 (fp32 -> tf32 MMA)
+  int tiles_m, tiles_n, num_kb;
+
+  // Workspace layout.
+  size_t ws_bytes;
+  size_t ws_counters_off;  // RS/DP: uint32 [R][tiles_m*tiles_n][4]
+  size_t ws_flags_off;     // AG copy transport: uint32 [R][R][tiles_m]
+
+  int32_t last_launches;
+  void* param_cache;       // host copy of the last kernel parameter block
+  int param_cache_kind;    // which call built it (0 = none)
+  const void* param_cache_key[4 * FO_MAX_R];  // the pointers it was built from
+};
+
+// Workspace header (offset 0): device status word and launch epoch.
+struct fo_ws_header {
+  int32_t code;            // 0 or FO_ERR_TIMEOUT
+  int32_t rank, step, chunk;
+  uint32_t epoch;          // incremented by the last CTA of every AG launch
+  uint32_t exit_count;     // CTAs of the current AG launch that finished
+  uint32_t pad[10];
+};

@@ -1,0 +1,402 @@
+// The persistent chunk-GEMM kernel of FlashOverlap on sm_103a.
+//
+// One CTA per SM walks a static list of 128 x 256 output tiles in step-major
+// order: all tiles of step 0 (every rank's first chunk task), then step 1,
+// and so on. This is the rank-adaptive order of Flash-RS / Flash-AG
+// (gist.science, "Technical Summary" section 2): for reduce-scatter each
+// rank's own chunk is its last task, for all-gather its first.
+//
+// Warp roles (192 threads):
+//   warp 0     TMA producer: loads 128-byte-wide K slices of both operands
+//              into a 4-stage shared-memory ring (128B swizzle).
+//   warp 1     MMA issuer: allocates 512 TMEM columns (two 128 x 256 fp32
+//              accumulators), issues tcgen05.mma, commits to mbarriers.
+//   warps 2-5  epilogue: tcgen05.ld the accumulator (each warp its 32-lane
+//              quarter), stage 32-row sub-tiles in shared memory and move
+//              them with TMA:
+//                RS/DP : the partial of chunk c goes to owner c's shard:
+//                        the first partial of a shard is stored, later ones
+//                        are added (TMA reduce-add, fp32, at L2) once the
+//                        per-tile counter says the shard holds the first.
+//                        This accumulate is the P2P transfer.
+//                AG    : bf16 store into rank r's output rows of the source
+//                        shard; the A operand was read straight from the
+//                        source rank's buffer (the transfer is the read).
+//                PARTIAL: fp32 store into the computing rank's own buffer
+//                        (pure-GEMM control, no transfer).
+// Synchronisation (shd-paper.top, 方法详解 "key design" paragraph, item 3):
+// mbarriers inside the CTA, acquire/release counters in global memory across
+// CTAs; every wait is bounded and failures land in a device status word.
+#pragma once
+
+#include "fo_device.cuh"
+#include "fo_internal.h"
+
+namespace fo {
+
+constexpr int kStages = 4;
+constexpr int kAStage = FO_BM * FO_BK_BYTES;   // 16 KB
+constexpr int kBStage = FO_BN * FO_BK_BYTES;   // 32 KB
+constexpr int kStageBytes = kAStage + kBStage;
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBuf = 32 * 128;              // 32 rows x 128 bytes
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kBarBytes = 128;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * 2 * kEpiBuf + kBarBytes;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kMbarLimitNs = 2000000000ull;
+
+enum Epi : int { EPI_RS = 0, EPI_AG = 1, EPI_PARTIAL = 2 };
+
+struct alignas(128) FoParams {
+  CUtensorMap tmA[FO_MAX_R];   // RS: X_r; DP: X_r ([T x M]); AG: X_src
+  CUtensorMap tmB[FO_MAX_R];   // W_r or dY_r
+  CUtensorMap tmD[FO_MAX_R];   // RS/DP: Y_c (2-D); AG: Y_r (3-D); PARTIAL: P_r (3-D)
+  int32_t table[FO_MAX_R][FO_MAX_R];
+  int32_t ord[FO_MAX_R][FO_MAX_R];
+  int32_t R;
+  int32_t tiles_m;             // m-tiles per chunk
+  int32_t tiles_n;
+  int32_t num_kb;
+  int32_t rows_per_chunk;
+  int32_t deterministic;
+  int32_t fault_inject;
+  int32_t pad0;
+  uint32_t* counters;          // RS/DP: [R][tiles_m * tiles_n][4]
+  int32_t* status;             // fo_ws_header
+  uint64_t timeout_ns;
+};
+
+template <bool A_MN, bool B_MN, bool TF32>
+__host__ __device__ constexpr uint32_t instr_desc() {
+  // kind::f16 / kind::tf32 instruction descriptor: D fp32 (bits 4-5 = 1),
+  // A and B format (bits 7-9, 10-12: bf16 = 1, tf32 = 2), A/B major (bits 15,
+  // 16: 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+  return (1u << 4) | ((TF32 ? 2u : 1u) << 7) | ((TF32 ? 2u : 1u) << 10) | ((A_MN ? 1u : 0u) << 15) |
+         ((B_MN ? 1u : 0u) << 16) | ((uint32_t)(FO_BN >> 3) << 17) | ((uint32_t)(FO_BM >> 4) << 24);
+}
+
+struct Tile {
+  int r, s, c, ord, mt, nt;
+};
+
+__device__ __forceinline__ Tile decode_tile(const FoParams& p, int L) {
+  const int tpt = p.tiles_m * p.tiles_n;
+  const int task = L / tpt;
+  const int t = L - task * tpt;
+  Tile ti;
+  ti.s = task / p.R;
+  ti.r = task - ti.s * p.R;
+  ti.mt = t / p.tiles_n;
+  ti.nt = t - ti.mt * p.tiles_n;
+  ti.c = p.table[ti.r][ti.s];
+  ti.ord = p.ord[ti.r][ti.s];
+  return ti;
+}
+
+// Write 32 registers (one 128-byte row per thread) into a 32 x 128 B staging
+// buffer in the TMA 128B-swizzle layout: 16-byte chunk j of row i lives at
+// chunk j ^ (i % 8).
+__device__ __forceinline__ void stage_row_sw128(uint32_t buf, int lane, const uint32_t (&w)[32]) {
+  const uint32_t row = buf + (uint32_t)lane * 128u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t addr = row + ((uint32_t)(j ^ (lane & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * j]), "r"(w[4 * j + 1]),
+                 "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
+                 : "memory");
+  }
+}
+
+template <int EPI, bool A_MN, bool B_MN, bool TF32>
+__global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid_constant__ FoParams p) {
+  constexpr int kEsz = TF32 ? 4 : 2;
+  constexpr int kBK = FO_BK_BYTES / kEsz;        // K elements per stage (= MN elements per 128B row)
+  constexpr int kMmaK = 32 / kEsz;               // K of one tcgen05.mma (32 bytes)
+  constexpr int kBoxBytes = kBK * 128;           // one MN-major box: kBK rows x 128 B
+  constexpr uint32_t kIdesc = instr_desc<A_MN, B_MN, TF32>();
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sStage = base;
+  const uint32_t sEpi = base + kStages * kStageBytes;
+  const uint32_t sBar = sEpi + kEpiWarps * 2 * kEpiBuf;
+  auto full_bar = [&](int i) { return sBar + 8u * i; };
+  auto empty_bar = [&](int i) { return sBar + 8u * (kStages + i); };
+  auto tfull_bar = [&](int a) { return sBar + 8u * (2 * kStages + a); };
+  auto tempty_bar = [&](int a) { return sBar + 8u * (2 * kStages + 2 + a); };
+  const uint32_t mma_done_bar = sBar + 8u * (2 * kStages + 4);
+  const uint32_t sTmemSlot = sBar + 8u * (2 * kStages + 5);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + (sTmemSlot - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (sTmemSlot - base) + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const volatile int32_t* gstatus = p.status;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), kEpiWarps);
+    }
+    mbar_init(mma_done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(sTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = p.R * p.R * p.tiles_m * p.tiles_n;
+  const int tpt = p.tiles_m * p.tiles_n;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int L = blockIdx.x; L < total; L += gridDim.x) {
+        if (*gstatus) *abort_flag = 1;
+        if (*abort_flag) break;
+        const Tile ti = decode_tile(p, L);
+        const CUtensorMap* mA = EPI == EPI_AG ? &p.tmA[ti.c] : &p.tmA[ti.r];
+        const CUtensorMap* mB = &p.tmB[ti.r];
+        // Row (or column, for MN-major A) where this tile's A block starts.
+        const int a_mn0 = (EPI == EPI_AG ? 0 : ti.c * p.rows_per_chunk) + ti.mt * FO_BM;
+        const int n0 = ti.nt * FO_BN;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int stage = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait(empty_bar(stage), ph ^ 1u, abort_flag, kMbarLimitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          const uint32_t sa = sStage + stage * kStageBytes;
+          const uint32_t sb = sa + kAStage;
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const int k0 = kb * kBK;
+          if constexpr (A_MN) {
+#pragma unroll
+            for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d(sa + j * kBoxBytes, mA, fb, a_mn0 + j * kBK, k0);
+          } else {
+            tma_load_2d(sa, mA, fb, k0, a_mn0);
+          }
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int j = 0; j < FO_BN / kBK; ++j) tma_load_2d(sb + j * kBoxBytes, mB, fb, n0 + j * kBK, k0);
+          } else {
+            tma_load_2d(sb, mB, fb, k0, n0);
+          }
+        }
+        if (!ok) break;
+      }
+      // Drain: every load still in flight lands before the CTA may exit.
+      const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+      volatile int never = 0;
+      for (uint32_t j = first; j < it; ++j)
+        mbar_wait(full_bar(j % kStages), (j / kStages) & 1u, &never, 100000000ull);
+      if (*abort_flag) record_error(p.status, FO_ERR_TIMEOUT, -1, -1, 0);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, tcount = 0;
+      for (int L = blockIdx.x; L < total; L += gridDim.x, ++tcount) {
+        if (*abort_flag) break;
+        const int acc = tcount & 1;
+        const uint32_t aph = (tcount >> 1) & 1u;
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, kMbarLimitNs)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * FO_BN);
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+          const int stage = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait(full_bar(stage), ph, abort_flag, kMbarLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sStage + stage * kStageBytes;
+          const uint32_t sb = sa + kAStage;
+#pragma unroll
+          for (int k = 0; k < FO_BK_BYTES / 32; ++k) {
+            // K-major: the k-th 32-byte column of the swizzled 128-byte rows.
+            // MN-major: kMmaK K-rows of 128 bytes further into each box.
+            const uint32_t aoff = A_MN ? (uint32_t)(k * kMmaK * 128) : (uint32_t)(k * 32);
+            const uint32_t boff = B_MN ? (uint32_t)(k * kMmaK * 128) : (uint32_t)(k * 32);
+            const uint64_t adesc =
+                A_MN ? smem_desc_sw128(sa + aoff, kBoxBytes, 1024) : smem_desc_sw128(sa + aoff, 16, 1024);
+            const uint64_t bdesc =
+                B_MN ? smem_desc_sw128(sb + boff, kBoxBytes, 1024) : smem_desc_sw128(sb + boff, 16, 1024);
+            tc_mma<TF32>(d, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));
+      }
+      // All issued MMAs complete before TMEM is released.
+      tc_commit(mma_done_bar);
+      volatile int never = 0;
+      mbar_wait(mma_done_bar, 0, &never, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - 2;        // staging buffers of this warp
+    const int q = warp & 3;        // TMEM lane quarter this warp may access
+    uint32_t tcount = 0;
+    for (int L = blockIdx.x; L < total; L += gridDim.x, ++tcount) {
+      if (*abort_flag) break;
+      const Tile ti = decode_tile(p, L);
+      const int acc = tcount & 1;
+      const uint32_t aph = (tcount >> 1) & 1u;
+      if (!mbar_wait(tfull_bar(acc), aph, abort_flag, kMbarLimitNs)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * FO_BN);
+      const int row0 = ti.mt * FO_BM + q * 32;   // first row of this quarter within the chunk
+      const int n0 = ti.nt * FO_BN;
+
+      uint32_t* ctr = nullptr;
+      bool ok = true;
+      if constexpr (EPI == EPI_RS) {
+        const int tile_in_chunk = ti.mt * p.tiles_n + ti.nt;
+        ctr = p.counters + ((size_t)(ti.c * tpt + tile_in_chunk) * 4 + q);
+        if (ti.ord > 0) {
+          // The shard must already hold its first (stored) partial; in
+          // deterministic mode, every partial that comes before this one.
+          int good = 1;
+          if (lane == 0) {
+            const uint32_t need = p.deterministic ? (uint32_t)ti.ord : 1u;
+            good = wait_counter_geq(ctr, need, p.timeout_ns, abort_flag, gstatus) ? 1 : 0;
+            if (!good && !*abort_flag && !*gstatus) record_error(p.status, FO_ERR_TIMEOUT, ti.r, ti.s, ti.c);
+            fence_proxy_async_global();
+          }
+          ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+          if (!ok) *abort_flag = 1;
+        }
+      }
+
+      if constexpr (EPI == EPI_AG) {
+        // 4 sub-tiles of 32 rows x 64 bf16 columns.
+#pragma unroll 1
+        for (int j = 0; j < FO_BN / 64; ++j) {
+          uint32_t v0[32], v1[32], w[32];
+          tmem_ld32(tbase + j * 64, v0);
+          tmem_ld32(tbase + j * 64 + 32, v1);
+          tmem_ld_wait();
+          reg_fence(v0);
+          reg_fence(v1);
+          if (j == FO_BN / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+            w[i] = *reinterpret_cast<uint32_t*>(&h0);
+            w[16 + i] = *reinterpret_cast<uint32_t*>(&h1);
+          }
+          const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          stage_row_sw128(buf, lane, w);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&p.tmD[ti.r], buf, n0 + j * 64, row0, ti.c);
+            bulk_commit();
+          }
+        }
+      } else {
+        // 8 sub-tiles of 32 rows x 32 fp32 columns.
+#pragma unroll 1
+        for (int j = 0; j < FO_BN / 32; ++j) {
+          uint32_t v[32];
+          tmem_ld32(tbase + j * 32, v);
+          tmem_ld_wait();
+          reg_fence(v);
+          if (j == FO_BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+          }
+          if (!ok) continue;
+          const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          stage_row_sw128(buf, lane, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (EPI == EPI_PARTIAL) {
+              tma_store_3d(&p.tmD[ti.r], buf, n0 + j * 32, row0, ti.c);
+            } else {
+              if (ti.ord == 0) tma_store_2d(&p.tmD[ti.c], buf, n0 + j * 32, row0);
+              else tma_reduce_add_2d(&p.tmD[ti.c], buf, n0 + j * 32, row0);
+            }
+            bulk_commit();
+          }
+        }
+        if constexpr (EPI == EPI_RS) {
+          if (ok && lane == 0) {
+            // The partial is in the shard: publish it.
+            bulk_wait<0>();
+            fence_proxy_async_global();
+            const bool skip = p.fault_inject == FO_INJECT_SKIP_SIGNAL && ti.c == 0 && ti.mt == 0 && ti.nt == 0 &&
+                              q == 0 && ti.ord == 0;
+            if (!skip) {
+              const uint32_t old = atom_add_release_u32(ctr, 1u);
+              if (old + 1u == (uint32_t)p.R) atomicExch(ctr, 0u);   // last partial: ready for the next call
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace fo
+
+// Launchers, one per compiled variant (defined in the fo_kern_*.cu files).
+enum fo_variant {
+  FO_V_RS_BF16_KN = 0,
+  FO_V_RS_BF16_NK,
+  FO_V_RS_TF32_NK,
+  FO_V_DP_BF16,
+  FO_V_AG_BF16_KN,
+  FO_V_AG_BF16_NK,
+  FO_V_PART_BF16_KN,
+  FO_V_PART_BF16_NK,
+  FO_V_PART_TF32_NK,
+  FO_V_PART_DP,
+  FO_V_COUNT
+};
+
+cudaError_t fo_launch_variant(int variant, const fo::FoParams& p, int grid, cudaStream_t stream);

@@ -1,0 +1,309 @@
+// Host-side schedule builder and validator (fo_plan and its accessors).
+//
+// The schedule follows the pages about FlashOverlap (arXiv 2604.24013):
+//  * a collective becomes a set of directed P2P chunk transfers (euno.news,
+//    "Methodology" item 1);
+//  * Flash-RS computes the chunk that stays on the rank last (gist.science,
+//    "Technical Summary" section 2, Flash-Reduce-Scatter);
+//  * Flash-AG computes the rank's own shard first and then the shards that
+//    arrive along a ring (same section, Flash-All-Gather);
+//  * the transfers and compute fragments form a dependency graph in which no
+//    sub-task waits for a last piece of data (euno.news, "Methodology" 3).
+// The order of the chunks in between is this library's reading: RS follows
+// the ring reduce-scatter order, chunk (r - 1 - s) mod R at step s, so that
+// every owner receives exactly one partial per step; AG consumes the shard of
+// rank (r - s) mod R, which its ring predecessor forwarded one step earlier.
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+
+#include "fo_internal.h"
+
+namespace {
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool is_perm(const int32_t* v, int n, int stride) {
+  bool seen[FO_MAX_R] = {false};
+  for (int i = 0; i < n; ++i) {
+    int x = v[i * stride];
+    if (x < 0 || x >= n || seen[x]) return false;
+    seen[x] = true;
+  }
+  return true;
+}
+
+void build_table(fo_plan_s* p) {
+  const int R = p->R;
+  const bool ag = p->d.op == FO_OP_AG_GEMM;
+  for (int r = 0; r < R; ++r)
+    for (int s = 0; s < R; ++s) {
+      if (p->d.sched == FO_SCHED_SLICED) p->table[r][s] = s;
+      else if (ag) p->table[r][s] = ((r - s) % R + R) % R;
+      else p->table[r][s] = ((r - 1 - s) % R + 2 * R) % R;
+    }
+  // Contribution order of every (r, s) into its chunk, in (step, rank) order.
+  int seen[FO_MAX_R] = {0};
+  for (int s = 0; s < R; ++s)
+    for (int r = 0; r < R; ++r) p->ord[r][s] = seen[p->table[r][s]]++;
+}
+
+void build_transfers_and_edges(fo_plan_s* p) {
+  const int R = p->R;
+  p->transfers.clear();
+  p->edges.clear();
+  for (int r = 0; r < R; ++r)
+    for (int s = 0; s + 1 < R; ++s) p->edges.push_back({r, s, r, s + 1});
+  if (p->d.op == FO_OP_AG_GEMM) {
+    // Ring: after using shard table[r][s], rank r forwards it to r+1, which
+    // consumes it at step s+1. Nothing is forwarded after the last step.
+    for (int s = 0; s + 1 < R; ++s)
+      for (int r = 0; r < R; ++r) p->transfers.push_back({r, (r + 1) % R, p->table[r][s], s});
+    for (const fo_transfer& t : p->transfers) p->edges.push_back({t.src, t.step, t.dst, t.step + 1});
+  } else {
+    // Direct RS: a non-own partial goes to its owner, whose own-chunk task
+    // (the one that finalises its shard) must come after it.
+    for (int s = 0; s < R; ++s)
+      for (int r = 0; r < R; ++r) {
+        int c = p->table[r][s];
+        if (c != r) p->transfers.push_back({r, c, c, s});
+      }
+    for (const fo_transfer& t : p->transfers) {
+      int own = 0;
+      for (int s = 0; s < R; ++s)
+        if (p->table[t.dst][s] == t.dst) own = s;
+      p->edges.push_back({t.src, t.step, t.dst, own});
+    }
+  }
+  if (p->d.fault_inject == FO_INJECT_DROP_TRANSFER && !p->transfers.empty()) p->transfers.pop_back();
+}
+
+bool dag_acyclic(const fo_plan_s* p) {
+  const int R = p->R, n = R * R;
+  std::vector<int> indeg(n, 0);
+  std::vector<std::vector<int>> adj(n);
+  for (const fo_edge& e : p->edges) {
+    int a = e.ra * R + e.sa, b = e.rb * R + e.sb;
+    if (a == b) continue;  // an edge from a task to itself orders nothing
+    adj[a].push_back(b);
+    indeg[b]++;
+  }
+  std::vector<int> stack;
+  for (int i = 0; i < n; ++i)
+    if (!indeg[i]) stack.push_back(i);
+  int seen = 0;
+  while (!stack.empty()) {
+    int a = stack.back();
+    stack.pop_back();
+    ++seen;
+    for (int b : adj[a])
+      if (--indeg[b] == 0) stack.push_back(b);
+  }
+  return seen == n;
+}
+
+fo_status validate(const fo_plan_s* p) {
+  const int R = p->R;
+  const bool ag = p->d.op == FO_OP_AG_GEMM;
+  const bool adaptive = p->d.sched == FO_SCHED_RANK_ADAPTIVE;
+  for (int r = 0; r < R; ++r)
+    if (!is_perm(&p->table[r][0], R, 1)) return FO_ERR_PLAN_INVARIANT;          // (i)
+  if ((int64_t)p->transfers.size() != (int64_t)R * (R - 1)) return FO_ERR_PLAN_INVARIANT;  // (v)
+  if (!dag_acyclic(p)) return FO_ERR_PLAN_INVARIANT;                             // (iv)
+  if (!adaptive) return FO_OK;
+  for (int r = 0; r < R; ++r) {                                                  // (ii)
+    if (ag ? p->table[r][0] != r : p->table[r][R - 1] != r) return FO_ERR_PLAN_INVARIANT;
+  }
+  for (const fo_transfer& t : p->transfers)
+    if (t.step >= R - 1) return FO_ERR_PLAN_INVARIANT;                           // no tail send
+  for (int s = 0; s < R; ++s)
+    if (!is_perm(&p->table[0][s], R, FO_MAX_R)) return FO_ERR_PLAN_INVARIANT;   // (iii)
+  if (ag) {
+    // Every shard a rank consumes after step 0 arrives by a transfer of that
+    // shard to that rank at an earlier step.
+    for (int r = 0; r < R; ++r)
+      for (int s = 1; s < R; ++s) {
+        bool ok = false;
+        for (const fo_transfer& t : p->transfers)
+          ok |= t.dst == r && t.chunk == p->table[r][s] && t.step < s;
+        if (!ok) return FO_ERR_PLAN_INVARIANT;
+      }
+  } else {
+    // Every partial for owner c is sent before c's own-chunk task, and each
+    // owner receives exactly R-1 partials, one per other rank.
+    for (int c = 0; c < R; ++c) {
+      int n = 0;
+      for (const fo_transfer& t : p->transfers)
+        if (t.dst == c) {
+          ++n;
+          if (t.step >= R - 1 || t.src == c) return FO_ERR_PLAN_INVARIANT;
+        }
+      if (n != R - 1) return FO_ERR_PLAN_INVARIANT;
+    }
+  }
+  return FO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
+  if (!d || !out) return FO_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (d->op < FO_OP_AG_GEMM || d->op > FO_OP_DP_GRAD_RS) return FO_ERR_INVALID_ARG;
+  if (d->R < 1 || d->R > FO_MAX_R) return FO_ERR_INVALID_ARG;
+  if (d->sched != FO_SCHED_RANK_ADAPTIVE && d->sched != FO_SCHED_SLICED) return FO_ERR_INVALID_ARG;
+  if (d->ag_transport != FO_AG_PEER_READ && d->ag_transport != FO_AG_COPY) return FO_ERR_INVALID_ARG;
+  if (d->w_layout != FO_W_KN && d->w_layout != FO_W_NK) return FO_ERR_INVALID_ARG;
+  if (d->fault_inject < FO_INJECT_NONE || d->fault_inject > FO_INJECT_SKIP_SIGNAL) return FO_ERR_INVALID_ARG;
+  for (int i = 0; i < 7; ++i)
+    if (d->reserved[i]) return FO_ERR_INVALID_ARG;
+  if (d->M <= 0 || d->N <= 0 || d->K <= 0) return FO_ERR_SHAPE;
+  const int R = d->R;
+  const int64_t M = d->M, N = d->N, K = d->K;
+  if (M % R) return FO_ERR_SHAPE;
+  if (M / R > (int64_t)1 << 30 || N > (int64_t)1 << 30 || K > (int64_t)1 << 30) return FO_ERR_SHAPE;
+
+  int eb = 2;
+  switch (d->op) {
+    case FO_OP_GEMM_RS:
+      if (K % R) return FO_ERR_SHAPE;
+      if (d->out_dtype != FO_F32) return FO_ERR_DTYPE;
+      if (d->in_dtype == FO_F32) {
+        eb = 4;
+        // fp32 operands feed the tf32 MMA only with both operands K-major.
+        if (d->w_layout != FO_W_NK) return FO_ERR_UNSUPPORTED;
+      } else if (d->in_dtype != FO_BF16) {
+        return FO_ERR_DTYPE;
+      }
+      if (((K / R) * eb) % 16) return FO_ERR_ALIGN;   // rows of X_r (and of W_r if NK)
+      if ((N * eb) % 16) return FO_ERR_ALIGN;         // rows of W_r (KN)
+      if ((N * 4) % 16) return FO_ERR_ALIGN;          // rows of Y
+      break;
+    case FO_OP_AG_GEMM:
+      if (N % R) return FO_ERR_SHAPE;
+      if (d->in_dtype != FO_BF16 || d->out_dtype != FO_BF16) return FO_ERR_DTYPE;
+      if (d->sched != FO_SCHED_RANK_ADAPTIVE) return FO_ERR_UNSUPPORTED;
+      if ((K * 2) % 16 || ((N / R) * 2) % 16) return FO_ERR_ALIGN;
+      break;
+    case FO_OP_DP_GRAD_RS:
+      if (d->in_dtype != FO_BF16) return FO_ERR_DTYPE;
+      if (d->out_dtype != FO_F32) return FO_ERR_DTYPE;
+      if (d->w_layout != FO_W_KN) return FO_ERR_INVALID_ARG;
+      // A chunk starts at column c*M/R of X_r: a TMA coordinate along the
+      // contiguous dimension, so it must fall on a 16-byte boundary.
+      if (((M / R) * 2) % 16) return FO_ERR_ALIGN;
+      if ((M * 2) % 16 || (N * 2) % 16) return FO_ERR_ALIGN;
+      break;
+  }
+
+  fo_plan_s* p = new (std::nothrow) fo_plan_s();
+  if (!p) return FO_ERR_INVALID_ARG;
+  p->d = *d;
+  if (!p->d.timeout_ns) p->d.timeout_ns = 1000000000ull;
+  p->R = R;
+  p->elem_bytes = eb;
+  p->rows_per_chunk = M / R;
+  switch (d->op) {
+    case FO_OP_GEMM_RS: p->k_red = K / R; p->n_out = N; break;
+    case FO_OP_AG_GEMM: p->k_red = K; p->n_out = N / R; break;
+    default: p->k_red = K; p->n_out = N; break;
+  }
+  p->tiles_m = (int)cdiv(p->rows_per_chunk, FO_BM);
+  p->tiles_n = (int)cdiv(p->n_out, FO_BN);
+  p->num_kb = (int)cdiv(p->k_red * eb, FO_BK_BYTES);
+  if ((int64_t)R * R * p->tiles_m * p->tiles_n > ((int64_t)1 << 31) - 1) {
+    delete p;
+    return FO_ERR_SHAPE;
+  }
+  build_table(p);
+  build_transfers_and_edges(p);
+  fo_status st = validate(p);
+  if (st != FO_OK) {
+    delete p;
+    return st;
+  }
+  size_t off = align_up(sizeof(fo_ws_header), 256);
+  p->ws_counters_off = off;
+  p->ws_flags_off = off;
+  if (d->op == FO_OP_AG_GEMM) {
+    off += align_up((size_t)R * R * p->tiles_m * sizeof(uint32_t), 256);
+  } else {
+    off += align_up((size_t)R * p->tiles_m * p->tiles_n * 4 * sizeof(uint32_t), 256);
+  }
+  p->ws_bytes = off;
+  p->last_launches = 0;
+  p->param_cache = nullptr;
+  *out = p;
+  return FO_OK;
+}
+
+void fo_plan_destroy(fo_plan_t p) {
+  if (!p) return;
+  free(p->param_cache);
+  delete p;
+}
+
+fo_status fo_plan_table(fo_plan_t p, int32_t* table) {
+  if (!p || !table) return FO_ERR_INVALID_ARG;
+  for (int r = 0; r < p->R; ++r)
+    for (int s = 0; s < p->R; ++s) table[r * p->R + s] = p->table[r][s];
+  return FO_OK;
+}
+
+fo_status fo_plan_transfers(fo_plan_t p, int32_t* out, int32_t cap, int32_t* n) {
+  if (!p || !n || (cap > 0 && !out) || cap < 0) return FO_ERR_INVALID_ARG;
+  *n = (int32_t)p->transfers.size();
+  for (int i = 0; i < *n && i < cap; ++i) {
+    const fo_transfer& t = p->transfers[i];
+    out[4 * i + 0] = t.src;
+    out[4 * i + 1] = t.dst;
+    out[4 * i + 2] = t.chunk;
+    out[4 * i + 3] = t.step;
+  }
+  return *n <= cap ? FO_OK : FO_ERR_INVALID_ARG;
+}
+
+fo_status fo_plan_edges(fo_plan_t p, int32_t* out, int32_t cap, int32_t* n) {
+  if (!p || !n || (cap > 0 && !out) || cap < 0) return FO_ERR_INVALID_ARG;
+  *n = (int32_t)p->edges.size();
+  for (int i = 0; i < *n && i < cap; ++i) {
+    const fo_edge& e = p->edges[i];
+    out[4 * i + 0] = e.ra;
+    out[4 * i + 1] = e.sa;
+    out[4 * i + 2] = e.rb;
+    out[4 * i + 3] = e.sb;
+  }
+  return *n <= cap ? FO_OK : FO_ERR_INVALID_ARG;
+}
+
+fo_status fo_workspace_size(fo_plan_t p, size_t* bytes) {
+  if (!p || !bytes) return FO_ERR_INVALID_ARG;
+  *bytes = p->ws_bytes;
+  return FO_OK;
+}
+
+int32_t fo_plan_last_launches(fo_plan_t p) { return p ? p->last_launches : -1; }
+
+const char* fo_status_string(fo_status s) {
+  switch (s) {
+    case FO_OK: return "ok";
+    case FO_ERR_INVALID_ARG: return "invalid argument";
+    case FO_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case FO_ERR_DTYPE: return "unsupported dtype combination";
+    case FO_ERR_ALIGN: return "pointer or row stride not 16-byte aligned";
+    case FO_ERR_UNSUPPORTED: return "option or device not supported";
+    case FO_ERR_CUDA: return "CUDA call failed";
+    case FO_ERR_TIMEOUT: return "device-side wait timed out";
+    case FO_ERR_PLAN_INVARIANT: return "schedule failed a validity check";
+  }
+  return "unknown status";
+}
+
+int32_t fo_version(void) { return 0x000100; }
+
+}  // extern "C"

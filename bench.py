@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Benchmark of the fused GEMM + reduce-scatter (FlashOverlap Flash-RS) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extras]
+
+One step = one fo_gemm_rs call over the whole workload: R = 8 virtual ranks,
+each X_r [8192 x 1792] . W_r [1792 x 4096] (bf16, fp32 accumulate), the
+partials reduce-scattered by rows into eight [1024 x 4096] fp32 shards (the
+TP-SP MLP down-projection: 8192 tokens, FFN 14336 / 8 per rank, hidden 4096).
+Inputs are seeded synthetic tensors (X ~ N(0,1), W ~ N(0,0.02)) already
+resident in HBM; together they exceed L2, so no L2 flush runs between steps.
+
+The JSON line reports whole-job TFLOP/s, the roofline fraction of the fused
+kernel against the measured bf16 dense peak, the same metric end to end with
+host buffers (host->device inputs and device->host outputs inside the timed
+region), the CPU oracle timed on a bounded sample, and, next to them, the
+pure-GEMM control, the unfused baseline (our GEMM + a separate reduce kernel)
+and cuBLAS through torch.matmul.
+
+With --gpus N > 1 (launched by torchrun) every rank runs an independent
+replica on its own GPU (the method here needs no cross-GPU exchange: the R
+ranks are buffers on one GPU); value = all ranks' FLOPs / max time.
+
+--impl reference times the CPU oracle (fp64 numpy) on a bounded sample of
+the same workload, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+RS/AG TFLOP/s (R virtual ranks, 1 GB300), % of bf16 tensor peak"
+DEFAULT_WORKLOAD = "gemm_rs_down_r8_t8192_k1792_n4096"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm = float(parts[1])
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                sms.append(sm)
+                maxes.append(mx)
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sms:
+            return None
+        sms.sort()
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_inputs(workload):
+    """The workload's seeded inputs as the float64 arrays the oracle takes."""
+    if workload.op != "gemm_rs":
+        raise ValueError("oracle sample implemented for gemm_rs workloads")
+    inp = workload.make()
+    return [x.double().numpy() for x in inp["X"]], [w.double().numpy() for w in inp["W"]]
+
+
+def oracle_pass(workload, arrays, rows: int):
+    """One pass of the CPU oracle over the first `rows` rows of every output
+    shard; returns (seconds, FLOPs)."""
+    import numpy as np
+
+    import oracle
+    d = workload.dims
+    Xn, Wn = arrays
+    idx = np.arange(rows)
+    t0 = time.perf_counter()
+    for sh in range(workload.R):
+        oracle.gemm_rs_rows(Xn, Wn, sh, idx)
+    return time.perf_counter() - t0, 2.0 * workload.R * rows * workload.R * d["K"] * d["N"]
+
+
+def oracle_rows_for(workload, arrays, target_s: float) -> int:
+    """Rows per shard whose oracle pass takes about target_s (doubling from 4,
+    at most the whole shard)."""
+    rpc = workload.dims["M"] // workload.R
+    rows = 4
+    while rows < rpc:
+        dt, _ = oracle_pass(workload, arrays, rows)
+        if dt >= target_s / 2:
+            break
+        rows = min(rpc, rows * 2)
+    return rows
+
+
+def oracle_sample(workload, arrays, budget_s: float = 12.0):
+    """Time the oracle for about budget_s on a bounded sample of the workload:
+    (TFLOP/s, description)."""
+    rows = oracle_rows_for(workload, arrays, min(budget_s, 4.0))
+    tot_t = tot_f = 0.0
+    passes = 0
+    while tot_t < budget_s and passes < 10:
+        dt, fl = oracle_pass(workload, arrays, rows)
+        tot_t += dt
+        tot_f += fl
+        passes += 1
+    desc = (f"{passes} pass(es) over {rows} of {workload.dims['M'] // workload.R} rows of each of the "
+            f"{workload.R} shards ({tot_f / 1e9:.0f} GFLOP fp64, {tot_t:.1f} s)")
+    return tot_f / tot_t / 1e12, desc
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from ag_gemm_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    arrays = oracle_inputs(w)
+    rows = oracle_rows_for(w, arrays, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    per = []
+    for i in range(args.warmup + args.steps):
+        dt, fl = oracle_pass(w, arrays, rows)
+        if i >= args.warmup:
+            per.append((dt, fl))
+    tot_t = sum(p[0] for p in per)
+    tot_flops = sum(p[1] for p in per)
+    value = tot_flops / tot_t / 1e12
+    desc = (f"per step: {rows} of {w.dims['M'] // w.R} rows of each of the {w.R} shards "
+            f"({per[0][1] / 1e9:.0f} GFLOP fp64 numpy)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / len(per),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "R": w.R, **w.dims, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from ag_gemm_gb300 import binding as B
+    from ag_gemm_gb300.inputs import WORKLOADS
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    w = WORKLOADS[args.workload]
+    if w.op != "gemm_rs":
+        raise SystemExit("bench.py times gemm_rs workloads")
+    R, M, K, N = w.R, w.dims["M"], w.dims["K"], w.dims["N"]
+    flops = w.flops()
+    peaks, peak_src = load_peaks()
+
+    inp = w.make()
+    X = [x.to(dev) for x in inp["X"]]
+    W = [x.to(dev) for x in inp["W"]]
+    Y = [torch.empty(M // R, N, dtype=torch.float32, device=dev) for _ in range(R)]
+    plan = B.fo_plan("gemm_rs", R, M, N, K * R)
+    ws = torch.empty(B.fo_workspace_size(plan), dtype=torch.uint8, device=dev)
+    B.fo_workspace_init(plan, ws)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.fo_gemm_rs(plan, X, W, Y, ws, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    code, info = B.fo_status_query(plan, ws, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} {info}")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches = 0
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+            launches += B.fo_plan_last_launches(plan)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    code, info = B.fo_status_query(plan, ws, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} {info}")
+    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    ms_per_step = elapsed_ms / args.steps
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+
+    # End to end through the public API with host buffers: pinned host inputs
+    # copied in, the fused call, the shards copied back, every step.
+    hX = [x.pin_memory() for x in inp["X"]]
+    hW = [x.pin_memory() for x in inp["W"]]
+    hY = [torch.empty(M // R, N, dtype=torch.float32).pin_memory() for _ in range(R)]
+    h2d = sum(t.numel() * t.element_size() for t in hX + hW)
+    d2h = sum(t.numel() * t.element_size() for t in hY)
+
+    def e2e_step():
+        for d_, h_ in zip(X, hX):
+            d_.copy_(h_, non_blocking=True)
+        for d_, h_ in zip(W, hW):
+            d_.copy_(h_, non_blocking=True)
+        B.fo_gemm_rs(plan, X, W, Y, ws, stream)
+        for h_, d_ in zip(hY, Y):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev) / e2e_steps
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    extras = {}
+    if not args.no_extras:
+        extras = measure_extras(B, plan, X, W, Y, ws, stream, flops, dev)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "R": R, "M": M, "K_per_rank": K, "N": N,
+                   "l2": "no flush: inputs (352 MB) and output (134 MB) of a step exceed the 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU, 8 virtual ranks"},
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": args.traffic,
+                     "peak_source": f"bf16_tflops burst, {peak_src}",
+                     "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "baselines": extras,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, desc = oracle_sample(w, oracle_inputs(w))
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _time(fn, stream, iters=10, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(iters):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
+    """Same-GPU comparisons: pure-GEMM control (no transfer), unfused
+    (GEMM to per-rank partials, then a separate reduce kernel), cuBLAS."""
+    import torch
+    R = len(X)
+    M, N = X[0].shape[0], W[0].shape[1]
+    fused = _time(lambda: B.fo_gemm_rs(plan, X, W, Y, ws, stream), stream)
+    P = [torch.empty(M, N, dtype=torch.float32, device=dev) for _ in range(R)]
+    pure = _time(lambda: B.fo_gemm_partials(plan, X, W, P, ws, stream), stream)
+    red = _time(lambda: B.fo_reduce_scatter_f32(plan, P, Y, stream), stream)
+
+    def unfused():
+        B.fo_gemm_partials(plan, X, W, P, ws, stream)
+        B.fo_reduce_scatter_f32(plan, P, Y, stream)
+
+    unf = _time(unfused, stream)
+
+    def cublas():
+        for r in range(R):
+            torch.matmul(X[r], W[r])
+
+    cub = _time(cublas, stream)
+    del P
+    torch.cuda.empty_cache()
+    return {
+        "fused_ms": fused, "fused_tflops": flops / fused / 1e9,
+        "pure_gemm_control_ms": pure, "pure_gemm_control_tflops": flops / pure / 1e9,
+        "exposed_move_pct": 100.0 * (fused - pure) / pure,
+        "unfused_ms": unf, "unfused_tflops": flops / unf / 1e9, "unfused_reduce_kernel_ms": red,
+        "cublas_matmul_bf16_out_ms": cub, "cublas_matmul_tflops": flops / cub / 1e9,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-extras", action="store_true", help="skip the control/unfused/cuBLAS comparisons")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the fused kernel from an ncu capture of this build")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,211 @@
+/*
+ * flashoverlap.h - C ABI of libflashoverlap.so: FlashOverlap's partitioned
+ * GEMM fused with a decomposed reduce-scatter or all-gather, with R virtual
+ * ranks held as separate buffers on one GB300 (sm_103a).
+ *
+ * The method (arXiv 2604.24013, as described on the pages cited below):
+ *   - a collective (reduce-scatter, all-gather) is replaced by directed
+ *     point-to-point chunk transfers (euno.news summary, "Methodology" item 1;
+ *     gist.science "Technical Summary" section 2);
+ *   - the GEMM is split into sub-tasks over exactly the slices that are
+ *     communicated (euno.news, "Methodology" item 2);
+ *   - the sub-tasks run in a rank-adaptive order: Flash-RS computes the slice
+ *     that stays on the rank last, Flash-AG computes the rank's own slice
+ *     first and then the slices received along a ring (gist.science,
+ *     "Technical Summary" section 2, Flash-Reduce-Scatter / Flash-All-Gather);
+ *   - a dependency graph of transfers and compute fragments is scheduled so
+ *     that no sub-task waits for a last piece of data (euno.news,
+ *     "Methodology" item 3); a synchronisation mechanism keeps the data
+ *     consistent (shd-paper.top, 方法详解 "key design" paragraph, item 3).
+ *
+ * On one GPU a "rank" is a set of buffers and a "P2P transfer" is either an
+ * fp32 accumulate of a partial tile into the owning rank's shard (RS) or an
+ * in-kernel read of another rank's buffer (AG). No NCCL, no second GPU.
+ *
+ * Conventions for every call below:
+ *   - Ownership: the caller owns every device buffer (inputs, outputs, the
+ *     workspace) and the stream. The library owns the plan (host memory only;
+ *     a plan holds no device memory) and frees it in fo_plan_destroy.
+ *   - Pointer arrays (X, W, Y, ...) are HOST arrays of R DEVICE pointers, one
+ *     per virtual rank; each device pointer must be 16-byte aligned.
+ *   - All matrices are dense row-major with no padding between rows.
+ *   - Launching calls are asynchronous on `stream` and return after launch.
+ *   - Errors found on the host return at once and launch nothing. Errors
+ *     found on the device (a bounded wait that ran out) are recorded in the
+ *     workspace and reported by fo_status_query.
+ *   - No call aborts the process or lets a C++ exception escape.
+ *   - One call per workspace may be in flight at a time.
+ */
+#ifndef FLASHOVERLAP_H
+#define FLASHOVERLAP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* fo_stream_t;
+
+typedef enum {
+  FO_OK = 0,
+  FO_ERR_INVALID_ARG = 1,     /* NULL pointer, bad enum value, R out of range */
+  FO_ERR_SHAPE = 2,           /* a size is not positive or not divisible by R */
+  FO_ERR_DTYPE = 3,           /* dtype combination not offered for this op */
+  FO_ERR_ALIGN = 4,           /* pointer or row stride not 16-byte aligned */
+  FO_ERR_UNSUPPORTED = 5,     /* option not built, or device is not sm_103 */
+  FO_ERR_CUDA = 6,            /* a CUDA runtime/driver call failed */
+  FO_ERR_TIMEOUT = 7,         /* a device-side bounded wait ran out */
+  FO_ERR_PLAN_INVARIANT = 8   /* the schedule failed a validity check */
+} fo_status;
+
+typedef enum {
+  FO_OP_AG_GEMM = 0,          /* Y_r = AllGather(X) . W_r           */
+  FO_OP_GEMM_RS = 1,          /* Y   = ReduceScatter(X_r . W_r)     */
+  FO_OP_DP_GRAD_RS = 2        /* dW  = ReduceScatter(X_r^T . dY_r)  */
+} fo_op;
+
+typedef enum { FO_BF16 = 0, FO_F32 = 1 } fo_dtype;
+
+/* Per-rank order of the chunk tasks. RANK_ADAPTIVE is the method's order.
+ * SLICED is the data-slicing baseline (every rank works on slice s at step
+ * s; gist.science "Technical Summary" section 1), kept for ablations only. */
+typedef enum { FO_SCHED_RANK_ADAPTIVE = 0, FO_SCHED_SLICED = 1 } fo_sched;
+
+/* How rank r gets another rank's X shard in fo_ag_gemm.
+ * PEER_READ: the GEMM reads the shard straight from its owner's buffer.
+ * COPY: the shard is forwarded along the ring into r's gather buffer G_r by
+ *       128-bit copies, and the GEMM waits for a per-block ready flag. */
+typedef enum { FO_AG_PEER_READ = 0, FO_AG_COPY = 1 } fo_ag_transport;
+
+/* Storage of each W_r: KN = [K_r x N_r] row-major (default); NK = [N_r x K_r]
+ * row-major (the nn.Linear weight layout, i.e. W_r transposed). */
+typedef enum { FO_W_KN = 0, FO_W_NK = 1 } fo_w_layout;
+
+/* Test hooks. DROP_TRANSFER makes fo_plan omit one transfer (the validator
+ * must reject the plan). SKIP_SIGNAL makes the kernel omit the readiness
+ * signal of one tile, so that a bounded wait runs out on the device. */
+typedef enum { FO_INJECT_NONE = 0, FO_INJECT_DROP_TRANSFER = 1, FO_INJECT_SKIP_SIGNAL = 2 } fo_inject;
+
+/* Global GEMM sizes (M, N, K); the per-rank operands are, for each op:
+ *   FO_OP_GEMM_RS    X_r [M x K/R], W_r [K/R x N] (or [N x K/R]), Y_r [M/R x N] fp32
+ *   FO_OP_AG_GEMM    X_r [M/R x K], W_r [K x N/R] (or [N/R x K]), Y_r [M x N/R] bf16,
+ *                    optional G_r [M x K] bf16 (the gathered X)
+ *   FO_OP_DP_GRAD_RS X_r [K x M], dY_r [K x N] (K = tokens), dW_r [M/R x N] fp32
+ * Row block d of an RS output (rows d*M/R .. (d+1)*M/R-1 of the sum over
+ * ranks) belongs to rank d. The all-gather concatenates shards in rank order. */
+typedef struct {
+  int32_t op;                 /* fo_op */
+  int32_t R;                  /* virtual ranks, 1..16 */
+  int64_t M, N, K;
+  int32_t in_dtype;           /* FO_BF16; FO_F32 (tf32 MMA) for GEMM_RS only */
+  int32_t out_dtype;          /* FO_F32 for GEMM_RS / DP_GRAD_RS, FO_BF16 for AG_GEMM */
+  int32_t sched;              /* fo_sched */
+  int32_t ag_transport;       /* fo_ag_transport (AG_GEMM only) */
+  int32_t w_layout;           /* fo_w_layout (GEMM_RS and AG_GEMM) */
+  int32_t deterministic;      /* RS: 1 = partials are added in step order (bitwise
+                                 reproducible); 0 = each add may start once the
+                                 shard's first partial is stored */
+  uint64_t timeout_ns;        /* bound of every device-side wait; 0 = 1 s */
+  int32_t fault_inject;       /* fo_inject (tests only) */
+  int32_t reserved[7];        /* must be zero */
+} fo_plan_desc;
+
+typedef struct fo_plan_s* fo_plan_t;
+
+/* Build and validate the schedule: per-rank step table, transfer list and
+ * dependency graph (the decomposition and the rank-adaptive order cited in
+ * the file header). Host only; touches no GPU. On success *out owns a new
+ * plan. Returns FO_ERR_PLAN_INVARIANT when the schedule fails a check:
+ * every rank's order is a permutation; RS computes its own chunk last and
+ * sends nothing at its last step; AG consumes its own shard first and
+ * forwards nothing at its last step; at every step the map rank -> chunk is
+ * one-to-one; R(R-1) transfers; the dependency graph is acyclic and every
+ * transfer precedes its consumer. (SLICED, an ablation, is checked only for
+ * permutations, transfer count and acyclicity.) */
+fo_status fo_plan(const fo_plan_desc* desc, fo_plan_t* out);
+void fo_plan_destroy(fo_plan_t plan);
+
+/* Copy out the R x R step table: table[r*R + s] = chunk handled by rank r at
+ * step s (RS/DP: the chunk = owner of the partial; AG: the source shard). */
+fo_status fo_plan_table(fo_plan_t plan, int32_t* table);
+
+/* Copy out the transfers, 4 int32 each: (src_rank, dst_rank, chunk, step).
+ * `cap` is the capacity of `out` in transfers; *n gets the count. */
+fo_status fo_plan_transfers(fo_plan_t plan, int32_t* out, int32_t cap, int32_t* n);
+
+/* Copy out the dependency edges, 4 int32 each: (rank_a, step_a, rank_b,
+ * step_b) meaning task (rank_a, step_a) must finish before (rank_b, step_b)
+ * may complete. `cap` in edges; *n gets the count. */
+fo_status fo_plan_edges(fo_plan_t plan, int32_t* out, int32_t cap, int32_t* n);
+
+/* Bytes of device workspace the launching calls need (readiness counters,
+ * flags and the device status word). Never zero. */
+fo_status fo_workspace_size(fo_plan_t plan, size_t* bytes);
+
+/* Zero the workspace on `stream`. Required once before the first call that
+ * uses it; calls leave it ready for the next call. */
+fo_status fo_workspace_init(fo_plan_t plan, void* ws, fo_stream_t stream);
+
+/* Flash-AG: Y_r = AllGather(X_0..X_{R-1}) . W_r for every rank r, bf16 out,
+ * fp32 accumulation, rounded once (gist.science "Technical Summary" section 2,
+ * Flash-All-Gather). Rank r's step s computes the rows of shard
+ * (r - s) mod R. G may be NULL (no gathered copy; PEER_READ only) or an array
+ * of R pointers to [M x K] bf16 buffers that receive the gathered X. */
+fo_status fo_ag_gemm(fo_plan_t plan, const void* const* X, const void* const* W,
+                     void* const* Y, void* const* G, void* ws, fo_stream_t stream);
+
+/* Flash-RS: Y_d = sum_r (X_r . W_r)[rows of d], fp32 (gist.science
+ * "Technical Summary" section 2, Flash-Reduce-Scatter). Rank r's step s
+ * computes the partial of chunk (r - 1 - s) mod R and adds it into that
+ * owner's Y; the own chunk comes last. Y is overwritten. */
+fo_status fo_gemm_rs(fo_plan_t plan, const void* const* X, const void* const* W,
+                     void* const* Y, void* ws, fo_stream_t stream);
+
+/* Data-parallel weight gradient fused with its reduce-scatter:
+ * dW_d = sum_r (X_r^T . dY_r)[rows of d], fp32 (gist.science "Technical
+ * Summary" section 1: data parallelism needs a reduce-scatter). Same
+ * schedule as fo_gemm_rs. dW is overwritten. */
+fo_status fo_dp_grad_rs(fo_plan_t plan, const void* const* X, const void* const* dY,
+                        void* const* dW, void* ws, fo_stream_t stream);
+
+/* Synchronise `stream`, read the device status word from `ws` and return it
+ * (FO_OK or FO_ERR_TIMEOUT). info (may be NULL) receives
+ * {code, rank, step, chunk} of the first failure. A failure also re-zeroes
+ * the workspace, so the plan is usable again; the outputs of the failed call
+ * are undefined. */
+fo_status fo_status_query(fo_plan_t plan, void* ws, fo_stream_t stream, int32_t info[4]);
+
+/* ---- measurement controls (not part of the method) --------------------- */
+
+/* Pure-GEMM control for GEMM_RS / DP_GRAD_RS plans: the same chunk GEMM
+ * tasks in the same order, but every partial is stored into its own rank's
+ * [M x N] fp32 buffer P_r (no transfer, no accumulate). */
+fo_status fo_gemm_partials(fo_plan_t plan, const void* const* A, const void* const* B,
+                           void* const* P, void* ws, fo_stream_t stream);
+
+/* Unfused baseline's separate reduce kernel: Y_d = sum_r P_r[rows of d] for
+ * R buffers P_r [M x N] fp32 (summed in ascending r). */
+fo_status fo_reduce_scatter_f32(fo_plan_t plan, const void* const* P, void* const* Y,
+                                fo_stream_t stream);
+
+/* Unfused all-gather baseline: G_r = concat(X_0..X_{R-1}) for every r, by
+ * 128-bit copies (X_r [M/R x K] bf16, G_r [M x K]). */
+fo_status fo_all_gather_copy(fo_plan_t plan, const void* const* X, void* const* G,
+                             fo_stream_t stream);
+
+/* Number of our kernels the last launching call on this plan enqueued. */
+int32_t fo_plan_last_launches(fo_plan_t plan);
+
+const char* fo_status_string(fo_status s);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int32_t fo_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASHOVERLAP_H */

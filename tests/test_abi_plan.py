@@ -1,0 +1,137 @@
+"""CPU tests of the C ABI: the library loads, exports every declared symbol,
+and fo_plan (host only) builds the schedule the oracle's reading gives."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from ag_gemm_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return B.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "flashoverlap.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fo_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(B.EXPORTED) == names
+
+
+def test_version_and_status_strings(lib):
+    assert B.fo_version() == 0x000100
+    for code in range(9):
+        assert B.status_string(code)
+    assert B.status_string(B.FO_ERR_TIMEOUT) == "device-side wait timed out"
+
+
+@pytest.mark.parametrize("R", list(range(1, 17)))
+def test_plan_tables_match_oracle(R):
+    rs = B.fo_plan("gemm_rs", R, 128 * R, 256, 64 * R)
+    assert B.fo_plan_table(rs) == oracle.rs_schedule(R).tolist()
+    ag = B.fo_plan("ag_gemm", R, 128 * R, 64 * R, 256)
+    assert B.fo_plan_table(ag) == oracle.ag_schedule(R).tolist()
+    dp = B.fo_plan("dp_grad_rs", R, 8 * R, 256, 64)
+    assert B.fo_plan_table(dp) == oracle.rs_schedule(R).tolist()
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
+def test_plan_transfers_match_oracle(R):
+    rs = B.fo_plan("gemm_rs", R, 128 * R, 256, 64 * R)
+    assert sorted(B.fo_plan_transfers(rs)) == sorted(oracle.rs_transfers(R))
+    ag = B.fo_plan("ag_gemm", R, 128 * R, 64 * R, 256)
+    assert sorted(B.fo_plan_transfers(ag)) == sorted(oracle.ag_transfers(R))
+
+
+@pytest.mark.parametrize("R", [2, 3, 5])
+def test_plan_edges_form_the_oracle_dag(R):
+    rs = B.fo_plan("gemm_rs", R, 128 * R, 256, 64 * R)
+    got = sorted((a, b, c, d) for (a, b, c, d) in B.fo_plan_edges(rs))
+    want = sorted((a[0], a[1], b[0], b[1]) for a, b in oracle.rs_dependency_edges(R))
+    assert got == want
+
+
+def test_sliced_schedule_is_the_ablation_table():
+    R = 4
+    p = B.fo_plan("gemm_rs", R, 128 * R, 256, 64 * R, sched="sliced")
+    assert B.fo_plan_table(p) == oracle.sliced_schedule(R).tolist()
+    assert len(B.fo_plan_transfers(p)) == R * (R - 1)
+
+
+def test_dropped_transfer_is_rejected():
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_plan("gemm_rs", 4, 512, 256, 256, fault_inject="drop_transfer")
+    assert e.value.code == B.FO_ERR_PLAN_INVARIANT
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_plan("ag_gemm", 4, 512, 256, 256, fault_inject="drop_transfer")
+    assert e.value.code == B.FO_ERR_PLAN_INVARIANT
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(op="gemm_rs", R=0, M=8, N=8, K=8), B.FO_ERR_INVALID_ARG),
+    (dict(op="gemm_rs", R=17, M=17, N=8, K=17), B.FO_ERR_INVALID_ARG),
+    (dict(op="gemm_rs", R=3, M=8, N=8, K=24), B.FO_ERR_SHAPE),          # M % R
+    (dict(op="gemm_rs", R=2, M=8, N=8, K=9), B.FO_ERR_SHAPE),           # K % R
+    (dict(op="gemm_rs", R=2, M=8, N=6, K=32), B.FO_ERR_ALIGN),          # rows of W not 16 B
+    (dict(op="gemm_rs", R=2, M=8, N=8, K=12), B.FO_ERR_ALIGN),          # rows of X_r not 16 B
+    (dict(op="gemm_rs", R=2, M=0, N=8, K=16), B.FO_ERR_SHAPE),
+    (dict(op="ag_gemm", R=2, M=8, N=10, K=16), B.FO_ERR_ALIGN),         # N/R = 5
+    (dict(op="ag_gemm", R=3, M=9, N=8, K=16), B.FO_ERR_SHAPE),          # N % R
+    (dict(op="dp_grad_rs", R=2, M=8, N=8, K=16), B.FO_ERR_ALIGN),       # M/R = 4 columns
+    (dict(op="ag_gemm", R=2, M=8, N=16, K=16, out_dtype="f32"), B.FO_ERR_DTYPE),
+    (dict(op="gemm_rs", R=2, M=8, N=16, K=16, out_dtype="bf16"), B.FO_ERR_DTYPE),
+    (dict(op="gemm_rs", R=2, M=8, N=16, K=16, in_dtype="f32"), B.FO_ERR_UNSUPPORTED),  # tf32 needs W as [N x K]
+    (dict(op="ag_gemm", R=2, M=8, N=16, K=16, sched="sliced"), B.FO_ERR_UNSUPPORTED),
+])
+def test_plan_rejects_bad_descriptors(kw, code):
+    kw = dict(kw)
+    op, R, M, N, K = kw.pop("op"), kw.pop("R"), kw.pop("M"), kw.pop("N"), kw.pop("K")
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_plan(op, R, M, N, K, **kw)
+    assert e.value.code == code
+
+
+def test_workspace_size_covers_counters():
+    R = 8
+    p = B.fo_plan("gemm_rs", R, 8192, 4096, 14336)
+    tiles = (1024 // 128) * (4096 // 256)
+    assert B.fo_workspace_size(p) >= 256 + R * tiles * 4 * 4
+    assert B.fo_workspace_size(p) % 256 == 0
+
+
+def test_launch_without_gpu_fails_loudly():
+    # On a machine without a GPU (or not sm_103) a launching call must return
+    # an error, never fall back to the CPU.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    p = B.fo_plan("gemm_rs", 2, 256, 512, 1024)
+    fake = [16 * (i + 1) for i in range(2)]
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_gemm_rs(p, fake, fake, fake, 4096, stream=0)
+    assert e.value.code in (B.FO_ERR_CUDA, B.FO_ERR_UNSUPPORTED)
+
+
+def test_null_arguments_are_rejected():
+    p = B.fo_plan("gemm_rs", 2, 256, 512, 1024)
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_gemm_rs(p, [0, 0], [16, 16], [16, 16], 4096, stream=0)
+    assert e.value.code == B.FO_ERR_INVALID_ARG
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_gemm_rs(p, [24, 16], [16, 16], [16, 16], 4096, stream=0)
+    assert e.value.code == B.FO_ERR_ALIGN

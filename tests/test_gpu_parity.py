@@ -1,0 +1,351 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Integer-valued inputs must match bit for bit (every fp32 partial sum is an
+exact integer); random bf16 inputs must be within relative Frobenius error
+1e-3 and max elementwise relative error 2e-2 (elementwise denominators
+clamped at 1e-3 * rms) of the fp64 oracle. bf16 outputs (AG-GEMM) are
+compared with the oracle's value rounded once to bf16.
+Shapes span several tiles and ragged tails (rows per chunk, K and N that are
+not multiples of the 128 x 256 x 64 tile); guard bands around every output
+buffer must come back untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ag_gemm_gb300 import binding as B
+from ag_gemm_gb300.inputs import WORKLOADS, ag_gemm_inputs, dp_grad_inputs, gemm_rs_inputs
+
+pytestmark = pytest.mark.gpu
+
+FRO_TOL = 1e-3
+MAX_TOL = 2e-2
+GUARD = 64          # fp32 / bf16 elements of canary on each side of an output
+CANARY_F32 = -7.0e33
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a GB300"
+    return torch.device("cuda:0")
+
+
+def _np(t):
+    return t.detach().to("cpu").double().numpy()
+
+
+class Guarded:
+    """R output buffers, each inside a larger allocation whose head and tail
+    hold a canary value."""
+
+    def __init__(self, R, shape, dtype, dev):
+        n = int(np.prod(shape))
+        self.shape = shape
+        self.bufs = []
+        self.views = []
+        for _ in range(R):
+            b = torch.full((n + 2 * GUARD,), CANARY_F32, dtype=dtype, device=dev)
+            self.bufs.append(b)
+            self.views.append(b[GUARD:GUARD + n].view(*shape))
+        self.canary = self.bufs[0][:GUARD].clone()
+
+    def check(self):
+        for b in self.bufs:
+            assert torch.equal(b[:GUARD], self.canary), "write before the output buffer"
+            assert torch.equal(b[-GUARD:], self.canary), "write past the output buffer"
+
+
+def _ws(plan, dev):
+    ws = torch.empty(B.fo_workspace_size(plan), dtype=torch.uint8, device=dev)
+    B.fo_workspace_init(plan, ws)
+    return ws
+
+
+def _status_ok(plan, ws):
+    code, info = B.fo_status_query(plan, ws)
+    assert code == 0, f"device status {code} {info}"
+
+
+def run_gemm_rs(dev, R, M, K, N, *, dtype="bf16", mode="int", w_layout="kn", seed=0, sched="rank_adaptive",
+                deterministic=False, repeat=1):
+    inp = gemm_rs_inputs(R, M, K, N, dtype=dtype, mode=mode, seed=seed)
+    plan = B.fo_plan("gemm_rs", R, M, N, K * R, in_dtype=dtype, w_layout=w_layout, sched=sched,
+                     deterministic=deterministic)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [(w if w_layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
+    Y = Guarded(R, (M // R, N), torch.float32, dev)
+    ws = _ws(plan, dev)
+    outs = []
+    for _ in range(repeat):
+        B.fo_gemm_rs(plan, X, W, Y.views, ws)
+        _status_ok(plan, ws)
+        outs.append([_np(y) for y in Y.views])
+    Y.check()
+    assert B.fo_plan_last_launches(plan) == 1
+    ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    return outs, ref
+
+
+def _assert_close(got, ref):
+    fro, mx, _ = oracle.rel_errors(got, ref)
+    assert fro <= FRO_TOL and mx <= MAX_TOL, f"rel fro {fro:.3e}, max rel {mx:.3e}"
+
+
+# ------------------------------------------------------------------ GEMM-RS
+
+@pytest.mark.parametrize("R,M,K,N,layout", [
+    (2, 256, 512, 512, "kn"),       # the 256x512x512 R=2 shape in bf16
+    (4, 800, 200, 328, "kn"),       # ragged: 200 rows per chunk, K 200, N 328
+    (3, 384, 64, 256, "nk"),
+    (1, 128, 128, 256, "kn"),       # R = 1: plain GEMM
+    (8, 1024, 136, 264, "nk"),
+    (5, 640, 256, 1024, "kn"),      # several N tiles, 5 ranks
+])
+def test_gemm_rs_integer_bit_exact(dev, R, M, K, N, layout):
+    outs, ref = run_gemm_rs(dev, R, M, K, N, w_layout=layout)
+    for d in range(R):
+        assert np.array_equal(outs[0][d], ref[d]), f"shard {d}"
+
+
+@pytest.mark.parametrize("R,M,K,N", [(2, 256, 512, 512), (3, 600, 100, 132)])
+def test_gemm_rs_fp32_inputs_tf32_bit_exact(dev, R, M, K, N):
+    outs, ref = run_gemm_rs(dev, R, M, K, N, dtype="f32", w_layout="nk")
+    for d in range(R):
+        assert np.array_equal(outs[0][d], ref[d]), f"shard {d}"
+
+
+@pytest.mark.parametrize("R,M,K,N,layout", [(4, 1024, 512, 512, "kn"), (8, 1024, 200, 328, "nk")])
+def test_gemm_rs_random_bf16_within_tolerance(dev, R, M, K, N, layout):
+    outs, ref = run_gemm_rs(dev, R, M, K, N, mode="randn", w_layout=layout, seed=2)
+    for d in range(R):
+        _assert_close(outs[0][d], ref[d])
+
+
+def test_gemm_rs_deterministic_mode_is_bitwise_repeatable(dev):
+    outs, ref = run_gemm_rs(dev, 4, 1024, 384, 512, mode="randn", deterministic=True, repeat=3, seed=5)
+    for rep in outs[1:]:
+        for d in range(4):
+            assert np.array_equal(rep[d], outs[0][d])
+    for d in range(4):
+        _assert_close(outs[0][d], ref[d])
+
+
+def test_gemm_rs_repeated_calls_reuse_workspace(dev):
+    # Counters reset themselves: many calls in a row on one workspace stay exact.
+    outs, ref = run_gemm_rs(dev, 4, 512, 128, 256, repeat=5)
+    for rep in outs:
+        for d in range(4):
+            assert np.array_equal(rep[d], ref[d])
+
+
+def test_gemm_rs_sliced_ablation_same_result(dev):
+    outs, ref = run_gemm_rs(dev, 4, 512, 128, 512, sched="sliced")
+    for d in range(4):
+        assert np.array_equal(outs[0][d], ref[d])
+
+
+def test_gemm_rs_new_buffers_after_cached_call(dev):
+    R, M, K, N = 2, 256, 128, 256
+    plan = B.fo_plan("gemm_rs", R, M, N, K * R)
+    ws = _ws(plan, dev)
+    for seed in (1, 2):
+        inp = gemm_rs_inputs(R, M, K, N, mode="int", seed=seed)
+        X = [x.to(dev) for x in inp["X"]]
+        W = [w.to(dev) for w in inp["W"]]
+        Y = [torch.empty(M // R, N, device=dev) for _ in range(R)]
+        B.fo_gemm_rs(plan, X, W, Y, ws)
+        _status_ok(plan, ws)
+        ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+        for d in range(R):
+            assert np.array_equal(_np(Y[d]), ref[d])
+
+
+# ------------------------------------------------------------------ AG-GEMM
+
+def run_ag(dev, R, M, K, N, *, mode="int", layout="kn", seed=1):
+    inp = ag_gemm_inputs(R, M, K, N // R, mode=mode, seed=seed)
+    plan = B.fo_plan("ag_gemm", R, M, N, K, w_layout=layout)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [(w if layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
+    Y = Guarded(R, (M, N // R), torch.bfloat16, dev)
+    ws = _ws(plan, dev)
+    B.fo_ag_gemm(plan, X, W, Y.views, None, ws)
+    _status_ok(plan, ws)
+    Y.check()
+    ref, _ = oracle.ag_gemm([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    return [_np(y) for y in Y.views], ref
+
+
+@pytest.mark.parametrize("R,M,K,N,layout", [
+    (4, 512, 256, 512, "kn"),
+    (2, 400, 200, 336, "kn"),       # ragged: 200-row shards, K 200, 168 columns per rank
+    (3, 384, 64, 768, "nk"),
+    (1, 256, 128, 256, "kn"),
+])
+def test_ag_gemm_integer_bit_exact(dev, R, M, K, N, layout):
+    got, ref = run_ag(dev, R, M, K, N, layout=layout)
+    for r in range(R):
+        assert np.array_equal(got[r], oracle.round_bf16(ref[r])), f"rank {r}"
+
+
+@pytest.mark.parametrize("R,M,K,N", [(4, 1024, 512, 1024), (2, 400, 200, 336)])
+def test_ag_gemm_random_bf16_within_tolerance(dev, R, M, K, N):
+    got, ref = run_ag(dev, R, M, K, N, mode="randn")
+    for r in range(R):
+        _assert_close(got[r], oracle.round_bf16(ref[r]))
+
+
+# ------------------------------------------------------------------ DP grad
+
+def run_dp(dev, R, T, M, N, *, mode="int", seed=3):
+    inp = dp_grad_inputs(R, T, M, N, mode=mode, seed=seed)
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T)
+    X = [x.to(dev) for x in inp["X"]]
+    dY = [y.to(dev) for y in inp["dY"]]
+    dW = Guarded(R, (M // R, N), torch.float32, dev)
+    ws = _ws(plan, dev)
+    B.fo_dp_grad_rs(plan, X, dY, dW.views, ws)
+    _status_ok(plan, ws)
+    dW.check()
+    ref = oracle.dp_grad_rs([_np(x) for x in inp["X"]], [_np(y) for y in inp["dY"]])
+    return [_np(w) for w in dW.views], ref
+
+
+@pytest.mark.parametrize("R,T,M,N", [(2, 256, 256, 256), (4, 200, 800, 328), (8, 128, 1024, 256)])
+def test_dp_grad_rs_integer_bit_exact(dev, R, T, M, N):
+    got, ref = run_dp(dev, R, T, M, N)
+    for d in range(R):
+        assert np.array_equal(got[d], ref[d]), f"shard {d}"
+
+
+def test_dp_grad_rs_random_bf16_within_tolerance(dev):
+    got, ref = run_dp(dev, 4, 512, 1024, 512, mode="randn")
+    for d in range(4):
+        _assert_close(got[d], ref[d])
+
+
+# ------------------------------------------------------------------ controls
+
+def test_partials_control_stores_each_ranks_gemm(dev):
+    R, M, K, N = 4, 512, 192, 256
+    inp = gemm_rs_inputs(R, M, K, N, mode="int", seed=9)
+    plan = B.fo_plan("gemm_rs", R, M, N, K * R)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [w.to(dev) for w in inp["W"]]
+    P = [torch.empty(M, N, device=dev) for _ in range(R)]
+    ws = _ws(plan, dev)
+    B.fo_gemm_partials(plan, X, W, P, ws)
+    _status_ok(plan, ws)
+    for r in range(R):
+        assert np.array_equal(_np(P[r]), _np(inp["X"][r]) @ _np(inp["W"][r]))
+    Y = [torch.empty(M // R, N, device=dev) for _ in range(R)]
+    B.fo_reduce_scatter_f32(plan, P, Y)
+    torch.cuda.synchronize()
+    ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for d in range(R):
+        assert np.array_equal(_np(Y[d]), ref[d])
+
+
+def test_all_gather_copy(dev):
+    R, M, K, N = 4, 512, 256, 512
+    inp = ag_gemm_inputs(R, M, K, N // R, mode="randn", seed=4)
+    plan = B.fo_plan("ag_gemm", R, M, N, K)
+    X = [x.to(dev) for x in inp["X"]]
+    G = [torch.empty(M, K, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    B.fo_all_gather_copy(plan, X, G)
+    torch.cuda.synchronize()
+    want = oracle.all_gather_rows([_np(x) for x in inp["X"]])
+    for r in range(R):
+        assert np.array_equal(_np(G[r]), want)
+
+
+# ------------------------------------------------------------------ failure detection
+
+def test_missing_signal_times_out_and_workspace_recovers(dev):
+    R, M, K, N = 2, 256, 128, 256
+    inp = gemm_rs_inputs(R, M, K, N, mode="int", seed=0)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [w.to(dev) for w in inp["W"]]
+    Y = [torch.empty(M // R, N, device=dev) for _ in range(R)]
+    bad = B.fo_plan("gemm_rs", R, M, N, K * R, fault_inject="skip_signal", timeout_ns=20_000_000)
+    ws = _ws(bad, dev)
+    B.fo_gemm_rs(bad, X, W, Y, ws)
+    code, info = B.fo_status_query(bad, ws)
+    assert code == B.FO_ERR_TIMEOUT
+    # chunk 0 gets its second partial from rank 0 at step 1 (its own chunk, last)
+    assert info == [B.FO_ERR_TIMEOUT, 0, 1, 0]
+    good = B.fo_plan("gemm_rs", R, M, N, K * R)
+    B.fo_gemm_rs(good, X, W, Y, ws)
+    _status_ok(good, ws)
+    ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for d in range(R):
+        assert np.array_equal(_np(Y[d]), ref[d])
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled rows)
+
+def _sample_rows(rng, n, k=48):
+    rows = rng.choice(n, size=min(k, n), replace=False)
+    rows[:2] = [0, n - 1]
+    return np.sort(rows)
+
+
+def test_full_size_gemm_rs_down_proj(dev):
+    w = WORKLOADS["gemm_rs_down_r8_t8192_k1792_n4096"]
+    R, M, K, N = w.R, w.dims["M"], w.dims["K"], w.dims["N"]
+    inp = w.make()
+    plan = B.fo_plan("gemm_rs", R, M, N, K * R)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [x.to(dev) for x in inp["W"]]
+    Y = [torch.empty(M // R, N, device=dev) for _ in range(R)]
+    ws = _ws(plan, dev)
+    B.fo_gemm_rs(plan, X, W, Y, ws)
+    _status_ok(plan, ws)
+    Xn = [_np(x) for x in inp["X"]]
+    Wn = [_np(x) for x in inp["W"]]
+    rng = np.random.default_rng(0)
+    for d in range(R):
+        rows = _sample_rows(rng, M // R)
+        _assert_close(_np(Y[d][torch.as_tensor(rows, device=dev)]), oracle.gemm_rs_rows(Xn, Wn, d, rows))
+
+
+def test_full_size_ag_gemm_qkv(dev):
+    w = WORKLOADS["ag_gemm_qkv_r4_s4096_h4096_n3072"]
+    R, M, K, Nr = w.R, w.dims["M"], w.dims["K"], w.dims["N"]
+    inp = w.make()
+    plan = B.fo_plan("ag_gemm", R, M, Nr * R, K)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [x.to(dev) for x in inp["W"]]
+    Y = [torch.empty(M, Nr, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    ws = _ws(plan, dev)
+    B.fo_ag_gemm(plan, X, W, Y, None, ws)
+    _status_ok(plan, ws)
+    Xn = [_np(x) for x in inp["X"]]
+    Wn = [_np(x) for x in inp["W"]]
+    rng = np.random.default_rng(1)
+    for r in range(R):
+        rows = _sample_rows(rng, M)
+        got = _np(Y[r][torch.as_tensor(rows, device=dev)])
+        _assert_close(got, oracle.round_bf16(oracle.ag_gemm_rows(Xn, Wn, r, rows)))
+
+
+def test_full_size_dp_grad(dev):
+    w = WORKLOADS["dp_grad_rs_r8_t4096_4096x4096"]
+    R, T, M, N = w.R, w.dims["T"], w.dims["M"], w.dims["N"]
+    inp = w.make()
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T)
+    X = [x.to(dev) for x in inp["X"]]
+    dY = [x.to(dev) for x in inp["dY"]]
+    dW = [torch.empty(M // R, N, device=dev) for _ in range(R)]
+    ws = _ws(plan, dev)
+    B.fo_dp_grad_rs(plan, X, dY, dW, ws)
+    _status_ok(plan, ws)
+    Xn = [_np(x) for x in inp["X"]]
+    dYn = [_np(x) for x in inp["dY"]]
+    rng = np.random.default_rng(3)
+    for d in range(R):
+        rows = _sample_rows(rng, M // R, 16)
+        _assert_close(_np(dW[d][torch.as_tensor(rows, device=dev)]), oracle.dp_grad_rs_rows(Xn, dYn, d, rows))
