@@ -32,6 +32,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -50,6 +51,34 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("fo_device.cuh", "fo_kernel.cuh"):
+        with open(os.path.join(ROOT, "ag_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary of this workload, or None when that capture was taken on other
+    kernel source than the one built now."""
+    path = os.path.join(ROOT, "profiles", f"fused_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    sha = traffic = None
+    with open(path) as f:
+        for line in f:
+            if line.startswith("kernel_source_sha256:"):
+                sha = line.split(":", 1)[1].strip()
+            elif line.startswith("traffic_bytes_per_launch:"):
+                traffic = float(line.split(":", 1)[1].strip())
+    if sha and traffic and sha == kernel_source_sha256():
+        return traffic
+    return None
 
 
 # ---------------------------------------------------------------- distributed helpers
@@ -77,22 +106,21 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while running."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, gpu: str):
+        self.gpu = gpu
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"fo_bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -107,31 +135,38 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
+    def mark(self, what: str):
+        setattr(self, what, time.time())
+
     def summary(self):
+        """Median SM clock and throttle reasons over the samples taken between
+        mark("t0") and mark("t1") (all samples if fewer than 3 fall inside)."""
         if self.proc is None or not os.path.exists(self.path):
             return None
-        sms, maxes, reasons = [], [], set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) < 9:
                     continue
                 try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
                     sm = float(parts[1])
                     mx = float(parts[2])
                 except ValueError:
                     continue
-                sms.append(sm)
-                maxes.append(mx)
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
-        if not sms:
+                samples.append((ts, sm, mx, [n for n, v in zip(names, parts[5:9]) if v.lower().startswith("active")]))
+        if not samples:
             return None
-        sms.sort()
-        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
-                "samples": len(sms)}
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
+        inside = [x for x in samples if t0 is not None and t1 is not None and t0 - 0.05 <= x[0] <= t1 + 0.05]
+        used = inside if len(inside) >= 3 else samples
+        sms = sorted(x[1] for x in used)
+        reasons = sorted({r for x in used for r in x[3]})
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(x[2] for x in used), "reasons": reasons,
+                "samples": len(used), "samples_in_timed_region": len(inside)}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -271,10 +306,11 @@ def run_ours(args):
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     launches = 0
-    with ClockSampler(torch.cuda.current_device()) as clk:
+    with ClockSampler(_smi_id(dev)) as clk:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
+        clk.mark("t0")
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -285,6 +321,7 @@ def run_ours(args):
             launches += B.fo_plan_last_launches(plan)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark("t1")
         if world > 1:
             dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
@@ -343,7 +380,8 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU, 8 virtual ranks"},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": args.traffic,
+                     "frac": achieved / peak,
+                     "traffic": args.traffic if args.traffic is not None else profiled_traffic(w.name),
                      "peak_source": f"bf16_tflops burst, {peak_src}",
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -360,6 +398,15 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def _smi_id(dev) -> str:
+    """nvidia-smi selector of a torch device (its UUID when torch exposes it)."""
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return str(dev.index or 0)
 
 
 def _time(fn, stream, iters=10, warm=2):
@@ -413,8 +460,8 @@ def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-extras", action="store_true", help="skip the control/unfused/cuBLAS comparisons")
