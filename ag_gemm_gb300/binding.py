@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(_PKG, "_build", "libflashoverlap.so")
 
 FO_OK, FO_ERR_INVALID_ARG, FO_ERR_SHAPE, FO_ERR_DTYPE, FO_ERR_ALIGN = 0, 1, 2, 3, 4
 FO_ERR_UNSUPPORTED, FO_ERR_CUDA, FO_ERR_TIMEOUT, FO_ERR_PLAN_INVARIANT = 5, 6, 7, 8
+FO_ERR_SCRATCH_LIMIT = 9
+FO_NOALLOC_SCRATCH_BYTES = 64 * 1024
 OPS = {"ag_gemm": 0, "gemm_rs": 1, "dp_grad_rs": 2}
 DTYPES = {"bf16": 0, "f32": 1}
 SCHEDS = {"rank_adaptive": 0, "sliced": 1}
@@ -30,7 +32,7 @@ EXPORTED = [
     "fo_plan", "fo_plan_destroy", "fo_plan_table", "fo_plan_transfers", "fo_plan_edges",
     "fo_workspace_size", "fo_workspace_init", "fo_ag_gemm", "fo_gemm_rs", "fo_dp_grad_rs",
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
-    "fo_plan_last_launches", "fo_status_string", "fo_version",
+    "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc",
 ]
 
 
@@ -79,6 +81,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_ag_gemm": ([P, PP, PP, PP, PP, P, P], c_int32),
         "fo_gemm_rs": ([P, PP, PP, PP, P, P], c_int32),
         "fo_dp_grad_rs": ([P, PP, PP, PP, P, P], c_int32),
+        "fo_gemm_rs_noalloc": ([P, PP, PP, PP, P], c_int32),
         "fo_status_query": ([P, P, P, POINTER(c_int32)], c_int32),
         "fo_gemm_partials": ([P, PP, PP, PP, P, P], c_int32),
         "fo_reduce_scatter_f32": ([P, PP, PP, P], c_int32),
@@ -226,6 +229,12 @@ def fo_gemm_rs(plan: Plan, X, W, Y, ws, stream=None) -> None:
 def fo_ag_gemm(plan: Plan, X, W, Y, G=None, ws=None, stream=None) -> None:
     _check(load().fo_ag_gemm(plan, _ptr_array(X), _ptr_array(W), _ptr_array(Y), _ptr_array(G), _ptr(ws),
                              _stream(stream)), "fo_ag_gemm")
+
+
+def fo_gemm_rs_noalloc(plan: Plan, X, W, Y, stream=None) -> None:
+    """fo_gemm_rs without a workspace (static device scratch; see the header)."""
+    _check(load().fo_gemm_rs_noalloc(plan, _ptr_array(X), _ptr_array(W), _ptr_array(Y), _stream(stream)),
+           "fo_gemm_rs_noalloc")
 
 
 def fo_dp_grad_rs(plan: Plan, X, dY, dW, ws, stream=None) -> None:

@@ -268,6 +268,39 @@ __global__ void all_gather_copy_kernel(PtrArray X, MutPtrArray G, int R, int64_t
 
 }  // namespace
 
+// Parameters of one fo_gemm_rs launch built into caller storage (no plan
+// cache, no allocation), with the readiness counters and status word in
+// `scratch`. Used by the allocation-free entry point.
+fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const void* const* W,
+                                        void* const* Y, void* scratch, fo::FoParams* k, int* variant,
+                                        int* grid) {
+  DevInfo di;
+  fo_status st = preflight(p, &di);
+  if (st != FO_OK) return st;
+  memset(static_cast<void*>(k), 0, sizeof(*k));
+  const int R = p->R;
+  const uint64_t M = (uint64_t)p->d.M, N = (uint64_t)p->d.N, rpc = (uint64_t)p->rows_per_chunk;
+  const uint64_t kr = (uint64_t)p->k_red;
+  const int es = p->elem_bytes;
+  const CUtensorMapDataType dt = es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const uint32_t bk = FO_BK_BYTES / es;
+  bool ok = true;
+  for (int r = 0; r < R && ok; ++r) {
+    ok &= enc2d(&k->tmA[r], dt, X[r], kr, M, kr * es, bk, FO_BM);
+    if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, W[r], N, kr, N * es, bk, bk);
+    else ok &= enc2d(&k->tmB[r], dt, W[r], kr, N, kr * es, bk, FO_BN);
+    ok &= enc2d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Y[r], N, rpc, N * 4, 32, 32);
+  }
+  if (!ok) return FO_ERR_CUDA;
+  fill_common(p, k, scratch);
+  *variant = es == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
+  const int total = p->R * p->R * p->tiles_m * p->tiles_n;
+  *grid = total < di.sms ? total : di.sms;
+  return FO_OK;
+}
+
+fo_status fo_internal_check_ptrs(int R, const void* const* a) { return check_ptrs(R, a); }
+
 extern "C" {
 
 fo_status fo_workspace_init(fo_plan_t p, void* ws, fo_stream_t stream) {

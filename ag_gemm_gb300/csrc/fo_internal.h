@@ -59,3 +59,11 @@ struct fo_ws_header {
   uint32_t exit_count;     // CTAs of the current AG launch that finished
   uint32_t pad[10];
 };
+
+// Helpers of fo_api.cu used by the allocation-free entry point
+// (fo_noalloc.cu). FoParams is declared in fo_kernel.cuh.
+namespace fo { struct FoParams; }
+fo_status fo_internal_check_ptrs(int R, const void* const* a);
+fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const void* const* W,
+                                        void* const* Y, void* scratch, fo::FoParams* k, int* variant,
+                                        int* grid);

@@ -1,0 +1,72 @@
+// fo_gemm_rs_noalloc: the fused GEMM + reduce-scatter for callers that cannot
+// allocate device memory (see include/flashoverlap.h). Same kernel and result
+// as fo_gemm_rs; its readiness counters and status word live in a file-scope
+// __device__ array instead of a caller-provided workspace.
+#include <string.h>
+
+#include <mutex>
+
+#include "fo_internal.h"
+#include "fo_kernel.cuh"
+
+// The scratch every fo_gemm_rs_noalloc call uses. In host code this name is
+// only a stand-in for the symbol: its device address comes from
+// cudaGetSymbolAddress, looked up once per device below.
+static __device__ __align__(256) unsigned char g_fo_noalloc_scratch[FO_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices];
+
+// Device address of the scratch array on the current device (set up on the
+// first call per device, with that device current).
+fo_status scratch_on_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return FO_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fo_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return FO_ERR_CUDA;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return FO_OK;
+}
+
+}  // namespace
+
+extern "C" fo_status fo_gemm_rs_noalloc(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y,
+                                        fo_stream_t stream) {
+  if (!p || p->d.op != FO_OP_GEMM_RS) return FO_ERR_INVALID_ARG;
+  fo_status st;
+  if ((st = fo_internal_check_ptrs(p->R, X)) || (st = fo_internal_check_ptrs(p->R, W)) ||
+      (st = fo_internal_check_ptrs(p->R, (const void* const*)Y)))
+    return st;
+  if (p->ws_bytes > (size_t)FO_NOALLOC_SCRATCH_BYTES) return FO_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  if ((st = scratch_on_current_device(&scratch))) return st;
+  fo::FoParams params;   // on the stack: no host allocation either
+  int variant = 0, grid = 0;
+  if ((st = fo_internal_rs_params_nocache(p, X, W, Y, scratch, &params, &variant, &grid))) return st;
+  // The previous call's counters reset themselves, but a call that timed out
+  // leaves them (and the status word) set: start every call from zero.
+  if (cudaMemsetAsync(scratch, 0, p->ws_bytes, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  if (fo_launch_variant(variant, params, grid, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  p->last_launches = 1;
+  return FO_OK;
+}

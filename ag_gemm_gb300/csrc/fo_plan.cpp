@@ -300,6 +300,7 @@ const char* fo_status_string(fo_status s) {
     case FO_ERR_CUDA: return "CUDA call failed";
     case FO_ERR_TIMEOUT: return "device-side wait timed out";
     case FO_ERR_PLAN_INVARIANT: return "schedule failed a validity check";
+    case FO_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the static no-alloc buffer holds";
   }
   return "unknown status";
 }

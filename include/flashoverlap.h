@@ -58,7 +58,9 @@ typedef enum {
   FO_ERR_UNSUPPORTED = 5,     /* option not built, or device is not sm_103 */
   FO_ERR_CUDA = 6,            /* a CUDA runtime/driver call failed */
   FO_ERR_TIMEOUT = 7,         /* a device-side bounded wait ran out */
-  FO_ERR_PLAN_INVARIANT = 8   /* the schedule failed a validity check */
+  FO_ERR_PLAN_INVARIANT = 8,  /* the schedule failed a validity check */
+  FO_ERR_SCRATCH_LIMIT = 9    /* fo_gemm_rs_noalloc: problem needs more scratch
+                                 than its static buffer holds */
 } fo_status;
 
 typedef enum {
@@ -177,6 +179,40 @@ fo_status fo_dp_grad_rs(fo_plan_t plan, const void* const* X, const void* const*
  * the workspace, so the plan is usable again; the outputs of the failed call
  * are undefined. */
 fo_status fo_status_query(fo_plan_t plan, void* ws, fo_stream_t stream, int32_t info[4]);
+
+/* fo_gemm_rs without a workspace, for callers that cannot allocate device
+ * memory. The paper has no counterpart: this is a deployment variant of
+ * fo_gemm_rs, computing the same result with the same kernel.
+ *
+ * Who needs it: code that runs where cudaMalloc is off limits, such as
+ * inside a host callback or an allocator hook, in a process whose memory is
+ * capped or pooled by another runtime, or in a plugin handed pointers but no
+ * allocator. Such a caller cannot provide the workspace fo_gemm_rs takes.
+ *
+ * Scratch: the readiness counters and the status word live in one
+ * file-scope __device__ array of FO_NOALLOC_SCRATCH_BYTES (64 KiB). Every
+ * GPU that loads the library holds it until the process exits. A plan whose
+ * workspace (fo_workspace_size) is larger is rejected with
+ * FO_ERR_SCRATCH_LIMIT before anything is launched; 64 KiB covers, e.g.,
+ * R = 8 with 8192 x 4096 outputs (16.6 KB).
+ *
+ * Behaviour:
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *     The caller passes inputs and outputs exactly as for fo_gemm_rs.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - Each call first zeroes the part of the array it uses (cudaMemsetAsync
+ *     on `stream`), then launches the fused kernel.
+ *   - All calls share the one array: calls that can overlap on the GPU
+ *     (other streams, other host threads) race and must be serialised by the
+ *     caller, e.g. by issuing them on one stream.
+ *   - A device-side wait that runs out is recorded in the array and cleared
+ *     by the next call; it is not reported. Use fo_gemm_rs with a workspace
+ *     and fo_status_query where that report is needed. */
+#define FO_NOALLOC_SCRATCH_BYTES (64 * 1024)
+fo_status fo_gemm_rs_noalloc(fo_plan_t plan, const void* const* X, const void* const* W,
+                             void* const* Y, fo_stream_t stream);
 
 /* ---- measurement controls (not part of the method) --------------------- */
 
