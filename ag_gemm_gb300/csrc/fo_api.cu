@@ -120,6 +120,7 @@ void remember(fo_plan_t p, int kind, const void* const* a, const void* const* b,
 void fill_common(fo_plan_t p, fo::FoParams* k, void* ws) {
   memcpy(k->table, p->table, sizeof(k->table));
   memcpy(k->ord, p->ord, sizeof(k->ord));
+  memcpy(k->rank_order, p->rank_order, sizeof(k->rank_order));
   k->R = p->R;
   k->tiles_m = p->tiles_m;
   k->tiles_n = p->tiles_n;

@@ -27,8 +27,14 @@ struct fo_plan_s {
   // table[r][s]: chunk (RS/DP: owner of the partial) or source shard (AG)
   // handled by rank r at step s.
   int32_t table[FO_MAX_R][FO_MAX_R];
-  // ord[r][s]: how many partials of the same chunk come before (r, s) in
-  // (step, rank) order; 0 = the first partial, which stores instead of adds.
+  // rank_order[s][i]: the rank whose step-s tiles come i-th among the ranks
+  // of step s in the kernel's tile order. Ranks within a step are
+  // independent; RS/DP alternate the direction from step to step so that the
+  // shards written last in step s are the first ones written in step s+1
+  // (their lines are still in L2).
+  int32_t rank_order[FO_MAX_R][FO_MAX_R];
+  // ord[r][s]: how many partials of the same chunk come before (r, s) in the
+  // kernel's tile order; 0 = the first partial, which stores instead of adds.
   int32_t ord[FO_MAX_R][FO_MAX_R];
   std::vector<fo_transfer> transfers;
   std::vector<fo_edge> edges;

@@ -54,6 +54,7 @@ struct alignas(128) FoParams {
   CUtensorMap tmD[FO_MAX_R];   // RS/DP: Y_c (2-D); AG: Y_r (3-D); PARTIAL: P_r (3-D)
   int32_t table[FO_MAX_R][FO_MAX_R];
   int32_t ord[FO_MAX_R][FO_MAX_R];
+  int32_t rank_order[FO_MAX_R][FO_MAX_R];
   int32_t R;
   int32_t tiles_m;             // m-tiles per chunk
   int32_t tiles_n;
@@ -86,12 +87,19 @@ __device__ __forceinline__ Tile decode_tile(const FoParams& p, int L) {
   const int t = L - task * tpt;
   Tile ti;
   ti.s = task / p.R;
-  ti.r = task - ti.s * p.R;
+  ti.r = p.rank_order[ti.s][task - ti.s * p.R];
   ti.mt = t / p.tiles_n;
   ti.nt = t - ti.mt * p.tiles_n;
   ti.c = p.table[ti.r][ti.s];
   ti.ord = p.ord[ti.r][ti.s];
   return ti;
+}
+
+// A partial is in its owner's shard: count it. The partial that completes
+// the shard (the R-th) resets the counter for the next call.
+__device__ __forceinline__ void signal_partial(uint32_t* ctr, int R) {
+  const uint32_t old = atom_add_release_u32(ctr, 1u);
+  if (old + 1u == (uint32_t)R) atomicExch(ctr, 0u);
 }
 
 // Write 32 registers (one 128-byte row per thread) into a 32 x 128 B staging
@@ -260,11 +268,25 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
     const int e = warp - 2;        // staging buffers of this warp
     const int q = warp & 3;        // TMEM lane quarter this warp may access
     uint32_t tcount = 0;
+    uint32_t* pend_ctr = nullptr;  // RS: counter of this warp's last partial, not yet published
+    bool pend_skip = false;
     for (int L = blockIdx.x; L < total; L += gridDim.x, ++tcount) {
       if (*abort_flag) break;
       const Tile ti = decode_tile(p, L);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1u;
+      if constexpr (EPI == EPI_RS) {
+        // About to block until the next accumulator is ready: publish the
+        // deferred partial first (a warp never holds one while it waits, so
+        // a waiter elsewhere always sees it eventually).
+        if (lane == 0 && pend_ctr && !mbar_try_wait(tfull_bar(acc), aph)) {
+          bulk_wait<0>();
+          fence_proxy_async_global();
+          if (!pend_skip) signal_partial(pend_ctr, p.R);
+          pend_ctr = nullptr;
+        }
+        __syncwarp();
+      }
       if (!mbar_wait(tfull_bar(acc), aph, abort_flag, kMbarLimitNs)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * FO_BN);
@@ -282,8 +304,18 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
           int good = 1;
           if (lane == 0) {
             const uint32_t need = p.deterministic ? (uint32_t)ti.ord : 1u;
-            good = wait_counter_geq(ctr, need, p.timeout_ns, abort_flag, gstatus) ? 1 : 0;
-            if (!good && !*abort_flag && !*gstatus) record_error(p.status, FO_ERR_TIMEOUT, ti.r, ti.s, ti.c);
+            if (ld_acquire_u32(ctr) < need) {
+              // Not yet: first publish this warp's own deferred partial (it
+              // may be the one being waited for), then wait.
+              if (pend_ctr) {
+                bulk_wait<0>();
+                fence_proxy_async_global();
+                if (!pend_skip) signal_partial(pend_ctr, p.R);
+                pend_ctr = nullptr;
+              }
+              good = wait_counter_geq(ctr, need, p.timeout_ns, abort_flag, gstatus) ? 1 : 0;
+              if (!good && !*abort_flag && !*gstatus) record_error(p.status, FO_ERR_TIMEOUT, ti.r, ti.s, ti.c);
+            }
             fence_proxy_async_global();
           }
           ok = __shfl_sync(0xffffffffu, good, 0) != 0;
@@ -325,14 +357,18 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
           }
         }
       } else {
-        // 8 sub-tiles of 32 rows x 32 fp32 columns.
-#pragma unroll 1
-        for (int j = 0; j < FO_BN / 32; ++j) {
-          uint32_t v[32];
-          tmem_ld32(tbase + j * 32, v);
+        // 8 sub-tiles of 32 rows x 32 fp32 columns. The TMEM load of sub-tile
+        // j+1 is in flight while sub-tile j is staged and sent.
+        constexpr int kSub = FO_BN / 32;
+        uint32_t v[2][32];
+        tmem_ld32(tbase, v[0]);
+#pragma unroll
+        for (int j = 0; j < kSub; ++j) {
           tmem_ld_wait();
-          reg_fence(v);
-          if (j == FO_BN / 32 - 1) {
+          reg_fence(v[j & 1]);
+          if (j + 1 < kSub) {
+            tmem_ld32(tbase + (j + 1) * 32, v[(j + 1) & 1]);
+          } else {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -341,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
           const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
-          stage_row_sw128(buf, lane, v);
+          stage_row_sw128(buf, lane, v[j & 1]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -356,20 +392,30 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
         }
         if constexpr (EPI == EPI_RS) {
           if (ok && lane == 0) {
-            // The partial is in the shard: publish it.
-            bulk_wait<0>();
-            fence_proxy_async_global();
-            const bool skip = p.fault_inject == FO_INJECT_SKIP_SIGNAL && ti.c == 0 && ti.mt == 0 && ti.nt == 0 &&
-                              q == 0 && ti.ord == 0;
-            if (!skip) {
-              const uint32_t old = atom_add_release_u32(ctr, 1u);
-              if (old + 1u == (uint32_t)p.R) atomicExch(ctr, 0u);   // last partial: ready for the next call
+            // Publish the previous tile's partial (its 8 bulk groups are
+            // older than this tile's 8) and keep this one pending, so the
+            // warp never stalls on its own latest writes.
+            if (pend_ctr) {
+              bulk_wait<kSub>();
+              fence_proxy_async_global();
+              if (!pend_skip) signal_partial(pend_ctr, p.R);
             }
+            pend_ctr = ctr;
+            pend_skip = p.fault_inject == FO_INJECT_SKIP_SIGNAL && ti.c == 0 && ti.mt == 0 && ti.nt == 0 &&
+                        q == 0 && ti.ord == 0;
           }
         }
       }
     }
-    if (lane == 0) bulk_wait<0>();
+    if (lane == 0) {
+      bulk_wait<0>();
+      if constexpr (EPI == EPI_RS) {
+        if (pend_ctr && !*abort_flag) {
+          fence_proxy_async_global();
+          if (!pend_skip) signal_partial(pend_ctr, p.R);
+        }
+      }
+    }
     __syncwarp();
   }
 

@@ -45,10 +45,20 @@ void build_table(fo_plan_s* p) {
       else if (ag) p->table[r][s] = ((r - s) % R + R) % R;
       else p->table[r][s] = ((r - 1 - s) % R + 2 * R) % R;
     }
-  // Contribution order of every (r, s) into its chunk, in (step, rank) order.
+  // Order of the ranks inside each step. Step s+1 writes its shards in the
+  // reverse of the order step s wrote them (RS/DP), so the most recently
+  // written shards are reused first.
+  for (int i = 0; i < R; ++i) p->rank_order[0][i] = i;
+  for (int s = 0; s + 1 < R; ++s)
+    for (int i = 0; i < R; ++i)
+      p->rank_order[s + 1][i] = ag ? i : (p->rank_order[s][R - 1 - i] + 1) % R;
+  // Contribution order of every (r, s) into its chunk, in the kernel's order.
   int seen[FO_MAX_R] = {0};
   for (int s = 0; s < R; ++s)
-    for (int r = 0; r < R; ++r) p->ord[r][s] = seen[p->table[r][s]]++;
+    for (int i = 0; i < R; ++i) {
+      const int r = p->rank_order[s][i];
+      p->ord[r][s] = seen[p->table[r][s]]++;
+    }
 }
 
 void build_transfers_and_edges(fo_plan_s* p) {

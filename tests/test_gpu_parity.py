@@ -141,6 +141,19 @@ def test_gemm_rs_repeated_calls_reuse_workspace(dev):
             assert np.array_equal(rep[d], ref[d])
 
 
+@pytest.mark.parametrize("det", [False, True])
+def test_gemm_rs_one_cta_holds_first_and_second_partial_of_a_tile(dev, det):
+    # One m-tile per chunk and exactly one n-tile per SM: the CTA that stores
+    # a shard tile's first partial is the one that adds its second partial
+    # next, so the epilogue must publish its own deferred partial before it
+    # waits for it.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    R, M, K, N = 2, 256, 64, 256 * sms
+    outs, ref = run_gemm_rs(dev, R, M, K, N, deterministic=det)
+    for d in range(R):
+        assert np.array_equal(outs[0][d], ref[d])
+
+
 def test_gemm_rs_sliced_ablation_same_result(dev):
     outs, ref = run_gemm_rs(dev, 4, 512, 128, 512, sched="sliced")
     for d in range(4):
