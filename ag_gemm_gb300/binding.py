@@ -26,6 +26,7 @@ SCHEDS = {"rank_adaptive": 0, "sliced": 1}
 TRANSPORTS = {"peer_read": 0, "copy": 1}
 W_LAYOUTS = {"kn": 0, "nk": 1}
 INJECT = {"none": 0, "drop_transfer": 1, "skip_signal": 2}
+TILE_CONFIGS = {"auto": 0, "single": 1}
 
 # Every symbol include/flashoverlap.h declares.
 EXPORTED = [
@@ -51,7 +52,7 @@ class PlanDesc(ctypes.Structure):
         ("op", c_int32), ("R", c_int32), ("M", c_int64), ("N", c_int64), ("K", c_int64),
         ("in_dtype", c_int32), ("out_dtype", c_int32), ("sched", c_int32), ("ag_transport", c_int32),
         ("w_layout", c_int32), ("deterministic", c_int32), ("timeout_ns", c_uint64),
-        ("fault_inject", c_int32), ("reserved", c_int32 * 7),
+        ("fault_inject", c_int32), ("tile_config", c_int32), ("reserved", c_int32 * 6),
     ]
 
 
@@ -160,7 +161,7 @@ class Plan:
 
 def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dtype=None,
             sched="rank_adaptive", ag_transport="peer_read", w_layout="kn", deterministic=False,
-            timeout_ns=0, fault_inject="none") -> Plan:
+            timeout_ns=0, fault_inject="none", tile_config="auto") -> Plan:
     lib = load()
     if out_dtype is None:
         out_dtype = "bf16" if op == "ag_gemm" else "f32"
@@ -176,6 +177,7 @@ def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dty
     d.deterministic = 1 if deterministic else 0
     d.timeout_ns = timeout_ns
     d.fault_inject = INJECT[fault_inject]
+    d.tile_config = TILE_CONFIGS[tile_config]
     h = c_void_p()
     _check(lib.fo_plan(ctypes.byref(d), ctypes.byref(h)), "fo_plan")
     return Plan(h.value, d)

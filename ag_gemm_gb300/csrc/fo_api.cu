@@ -123,6 +123,7 @@ void fill_common(fo_plan_t p, fo::FoParams* k, void* ws) {
   memcpy(k->rank_order, p->rank_order, sizeof(k->rank_order));
   k->R = p->R;
   k->tiles_m = p->tiles_m;
+  k->ctr_tiles_m = p->ctr_tiles_m;
   k->tiles_n = p->tiles_n;
   k->num_kb = p->num_kb;
   k->rows_per_chunk = (int32_t)p->rows_per_chunk;
@@ -165,7 +166,7 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
     if (!dp) {
       ok &= enc2d(&k->tmA[r], dt, A[r], kr, M, kr * es, bk, FO_BM);
       if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, B[r], N, kr, N * es, bk, bk);
-      else ok &= enc2d(&k->tmB[r], dt, B[r], kr, N, kr * es, bk, FO_BN);
+      else ok &= enc2d(&k->tmB[r], dt, B[r], kr, N, kr * es, bk, p->pair ? FO_BN / 2 : FO_BN);
     } else {
       ok &= enc2d(&k->tmA[r], dt, A[r], M, kr, M * es, bk, bk);
       ok &= enc2d(&k->tmB[r], dt, B[r], N, kr, N * es, bk, bk);
@@ -197,7 +198,7 @@ fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void
   for (int r = 0; r < R && ok; ++r) {
     ok &= enc2d(&k->tmA[r], dt, X[r], K, rpc, K * 2, 64, FO_BM);
     if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, W[r], nr, K, nr * 2, 64, 64);
-    else ok &= enc2d(&k->tmB[r], dt, W[r], K, nr, K * 2, 64, FO_BN);
+    else ok &= enc2d(&k->tmB[r], dt, W[r], K, nr, K * 2, 64, p->pair ? FO_BN / 2 : FO_BN);
     ok &= enc3d(&k->tmD[r], dt, Y[r], nr, rpc, R, nr * 2, rpc * nr * 2, 64, 32);
   }
   if (!ok) return FO_ERR_CUDA;
@@ -216,10 +217,45 @@ fo_status preflight(fo_plan_t p, DevInfo* di) {
   return FO_OK;
 }
 
-fo_status run_chunk_gemm(fo_plan_t p, int variant, const fo::FoParams* k, const DevInfo& di, cudaStream_t s) {
+// Launch grid for a plan: single-CTA tiles use min(tiles, resident CTAs);
+// pair tiles use an even number of CTAs, at most the pairs resident at once.
+fo_status launch_grid(fo_plan_t p, int variant, const DevInfo& di, int* grid) {
+  static std::mutex mu;
+  static int cache[64][FO_V_COUNT][2];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  int cap = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    cap = cache[dev][variant][p->pair ? 1 : 0];
+  }
+  if (cap <= 0) {
+    if (fo_max_resident_ctas(variant, p->pair, &cap) != cudaSuccess || cap <= 0) {
+      cudaGetLastError();
+      return FO_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[dev][variant][p->pair ? 1 : 0] = cap;
+  }
   const int total = p->R * p->R * p->tiles_m * p->tiles_n;
-  const int grid = total < di.sms ? total : di.sms;
-  cudaError_t e = fo_launch_variant(variant, *k, grid, s);
+  if (p->pair) {
+    const int units = total < cap / 2 ? total : cap / 2;
+    *grid = 2 * units;
+  } else {
+    int g = total < di.sms ? total : di.sms;
+    *grid = g < cap ? g : cap;
+  }
+  return *grid > 0 ? FO_OK : FO_ERR_CUDA;
+}
+
+fo_status run_chunk_gemm(fo_plan_t p, int variant, const fo::FoParams* k, const DevInfo& di, cudaStream_t s) {
+  int grid = 0;
+  fo_status st = launch_grid(p, variant, di, &grid);
+  if (st != FO_OK) return st;
+  cudaError_t e = fo_launch_variant(variant, p->pair, *k, grid, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FO_ERR_CUDA;
@@ -289,15 +325,13 @@ fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const
   for (int r = 0; r < R && ok; ++r) {
     ok &= enc2d(&k->tmA[r], dt, X[r], kr, M, kr * es, bk, FO_BM);
     if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, W[r], N, kr, N * es, bk, bk);
-    else ok &= enc2d(&k->tmB[r], dt, W[r], kr, N, kr * es, bk, FO_BN);
+    else ok &= enc2d(&k->tmB[r], dt, W[r], kr, N, kr * es, bk, p->pair ? FO_BN / 2 : FO_BN);
     ok &= enc2d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Y[r], N, rpc, N * 4, 32, 32);
   }
   if (!ok) return FO_ERR_CUDA;
   fill_common(p, k, scratch);
   *variant = es == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
-  const int total = p->R * p->R * p->tiles_m * p->tiles_n;
-  *grid = total < di.sms ? total : di.sms;
-  return FO_OK;
+  return launch_grid(p, *variant, di, grid);
 }
 
 fo_status fo_internal_check_ptrs(int R, const void* const* a) { return check_ptrs(R, a); }
@@ -445,23 +479,31 @@ fo_status fo_status_query(fo_plan_t p, void* ws, fo_stream_t stream, int32_t inf
 
 }  // extern "C"
 
-cudaError_t fo_launch_rs(int v, const fo::FoParams& p, int grid, cudaStream_t s);
-cudaError_t fo_launch_dp(int v, const fo::FoParams& p, int grid, cudaStream_t s);
-cudaError_t fo_launch_ag(int v, const fo::FoParams& p, int grid, cudaStream_t s);
-cudaError_t fo_launch_part(int v, const fo::FoParams& p, int grid, cudaStream_t s);
+cudaError_t fo_variant_rs(int v, bool pair, const fo::FoParams* p, int grid, cudaStream_t s, int* ctas);
+cudaError_t fo_variant_dp(int v, bool pair, const fo::FoParams* p, int grid, cudaStream_t s, int* ctas);
+cudaError_t fo_variant_ag(int v, bool pair, const fo::FoParams* p, int grid, cudaStream_t s, int* ctas);
+cudaError_t fo_variant_part(int v, bool pair, const fo::FoParams* p, int grid, cudaStream_t s, int* ctas);
 
-cudaError_t fo_launch_variant(int v, const fo::FoParams& p, int grid, cudaStream_t s) {
+static cudaError_t fo_variant_call(int v, bool pair, const fo::FoParams* p, int grid, cudaStream_t s, int* ctas) {
   switch (v) {
     case FO_V_RS_BF16_KN:
     case FO_V_RS_BF16_NK:
-    case FO_V_RS_TF32_NK: return fo_launch_rs(v, p, grid, s);
+    case FO_V_RS_TF32_NK: return fo_variant_rs(v, pair, p, grid, s, ctas);
     case FO_V_DP_BF16:
-    case FO_V_PART_DP: return fo_launch_dp(v, p, grid, s);
+    case FO_V_PART_DP: return fo_variant_dp(v, pair, p, grid, s, ctas);
     case FO_V_AG_BF16_KN:
-    case FO_V_AG_BF16_NK: return fo_launch_ag(v, p, grid, s);
+    case FO_V_AG_BF16_NK: return fo_variant_ag(v, pair, p, grid, s, ctas);
     case FO_V_PART_BF16_KN:
     case FO_V_PART_BF16_NK:
-    case FO_V_PART_TF32_NK: return fo_launch_part(v, p, grid, s);
+    case FO_V_PART_TF32_NK: return fo_variant_part(v, pair, p, grid, s, ctas);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t fo_launch_variant(int v, bool pair, const fo::FoParams& p, int grid, cudaStream_t s) {
+  return fo_variant_call(v, pair, &p, grid, s, nullptr);
+}
+
+cudaError_t fo_max_resident_ctas(int v, bool pair, int* ctas) {
+  return fo_variant_call(v, pair, nullptr, 0, nullptr, ctas);
 }

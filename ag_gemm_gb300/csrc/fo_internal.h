@@ -44,7 +44,9 @@ struct fo_plan_s {
   int64_t k_red;           // reduction length of one task
   int64_t n_out;           // output columns of one task
   int elem_bytes;          // 2 (bf16) or 4 (fp32 -> tf32 MMA)
-  int tiles_m, tiles_n, num_kb;
+  bool pair;               // CTA-pair 256 x 256 tiles (else single-CTA 128 x 256)
+  int tiles_m, tiles_n, num_kb;   // tiles_m: m-tiles per chunk of the chosen tile height
+  int ctr_tiles_m;         // 128-row tiles per chunk in the counter array (covers both heights)
 
   // Workspace layout.
   size_t ws_bytes;

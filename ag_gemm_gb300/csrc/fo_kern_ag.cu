@@ -1,10 +1,11 @@
-// Kernel instantiations: AG-GEMM (bf16 out) with W as [K x N] or [N x K].
+// Kernel instantiations: AG-GEMM (bf16 out) with W as [K x N] or [N x K],
+// single CTA or CTA pair.
 #include "fo_launch.cuh"
 
-cudaError_t fo_launch_ag(int v, const fo::FoParams& p, int grid, cudaStream_t s) {
+cudaError_t fo_variant_ag(int v, bool pair, const fo::FoParams* p, int grid, cudaStream_t s, int* ctas) {
   switch (v) {
-    case FO_V_AG_BF16_KN: return fo_launch_one<fo::EPI_AG, false, true, false>(p, grid, s);
-    case FO_V_AG_BF16_NK: return fo_launch_one<fo::EPI_AG, false, false, false>(p, grid, s);
+    case FO_V_AG_BF16_KN: return FO_DISPATCH_PAIR(fo::EPI_AG, false, true, false);
+    case FO_V_AG_BF16_NK: return FO_DISPATCH_PAIR(fo::EPI_AG, false, false, false);
   }
   return cudaErrorInvalidValue;
 }

@@ -2,11 +2,11 @@
 // the computing rank's own buffer, no transfer).
 #include "fo_launch.cuh"
 
-cudaError_t fo_launch_part(int v, const fo::FoParams& p, int grid, cudaStream_t s) {
+cudaError_t fo_variant_part(int v, bool pair, const fo::FoParams* p, int grid, cudaStream_t s, int* ctas) {
   switch (v) {
-    case FO_V_PART_BF16_KN: return fo_launch_one<fo::EPI_PARTIAL, false, true, false>(p, grid, s);
-    case FO_V_PART_BF16_NK: return fo_launch_one<fo::EPI_PARTIAL, false, false, false>(p, grid, s);
-    case FO_V_PART_TF32_NK: return fo_launch_one<fo::EPI_PARTIAL, false, false, true>(p, grid, s);
+    case FO_V_PART_BF16_KN: return FO_DISPATCH_PAIR(fo::EPI_PARTIAL, false, true, false);
+    case FO_V_PART_BF16_NK: return FO_DISPATCH_PAIR(fo::EPI_PARTIAL, false, false, false);
+    case FO_V_PART_TF32_NK: return FO_DISPATCH_SINGLE(fo::EPI_PARTIAL, false, false, true);
   }
   return cudaErrorInvalidValue;
 }

@@ -1,12 +1,13 @@
-// Kernel instantiations: GEMM-RS (bf16 with W as [K x N] or [N x K]; fp32
-// inputs on the tf32 MMA with W as [N x K]).
+// Kernel instantiations: GEMM-RS (bf16 with W as [K x N] or [N x K], single
+// CTA or CTA pair; fp32 inputs on the tf32 MMA with W as [N x K], single CTA).
 #include "fo_launch.cuh"
 
-cudaError_t fo_launch_rs(int v, const fo::FoParams& p, int grid, cudaStream_t s) {
+// Launch (ctas == nullptr) or report the resident-CTA limit of a variant.
+cudaError_t fo_variant_rs(int v, bool pair, const fo::FoParams* p, int grid, cudaStream_t s, int* ctas) {
   switch (v) {
-    case FO_V_RS_BF16_KN: return fo_launch_one<fo::EPI_RS, false, true, false>(p, grid, s);
-    case FO_V_RS_BF16_NK: return fo_launch_one<fo::EPI_RS, false, false, false>(p, grid, s);
-    case FO_V_RS_TF32_NK: return fo_launch_one<fo::EPI_RS, false, false, true>(p, grid, s);
+    case FO_V_RS_BF16_KN: return FO_DISPATCH_PAIR(fo::EPI_RS, false, true, false);
+    case FO_V_RS_BF16_NK: return FO_DISPATCH_PAIR(fo::EPI_RS, false, false, false);
+    case FO_V_RS_TF32_NK: return FO_DISPATCH_SINGLE(fo::EPI_RS, false, false, true);
   }
   return cudaErrorInvalidValue;
 }

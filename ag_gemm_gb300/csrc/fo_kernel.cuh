@@ -1,32 +1,43 @@
 // The persistent chunk-GEMM kernel of FlashOverlap on sm_103a.
 //
-// One CTA per SM walks a static list of 128 x 256 output tiles in step-major
-// order: all tiles of step 0 (every rank's first chunk task), then step 1,
-// and so on. This is the rank-adaptive order of Flash-RS / Flash-AG
-// (gist.science, "Technical Summary" section 2): for reduce-scatter each
-// rank's own chunk is its last task, for all-gather its first.
+// Persistent CTAs walk a static list of output tiles in step-major order:
+// all tiles of step 0 (every rank's first chunk task), then step 1, and so
+// on. This is the rank-adaptive order of Flash-RS / Flash-AG (gist.science,
+// "Technical Summary" section 2): for reduce-scatter each rank's own chunk is
+// its last task, for all-gather its first.
 //
-// Warp roles (192 threads):
-//   warp 0     TMA producer: loads 128-byte-wide K slices of both operands
-//              into a 4-stage shared-memory ring (128B swizzle).
-//   warp 1     MMA issuer: allocates 512 TMEM columns (two 128 x 256 fp32
-//              accumulators), issues tcgen05.mma, commits to mbarriers.
+// Two tile configurations:
+//   PAIR = false  one CTA per SM owns a 128 x 256 fp32 accumulator; the MMA
+//                 is tcgen05.mma.cta_group::1 (M = 128, N = 256).
+//   PAIR = true   a cluster of two CTAs (two SMs) owns a 256 x 256 tile:
+//                 each CTA loads 128 rows of A and 128 columns of B, the
+//                 leader issues tcgen05.mma.cta_group::2 (M = 256, N = 256)
+//                 reading both CTAs' shared memory, and each CTA's TMEM holds
+//                 its 128 rows x 256 columns. Operand traffic into each SM
+//                 is 2/3 of the single-CTA tile's.
+//
+// Warp roles (192 threads per CTA):
+//   warp 0     TMA producer: 128-byte-wide K slices of both operands into a
+//              shared-memory ring (128B swizzle); 4 stages of 48 KB, or 6 of
+//              32 KB per CTA in the pair.
+//   warp 1     allocates 512 TMEM columns (two fp32 accumulators); in the
+//              single-CTA kernel and in the pair's leader it issues the MMAs.
 //   warps 2-5  epilogue: tcgen05.ld the accumulator (each warp its 32-lane
-//              quarter), stage 32-row sub-tiles in shared memory and move
-//              them with TMA:
-//                RS/DP : the partial of chunk c goes to owner c's shard:
-//                        the first partial of a shard is stored, later ones
-//                        are added (TMA reduce-add, fp32, at L2) once the
-//                        per-tile counter says the shard holds the first.
-//                        This accumulate is the P2P transfer.
-//                AG    : bf16 store into rank r's output rows of the source
-//                        shard; the A operand was read straight from the
-//                        source rank's buffer (the transfer is the read).
-//                PARTIAL: fp32 store into the computing rank's own buffer
-//                        (pure-GEMM control, no transfer).
+//              quarter), stage 32-row sub-tiles in shared memory, move them
+//              with TMA:
+//                RS/DP  the partial of chunk c goes to owner c's shard: the
+//                       first partial of a shard tile is stored, later ones
+//                       are added (TMA reduce-add, fp32, at L2) once the
+//                       per-tile counter says the shard holds the first. This
+//                       accumulate is the P2P transfer.
+//                AG     bf16 store into rank r's output rows of the source
+//                       shard; the A operand was read straight from the
+//                       source rank's buffer (the transfer is the read).
+//                PARTIAL fp32 store into the computing rank's own buffer
+//                       (pure-GEMM control, no transfer).
 // Synchronisation (shd-paper.top, 方法详解 "key design" paragraph, item 3):
-// mbarriers inside the CTA, acquire/release counters in global memory across
-// CTAs; every wait is bounded and failures land in a device status word.
+// mbarriers inside the CTA / pair, acquire/release counters in global memory
+// across CTAs; every wait is bounded and failures land in a status word.
 #pragma once
 
 #include "fo_device.cuh"
@@ -34,17 +45,23 @@
 
 namespace fo {
 
-constexpr int kStages = 4;
-constexpr int kAStage = FO_BM * FO_BK_BYTES;   // 16 KB
-constexpr int kBStage = FO_BN * FO_BK_BYTES;   // 32 KB
-constexpr int kStageBytes = kAStage + kBStage;
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBuf = 32 * 128;              // 32 rows x 128 bytes
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kBarBytes = 128;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * 2 * kEpiBuf + kBarBytes;
+constexpr int kBarBytes = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kMbarLimitNs = 2000000000ull;
+
+template <bool PAIR>
+struct Cfg {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kAStage = FO_BM * FO_BK_BYTES;                       // 16 KB
+  static constexpr int kBRows = PAIR ? FO_BN / 2 : FO_BN;                   // B rows (N) in this CTA
+  static constexpr int kBStage = kBRows * FO_BK_BYTES;                      // 16 or 32 KB
+  static constexpr int kStageBytes = kAStage + kBStage;
+  static constexpr int kTileM = PAIR ? 2 * FO_BM : FO_BM;                   // rows of one tile
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * 2 * kEpiBuf + kBarBytes;
+};
 
 enum Epi : int { EPI_RS = 0, EPI_AG = 1, EPI_PARTIAL = 2 };
 
@@ -56,29 +73,30 @@ struct alignas(128) FoParams {
   int32_t ord[FO_MAX_R][FO_MAX_R];
   int32_t rank_order[FO_MAX_R][FO_MAX_R];
   int32_t R;
-  int32_t tiles_m;             // m-tiles per chunk
+  int32_t tiles_m;             // m-tiles per chunk, of this kernel's tile height (128 or 256 rows)
   int32_t tiles_n;
   int32_t num_kb;
   int32_t rows_per_chunk;
   int32_t deterministic;
   int32_t fault_inject;
-  int32_t pad0;
-  uint32_t* counters;          // RS/DP: [R][tiles_m * tiles_n][4]
+  int32_t ctr_tiles_m;         // 128-row tiles per chunk in the counter array
+  uint32_t* counters;          // RS/DP: [R][ctr_tiles_m][tiles_n][4]
   int32_t* status;             // fo_ws_header
   uint64_t timeout_ns;
 };
 
-template <bool A_MN, bool B_MN, bool TF32>
+template <bool A_MN, bool B_MN, bool TF32, bool PAIR>
 __host__ __device__ constexpr uint32_t instr_desc() {
   // kind::f16 / kind::tf32 instruction descriptor: D fp32 (bits 4-5 = 1),
   // A and B format (bits 7-9, 10-12: bf16 = 1, tf32 = 2), A/B major (bits 15,
   // 16: 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
   return (1u << 4) | ((TF32 ? 2u : 1u) << 7) | ((TF32 ? 2u : 1u) << 10) | ((A_MN ? 1u : 0u) << 15) |
-         ((B_MN ? 1u : 0u) << 16) | ((uint32_t)(FO_BN >> 3) << 17) | ((uint32_t)(FO_BM >> 4) << 24);
+         ((B_MN ? 1u : 0u) << 16) | ((uint32_t)(FO_BN >> 3) << 17) |
+         ((uint32_t)((PAIR ? 2 * FO_BM : FO_BM) >> 4) << 24);
 }
 
 struct Tile {
-  int r, s, c, ord, mt, nt;
+  int r, s, c, ord, mt, nt;    // mt: m-tile of this kernel's tile height
 };
 
 __device__ __forceinline__ Tile decode_tile(const FoParams& p, int L) {
@@ -116,20 +134,24 @@ __device__ __forceinline__ void stage_row_sw128(uint32_t buf, int lane, const ui
   }
 }
 
-template <int EPI, bool A_MN, bool B_MN, bool TF32>
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid_constant__ FoParams p) {
+  using C = Cfg<PAIR>;
+  constexpr int CG = PAIR ? 2 : 1;
+  constexpr int kStages = C::kStages;
   constexpr int kEsz = TF32 ? 4 : 2;
   constexpr int kBK = FO_BK_BYTES / kEsz;        // K elements per stage (= MN elements per 128B row)
   constexpr int kMmaK = 32 / kEsz;               // K of one tcgen05.mma (32 bytes)
   constexpr int kBoxBytes = kBK * 128;           // one MN-major box: kBK rows x 128 B
-  constexpr uint32_t kIdesc = instr_desc<A_MN, B_MN, TF32>();
+  constexpr uint32_t kIdesc = instr_desc<A_MN, B_MN, TF32, PAIR>();
+  constexpr uint32_t kTxBytes = (PAIR ? 2 : 1) * C::kStageBytes;   // both halves land on the leader's barrier
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sStage = base;
-  const uint32_t sEpi = base + kStages * kStageBytes;
+  const uint32_t sEpi = base + kStages * C::kStageBytes;
   const uint32_t sBar = sEpi + kEpiWarps * 2 * kEpiBuf;
   auto full_bar = [&](int i) { return sBar + 8u * i; };
   auto empty_bar = [&](int i) { return sBar + 8u * (kStages + i); };
@@ -143,6 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const volatile int32_t* gstatus = p.status;
+  // Position in the pair (0 = leader) and the pair's index; a single-CTA
+  // kernel is its own leader.
+  const uint32_t prank = PAIR ? cluster_ctarank() : 0u;
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const bool leader = prank == 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -151,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), kEpiWarps);
+      mbar_init(tempty_bar(a), PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(mma_done_bar, 1);
     *abort_flag = 0;
@@ -160,30 +188,31 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
   }
   if (warp == 1) {
     __syncwarp();
-    tmem_alloc(sTmemSlot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(sTmemSlot, kTmemCols);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();   // the peer's barriers are initialised before any remote arrive
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int total = p.R * p.R * p.tiles_m * p.tiles_n;
-  const int tpt = p.tiles_m * p.tiles_n;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
-      for (int L = blockIdx.x; L < total; L += gridDim.x) {
+      for (int L = unit; L < total; L += units) {
         if (*gstatus) *abort_flag = 1;
         if (*abort_flag) break;
         const Tile ti = decode_tile(p, L);
         const CUtensorMap* mA = EPI == EPI_AG ? &p.tmA[ti.c] : &p.tmA[ti.r];
         const CUtensorMap* mB = &p.tmB[ti.r];
-        // Row (or column, for MN-major A) where this tile's A block starts.
-        const int a_mn0 = (EPI == EPI_AG ? 0 : ti.c * p.rows_per_chunk) + ti.mt * FO_BM;
-        const int n0 = ti.nt * FO_BN;
+        // Row (or column, for MN-major A) where this CTA's A block starts,
+        // and the first output column of its B block.
+        const int a_mn0 = (EPI == EPI_AG ? 0 : ti.c * p.rows_per_chunk) + ti.mt * C::kTileM + (int)prank * FO_BM;
+        const int b_n0 = ti.nt * FO_BN + (int)prank * C::kBRows;
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int stage = it % kStages;
@@ -192,38 +221,63 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
             ok = false;
             break;
           }
-          const uint32_t fb = full_bar(stage);
-          const uint32_t sa = sStage + stage * kStageBytes;
-          const uint32_t sb = sa + kAStage;
-          mbar_arrive_expect_tx(fb, kStageBytes);
+          const uint32_t sa = sStage + stage * C::kStageBytes;
+          const uint32_t sb = sa + C::kAStage;
           const int k0 = kb * kBK;
-          if constexpr (A_MN) {
+          if constexpr (PAIR) {
+            const uint32_t fb = mapa_shared(full_bar(stage), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxBytes);
+            if constexpr (A_MN) {
 #pragma unroll
-            for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d(sa + j * kBoxBytes, mA, fb, a_mn0 + j * kBK, k0);
-          } else {
-            tma_load_2d(sa, mA, fb, k0, a_mn0);
-          }
-          if constexpr (B_MN) {
+              for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d_pair(sa + j * kBoxBytes, mA, fb, a_mn0 + j * kBK, k0);
+            } else {
+              tma_load_2d_pair(sa, mA, fb, k0, a_mn0);
+            }
+            if constexpr (B_MN) {
 #pragma unroll
-            for (int j = 0; j < FO_BN / kBK; ++j) tma_load_2d(sb + j * kBoxBytes, mB, fb, n0 + j * kBK, k0);
+              for (int j = 0; j < C::kBRows / kBK; ++j)
+                tma_load_2d_pair(sb + j * kBoxBytes, mB, fb, b_n0 + j * kBK, k0);
+            } else {
+              tma_load_2d_pair(sb, mB, fb, k0, b_n0);
+            }
           } else {
-            tma_load_2d(sb, mB, fb, k0, n0);
+            const uint32_t fb = full_bar(stage);
+            mbar_arrive_expect_tx(fb, kTxBytes);
+            if constexpr (A_MN) {
+#pragma unroll
+              for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d(sa + j * kBoxBytes, mA, fb, a_mn0 + j * kBK, k0);
+            } else {
+              tma_load_2d(sa, mA, fb, k0, a_mn0);
+            }
+            if constexpr (B_MN) {
+#pragma unroll
+              for (int j = 0; j < C::kBRows / kBK; ++j) tma_load_2d(sb + j * kBoxBytes, mB, fb, b_n0 + j * kBK, k0);
+            } else {
+              tma_load_2d(sb, mB, fb, k0, b_n0);
+            }
           }
         }
         if (!ok) break;
       }
       // Drain: every load still in flight lands before the CTA may exit.
-      const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+      // The pair's loads complete on the leader's barriers, which count both
+      // halves; after an abort the peer gives its own loads a fixed time.
       volatile int never = 0;
-      for (uint32_t j = first; j < it; ++j)
-        mbar_wait(full_bar(j % kStages), (j / kStages) & 1u, &never, 100000000ull);
+      if (leader) {
+        const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          mbar_wait(full_bar(j % kStages), (j / kStages) & 1u, &never, 100000000ull);
+      } else if (*abort_flag) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
+      }
       if (*abort_flag) record_error(p.status, FO_ERR_TIMEOUT, -1, -1, 0);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t it = 0, tcount = 0;
-      for (int L = blockIdx.x; L < total; L += gridDim.x, ++tcount) {
+      for (int L = unit; L < total; L += units, ++tcount) {
         if (*abort_flag) break;
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1u;
@@ -239,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
             break;
           }
           tc_fence_after();
-          const uint32_t sa = sStage + stage * kStageBytes;
-          const uint32_t sb = sa + kAStage;
+          const uint32_t sa = sStage + stage * C::kStageBytes;
+          const uint32_t sb = sa + C::kAStage;
 #pragma unroll
           for (int k = 0; k < FO_BK_BYTES / 32; ++k) {
             // K-major: the k-th 32-byte column of the swizzled 128-byte rows.
@@ -251,15 +305,17 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
                 A_MN ? smem_desc_sw128(sa + aoff, kBoxBytes, 1024) : smem_desc_sw128(sa + aoff, 16, 1024);
             const uint64_t bdesc =
                 B_MN ? smem_desc_sw128(sb + boff, kBoxBytes, 1024) : smem_desc_sw128(sb + boff, 16, 1024);
-            tc_mma<TF32>(d, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            tc_mma<CG, TF32>(d, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
           }
-          tc_commit(empty_bar(stage));
+          if constexpr (PAIR) tc_commit_pair_multicast(empty_bar(stage), 0x3);
+          else tc_commit<1>(empty_bar(stage));
         }
         if (!ok) break;
-        tc_commit(tfull_bar(acc));
+        if constexpr (PAIR) tc_commit_pair_multicast(tfull_bar(acc), 0x3);
+        else tc_commit<1>(tfull_bar(acc));
       }
       // All issued MMAs complete before TMEM is released.
-      tc_commit(mma_done_bar);
+      tc_commit<CG>(mma_done_bar);
       volatile int never = 0;
       mbar_wait(mma_done_bar, 0, &never, 100000000ull);
     }
@@ -270,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
     uint32_t tcount = 0;
     uint32_t* pend_ctr = nullptr;  // RS: counter of this warp's last partial, not yet published
     bool pend_skip = false;
-    for (int L = blockIdx.x; L < total; L += gridDim.x, ++tcount) {
+    for (int L = unit; L < total; L += units, ++tcount) {
       if (*abort_flag) break;
       const Tile ti = decode_tile(p, L);
       const int acc = tcount & 1;
@@ -290,14 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
       if (!mbar_wait(tfull_bar(acc), aph, abort_flag, kMbarLimitNs)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * FO_BN);
-      const int row0 = ti.mt * FO_BM + q * 32;   // first row of this quarter within the chunk
+      const int mt128 = ti.mt * (PAIR ? 2 : 1) + (int)prank;   // 128-row tile of this CTA within the chunk
+      const int row0 = mt128 * FO_BM + q * 32;                   // first row of this quarter within the chunk
       const int n0 = ti.nt * FO_BN;
 
       uint32_t* ctr = nullptr;
       bool ok = true;
       if constexpr (EPI == EPI_RS) {
-        const int tile_in_chunk = ti.mt * p.tiles_n + ti.nt;
-        ctr = p.counters + ((size_t)(ti.c * tpt + tile_in_chunk) * 4 + q);
+        ctr = p.counters + (((size_t)ti.c * p.ctr_tiles_m + mt128) * p.tiles_n + ti.nt) * 4 + q;
         if (ti.ord > 0) {
           // The shard must already hold its first (stored) partial; in
           // deterministic mode, every partial that comes before this one.
@@ -334,9 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
           reg_fence(v0);
           reg_fence(v1);
           if (j == FO_BN / 64 - 1) {
+            // The accumulator may be refilled once every epilogue warp (of
+            // both CTAs, for a pair) has read its quarter.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0) {
+              if constexpr (PAIR) mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+              else mbar_arrive(tempty_bar(acc));
+            }
           }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -369,9 +430,14 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
           if (j + 1 < kSub) {
             tmem_ld32(tbase + (j + 1) * 32, v[(j + 1) & 1]);
           } else {
+            // The accumulator may be refilled once every epilogue warp (of
+            // both CTAs, for a pair) has read its quarter.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (lane == 0) {
+              if constexpr (PAIR) mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+              else mbar_arrive(tempty_bar(acc));
+            }
           }
           if (!ok) continue;
           const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
@@ -401,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
               if (!pend_skip) signal_partial(pend_ctr, p.R);
             }
             pend_ctr = ctr;
-            pend_skip = p.fault_inject == FO_INJECT_SKIP_SIGNAL && ti.c == 0 && ti.mt == 0 && ti.nt == 0 &&
+            pend_skip = p.fault_inject == FO_INJECT_SKIP_SIGNAL && ti.c == 0 && mt128 == 0 && ti.nt == 0 &&
                         q == 0 && ti.ord == 0;
           }
         }
@@ -420,11 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();   // neither CTA leaves while the pair still uses its memory
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     __syncwarp();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc<CG>(tmem_base, kTmemCols);
   }
 }
 
@@ -445,4 +512,8 @@ enum fo_variant {
   FO_V_COUNT
 };
 
-cudaError_t fo_launch_variant(int variant, const fo::FoParams& p, int grid, cudaStream_t stream);
+// Launch `variant` with single-CTA tiles (pair = false) or CTA-pair tiles;
+// `grid` counts CTAs (even for pairs).
+cudaError_t fo_launch_variant(int variant, bool pair, const fo::FoParams& p, int grid, cudaStream_t stream);
+// Largest grid (CTAs) of this variant that can be resident at once.
+cudaError_t fo_max_resident_ctas(int variant, bool pair, int* ctas);

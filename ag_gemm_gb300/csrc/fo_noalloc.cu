@@ -63,7 +63,7 @@ extern "C" fo_status fo_gemm_rs_noalloc(fo_plan_t p, const void* const* X, const
     cudaGetLastError();
     return FO_ERR_CUDA;
   }
-  if (fo_launch_variant(variant, params, grid, (cudaStream_t)stream) != cudaSuccess) {
+  if (fo_launch_variant(variant, p->pair, params, grid, (cudaStream_t)stream) != cudaSuccess) {
     cudaGetLastError();
     return FO_ERR_CUDA;
   }

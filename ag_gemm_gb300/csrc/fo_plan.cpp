@@ -170,7 +170,8 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (d->ag_transport != FO_AG_PEER_READ && d->ag_transport != FO_AG_COPY) return FO_ERR_INVALID_ARG;
   if (d->w_layout != FO_W_KN && d->w_layout != FO_W_NK) return FO_ERR_INVALID_ARG;
   if (d->fault_inject < FO_INJECT_NONE || d->fault_inject > FO_INJECT_SKIP_SIGNAL) return FO_ERR_INVALID_ARG;
-  for (int i = 0; i < 7; ++i)
+  if (d->tile_config != FO_TILE_AUTO && d->tile_config != FO_TILE_SINGLE) return FO_ERR_INVALID_ARG;
+  for (int i = 0; i < 6; ++i)
     if (d->reserved[i]) return FO_ERR_INVALID_ARG;
   if (d->M <= 0 || d->N <= 0 || d->K <= 0) return FO_ERR_SHAPE;
   const int R = d->R;
@@ -223,7 +224,9 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
     case FO_OP_AG_GEMM: p->k_red = K; p->n_out = N / R; break;
     default: p->k_red = K; p->n_out = N; break;
   }
-  p->tiles_m = (int)cdiv(p->rows_per_chunk, FO_BM);
+  p->pair = eb == 2 && d->tile_config == FO_TILE_AUTO;
+  p->tiles_m = (int)cdiv(p->rows_per_chunk, p->pair ? 2 * FO_BM : FO_BM);
+  p->ctr_tiles_m = 2 * (int)cdiv(p->rows_per_chunk, 2 * FO_BM);
   p->tiles_n = (int)cdiv(p->n_out, FO_BN);
   p->num_kb = (int)cdiv(p->k_red * eb, FO_BK_BYTES);
   if ((int64_t)R * R * p->tiles_m * p->tiles_n > ((int64_t)1 << 31) - 1) {
@@ -243,7 +246,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (d->op == FO_OP_AG_GEMM) {
     off += align_up((size_t)R * R * p->tiles_m * sizeof(uint32_t), 256);
   } else {
-    off += align_up((size_t)R * p->tiles_m * p->tiles_n * 4 * sizeof(uint32_t), 256);
+    off += align_up((size_t)R * p->ctr_tiles_m * p->tiles_n * 4 * sizeof(uint32_t), 256);
   }
   p->ws_bytes = off;
   p->last_launches = 0;

@@ -91,6 +91,12 @@ typedef enum { FO_W_KN = 0, FO_W_NK = 1 } fo_w_layout;
  * signal of one tile, so that a bounded wait runs out on the device. */
 typedef enum { FO_INJECT_NONE = 0, FO_INJECT_DROP_TRANSFER = 1, FO_INJECT_SKIP_SIGNAL = 2 } fo_inject;
 
+/* Output tile of the fused kernel. AUTO: a pair of CTAs on two SMs shares
+ * one 256 x 256 tile (tcgen05 cta_group::2) for bf16 inputs; fp32 inputs use
+ * SINGLE. SINGLE: one CTA per SM, 128 x 256 tiles (cta_group::1). Both give
+ * the same results; SINGLE exists for small problems and for comparison. */
+typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
+
 /* Global GEMM sizes (M, N, K); the per-rank operands are, for each op:
  *   FO_OP_GEMM_RS    X_r [M x K/R], W_r [K/R x N] (or [N x K/R]), Y_r [M/R x N] fp32
  *   FO_OP_AG_GEMM    X_r [M/R x K], W_r [K x N/R] (or [N/R x K]), Y_r [M x N/R] bf16,
@@ -112,7 +118,8 @@ typedef struct {
                                  shard's first partial is stored */
   uint64_t timeout_ns;        /* bound of every device-side wait; 0 = 1 s */
   int32_t fault_inject;       /* fo_inject (tests only) */
-  int32_t reserved[7];        /* must be zero */
+  int32_t tile_config;        /* fo_tile_config */
+  int32_t reserved[6];        /* must be zero */
 } fo_plan_desc;
 
 typedef struct fo_plan_s* fo_plan_t;

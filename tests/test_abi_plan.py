@@ -135,3 +135,19 @@ def test_null_arguments_are_rejected():
     with pytest.raises(B.FlashOverlapError) as e:
         B.fo_gemm_rs(p, [24, 16], [16, 16], [16, 16], 4096, stream=0)
     assert e.value.code == B.FO_ERR_ALIGN
+
+
+def test_plan_rejects_unknown_tile_config():
+    d = B.PlanDesc()
+    d.op, d.R, d.M, d.N, d.K = 1, 2, 256, 256, 256
+    d.out_dtype = 1
+    d.tile_config = 7
+    import ctypes
+    h = ctypes.c_void_p()
+    assert B.load().fo_plan(ctypes.byref(d), ctypes.byref(h)) == B.FO_ERR_INVALID_ARG
+
+
+def test_workspace_counts_pair_tiles():
+    # 600-row chunks: 3 single-CTA m-tiles, 2 pair m-tiles = 4 128-row counter rows.
+    p = B.fo_plan("gemm_rs", 2, 1200, 512, 512)
+    assert B.fo_workspace_size(p) >= 256 + 2 * 4 * 2 * 4 * 4

@@ -70,10 +70,10 @@ def _status_ok(plan, ws):
 
 
 def run_gemm_rs(dev, R, M, K, N, *, dtype="bf16", mode="int", w_layout="kn", seed=0, sched="rank_adaptive",
-                deterministic=False, repeat=1):
+                deterministic=False, repeat=1, tile="auto"):
     inp = gemm_rs_inputs(R, M, K, N, dtype=dtype, mode=mode, seed=seed)
     plan = B.fo_plan("gemm_rs", R, M, N, K * R, in_dtype=dtype, w_layout=w_layout, sched=sched,
-                     deterministic=deterministic)
+                     deterministic=deterministic, tile_config=tile)
     X = [x.to(dev) for x in inp["X"]]
     W = [(w if w_layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
     Y = Guarded(R, (M // R, N), torch.float32, dev)
@@ -96,6 +96,10 @@ def _assert_close(got, ref):
 
 # ------------------------------------------------------------------ GEMM-RS
 
+TILES = ["auto", "single"]   # CTA-pair 256x256 tiles (bf16 default) and single-CTA 128x256 tiles
+
+
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("R,M,K,N,layout", [
     (2, 256, 512, 512, "kn"),       # the 256x512x512 R=2 shape in bf16
     (4, 800, 200, 328, "kn"),       # ragged: 200 rows per chunk, K 200, N 328
@@ -103,9 +107,10 @@ def _assert_close(got, ref):
     (1, 128, 128, 256, "kn"),       # R = 1: plain GEMM
     (8, 1024, 136, 264, "nk"),
     (5, 640, 256, 1024, "kn"),      # several N tiles, 5 ranks
+    (2, 1200, 320, 776, "nk"),      # 600-row chunks: a pair tile's second half partly out of the chunk
 ])
-def test_gemm_rs_integer_bit_exact(dev, R, M, K, N, layout):
-    outs, ref = run_gemm_rs(dev, R, M, K, N, w_layout=layout)
+def test_gemm_rs_integer_bit_exact(dev, R, M, K, N, layout, tile):
+    outs, ref = run_gemm_rs(dev, R, M, K, N, w_layout=layout, tile=tile)
     for d in range(R):
         assert np.array_equal(outs[0][d], ref[d]), f"shard {d}"
 
@@ -117,9 +122,10 @@ def test_gemm_rs_fp32_inputs_tf32_bit_exact(dev, R, M, K, N):
         assert np.array_equal(outs[0][d], ref[d]), f"shard {d}"
 
 
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("R,M,K,N,layout", [(4, 1024, 512, 512, "kn"), (8, 1024, 200, 328, "nk")])
-def test_gemm_rs_random_bf16_within_tolerance(dev, R, M, K, N, layout):
-    outs, ref = run_gemm_rs(dev, R, M, K, N, mode="randn", w_layout=layout, seed=2)
+def test_gemm_rs_random_bf16_within_tolerance(dev, R, M, K, N, layout, tile):
+    outs, ref = run_gemm_rs(dev, R, M, K, N, mode="randn", w_layout=layout, seed=2, tile=tile)
     for d in range(R):
         _assert_close(outs[0][d], ref[d])
 
@@ -141,15 +147,17 @@ def test_gemm_rs_repeated_calls_reuse_workspace(dev):
             assert np.array_equal(rep[d], ref[d])
 
 
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("det", [False, True])
-def test_gemm_rs_one_cta_holds_first_and_second_partial_of_a_tile(dev, det):
-    # One m-tile per chunk and exactly one n-tile per SM: the CTA that stores
-    # a shard tile's first partial is the one that adds its second partial
-    # next, so the epilogue must publish its own deferred partial before it
-    # waits for it.
+def test_gemm_rs_one_cta_holds_first_and_second_partial_of_a_tile(dev, det, tile):
+    # One m-tile per chunk and exactly one n-tile per SM (per SM pair): the
+    # CTA that stores a shard tile's first partial is the one that adds its
+    # second partial next, so the epilogue must publish its own deferred
+    # partial before it waits for it.
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    R, M, K, N = 2, 256, 64, 256 * sms
-    outs, ref = run_gemm_rs(dev, R, M, K, N, deterministic=det)
+    units = sms if tile == "single" else sms // 2
+    R, M, K, N = 2, 2 * (128 if tile == "single" else 256), 64, 256 * units
+    outs, ref = run_gemm_rs(dev, R, M, K, N, deterministic=det, tile=tile)
     for d in range(R):
         assert np.array_equal(outs[0][d], ref[d])
 
@@ -178,9 +186,9 @@ def test_gemm_rs_new_buffers_after_cached_call(dev):
 
 # ------------------------------------------------------------------ AG-GEMM
 
-def run_ag(dev, R, M, K, N, *, mode="int", layout="kn", seed=1):
+def run_ag(dev, R, M, K, N, *, mode="int", layout="kn", seed=1, tile="auto"):
     inp = ag_gemm_inputs(R, M, K, N // R, mode=mode, seed=seed)
-    plan = B.fo_plan("ag_gemm", R, M, N, K, w_layout=layout)
+    plan = B.fo_plan("ag_gemm", R, M, N, K, w_layout=layout, tile_config=tile)
     X = [x.to(dev) for x in inp["X"]]
     W = [(w if layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
     Y = Guarded(R, (M, N // R), torch.bfloat16, dev)
@@ -192,14 +200,16 @@ def run_ag(dev, R, M, K, N, *, mode="int", layout="kn", seed=1):
     return [_np(y) for y in Y.views], ref
 
 
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("R,M,K,N,layout", [
     (4, 512, 256, 512, "kn"),
     (2, 400, 200, 336, "kn"),       # ragged: 200-row shards, K 200, 168 columns per rank
     (3, 384, 64, 768, "nk"),
     (1, 256, 128, 256, "kn"),
+    (2, 1200, 136, 1040, "nk"),     # 600-row shards, 520 columns per rank
 ])
-def test_ag_gemm_integer_bit_exact(dev, R, M, K, N, layout):
-    got, ref = run_ag(dev, R, M, K, N, layout=layout)
+def test_ag_gemm_integer_bit_exact(dev, R, M, K, N, layout, tile):
+    got, ref = run_ag(dev, R, M, K, N, layout=layout, tile=tile)
     for r in range(R):
         assert np.array_equal(got[r], oracle.round_bf16(ref[r])), f"rank {r}"
 
@@ -213,9 +223,9 @@ def test_ag_gemm_random_bf16_within_tolerance(dev, R, M, K, N):
 
 # ------------------------------------------------------------------ DP grad
 
-def run_dp(dev, R, T, M, N, *, mode="int", seed=3):
+def run_dp(dev, R, T, M, N, *, mode="int", seed=3, tile="auto"):
     inp = dp_grad_inputs(R, T, M, N, mode=mode, seed=seed)
-    plan = B.fo_plan("dp_grad_rs", R, M, N, T)
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T, tile_config=tile)
     X = [x.to(dev) for x in inp["X"]]
     dY = [y.to(dev) for y in inp["dY"]]
     dW = Guarded(R, (M // R, N), torch.float32, dev)
@@ -227,9 +237,10 @@ def run_dp(dev, R, T, M, N, *, mode="int", seed=3):
     return [_np(w) for w in dW.views], ref
 
 
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("R,T,M,N", [(2, 256, 256, 256), (4, 200, 800, 328), (8, 128, 1024, 256)])
-def test_dp_grad_rs_integer_bit_exact(dev, R, T, M, N):
-    got, ref = run_dp(dev, R, T, M, N)
+def test_dp_grad_rs_integer_bit_exact(dev, R, T, M, N, tile):
+    got, ref = run_dp(dev, R, T, M, N, tile=tile)
     for d in range(R):
         assert np.array_equal(got[d], ref[d]), f"shard {d}"
 
