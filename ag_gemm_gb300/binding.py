@@ -27,13 +27,14 @@ TRANSPORTS = {"peer_read": 0, "copy": 1}
 W_LAYOUTS = {"kn": 0, "nk": 1}
 INJECT = {"none": 0, "drop_transfer": 1, "skip_signal": 2}
 TILE_CONFIGS = {"auto": 0, "single": 1}
+INTERLEAVES = {"auto": 0, "lockstep": 1, "skewed": 2}
 
 # Every symbol include/flashoverlap.h declares.
 EXPORTED = [
     "fo_plan", "fo_plan_destroy", "fo_plan_table", "fo_plan_transfers", "fo_plan_edges",
     "fo_workspace_size", "fo_workspace_init", "fo_ag_gemm", "fo_gemm_rs", "fo_dp_grad_rs",
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
-    "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc",
+    "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc", "fo_plan_task_order",
 ]
 
 
@@ -52,7 +53,7 @@ class PlanDesc(ctypes.Structure):
         ("op", c_int32), ("R", c_int32), ("M", c_int64), ("N", c_int64), ("K", c_int64),
         ("in_dtype", c_int32), ("out_dtype", c_int32), ("sched", c_int32), ("ag_transport", c_int32),
         ("w_layout", c_int32), ("deterministic", c_int32), ("timeout_ns", c_uint64),
-        ("fault_inject", c_int32), ("tile_config", c_int32), ("reserved", c_int32 * 6),
+        ("fault_inject", c_int32), ("tile_config", c_int32), ("interleave", c_int32), ("reserved", c_int32 * 5),
     ]
 
 
@@ -75,6 +76,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_plan": ([POINTER(PlanDesc), POINTER(c_void_p)], c_int32),
         "fo_plan_destroy": ([P], None),
         "fo_plan_table": ([P, POINTER(c_int32)], c_int32),
+        "fo_plan_task_order": ([P, POINTER(c_int32)], c_int32),
         "fo_plan_transfers": ([P, POINTER(c_int32), c_int32, POINTER(c_int32)], c_int32),
         "fo_plan_edges": ([P, POINTER(c_int32), c_int32, POINTER(c_int32)], c_int32),
         "fo_workspace_size": ([P, POINTER(c_size_t)], c_int32),
@@ -161,7 +163,7 @@ class Plan:
 
 def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dtype=None,
             sched="rank_adaptive", ag_transport="peer_read", w_layout="kn", deterministic=False,
-            timeout_ns=0, fault_inject="none", tile_config="auto") -> Plan:
+            timeout_ns=0, fault_inject="none", tile_config="auto", interleave="auto") -> Plan:
     lib = load()
     if out_dtype is None:
         out_dtype = "bf16" if op == "ag_gemm" else "f32"
@@ -178,6 +180,7 @@ def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dty
     d.timeout_ns = timeout_ns
     d.fault_inject = INJECT[fault_inject]
     d.tile_config = TILE_CONFIGS[tile_config]
+    d.interleave = INTERLEAVES[interleave]
     h = c_void_p()
     _check(lib.fo_plan(ctypes.byref(d), ctypes.byref(h)), "fo_plan")
     return Plan(h.value, d)
@@ -194,6 +197,14 @@ def fo_plan_table(plan: Plan) -> List[List[int]]:
     buf = (c_int32 * (R * R))()
     _check(load().fo_plan_table(plan, buf), "fo_plan_table")
     return [[buf[r * R + s] for s in range(R)] for r in range(R)]
+
+
+def fo_plan_task_order(plan: Plan):
+    """[(rank, step), ...] in the order the kernel runs the chunk tasks."""
+    n = plan.R * plan.R
+    buf = (c_int32 * (2 * n))()
+    _check(load().fo_plan_task_order(plan, buf), "fo_plan_task_order")
+    return [(buf[2 * i], buf[2 * i + 1]) for i in range(n)]
 
 
 def _quads(fn, plan: Plan, what: str):

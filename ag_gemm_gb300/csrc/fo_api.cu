@@ -88,11 +88,11 @@ enum CallKind { KIND_NONE = 0, KIND_RS = 1, KIND_DP = 2, KIND_AG = 3, KIND_PART 
 // Returns the cached parameter block when the same call kind is made with
 // the same pointers again, else nullptr.
 fo::FoParams* cached_params(fo_plan_t p, int kind, const void* const* a, const void* const* b,
-                            const void* const* d) {
+                            const void* const* d, const void* const* g = nullptr) {
   if (!p->param_cache || p->param_cache_kind != kind) return nullptr;
   for (int r = 0; r < p->R; ++r)
     if (p->param_cache_key[r] != a[r] || p->param_cache_key[FO_MAX_R + r] != b[r] ||
-        p->param_cache_key[2 * FO_MAX_R + r] != d[r])
+        p->param_cache_key[2 * FO_MAX_R + r] != d[r] || p->param_cache_key[3 * FO_MAX_R + r] != (g ? g[r] : nullptr))
       return nullptr;
   return static_cast<fo::FoParams*>(p->param_cache);
 }
@@ -108,11 +108,13 @@ fo::FoParams* fresh_params(fo_plan_t p) {
   return static_cast<fo::FoParams*>(p->param_cache);
 }
 
-void remember(fo_plan_t p, int kind, const void* const* a, const void* const* b, const void* const* d) {
+void remember(fo_plan_t p, int kind, const void* const* a, const void* const* b, const void* const* d,
+              const void* const* g = nullptr) {
   for (int r = 0; r < p->R; ++r) {
     p->param_cache_key[r] = a[r];
     p->param_cache_key[FO_MAX_R + r] = b[r];
     p->param_cache_key[2 * FO_MAX_R + r] = d[r];
+    p->param_cache_key[3 * FO_MAX_R + r] = g ? g[r] : nullptr;
   }
   p->param_cache_kind = kind;
 }
@@ -120,7 +122,8 @@ void remember(fo_plan_t p, int kind, const void* const* a, const void* const* b,
 void fill_common(fo_plan_t p, fo::FoParams* k, void* ws) {
   memcpy(k->table, p->table, sizeof(k->table));
   memcpy(k->ord, p->ord, sizeof(k->ord));
-  memcpy(k->rank_order, p->rank_order, sizeof(k->rank_order));
+  memcpy(k->task_r, p->task_r, sizeof(k->task_r));
+  memcpy(k->task_s, p->task_s, sizeof(k->task_s));
   k->R = p->R;
   k->tiles_m = p->tiles_m;
   k->ctr_tiles_m = p->ctr_tiles_m;
@@ -132,6 +135,11 @@ void fill_common(fo_plan_t p, fo::FoParams* k, void* ws) {
   k->counters = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + p->ws_counters_off);
   k->status = static_cast<int32_t*>(ws);
   k->timeout_ns = p->d.timeout_ns;
+  k->flags = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + p->ws_flags_off);
+  k->epoch = &static_cast<fo_ws_header*>(ws)->epoch;
+  k->pieces = p->pieces;
+  k->row_bytes = p->d.K * 2;
+  k->ag_copy = p->d.op == FO_OP_AG_GEMM && p->d.ag_transport == FO_AG_COPY ? 1 : 0;
 }
 
 fo_status check_ptrs(int R, const void* const* a) {
@@ -181,9 +189,9 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
   return FO_OK;
 }
 
-fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* ws,
-                   fo::FoParams** out) {
-  fo::FoParams* k = cached_params(p, KIND_AG, X, W, (const void* const*)Y);
+fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* const* G,
+                   void* ws, fo::FoParams** out) {
+  fo::FoParams* k = cached_params(p, KIND_AG, X, W, (const void* const*)Y, (const void* const*)G);
   if (k) {
     fill_common(p, k, ws);
     *out = k;
@@ -193,6 +201,7 @@ fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void
   if (!k) return FO_ERR_INVALID_ARG;
   const int R = p->R;
   const uint64_t K = (uint64_t)p->d.K, nr = (uint64_t)p->n_out, rpc = (uint64_t)p->rows_per_chunk;
+  const uint64_t M = (uint64_t)p->d.M;
   const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   bool ok = true;
   for (int r = 0; r < R && ok; ++r) {
@@ -200,9 +209,14 @@ fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void
     if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, W[r], nr, K, nr * 2, 64, 64);
     else ok &= enc2d(&k->tmB[r], dt, W[r], K, nr, K * 2, 64, p->pair ? FO_BN / 2 : FO_BN);
     ok &= enc3d(&k->tmD[r], dt, Y[r], nr, rpc, R, nr * 2, rpc * nr * 2, 64, 32);
+    if (G) {
+      ok &= enc2d(&k->tmG[r], dt, G[r], K, M, K * 2, 64, FO_BM);
+      k->xsrc[r] = X[r];
+      k->gdst[r] = G[r];
+    }
   }
   if (!ok) return FO_ERR_CUDA;
-  remember(p, KIND_AG, X, W, (const void* const*)Y);
+  remember(p, KIND_AG, X, W, (const void* const*)Y, (const void* const*)G);
   fill_common(p, k, ws);
   *out = k;
   return FO_OK;
@@ -382,17 +396,19 @@ fo_status fo_ag_gemm(fo_plan_t p, const void* const* X, const void* const* W, vo
                      void* ws, fo_stream_t stream) {
   if (!p || !ws) return FO_ERR_INVALID_ARG;
   if (p->d.op != FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
-  if (p->d.ag_transport != FO_AG_PEER_READ) return FO_ERR_UNSUPPORTED;
-  if (G) return FO_ERR_UNSUPPORTED;
+  if (p->d.ag_transport == FO_AG_COPY && !G) return FO_ERR_INVALID_ARG;   // the ring needs gather buffers
   fo_status st;
   if ((st = check_ptrs(p->R, X)) || (st = check_ptrs(p->R, W)) || (st = check_ptrs(p->R, (const void* const*)Y)))
     return st;
+  if (G && (st = check_ptrs(p->R, (const void* const*)G))) return st;
   if (!aligned16(ws)) return FO_ERR_ALIGN;
   DevInfo di;
   if ((st = preflight(p, &di))) return st;
   fo::FoParams* k = nullptr;
-  if ((st = build_ag(p, X, W, Y, ws, &k))) return st;
-  int v = p->d.w_layout == FO_W_KN ? FO_V_AG_BF16_KN : FO_V_AG_BF16_NK;
+  if ((st = build_ag(p, X, W, Y, G, ws, &k))) return st;
+  int v;
+  if (G) v = p->d.w_layout == FO_W_KN ? FO_V_AG_BF16_KN_MOV : FO_V_AG_BF16_NK_MOV;
+  else v = p->d.w_layout == FO_W_KN ? FO_V_AG_BF16_KN : FO_V_AG_BF16_NK;
   return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
 }
 
@@ -492,7 +508,9 @@ static cudaError_t fo_variant_call(int v, bool pair, const fo::FoParams* p, int 
     case FO_V_DP_BF16:
     case FO_V_PART_DP: return fo_variant_dp(v, pair, p, grid, s, ctas);
     case FO_V_AG_BF16_KN:
-    case FO_V_AG_BF16_NK: return fo_variant_ag(v, pair, p, grid, s, ctas);
+    case FO_V_AG_BF16_NK:
+    case FO_V_AG_BF16_KN_MOV:
+    case FO_V_AG_BF16_NK_MOV: return fo_variant_ag(v, pair, p, grid, s, ctas);
     case FO_V_PART_BF16_KN:
     case FO_V_PART_BF16_NK:
     case FO_V_PART_TF32_NK: return fo_variant_part(v, pair, p, grid, s, ctas);

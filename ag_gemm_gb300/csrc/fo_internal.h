@@ -27,12 +27,12 @@ struct fo_plan_s {
   // table[r][s]: chunk (RS/DP: owner of the partial) or source shard (AG)
   // handled by rank r at step s.
   int32_t table[FO_MAX_R][FO_MAX_R];
-  // rank_order[s][i]: the rank whose step-s tiles come i-th among the ranks
-  // of step s in the kernel's tile order. Ranks within a step are
-  // independent; RS/DP alternate the direction from step to step so that the
-  // shards written last in step s are the first ones written in step s+1
-  // (their lines are still in L2).
-  int32_t rank_order[FO_MAX_R][FO_MAX_R];
+  // task_r[i], task_s[i]: rank and step of the i-th chunk task in the
+  // kernel's order (see fo_interleave). Within one lockstep step the RS/DP
+  // ranks alternate direction from step to step, so the shards written last
+  // in step s are the first ones written in step s+1.
+  int32_t task_r[FO_MAX_R * FO_MAX_R];
+  int32_t task_s[FO_MAX_R * FO_MAX_R];
   // ord[r][s]: how many partials of the same chunk come before (r, s) in the
   // kernel's tile order; 0 = the first partial, which stores instead of adds.
   int32_t ord[FO_MAX_R][FO_MAX_R];
@@ -47,16 +47,17 @@ struct fo_plan_s {
   bool pair;               // CTA-pair 256 x 256 tiles (else single-CTA 128 x 256)
   int tiles_m, tiles_n, num_kb;   // tiles_m: m-tiles per chunk of the chosen tile height
   int ctr_tiles_m;         // 128-row tiles per chunk in the counter array (covers both heights)
+  int pieces;              // AG: 32-row pieces per shard (mover / ready-flag granularity)
 
   // Workspace layout.
   size_t ws_bytes;
   size_t ws_counters_off;  // RS/DP: uint32 [R][tiles_m*tiles_n][4]
-  size_t ws_flags_off;     // AG copy transport: uint32 [R][R][tiles_m]
+  size_t ws_flags_off;     // AG copy transport: uint32 [R][R][pieces]
 
   int32_t last_launches;
   void* param_cache;       // host copy of the last kernel parameter block
   int param_cache_kind;    // which call built it (0 = none)
-  const void* param_cache_key[4 * FO_MAX_R];  // the pointers it was built from
+  const void* param_cache_key[4 * FO_MAX_R];  // the pointers it was built from (X/A, W/B, Y/D, G)
 };
 
 // Workspace header (offset 0): device status word and launch epoch.

@@ -48,6 +48,11 @@ namespace fo {
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBuf = 32 * 128;              // 32 rows x 128 bytes
 constexpr int kThreads = 32 * (2 + kEpiWarps);
+// AG variants that also move X shards into the gather buffers G_r carry four
+// more warps; a piece is 32 rows of one shard.
+constexpr int kMoverWarps = 4;
+constexpr int kPieceRows = 32;
+__host__ __device__ constexpr int threads_for(bool movers) { return 32 * (2 + kEpiWarps + (movers ? kMoverWarps : 0)); }
 constexpr int kBarBytes = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kMbarLimitNs = 2000000000ull;
@@ -71,7 +76,8 @@ struct alignas(128) FoParams {
   CUtensorMap tmD[FO_MAX_R];   // RS/DP: Y_c (2-D); AG: Y_r (3-D); PARTIAL: P_r (3-D)
   int32_t table[FO_MAX_R][FO_MAX_R];
   int32_t ord[FO_MAX_R][FO_MAX_R];
-  int32_t rank_order[FO_MAX_R][FO_MAX_R];
+  int32_t task_r[FO_MAX_R * FO_MAX_R];   // rank and step of the i-th chunk task in execution order
+  int32_t task_s[FO_MAX_R * FO_MAX_R];
   int32_t R;
   int32_t tiles_m;             // m-tiles per chunk, of this kernel's tile height (128 or 256 rows)
   int32_t tiles_n;
@@ -83,6 +89,15 @@ struct alignas(128) FoParams {
   uint32_t* counters;          // RS/DP: [R][ctr_tiles_m][tiles_n][4]
   int32_t* status;             // fo_ws_header
   uint64_t timeout_ns;
+  // AG with a gather buffer (movers):
+  CUtensorMap tmG[FO_MAX_R];   // G_r [M x K]: the A operand of steps >= 1 under the copy transport
+  const void* xsrc[FO_MAX_R];  // X_r
+  void* gdst[FO_MAX_R];        // G_r
+  uint32_t* flags;             // copy transport: ready flags [R][R][pieces]
+  uint32_t* epoch;             // fo_ws_header::epoch (exit_count follows)
+  int64_t row_bytes;           // K * 2
+  int32_t pieces;              // 32-row pieces per shard
+  int32_t ag_copy;             // 1: shards reach G_r along the ring and the GEMM reads them there
 };
 
 template <bool A_MN, bool B_MN, bool TF32, bool PAIR>
@@ -104,8 +119,8 @@ __device__ __forceinline__ Tile decode_tile(const FoParams& p, int L) {
   const int task = L / tpt;
   const int t = L - task * tpt;
   Tile ti;
-  ti.s = task / p.R;
-  ti.r = p.rank_order[ti.s][task - ti.s * p.R];
+  ti.s = p.task_s[task];
+  ti.r = p.task_r[task];
   ti.mt = t / p.tiles_n;
   ti.nt = t - ti.mt * p.tiles_n;
   ti.c = p.table[ti.r][ti.s];
@@ -118,6 +133,27 @@ __device__ __forceinline__ Tile decode_tile(const FoParams& p, int L) {
 __device__ __forceinline__ void signal_partial(uint32_t* ctr, int R) {
   const uint32_t old = atom_add_release_u32(ctr, 1u);
   if (old + 1u == (uint32_t)R) atomicExch(ctr, 0u);
+}
+
+// Copy n16 16-byte words with nthr threads (thread tid handles words tid,
+// tid + nthr, ...), eight loads in flight per thread; L2-only caching.
+__device__ __forceinline__ void copy16(const uint8_t* from, uint8_t* to, size_t n16, int tid, int nthr) {
+  const uint4* s = reinterpret_cast<const uint4*>(from);
+  uint4* d = reinterpret_cast<uint4*>(to);
+  constexpr int U = 8;
+  size_t i = (size_t)tid;
+  for (; i + (size_t)(U - 1) * nthr < n16; i += (size_t)U * nthr) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = __ldcg(s + i + (size_t)u * nthr);
+#pragma unroll
+    for (int u = 0; u < U; ++u) __stcg(d + i + (size_t)u * nthr, v[u]);
+  }
+  for (; i < n16; i += nthr) __stcg(d + i, __ldcg(s + i));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Write 32 registers (one 128-byte row per thread) into a 32 x 128 B staging
@@ -134,8 +170,9 @@ __device__ __forceinline__ void stage_row_sw128(uint32_t buf, int lane, const ui
   }
 }
 
-template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid_constant__ FoParams p) {
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false>
+__global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(const __grid_constant__ FoParams p) {
+  static_assert(!MOV || EPI == EPI_AG, "movers belong to the all-gather kernel");
   using C = Cfg<PAIR>;
   constexpr int CG = PAIR ? 2 : 1;
   constexpr int kStages = C::kStages;
@@ -171,6 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
   const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const bool leader = prank == 0;
+  // Launch epoch of the copy transport's ready flags (read before this CTA
+  // can count itself out; the last CTA of the launch advances it).
+  const uint32_t epoch0 = MOV ? *reinterpret_cast<volatile uint32_t*>(p.epoch) : 0u;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -211,8 +251,29 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
         const CUtensorMap* mB = &p.tmB[ti.r];
         // Row (or column, for MN-major A) where this CTA's A block starts,
         // and the first output column of its B block.
-        const int a_mn0 = (EPI == EPI_AG ? 0 : ti.c * p.rows_per_chunk) + ti.mt * C::kTileM + (int)prank * FO_BM;
+        int a_mn0 = (EPI == EPI_AG ? 0 : ti.c * p.rows_per_chunk) + ti.mt * C::kTileM + (int)prank * FO_BM;
         const int b_n0 = ti.nt * FO_BN + (int)prank * C::kBRows;
+        if constexpr (MOV) {
+          if (p.ag_copy && ti.s > 0) {
+            // Copy transport: this shard reached G_r along the ring. Wait
+            // until the pieces holding this CTA's 128 rows are ready.
+            const int r0 = ti.mt * C::kTileM + (int)prank * FO_BM;
+            const int p0 = r0 / kPieceRows;
+            const int p1 = min(p.pieces, (r0 + FO_BM + kPieceRows - 1) / kPieceRows);
+            bool good = true;
+            for (int pc = p0; pc < p1 && good; ++pc)
+              good = wait_flag_eq(&p.flags[((size_t)ti.r * p.R + ti.c) * p.pieces + pc], epoch0 + 1u, p.timeout_ns,
+                                  abort_flag, gstatus);
+            if (!good) {
+              if (!*abort_flag && !*gstatus) record_error(p.status, FO_ERR_TIMEOUT, ti.r, ti.s, ti.c);
+              *abort_flag = 1;
+              break;
+            }
+            fence_proxy_async_global();
+            mA = &p.tmG[ti.r];
+            a_mn0 = ti.c * p.rows_per_chunk + r0;
+          }
+        }
         bool ok = true;
         for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
           const int stage = it % kStages;
@@ -319,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
       volatile int never = 0;
       mbar_wait(mma_done_bar, 0, &never, 100000000ull);
     }
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;        // staging buffers of this warp
     const int q = warp & 3;        // TMEM lane quarter this warp may access
@@ -485,6 +546,45 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
     __syncwarp();
   }
 
+  if constexpr (MOV) {
+    if (warp >= 2 + kEpiWarps) {
+      // ---------------------------------------------------------- movers
+      // Shard pieces into the gather buffers, 128-bit copies. Piece (src,
+      // pc) always belongs to the same CTA, so along the ring each copy reads
+      // what this CTA's movers wrote one step earlier (same threads, same
+      // bytes). Copy transport: rank r's piece of shard src = table[r][s]
+      // comes from X_r at step 0 and from G_{r-1} after; a release flag per
+      // piece tells the GEMM it is there. Peer-read transport: G_r[src] is a
+      // side output copied straight from X_src. Movers never wait.
+      const int mtid = threadIdx.x - 32 * (2 + kEpiWarps);
+      constexpr int kMovThreads = 32 * kMoverWarps;
+      const int R = p.R;
+      const size_t rb = (size_t)p.row_bytes;
+      const int rpc = p.rows_per_chunk;
+      for (int s = 0; s < R; ++s) {
+        for (int r = 0; r < R; ++r) {
+          const int src = p.table[r][s];
+          for (int pc = 0; pc < p.pieces; ++pc) {
+            if ((src * p.pieces + pc) % (int)gridDim.x != (int)blockIdx.x) continue;
+            const int rows = min(kPieceRows, rpc - pc * kPieceRows);
+            const size_t shard_off = ((size_t)src * rpc + (size_t)pc * kPieceRows) * rb;
+            const uint8_t* from = (p.ag_copy && s > 0)
+                                      ? static_cast<const uint8_t*>(p.gdst[(r + R - 1) % R]) + shard_off
+                                      : static_cast<const uint8_t*>(p.xsrc[src]) + (size_t)pc * kPieceRows * rb;
+            uint8_t* to = static_cast<uint8_t*>(p.gdst[r]) + shard_off;
+            copy16(from, to, (size_t)rows * rb / 16, mtid, kMovThreads);
+            if (p.ag_copy) {
+              __threadfence();
+              named_bar_sync(1, kMovThreads);
+              const bool skip = p.fault_inject == FO_INJECT_SKIP_SIGNAL && R > 1 && r == 1 && s == 1 && pc == 0;
+              if (mtid == 0 && !skip) st_release_u32(&p.flags[((size_t)r * R + src) * p.pieces + pc], epoch0 + 1u);
+            }
+          }
+        }
+      }
+    }
+  }
+
   tc_fence_before();
   if constexpr (PAIR) cluster_sync_all();   // neither CTA leaves while the pair still uses its memory
   else __syncthreads();
@@ -492,6 +592,18 @@ __global__ void __launch_bounds__(kThreads, 1) fo_chunk_gemm_kernel(const __grid
     tc_fence_after();
     __syncwarp();
     tmem_dealloc<CG>(tmem_base, kTmemCols);
+  }
+  if constexpr (MOV) {
+    // The last CTA of the launch advances the flag epoch for the next call.
+    if (threadIdx.x == 0 && p.ag_copy) {
+      __threadfence();
+      const uint32_t done = atomicAdd(p.epoch + 1, 1u);
+      if (done == gridDim.x - 1) {
+        atomicExch(p.epoch + 1, 0u);
+        __threadfence();
+        atomicAdd(p.epoch, 1u);
+      }
+    }
   }
 }
 
@@ -509,6 +621,8 @@ enum fo_variant {
   FO_V_PART_BF16_NK,
   FO_V_PART_TF32_NK,
   FO_V_PART_DP,
+  FO_V_AG_BF16_KN_MOV,
+  FO_V_AG_BF16_NK_MOV,
   FO_V_COUNT
 };
 

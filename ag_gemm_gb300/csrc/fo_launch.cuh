@@ -3,15 +3,15 @@
 
 #include "fo_kernel.cuh"
 
-template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR>
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false>
 cudaError_t fo_launch_one(const fo::FoParams& p, int grid, cudaStream_t stream) {
-  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR>;
+  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV>;
   constexpr int smem = fo::Cfg<PAIR>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(fo::kThreads);
+  cfg.blockDim = dim3(fo::threads_for(MOV));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -34,9 +34,9 @@ cudaError_t fo_launch_one(const fo::FoParams& p, int grid, cudaStream_t stream) 
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR>
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false>
 cudaError_t fo_max_ctas_one(int* ctas) {
-  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR>;
+  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV>;
   constexpr int smem = fo::Cfg<PAIR>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -46,7 +46,7 @@ cudaError_t fo_max_ctas_one(int* ctas) {
   if constexpr (PAIR) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(2 * sms));
-    cfg.blockDim = dim3(fo::kThreads);
+    cfg.blockDim = dim3(fo::threads_for(MOV));
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -60,7 +60,8 @@ cudaError_t fo_max_ctas_one(int* ctas) {
     *ctas = 2 * clusters;
   } else {
     int per_sm = 0;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, fo::kThreads, smem)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, fo::threads_for(MOV), smem)) != cudaSuccess)
+      return e;
     *ctas = per_sm * sms;
   }
   return cudaSuccess;
@@ -76,3 +77,8 @@ cudaError_t fo_max_ctas_one(int* ctas) {
   (pair ? cudaErrorInvalidValue                                                               \
         : (ctas ? fo_max_ctas_one<EPI, A_MN, B_MN, TF32, false>(ctas)                         \
                 : fo_launch_one<EPI, A_MN, B_MN, TF32, false>(*p, grid, s)))
+#define FO_DISPATCH_PAIR_MOV(EPI, A_MN, B_MN, TF32)                                          \
+  (pair ? (ctas ? fo_max_ctas_one<EPI, A_MN, B_MN, TF32, true, true>(ctas)                    \
+                : fo_launch_one<EPI, A_MN, B_MN, TF32, true, true>(*p, grid, s))               \
+        : (ctas ? fo_max_ctas_one<EPI, A_MN, B_MN, TF32, false, true>(ctas)                   \
+                : fo_launch_one<EPI, A_MN, B_MN, TF32, false, true>(*p, grid, s)))

@@ -45,20 +45,44 @@ void build_table(fo_plan_s* p) {
       else if (ag) p->table[r][s] = ((r - s) % R + R) % R;
       else p->table[r][s] = ((r - 1 - s) % R + 2 * R) % R;
     }
-  // Order of the ranks inside each step. Step s+1 writes its shards in the
-  // reverse of the order step s wrote them (RS/DP), so the most recently
-  // written shards are reused first.
-  for (int i = 0; i < R; ++i) p->rank_order[0][i] = i;
-  for (int s = 0; s + 1 < R; ++s)
-    for (int i = 0; i < R; ++i)
-      p->rank_order[s + 1][i] = ag ? i : (p->rank_order[s][R - 1 - i] + 1) % R;
+  // The kernel's task order.
+  int skew = p->d.interleave;
+  if (skew == FO_INTERLEAVE_AUTO) skew = ag ? FO_INTERLEAVE_LOCKSTEP : FO_INTERLEAVE_SKEWED;
+  int n = 0;
+  if (skew == FO_INTERLEAVE_SKEWED) {
+    // Slot t = s - r (rank r runs r steps behind rank 0); inside a slot by
+    // ascending step, so every shard receives its partials in step order.
+    for (int t = -(R - 1); t <= R - 1; ++t)
+      for (int s = 0; s < R; ++s) {
+        const int r = s - t;
+        if (r < 0 || r >= R) continue;
+        p->task_r[n] = r;
+        p->task_s[n] = s;
+        ++n;
+      }
+  } else {
+    // Lockstep; RS/DP ranks alternate direction from step to step.
+    int order[FO_MAX_R];
+    for (int i = 0; i < R; ++i) order[i] = i;
+    for (int s = 0; s < R; ++s) {
+      for (int i = 0; i < R; ++i) {
+        p->task_r[n] = order[i];
+        p->task_s[n] = s;
+        ++n;
+      }
+      if (!ag) {
+        int next[FO_MAX_R];
+        for (int i = 0; i < R; ++i) next[i] = (order[R - 1 - i] + 1) % R;
+        for (int i = 0; i < R; ++i) order[i] = next[i];
+      }
+    }
+  }
   // Contribution order of every (r, s) into its chunk, in the kernel's order.
   int seen[FO_MAX_R] = {0};
-  for (int s = 0; s < R; ++s)
-    for (int i = 0; i < R; ++i) {
-      const int r = p->rank_order[s][i];
-      p->ord[r][s] = seen[p->table[r][s]]++;
-    }
+  for (int i = 0; i < R * R; ++i) {
+    const int r = p->task_r[i], s = p->task_s[i];
+    p->ord[r][s] = seen[p->table[r][s]]++;
+  }
 }
 
 void build_transfers_and_edges(fo_plan_s* p) {
@@ -171,7 +195,8 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (d->w_layout != FO_W_KN && d->w_layout != FO_W_NK) return FO_ERR_INVALID_ARG;
   if (d->fault_inject < FO_INJECT_NONE || d->fault_inject > FO_INJECT_SKIP_SIGNAL) return FO_ERR_INVALID_ARG;
   if (d->tile_config != FO_TILE_AUTO && d->tile_config != FO_TILE_SINGLE) return FO_ERR_INVALID_ARG;
-  for (int i = 0; i < 6; ++i)
+  if (d->interleave < FO_INTERLEAVE_AUTO || d->interleave > FO_INTERLEAVE_SKEWED) return FO_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
     if (d->reserved[i]) return FO_ERR_INVALID_ARG;
   if (d->M <= 0 || d->N <= 0 || d->K <= 0) return FO_ERR_SHAPE;
   const int R = d->R;
@@ -227,6 +252,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   p->pair = eb == 2 && d->tile_config == FO_TILE_AUTO;
   p->tiles_m = (int)cdiv(p->rows_per_chunk, p->pair ? 2 * FO_BM : FO_BM);
   p->ctr_tiles_m = 2 * (int)cdiv(p->rows_per_chunk, 2 * FO_BM);
+  p->pieces = (int)cdiv(p->rows_per_chunk, 32);
   p->tiles_n = (int)cdiv(p->n_out, FO_BN);
   p->num_kb = (int)cdiv(p->k_red * eb, FO_BK_BYTES);
   if ((int64_t)R * R * p->tiles_m * p->tiles_n > ((int64_t)1 << 31) - 1) {
@@ -244,7 +270,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   p->ws_counters_off = off;
   p->ws_flags_off = off;
   if (d->op == FO_OP_AG_GEMM) {
-    off += align_up((size_t)R * R * p->tiles_m * sizeof(uint32_t), 256);
+    off += align_up((size_t)R * R * p->pieces * sizeof(uint32_t), 256);
   } else {
     off += align_up((size_t)R * p->ctr_tiles_m * p->tiles_n * 4 * sizeof(uint32_t), 256);
   }
@@ -265,6 +291,15 @@ fo_status fo_plan_table(fo_plan_t p, int32_t* table) {
   if (!p || !table) return FO_ERR_INVALID_ARG;
   for (int r = 0; r < p->R; ++r)
     for (int s = 0; s < p->R; ++s) table[r * p->R + s] = p->table[r][s];
+  return FO_OK;
+}
+
+fo_status fo_plan_task_order(fo_plan_t p, int32_t* order) {
+  if (!p || !order) return FO_ERR_INVALID_ARG;
+  for (int i = 0; i < p->R * p->R; ++i) {
+    order[2 * i] = p->task_r[i];
+    order[2 * i + 1] = p->task_s[i];
+  }
   return FO_OK;
 }
 

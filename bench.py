@@ -448,7 +448,18 @@ def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
     cub = _time(cublas, stream)
     del P
     torch.cuda.empty_cache()
+    # Schedule ablation: the data-slicing order (every rank on slice s at
+    # step s) instead of the rank-adaptive one, same kernel otherwise.
+    sl_plan = B.fo_plan("gemm_rs", R, M, N, X[0].shape[1] * R, sched="sliced")
+    sl_ws = torch.zeros(B.fo_workspace_size(sl_plan), dtype=torch.uint8, device=dev)
+    sliced = _time(lambda: B.fo_gemm_rs(sl_plan, X, W, Y, sl_ws, stream), stream)
+    # Single-CTA 128 x 256 tiles instead of CTA-pair 256 x 256 tiles.
+    one_plan = B.fo_plan("gemm_rs", R, M, N, X[0].shape[1] * R, tile_config="single")
+    one_ws = torch.zeros(B.fo_workspace_size(one_plan), dtype=torch.uint8, device=dev)
+    single = _time(lambda: B.fo_gemm_rs(one_plan, X, W, Y, one_ws, stream), stream)
     return {
+        "sliced_schedule_ms": sliced, "sliced_schedule_tflops": flops / sliced / 1e9,
+        "single_cta_tiles_ms": single, "single_cta_tiles_tflops": flops / single / 1e9,
         "fused_ms": fused, "fused_tflops": flops / fused / 1e9,
         "pure_gemm_control_ms": pure, "pure_gemm_control_tflops": flops / pure / 1e9,
         "exposed_move_pct": 100.0 * (fused - pure) / pure,

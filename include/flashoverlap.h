@@ -97,6 +97,18 @@ typedef enum { FO_INJECT_NONE = 0, FO_INJECT_DROP_TRANSFER = 1, FO_INJECT_SKIP_S
  * the same results; SINGLE exists for small problems and for comparison. */
 typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
 
+/* How the one GPU interleaves the R virtual ranks' step sequences. Every
+ * choice runs each rank's tasks in that rank's schedule order and respects
+ * the dependency graph; only the order across ranks differs.
+ * LOCKSTEP: all ranks' step s, then step s+1 (the ranks advance together, as
+ *           R GPUs would).
+ * SKEWED:   rank r runs r steps behind rank 0 (slot t = s - r). Under the
+ *           rank-adaptive RS order every partial of one slot is bound for the
+ *           same owner, so that owner's shard stays in L2 while its partials
+ *           are added.
+ * AUTO:     SKEWED for GEMM_RS / DP_GRAD_RS, LOCKSTEP for AG_GEMM. */
+typedef enum { FO_INTERLEAVE_AUTO = 0, FO_INTERLEAVE_LOCKSTEP = 1, FO_INTERLEAVE_SKEWED = 2 } fo_interleave;
+
 /* Global GEMM sizes (M, N, K); the per-rank operands are, for each op:
  *   FO_OP_GEMM_RS    X_r [M x K/R], W_r [K/R x N] (or [N x K/R]), Y_r [M/R x N] fp32
  *   FO_OP_AG_GEMM    X_r [M/R x K], W_r [K x N/R] (or [N/R x K]), Y_r [M x N/R] bf16,
@@ -119,7 +131,8 @@ typedef struct {
   uint64_t timeout_ns;        /* bound of every device-side wait; 0 = 1 s */
   int32_t fault_inject;       /* fo_inject (tests only) */
   int32_t tile_config;        /* fo_tile_config */
-  int32_t reserved[6];        /* must be zero */
+  int32_t interleave;         /* fo_interleave */
+  int32_t reserved[5];        /* must be zero */
 } fo_plan_desc;
 
 typedef struct fo_plan_s* fo_plan_t;
@@ -149,6 +162,10 @@ fo_status fo_plan_transfers(fo_plan_t plan, int32_t* out, int32_t cap, int32_t* 
  * step_b) meaning task (rank_a, step_a) must finish before (rank_b, step_b)
  * may complete. `cap` in edges; *n gets the count. */
 fo_status fo_plan_edges(fo_plan_t plan, int32_t* out, int32_t cap, int32_t* n);
+
+/* Copy out the order in which the kernel runs the R*R chunk tasks:
+ * order[2*i] = rank, order[2*i+1] = step of the i-th task. */
+fo_status fo_plan_task_order(fo_plan_t plan, int32_t* order);
 
 /* Bytes of device workspace the launching calls need (readiness counters,
  * flags and the device status word). Never zero. */

@@ -151,3 +151,49 @@ def test_workspace_counts_pair_tiles():
     # 600-row chunks: 3 single-CTA m-tiles, 2 pair m-tiles = 4 128-row counter rows.
     p = B.fo_plan("gemm_rs", 2, 1200, 512, 512)
     assert B.fo_workspace_size(p) >= 256 + 2 * 4 * 2 * 4 * 4
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("op", ["gemm_rs", "ag_gemm", "dp_grad_rs"])
+@pytest.mark.parametrize("interleave", ["auto", "lockstep", "skewed"])
+def test_task_order_keeps_every_ranks_schedule_order(R, op, interleave):
+    dims = {"gemm_rs": (128 * R, 256, 64 * R), "ag_gemm": (128 * R, 64 * R, 256), "dp_grad_rs": (8 * R, 256, 64)}[op]
+    p = B.fo_plan(op, R, *dims, interleave=interleave)
+    order = B.fo_plan_task_order(p)
+    assert sorted(order) == [(r, s) for r in range(R) for s in range(R)]
+    for r in range(R):
+        steps = [s for (rr, s) in order if rr == r]
+        assert steps == list(range(R))            # each rank runs its own steps in order
+
+
+@pytest.mark.parametrize("R", [2, 3, 4, 8])
+def test_skewed_order_groups_partials_by_owner_in_step_order(R):
+    p = B.fo_plan("gemm_rs", R, 128 * R, 256, 64 * R, interleave="skewed")
+    order = B.fo_plan_task_order(p)
+    table = oracle.rs_schedule(R)
+    chunks = [int(table[r, s]) for (r, s) in order]
+    # runs of equal owners: slots t = s - r; every slot sends to one owner
+    slots = {}
+    for (r, s), c in zip(order, chunks):
+        slots.setdefault(s - r, set()).add(c)
+    assert all(len(v) == 1 for v in slots.values())
+    # every owner gets its partials in step order (first partial stored first)
+    for c in range(R):
+        steps = [s for (r, s), cc in zip(order, chunks) if cc == c]
+        assert steps == sorted(steps) == list(range(R))
+
+
+def test_auto_interleave_is_skewed_for_rs_and_lockstep_for_ag():
+    R = 4
+    rs = B.fo_plan_task_order(B.fo_plan("gemm_rs", R, 512, 256, 256))
+    assert rs == B.fo_plan_task_order(B.fo_plan("gemm_rs", R, 512, 256, 256, interleave="skewed"))
+    ag = B.fo_plan_task_order(B.fo_plan("ag_gemm", R, 512, 256, 256))
+    assert ag == [(r, s) for s in range(R) for r in range(R)]
+
+
+def test_copy_transport_requires_gather_buffers():
+    p = B.fo_plan("ag_gemm", 2, 256, 256, 256, ag_transport="copy")
+    fake = [16 * (i + 1) for i in range(2)]
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_ag_gemm(p, fake, fake, fake, None, 4096, stream=0)
+    assert e.value.code == B.FO_ERR_INVALID_ARG

@@ -70,10 +70,10 @@ def _status_ok(plan, ws):
 
 
 def run_gemm_rs(dev, R, M, K, N, *, dtype="bf16", mode="int", w_layout="kn", seed=0, sched="rank_adaptive",
-                deterministic=False, repeat=1, tile="auto"):
+                deterministic=False, repeat=1, tile="auto", interleave="auto"):
     inp = gemm_rs_inputs(R, M, K, N, dtype=dtype, mode=mode, seed=seed)
     plan = B.fo_plan("gemm_rs", R, M, N, K * R, in_dtype=dtype, w_layout=w_layout, sched=sched,
-                     deterministic=deterministic, tile_config=tile)
+                     deterministic=deterministic, tile_config=tile, interleave=interleave)
     X = [x.to(dev) for x in inp["X"]]
     W = [(w if w_layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
     Y = Guarded(R, (M // R, N), torch.float32, dev)
@@ -137,6 +137,16 @@ def test_gemm_rs_deterministic_mode_is_bitwise_repeatable(dev):
             assert np.array_equal(rep[d], outs[0][d])
     for d in range(4):
         _assert_close(outs[0][d], ref[d])
+
+
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("interleave", ["lockstep", "skewed"])
+@pytest.mark.parametrize("det", [False, True])
+def test_gemm_rs_every_interleave_bit_exact(dev, tile, interleave, det):
+    outs, ref = run_gemm_rs(dev, 8, 2048, 136, 776, tile=tile, interleave=interleave, deterministic=det, repeat=2)
+    for rep in outs:
+        for d in range(8):
+            assert np.array_equal(rep[d], ref[d])
 
 
 def test_gemm_rs_repeated_calls_reuse_workspace(dev):
@@ -214,6 +224,60 @@ def test_ag_gemm_integer_bit_exact(dev, R, M, K, N, layout, tile):
         assert np.array_equal(got[r], oracle.round_bf16(ref[r])), f"rank {r}"
 
 
+def run_ag_gather(dev, R, M, K, N, *, transport, tile="auto", layout="kn", seeds=(1,), inject="none", timeout_ns=0):
+    plan = B.fo_plan("ag_gemm", R, M, N, K, w_layout=layout, tile_config=tile, ag_transport=transport,
+                     fault_inject=inject, timeout_ns=timeout_ns)
+    ws = _ws(plan, dev)
+    Y = Guarded(R, (M, N // R), torch.bfloat16, dev)
+    G = Guarded(R, (M, K), torch.bfloat16, dev)
+    X = [torch.empty(M // R, K, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    W = [torch.empty((K, N // R) if layout == "kn" else (N // R, K), dtype=torch.bfloat16, device=dev)
+         for _ in range(R)]
+    results = []
+    for seed in seeds:
+        inp = ag_gemm_inputs(R, M, K, N // R, mode="int", seed=seed)
+        for r in range(R):        # same buffers, new contents: stale data from a previous call must not pass
+            X[r].copy_(inp["X"][r])
+            W[r].copy_(inp["W"][r] if layout == "kn" else inp["W"][r].t())
+        B.fo_ag_gemm(plan, X, W, Y.views, G.views, ws)
+        code, info = B.fo_status_query(plan, ws)
+        results.append((code, info, [_np(y) for y in Y.views], [_np(g) for g in G.views], inp))
+    Y.check()
+    G.check()
+    return results
+
+
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("transport", ["copy", "peer_read"])
+@pytest.mark.parametrize("R,M,K,N,layout", [(4, 1024, 256, 512, "kn"), (2, 400, 200, 336, "nk"),
+                                             (3, 600, 136, 768, "kn")])
+def test_ag_gemm_gather_buffers_bit_exact(dev, tile, transport, R, M, K, N, layout):
+    # copy: shards travel the ring into G_r and the GEMM of steps >= 1 reads
+    # them there; peer_read: G_r is a side output. Either way Y_r and G_r are
+    # exact; two calls in a row with new inputs on one workspace.
+    for code, info, Y, G, inp in run_ag_gather(dev, R, M, K, N, transport=transport, tile=tile, layout=layout,
+                                               seeds=(1, 2)):
+        assert code == 0, info
+        ref, gathered = oracle.ag_gemm([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+        for r in range(R):
+            assert np.array_equal(Y[r], oracle.round_bf16(ref[r])), f"Y rank {r}"
+            assert np.array_equal(G[r], gathered), f"G rank {r}"
+
+
+def test_ag_copy_missing_ready_flag_times_out(dev):
+    R, M, K, N = 2, 512, 128, 512
+    (code, info, _, _, _), = run_ag_gather(dev, R, M, K, N, transport="copy", inject="skip_signal",
+                                           timeout_ns=20_000_000)
+    assert code == B.FO_ERR_TIMEOUT
+    assert info == [B.FO_ERR_TIMEOUT, 1, 1, 0]      # rank 1 waits at step 1 for shard 0
+    # the workspace was reset by the status query: a clean plan runs exactly
+    (code, info, Y, G, inp), = run_ag_gather(dev, R, M, K, N, transport="copy")
+    assert code == 0
+    ref, gathered = oracle.ag_gemm([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for r in range(R):
+        assert np.array_equal(Y[r], oracle.round_bf16(ref[r]))
+
+
 @pytest.mark.parametrize("R,M,K,N", [(4, 1024, 512, 1024), (2, 400, 200, 336)])
 def test_ag_gemm_random_bf16_within_tolerance(dev, R, M, K, N):
     got, ref = run_ag(dev, R, M, K, N, mode="randn")
@@ -223,9 +287,9 @@ def test_ag_gemm_random_bf16_within_tolerance(dev, R, M, K, N):
 
 # ------------------------------------------------------------------ DP grad
 
-def run_dp(dev, R, T, M, N, *, mode="int", seed=3, tile="auto"):
+def run_dp(dev, R, T, M, N, *, mode="int", seed=3, tile="auto", interleave="auto"):
     inp = dp_grad_inputs(R, T, M, N, mode=mode, seed=seed)
-    plan = B.fo_plan("dp_grad_rs", R, M, N, T, tile_config=tile)
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T, tile_config=tile, interleave=interleave)
     X = [x.to(dev) for x in inp["X"]]
     dY = [y.to(dev) for y in inp["dY"]]
     dW = Guarded(R, (M // R, N), torch.float32, dev)
@@ -243,6 +307,13 @@ def test_dp_grad_rs_integer_bit_exact(dev, R, T, M, N, tile):
     got, ref = run_dp(dev, R, T, M, N, tile=tile)
     for d in range(R):
         assert np.array_equal(got[d], ref[d]), f"shard {d}"
+
+
+@pytest.mark.parametrize("interleave", ["lockstep", "skewed"])
+def test_dp_grad_rs_interleaves_bit_exact(dev, interleave):
+    got, ref = run_dp(dev, 4, 200, 800, 328, interleave=interleave)
+    for d in range(4):
+        assert np.array_equal(got[d], ref[d])
 
 
 def test_dp_grad_rs_random_bf16_within_tolerance(dev):
