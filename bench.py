@@ -333,7 +333,12 @@ def run_ours(args):
     value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
     ms_per_step = elapsed_ms / args.steps
     achieved = flops / (kernel_ms * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops"])
+    # A timed region of a quarter second or more of back-to-back launches
+    # runs under the power cap: compare with the sustained measured peak;
+    # shorter bursts with the burst peak.
+    sustained = elapsed_ms >= 250.0
+    peak = float(peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"])
+    peak_name = "bf16_tflops_sustained" if sustained else "bf16_tflops (burst)"
 
     # End to end through the public API with host buffers: pinned host inputs
     # copied in, the fused call, the shards copied back, every step.
@@ -382,8 +387,8 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "traffic": args.traffic if args.traffic is not None else profiled_traffic(w.name),
-                     "peak_source": f"bf16_tflops burst, {peak_src}",
-                     "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))},
+                     "peak_source": f"{peak_name}, {peak_src}",
+                     "frac_of_burst_peak": achieved / float(peaks["bf16_tflops"])},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk.summary(),
