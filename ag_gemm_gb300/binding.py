@@ -20,7 +20,7 @@ FO_OK, FO_ERR_INVALID_ARG, FO_ERR_SHAPE, FO_ERR_DTYPE, FO_ERR_ALIGN = 0, 1, 2, 3
 FO_ERR_UNSUPPORTED, FO_ERR_CUDA, FO_ERR_TIMEOUT, FO_ERR_PLAN_INVARIANT = 5, 6, 7, 8
 FO_ERR_SCRATCH_LIMIT = 9
 FO_NOALLOC_SCRATCH_BYTES = 64 * 1024
-OPS = {"ag_gemm": 0, "gemm_rs": 1, "dp_grad_rs": 2}
+OPS = {"ag_gemm": 0, "gemm_rs": 1, "dp_grad_rs": 2, "gemm_ar": 3}
 DTYPES = {"bf16": 0, "f32": 1}
 SCHEDS = {"rank_adaptive": 0, "sliced": 1}
 TRANSPORTS = {"peer_read": 0, "copy": 1}
@@ -35,6 +35,7 @@ EXPORTED = [
     "fo_workspace_size", "fo_workspace_init", "fo_ag_gemm", "fo_gemm_rs", "fo_dp_grad_rs",
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
     "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc", "fo_plan_task_order",
+    "fo_gemm_ar",
 ]
 
 
@@ -85,6 +86,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_gemm_rs": ([P, PP, PP, PP, P, P], c_int32),
         "fo_dp_grad_rs": ([P, PP, PP, PP, P, P], c_int32),
         "fo_gemm_rs_noalloc": ([P, PP, PP, PP, P], c_int32),
+        "fo_gemm_ar": ([P, PP, PP, PP, P, P], c_int32),
         "fo_status_query": ([P, P, P, POINTER(c_int32)], c_int32),
         "fo_gemm_partials": ([P, PP, PP, PP, P, P], c_int32),
         "fo_reduce_scatter_f32": ([P, PP, PP, P], c_int32),
@@ -237,6 +239,11 @@ def fo_workspace_init(plan: Plan, ws, stream=None) -> None:
 def fo_gemm_rs(plan: Plan, X, W, Y, ws, stream=None) -> None:
     _check(load().fo_gemm_rs(plan, _ptr_array(X), _ptr_array(W), _ptr_array(Y), _ptr(ws), _stream(stream)),
            "fo_gemm_rs")
+
+
+def fo_gemm_ar(plan: Plan, X, W, Y, ws, stream=None) -> None:
+    _check(load().fo_gemm_ar(plan, _ptr_array(X), _ptr_array(W), _ptr_array(Y), _ptr(ws), _stream(stream)),
+           "fo_gemm_ar")
 
 
 def fo_ag_gemm(plan: Plan, X, W, Y, G=None, ws=None, stream=None) -> None:

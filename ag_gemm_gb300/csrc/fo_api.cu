@@ -140,6 +140,7 @@ void fill_common(fo_plan_t p, fo::FoParams* k, void* ws) {
   k->pieces = p->pieces;
   k->row_bytes = p->d.K * 2;
   k->ag_copy = p->d.op == FO_OP_AG_GEMM && p->d.ag_transport == FO_AG_COPY ? 1 : 0;
+  k->n_cols = p->n_out;
 }
 
 fo_status check_ptrs(int R, const void* const* a) {
@@ -151,12 +152,17 @@ fo_status check_ptrs(int R, const void* const* a) {
   return FO_OK;
 }
 
-// Encode the operand maps of a GEMM-RS / DP-grad-RS / pure-control call.
+// Encode the operand maps of a GEMM-RS / DP-grad-RS / GEMM-AR / pure-control
+// call. The fp32 destination of the partials is: Y_c (RS/DP with fp32 out),
+// the workspace's shard sums (bf16 out), rank c's own rows of its full
+// output (AR), or the computing rank's own buffer (partials control).
 fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A, const void* const* B,
                         void* const* D, void* ws, fo::FoParams** out) {
   const int kind = partial ? KIND_PART : (dp ? KIND_DP : KIND_RS);
+  const bool to_ws = !partial && p->d.out_dtype == FO_BF16;
+  const bool ar = !partial && p->d.op == FO_OP_GEMM_AR;
   fo::FoParams* k = cached_params(p, kind, A, B, (const void* const*)D);
-  if (k) {
+  if (k && (!to_ws || p->param_cache_ws == ws)) {
     fill_common(p, k, ws);
     *out = k;
     return FO_OK;
@@ -164,7 +170,7 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
   k = fresh_params(p);
   if (!k) return FO_ERR_INVALID_ARG;
   const int R = p->R;
-  const uint64_t M = (uint64_t)p->d.M, N = (uint64_t)p->d.N, rpc = (uint64_t)p->rows_per_chunk;
+  const uint64_t M = (uint64_t)p->d.M, N = (uint64_t)p->n_out, rpc = (uint64_t)p->rows_per_chunk;
   const uint64_t kr = (uint64_t)p->k_red;
   const int es = p->elem_bytes;
   const CUtensorMapDataType dt = es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -179,12 +185,24 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
       ok &= enc2d(&k->tmA[r], dt, A[r], M, kr, M * es, bk, bk);
       ok &= enc2d(&k->tmB[r], dt, B[r], N, kr, N * es, bk, bk);
     }
-    if (partial) ok &= enc3d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D[r], N, rpc, R, N * 4, rpc * N * 4, 32, 32);
-    else ok &= enc2d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D[r], N, rpc, N * 4, 32, 32);
+    if (partial) {
+      ok &= enc3d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D[r], N, rpc, R, N * 4, rpc * N * 4, 32, 32);
+      continue;
+    }
+    float* shard = static_cast<float*>(D[r]);
+    if (to_ws) shard = reinterpret_cast<float*>(static_cast<char*>(ws) + p->ws_shard_off + r * p->ws_shard_stride);
+    if (ar) shard = static_cast<float*>(D[r]) + (size_t)r * rpc * N;
+    ok &= enc2d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, shard, N, rpc, N * 4, 32, 32);
+    k->shard[r] = shard;
+    if (to_ws) k->fin_out[r] = D[r];
+    if (ar) k->ar_full[r] = static_cast<float*>(D[r]);
   }
   if (!ok) return FO_ERR_CUDA;
   remember(p, kind, A, B, (const void* const*)D);
+  p->param_cache_ws = ws;
   fill_common(p, k, ws);
+  k->completion = partial ? fo::FO_COMPLETE_NONE
+                          : (to_ws ? fo::FO_COMPLETE_BF16 : (ar ? fo::FO_COMPLETE_ALLREDUCE : fo::FO_COMPLETE_NONE));
   *out = k;
   return FO_OK;
 }
@@ -325,6 +343,7 @@ __global__ void all_gather_copy_kernel(PtrArray X, MutPtrArray G, int R, int64_t
 fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const void* const* W,
                                         void* const* Y, void* scratch, fo::FoParams* k, int* variant,
                                         int* grid) {
+  if (p->d.op != FO_OP_GEMM_RS || p->d.out_dtype != FO_F32) return FO_ERR_DTYPE;
   DevInfo di;
   fo_status st = preflight(p, &di);
   if (st != FO_OK) return st;
@@ -365,6 +384,22 @@ fo_status fo_gemm_rs(fo_plan_t p, const void* const* X, const void* const* W, vo
                      fo_stream_t stream) {
   if (!p || !ws) return FO_ERR_INVALID_ARG;
   if (p->d.op != FO_OP_GEMM_RS) return FO_ERR_INVALID_ARG;
+  fo_status st;
+  if ((st = check_ptrs(p->R, X)) || (st = check_ptrs(p->R, W)) || (st = check_ptrs(p->R, (const void* const*)Y)))
+    return st;
+  if (!aligned16(ws)) return FO_ERR_ALIGN;
+  DevInfo di;
+  if ((st = preflight(p, &di))) return st;
+  fo::FoParams* k = nullptr;
+  if ((st = build_rs_like(p, false, false, X, W, Y, ws, &k))) return st;
+  int v = p->elem_bytes == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
+  return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
+}
+
+fo_status fo_gemm_ar(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* ws,
+                     fo_stream_t stream) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (p->d.op != FO_OP_GEMM_AR) return FO_ERR_INVALID_ARG;
   fo_status st;
   if ((st = check_ptrs(p->R, X)) || (st = check_ptrs(p->R, W)) || (st = check_ptrs(p->R, (const void* const*)Y)))
     return st;

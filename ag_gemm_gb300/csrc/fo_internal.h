@@ -53,11 +53,14 @@ struct fo_plan_s {
   size_t ws_bytes;
   size_t ws_counters_off;  // RS/DP: uint32 [R][tiles_m*tiles_n][4]
   size_t ws_flags_off;     // AG copy transport: uint32 [R][R][pieces]
+  size_t ws_shard_off;     // bf16 output: fp32 shard sums, R x align256(rows/R * N * 4)
+  size_t ws_shard_stride;
 
   int32_t last_launches;
   void* param_cache;       // host copy of the last kernel parameter block
   int param_cache_kind;    // which call built it (0 = none)
   const void* param_cache_key[4 * FO_MAX_R];  // the pointers it was built from (X/A, W/B, Y/D, G)
+  const void* param_cache_ws;                 // and the workspace, where the maps point into it
 };
 
 // Workspace header (offset 0): device status word and launch epoch.

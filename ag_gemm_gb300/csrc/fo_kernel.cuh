@@ -98,7 +98,16 @@ struct alignas(128) FoParams {
   int64_t row_bytes;           // K * 2
   int32_t pieces;              // 32-row pieces per shard
   int32_t ag_copy;             // 1: shards reach G_r along the ring and the GEMM reads them there
+  // RS/DP completion action, run on a 32-row quarter of a shard tile by the
+  // warp that publishes its R-th partial:
+  int32_t completion;          // FO_COMPLETE_*
+  int64_t n_cols;              // N: columns of a shard row
+  float* shard[FO_MAX_R];      // fp32 shard rows that tmD[c] addresses
+  void* fin_out[FO_MAX_R];     // FINALIZE: bf16 shard outputs [rows/R x N]
+  float* ar_full[FO_MAX_R];    // ALLREDUCE: every rank's full fp32 output [M x N]
 };
+
+enum Completion : int { FO_COMPLETE_NONE = 0, FO_COMPLETE_BF16 = 1, FO_COMPLETE_ALLREDUCE = 2 };
 
 template <bool A_MN, bool B_MN, bool TF32, bool PAIR>
 __host__ __device__ constexpr uint32_t instr_desc() {
@@ -130,9 +139,58 @@ __device__ __forceinline__ Tile decode_tile(const FoParams& p, int L) {
 
 // A partial is in its owner's shard: count it. The partial that completes
 // the shard (the R-th) resets the counter for the next call.
-__device__ __forceinline__ void signal_partial(uint32_t* ctr, int R) {
-  const uint32_t old = atom_add_release_u32(ctr, 1u);
-  if (old + 1u == (uint32_t)R) atomicExch(ctr, 0u);
+// Returns true for the partial that completes the tile (it also acquires
+// every other partial's release, so the completed tile can be read).
+__device__ __forceinline__ bool signal_partial(uint32_t* ctr, int R) {
+  const uint32_t old = atom_add_acq_rel_u32(ctr, 1u);
+  if (old + 1u == (uint32_t)R) {
+    atomicExch(ctr, 0u);
+    return true;
+  }
+  return false;
+}
+
+// Completion action on the 32 x 256 quarter of shard c at (row0, n0), all
+// R partials in place (called by all 32 lanes of the publishing warp):
+//   BF16       round the fp32 sums once to bf16 into the bf16 output;
+//   ALLREDUCE  copy the finished rows into every other rank's full output
+//              (the all-gather half of reduce-scatter + all-gather).
+// 128-bit L2 loads, eight in flight per lane.
+static __device__ __noinline__ void complete_quarter(const FoParams& p, int c, int row0, int n0, int lane) {
+  const int rows = min(32, p.rows_per_chunk - row0);
+  const int cols = min(FO_BN, (int)p.n_cols - n0);
+  if (rows <= 0 || cols <= 0) return;
+  const size_t N = (size_t)p.n_cols;
+  const float* src = p.shard[c] + (size_t)row0 * N + n0;
+  for (int i0 = 0; i0 < rows; i0 += 4) {
+    float4 v[4][2];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const int i = i0 + a, j = lane * 4 + b * 128;
+        if (i < rows && j < cols) v[a][b] = __ldcg(reinterpret_cast<const float4*>(src + i * N + j));
+      }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const int i = i0 + a, j = lane * 4 + b * 128;
+        if (i >= rows || j >= cols) continue;
+        if (p.completion == FO_COMPLETE_BF16) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(v[a][b].x, v[a][b].y);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(v[a][b].z, v[a][b].w);
+          uint2 w;
+          w.x = *reinterpret_cast<uint32_t*>(&lo);
+          w.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.fin_out[c]) + (size_t)(row0 + i) * N + n0 + j) = w;
+        } else {
+          const size_t off = ((size_t)c * p.rows_per_chunk + row0 + i) * N + n0 + j;
+          for (int q = 0; q < p.R; ++q)
+            if (q != c) __stcg(reinterpret_cast<float4*>(p.ar_full[q] + off), v[a][b]);
+        }
+      }
+  }
 }
 
 // Copy n16 16-byte words with nthr threads (thread tid handles words tid,
@@ -385,8 +443,28 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
     const int e = warp - 2;        // staging buffers of this warp
     const int q = warp & 3;        // TMEM lane quarter this warp may access
     uint32_t tcount = 0;
-    uint32_t* pend_ctr = nullptr;  // RS: counter of this warp's last partial, not yet published
+    constexpr int kSubRS = FO_BN / 32;   // bulk groups per RS tile quarter
+    // RS: this warp's last partial, not yet published (same in every lane).
+    uint32_t* pend_ctr = nullptr;
     bool pend_skip = false;
+    int pend_c = 0, pend_row0 = 0, pend_n0 = 0;
+    // Publish the deferred partial (every lane calls; lane 0 owns the bulk
+    // groups): wait until its writes are performed (all groups, or all but
+    // the newest tile's), release-count it, and if it completes its tile,
+    // run the plan's completion action.
+    auto publish = [&](bool all) {
+      if (!pend_ctr) return;
+      uint32_t done = 0;
+      if (lane == 0) {
+        if (all) bulk_wait<0>();
+        else bulk_wait<kSubRS>();
+        fence_proxy_async_global();
+        if (!pend_skip) done = signal_partial(pend_ctr, p.R) ? 1u : 0u;
+      }
+      done = __shfl_sync(0xffffffffu, done, 0);
+      if (done && p.completion != FO_COMPLETE_NONE) complete_quarter(p, pend_c, pend_row0, pend_n0, lane);
+      pend_ctr = nullptr;
+    };
     for (int L = unit; L < total; L += units, ++tcount) {
       if (*abort_flag) break;
       const Tile ti = decode_tile(p, L);
@@ -396,13 +474,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
         // About to block until the next accumulator is ready: publish the
         // deferred partial first (a warp never holds one while it waits, so
         // a waiter elsewhere always sees it eventually).
-        if (lane == 0 && pend_ctr && !mbar_try_wait(tfull_bar(acc), aph)) {
-          bulk_wait<0>();
-          fence_proxy_async_global();
-          if (!pend_skip) signal_partial(pend_ctr, p.R);
-          pend_ctr = nullptr;
-        }
-        __syncwarp();
+        const uint32_t ready = (lane == 0 && pend_ctr) ? mbar_try_wait(tfull_bar(acc), aph) : 1u;
+        if (!__shfl_sync(0xffffffffu, ready, 0)) publish(true);
       }
       if (!mbar_wait(tfull_bar(acc), aph, abort_flag, kMbarLimitNs)) break;
       tc_fence_after();
@@ -418,23 +491,19 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
         if (ti.ord > 0) {
           // The shard must already hold its first (stored) partial; in
           // deterministic mode, every partial that comes before this one.
+          const uint32_t need = p.deterministic ? (uint32_t)ti.ord : 1u;
+          const uint32_t have = __shfl_sync(0xffffffffu, lane == 0 ? ld_acquire_u32(ctr) : 0u, 0);
           int good = 1;
-          if (lane == 0) {
-            const uint32_t need = p.deterministic ? (uint32_t)ti.ord : 1u;
-            if (ld_acquire_u32(ctr) < need) {
-              // Not yet: first publish this warp's own deferred partial (it
-              // may be the one being waited for), then wait.
-              if (pend_ctr) {
-                bulk_wait<0>();
-                fence_proxy_async_global();
-                if (!pend_skip) signal_partial(pend_ctr, p.R);
-                pend_ctr = nullptr;
-              }
+          if (have < need) {
+            // Not yet: first publish this warp's own deferred partial (it
+            // may be the one being waited for), then wait.
+            publish(true);
+            if (lane == 0) {
               good = wait_counter_geq(ctr, need, p.timeout_ns, abort_flag, gstatus) ? 1 : 0;
               if (!good && !*abort_flag && !*gstatus) record_error(p.status, FO_ERR_TIMEOUT, ti.r, ti.s, ti.c);
             }
-            fence_proxy_async_global();
           }
+          if (lane == 0) fence_proxy_async_global();
           ok = __shfl_sync(0xffffffffu, good, 0) != 0;
           if (!ok) *abort_flag = 1;
         }
@@ -518,31 +587,26 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           }
         }
         if constexpr (EPI == EPI_RS) {
-          if (ok && lane == 0) {
+          if (ok) {
             // Publish the previous tile's partial (its 8 bulk groups are
             // older than this tile's 8) and keep this one pending, so the
             // warp never stalls on its own latest writes.
-            if (pend_ctr) {
-              bulk_wait<kSub>();
-              fence_proxy_async_global();
-              if (!pend_skip) signal_partial(pend_ctr, p.R);
-            }
+            publish(false);
             pend_ctr = ctr;
             pend_skip = p.fault_inject == FO_INJECT_SKIP_SIGNAL && ti.c == 0 && mt128 == 0 && ti.nt == 0 &&
                         q == 0 && ti.ord == 0;
+            pend_c = ti.c;
+            pend_row0 = row0;
+            pend_n0 = n0;
           }
         }
       }
     }
-    if (lane == 0) {
-      bulk_wait<0>();
-      if constexpr (EPI == EPI_RS) {
-        if (pend_ctr && !*abort_flag) {
-          fence_proxy_async_global();
-          if (!pend_skip) signal_partial(pend_ctr, p.R);
-        }
-      }
+    if constexpr (EPI == EPI_RS) {
+      const int aborted = __shfl_sync(0xffffffffu, lane == 0 ? (int)*abort_flag : 0, 0);
+      if (!aborted) publish(true);
     }
+    if (lane == 0) bulk_wait<0>();
     __syncwarp();
   }
 

@@ -115,6 +115,15 @@ void build_transfers_and_edges(fo_plan_s* p) {
   if (p->d.fault_inject == FO_INJECT_DROP_TRANSFER && !p->transfers.empty()) p->transfers.pop_back();
 }
 
+// All-reduce = reduce-scatter then all-gather: once shard c is complete its
+// owner sends it to every other rank (listed as step R, after the RS steps).
+void add_allgather_half(fo_plan_s* p) {
+  const int R = p->R;
+  for (int c = 0; c < R; ++c)
+    for (int q = 0; q < R; ++q)
+      if (q != c) p->transfers.push_back({c, q, c, R});
+}
+
 bool dag_acyclic(const fo_plan_s* p) {
   const int R = p->R, n = R * R;
   std::vector<int> indeg(n, 0);
@@ -188,7 +197,7 @@ extern "C" {
 fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (!d || !out) return FO_ERR_INVALID_ARG;
   *out = nullptr;
-  if (d->op < FO_OP_AG_GEMM || d->op > FO_OP_DP_GRAD_RS) return FO_ERR_INVALID_ARG;
+  if (d->op < FO_OP_AG_GEMM || d->op > FO_OP_GEMM_AR) return FO_ERR_INVALID_ARG;
   if (d->R < 1 || d->R > FO_MAX_R) return FO_ERR_INVALID_ARG;
   if (d->sched != FO_SCHED_RANK_ADAPTIVE && d->sched != FO_SCHED_SLICED) return FO_ERR_INVALID_ARG;
   if (d->ag_transport != FO_AG_PEER_READ && d->ag_transport != FO_AG_COPY) return FO_ERR_INVALID_ARG;
@@ -207,8 +216,9 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   int eb = 2;
   switch (d->op) {
     case FO_OP_GEMM_RS:
+    case FO_OP_GEMM_AR:
       if (K % R) return FO_ERR_SHAPE;
-      if (d->out_dtype != FO_F32) return FO_ERR_DTYPE;
+      if (d->out_dtype != FO_F32 && !(d->op == FO_OP_GEMM_RS && d->out_dtype == FO_BF16)) return FO_ERR_DTYPE;
       if (d->in_dtype == FO_F32) {
         eb = 4;
         // fp32 operands feed the tf32 MMA only with both operands K-major.
@@ -228,7 +238,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
       break;
     case FO_OP_DP_GRAD_RS:
       if (d->in_dtype != FO_BF16) return FO_ERR_DTYPE;
-      if (d->out_dtype != FO_F32) return FO_ERR_DTYPE;
+      if (d->out_dtype != FO_F32 && d->out_dtype != FO_BF16) return FO_ERR_DTYPE;
       if (d->w_layout != FO_W_KN) return FO_ERR_INVALID_ARG;
       // A chunk starts at column c*M/R of X_r: a TMA coordinate along the
       // contiguous dimension, so it must fall on a 16-byte boundary.
@@ -245,7 +255,8 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   p->elem_bytes = eb;
   p->rows_per_chunk = M / R;
   switch (d->op) {
-    case FO_OP_GEMM_RS: p->k_red = K / R; p->n_out = N; break;
+    case FO_OP_GEMM_RS:
+    case FO_OP_GEMM_AR: p->k_red = K / R; p->n_out = N; break;
     case FO_OP_AG_GEMM: p->k_red = K; p->n_out = N / R; break;
     default: p->k_red = K; p->n_out = N; break;
   }
@@ -266,6 +277,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
     delete p;
     return st;
   }
+  if (d->op == FO_OP_GEMM_AR) add_allgather_half(p);
   size_t off = align_up(sizeof(fo_ws_header), 256);
   p->ws_counters_off = off;
   p->ws_flags_off = off;
@@ -273,6 +285,12 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
     off += align_up((size_t)R * R * p->pieces * sizeof(uint32_t), 256);
   } else {
     off += align_up((size_t)R * p->ctr_tiles_m * p->tiles_n * 4 * sizeof(uint32_t), 256);
+  }
+  p->ws_shard_off = off;
+  p->ws_shard_stride = 0;
+  if (d->op != FO_OP_AG_GEMM && d->out_dtype == FO_BF16) {
+    p->ws_shard_stride = align_up((size_t)p->rows_per_chunk * p->n_out * 4, 256);
+    off += (size_t)R * p->ws_shard_stride;
   }
   p->ws_bytes = off;
   p->last_launches = 0;

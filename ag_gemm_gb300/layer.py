@@ -1,0 +1,153 @@
+"""The projection GEMMs of one tensor- and sequence-parallel (TP-SP)
+transformer layer, forward and backward, on the fused collectives.
+
+The pages name this use: the method is instantiated for the row- and
+column-parallel projections of MLP and QKV layers (gist.science, "Technical
+Summary" section 2, "Architectural Versatility"), in training forward and
+backward (section 3). With R virtual ranks, a sequence of T tokens split
+T/R per rank, hidden size H and FFN size F:
+
+forward
+    QKV     column-parallel: AG-GEMM      Y_qkv_r = AllGather(x) . Wqkv_r    [H x 3H/R]
+    o       row-parallel:    GEMM-RS      h       = RS(attn_r . Wo_r)        [H/R x H]
+    up|gate column-parallel: AG-GEMM      Y_ug_r  = AllGather(h) . Wug_r     [H x 2F/R]
+    down    row-parallel:    GEMM-RS      y       = RS(act_r . Wd_r)         [F/R x H]
+backward (the usual TP-SP duals; the pages do not spell them out)
+    row-parallel GEMM-RS Y = RS(X_r . W_r):
+        dX_r = AllGather(dY) . W_r^T          AG-GEMM, W read as [N x K]
+        dW_r = X_r^T . AllGather(dY)          per-rank weight GEMM (partials)
+    column-parallel AG-GEMM Y_r = AllGather(X) . W_r:
+        dX   = RS(dY_r . W_r^T)               GEMM-RS, W read as [N x K]
+        dW_r = AllGather(X)^T . dY_r          per-rank weight GEMM (partials)
+
+The attention core, the SwiGLU and the norms are not part of the path: their
+outputs (attn_r, act_r) and upstream gradients are fixed synthetic tensors.
+Every GEMM runs in the library's kernels; this module only allocates
+buffers and issues the calls (16 launches per forward + backward: 4 + 4 + 4
+weight-gradient GEMMs + 4 more collective GEMMs).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Dict, List
+
+import torch
+
+from . import binding as B
+
+
+@dataclass(frozen=True)
+class LayerShape:
+    R: int = 8
+    T: int = 8192
+    H: int = 4096
+    F: int = 14336
+
+    def flops(self) -> Dict[str, float]:
+        T, H, F = self.T, self.H, self.F
+        fwd = 2.0 * T * H * (3 * H) + 2.0 * T * H * H + 2.0 * T * H * (2 * F) + 2.0 * T * F * H
+        return {"forward": fwd, "backward": 2 * fwd, "total": 3 * fwd}
+
+
+def _draw(g, shape, std, device):
+    return (torch.randn(shape, generator=g) * std).to(torch.bfloat16).to(device)
+
+
+def _ints(g, shape, device):
+    return torch.randint(-4, 5, shape, generator=g, dtype=torch.int32).to(torch.bfloat16).to(device)
+
+
+class TpspLayerProjections:
+    """Buffers, plans and launches for one layer's projections (R virtual ranks
+    on one GPU). `mode="randn"` draws weights ~N(0, 0.02) and activations /
+    gradients ~N(0, 1); `mode="int"` draws integers in [-4, 4] so every sum
+    is exact in fp32."""
+
+    def __init__(self, shape: LayerShape = LayerShape(), *, device="cuda", seed=4, mode="randn"):
+        self.s = s = shape
+        R, T, H, F = s.R, s.T, s.H, s.F
+        if T % R or H % R or F % R:
+            raise ValueError("T, H and F must be divisible by R")
+        dev = torch.device(device)
+        g = torch.Generator().manual_seed(seed)
+        w = (lambda shp: _ints(g, shp, dev)) if mode == "int" else (lambda shp: _draw(g, shp, 0.02, dev))
+        a = (lambda shp: _ints(g, shp, dev)) if mode == "int" else (lambda shp: _draw(g, shp, 1.0, dev))
+        bf, f32 = torch.bfloat16, torch.float32
+
+        def per_rank(shp, dtype=bf):
+            return [torch.empty(shp, dtype=dtype, device=dev) for _ in range(R)]
+
+        # weights (each rank's slice)
+        self.Wqkv = [w((H, 3 * H // R)) for _ in range(R)]
+        self.Wo = [w((H // R, H)) for _ in range(R)]
+        self.Wug = [w((H, 2 * F // R)) for _ in range(R)]
+        self.Wd = [w((F // R, H)) for _ in range(R)]
+        # forward inputs and the synthetic outputs of the skipped parts
+        self.x = [a((T // R, H)) for _ in range(R)]
+        self.attn = [a((T, H // R)) for _ in range(R)]
+        self.act = [a((T, F // R)) for _ in range(R)]
+        # upstream gradients
+        self.dy = [a((T // R, H)) for _ in range(R)]        # into the down projection's output
+        self.dh = [a((T // R, H)) for _ in range(R)]        # into the o projection's output
+        self.dug = [a((T, 2 * F // R)) for _ in range(R)]   # into up|gate's output (through SwiGLU)
+        self.dqkv = [a((T, 3 * H // R)) for _ in range(R)]  # into QKV's output (through attention)
+        # forward outputs (and the gathered inputs kept for the weight gradients)
+        self.Gx, self.Gh = per_rank((T, H)), per_rank((T, H))
+        self.y_qkv, self.y_ug = per_rank((T, 3 * H // R)), per_rank((T, 2 * F // R))
+        self.h, self.y = per_rank((T // R, H)), per_rank((T // R, H))
+        # backward outputs
+        self.G_dy, self.G_dh = per_rank((T, H)), per_rank((T, H))
+        self.d_act, self.d_attn = per_rank((T, F // R)), per_rank((T, H // R))
+        self.d_h_from_ug, self.d_x = per_rank((T // R, H)), per_rank((T // R, H))
+        self.dWd, self.dWo = per_rank((F // R, H), f32), per_rank((H // R, H), f32)
+        self.dWug, self.dWqkv = per_rank((H, 2 * F // R), f32), per_rank((H, 3 * H // R), f32)
+
+        P = {}
+        # forward
+        P["qkv"] = B.fo_plan("ag_gemm", R, T, 3 * H, H)
+        P["o"] = B.fo_plan("gemm_rs", R, T, H, H, out_dtype="bf16")
+        P["ug"] = B.fo_plan("ag_gemm", R, T, 2 * F, H)
+        P["down"] = B.fo_plan("gemm_rs", R, T, H, F, out_dtype="bf16")
+        # backward: data gradients
+        P["down_dx"] = B.fo_plan("ag_gemm", R, T, F, H, w_layout="nk")
+        P["ug_dx"] = B.fo_plan("gemm_rs", R, T, H, 2 * F, w_layout="nk", out_dtype="bf16")
+        P["o_dx"] = B.fo_plan("ag_gemm", R, T, H, H, w_layout="nk")
+        P["qkv_dx"] = B.fo_plan("gemm_rs", R, T, H, 3 * H, w_layout="nk", out_dtype="bf16")
+        # backward: weight gradients (per-rank GEMMs, no collective)
+        P["down_dw"] = B.fo_plan("dp_grad_rs", R, F // R, H, T)
+        P["ug_dw"] = B.fo_plan("dp_grad_rs", R, H, 2 * F // R, T)
+        P["o_dw"] = B.fo_plan("dp_grad_rs", R, H // R, H, T)
+        P["qkv_dw"] = B.fo_plan("dp_grad_rs", R, H, 3 * H // R, T)
+        self.plans = P
+        self.ws = {}
+        for k, p in P.items():
+            self.ws[k] = torch.empty(B.fo_workspace_size(p), dtype=torch.uint8, device=dev)
+            B.fo_workspace_init(p, self.ws[k])
+        self.launches = 0
+
+    def forward(self, stream=None):
+        P, ws = self.plans, self.ws
+        B.fo_ag_gemm(P["qkv"], self.x, self.Wqkv, self.y_qkv, self.Gx, ws["qkv"], stream)
+        B.fo_gemm_rs(P["o"], self.attn, self.Wo, self.h, ws["o"], stream)
+        B.fo_ag_gemm(P["ug"], self.h, self.Wug, self.y_ug, self.Gh, ws["ug"], stream)
+        B.fo_gemm_rs(P["down"], self.act, self.Wd, self.y, ws["down"], stream)
+        self.launches += 4
+
+    def backward(self, stream=None):
+        P, ws = self.plans, self.ws
+        # down (row-parallel): dAct = AG(dy) . Wd^T, dWd = act^T . AG(dy)
+        B.fo_ag_gemm(P["down_dx"], self.dy, self.Wd, self.d_act, self.G_dy, ws["down_dx"], stream)
+        B.fo_gemm_partials(P["down_dw"], self.act, self.G_dy, self.dWd, ws["down_dw"], stream)
+        # up|gate (column-parallel): dh = RS(dug . Wug^T), dWug = Gh^T . dug
+        B.fo_gemm_rs(P["ug_dx"], self.dug, self.Wug, self.d_h_from_ug, ws["ug_dx"], stream)
+        B.fo_gemm_partials(P["ug_dw"], self.Gh, self.dug, self.dWug, ws["ug_dw"], stream)
+        # o (row-parallel): dAttn = AG(dh) . Wo^T, dWo = attn^T . AG(dh)
+        B.fo_ag_gemm(P["o_dx"], self.dh, self.Wo, self.d_attn, self.G_dh, ws["o_dx"], stream)
+        B.fo_gemm_partials(P["o_dw"], self.attn, self.G_dh, self.dWo, ws["o_dw"], stream)
+        # QKV (column-parallel): dx = RS(dqkv . Wqkv^T), dWqkv = Gx^T . dqkv
+        B.fo_gemm_rs(P["qkv_dx"], self.dqkv, self.Wqkv, self.d_x, ws["qkv_dx"], stream)
+        B.fo_gemm_partials(P["qkv_dw"], self.Gx, self.dqkv, self.dWqkv, ws["qkv_dw"], stream)
+        self.launches += 8
+
+    def status(self) -> List[int]:
+        return [B.fo_status_query(p, self.ws[k])[0] for k, p in self.plans.items()]

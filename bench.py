@@ -279,6 +279,8 @@ def run_ours(args):
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
 
+    if args.workload == LAYER_WORKLOAD:
+        return run_layer(args, dev, world, rank)
     w = WORKLOADS[args.workload]
     if w.op != "gemm_rs":
         raise SystemExit("bench.py times gemm_rs workloads")
@@ -405,6 +407,129 @@ def run_ours(args):
     return 0
 
 
+LAYER_WORKLOAD = "tpsp_layer_r8_t8192_h4096_f14336"
+
+
+def run_layer(args, dev, world, rank):
+    """One step = forward + backward of the projections of one TP-SP layer
+    (R = 8, 8192 tokens, hidden 4096, FFN 14336): 4 fused collective GEMMs
+    forward, 4 fused collective GEMMs + 4 weight-gradient GEMMs backward."""
+    import torch
+    import torch.distributed as dist
+
+    from ag_gemm_gb300.layer import LayerShape, TpspLayerProjections
+    shape = LayerShape(R=8, T=8192, H=4096, F=14336)
+    L = TpspLayerProjections(shape, device=dev, seed=4)
+    flops = shape.flops()["total"]
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        L.forward(stream)
+        L.backward(stream)
+    torch.cuda.synchronize(dev)
+    if any(L.status()):
+        raise RuntimeError(f"device status {L.status()}")
+    L.launches = 0
+    steps = max(1, min(args.steps, 200))
+    with ClockSampler(_smi_id(dev)) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        clk.mark("t0")
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            L.forward(stream)
+            L.backward(stream)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark("t1")
+    ms = max_over_ranks(a.elapsed_time(b), world, dev) / steps
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops_sustained"])
+    value = world * flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": LAYER_WORKLOAD, "R": 8, "tokens": 8192, "hidden": 4096, "ffn": 14336,
+                   "heads": 32, "step": "forward + backward projections (attention core, SwiGLU, norms excluded)",
+                   "l2": "no flush: several GB of operands per step"},
+        "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / world / peak, "traffic": None,
+                     "peak_source": f"bf16_tflops_sustained, {peak_src}"},
+        "gpu_launches": L.launches,
+        "clocks": clk.summary(),
+        "flops_per_step": flops,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+def run_sweep(args):
+    """NEXT-style sweeps, one JSON line: the MLP block of a TP layer (AG-GEMM
+    up|gate, then GEMM-RS down; hidden 4096, FFN 14336, R = 4) over sequence
+    lengths, fused versus the unfused same-GPU path (gather copy + GEMMs;
+    GEMMs to partials + reduce kernel), plus the data-slicing order."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from ag_gemm_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    R, H, F = 4, 4096, 14336
+    seqs = [int(x) for x in args.sweep_seqs.split(",")]
+    g = torch.Generator().manual_seed(6)
+    rows = []
+    for T in seqs:
+        x = [(torch.randn(T // R, H, generator=g)).bfloat16().to(dev) for _ in range(R)]
+        Wug = [(torch.randn(H, 2 * F // R, generator=g) * 0.02).bfloat16().to(dev) for _ in range(R)]
+        act = [(torch.randn(T, F // R, generator=g)).bfloat16().to(dev) for _ in range(R)]
+        Wd = [(torch.randn(F // R, H, generator=g) * 0.02).bfloat16().to(dev) for _ in range(R)]
+        y_ug = [torch.empty(T, 2 * F // R, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        y = [torch.empty(T // R, H, device=dev) for _ in range(R)]
+        p_ug = B.fo_plan("ag_gemm", R, T, 2 * F, H)
+        p_d = B.fo_plan("gemm_rs", R, T, H, F)
+        p_ds = B.fo_plan("gemm_rs", R, T, H, F, sched="sliced")
+        ws = {k: torch.zeros(B.fo_workspace_size(pp), dtype=torch.uint8, device=dev)
+              for k, pp in (("ug", p_ug), ("d", p_d), ("ds", p_ds))}
+
+        def fused():
+            B.fo_ag_gemm(p_ug, x, Wug, y_ug, None, ws["ug"], stream)
+            B.fo_gemm_rs(p_d, act, Wd, y, ws["d"], stream)
+
+        def sliced():
+            B.fo_ag_gemm(p_ug, x, Wug, y_ug, None, ws["ug"], stream)
+            B.fo_gemm_rs(p_ds, act, Wd, y, ws["ds"], stream)
+
+        G = [torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        P = [torch.empty(T, H, device=dev) for _ in range(R)]
+        p_one = [B.fo_plan("ag_gemm", 1, T, 2 * F // R, H) for _ in range(R)]
+        ws1 = [torch.zeros(B.fo_workspace_size(pp), dtype=torch.uint8, device=dev) for pp in p_one]
+        p_part = B.fo_plan("gemm_rs", R, T, H, F)   # own plan: its launch parameters stay cached
+
+        def unfused():
+            B.fo_all_gather_copy(p_ug, x, G, stream)
+            for r in range(R):
+                B.fo_ag_gemm(p_one[r], [G[r]], [Wug[r]], [y_ug[r]], None, ws1[r], stream)
+            B.fo_gemm_partials(p_part, act, Wd, P, ws["d"], stream)
+            B.fo_reduce_scatter_f32(p_part, P, y, stream)
+
+        flops = 2.0 * T * H * 2 * F + 2.0 * T * F * H
+        t_f, t_s, t_u = _time(fused, stream), _time(sliced, stream), _time(unfused, stream)
+        rows.append({"seq": T, "fused_ms": t_f, "sliced_ms": t_s, "unfused_ms": t_u,
+                     "fused_tflops": flops / t_f / 1e9,
+                     "latency_reduction_vs_unfused_pct": 100.0 * (t_u - t_f) / t_u,
+                     "sliced_reduction_vs_unfused_pct": 100.0 * (t_u - t_s) / t_u})
+        del x, Wug, act, Wd, y_ug, y, G, P, ws, ws1
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "mlp_block_seq", "R": R, "hidden": H, "ffn": F, "rows": rows}))
+    return 0
+
+
 def _smi_id(dev) -> str:
     """nvidia-smi selector of a torch device (its UUID when torch exposes it)."""
     import torch
@@ -482,6 +607,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-extras", action="store_true", help="skip the control/unfused/cuBLAS comparisons")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: MLP-block sweep over --sweep-seqs (one JSON line)")
+    ap.add_argument("--sweep-seqs", default="128,512,1024,2048,4096,8192,16384")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the fused kernel from an ncu capture of this build")
     args = ap.parse_args(argv)
@@ -489,6 +617,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

@@ -66,7 +66,8 @@ typedef enum {
 typedef enum {
   FO_OP_AG_GEMM = 0,          /* Y_r = AllGather(X) . W_r           */
   FO_OP_GEMM_RS = 1,          /* Y   = ReduceScatter(X_r . W_r)     */
-  FO_OP_DP_GRAD_RS = 2        /* dW  = ReduceScatter(X_r^T . dY_r)  */
+  FO_OP_DP_GRAD_RS = 2,       /* dW  = ReduceScatter(X_r^T . dY_r)  */
+  FO_OP_GEMM_AR = 3           /* Y_r = AllReduce(X_q . W_q) = RS then AG */
 } fo_op;
 
 typedef enum { FO_BF16 = 0, FO_F32 = 1 } fo_dtype;
@@ -110,10 +111,15 @@ typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
 typedef enum { FO_INTERLEAVE_AUTO = 0, FO_INTERLEAVE_LOCKSTEP = 1, FO_INTERLEAVE_SKEWED = 2 } fo_interleave;
 
 /* Global GEMM sizes (M, N, K); the per-rank operands are, for each op:
- *   FO_OP_GEMM_RS    X_r [M x K/R], W_r [K/R x N] (or [N x K/R]), Y_r [M/R x N] fp32
+ *   FO_OP_GEMM_RS    X_r [M x K/R], W_r [K/R x N] (or [N x K/R]), Y_r [M/R x N]
+ *                    fp32, or bf16 with out_dtype FO_BF16
  *   FO_OP_AG_GEMM    X_r [M/R x K], W_r [K x N/R] (or [N/R x K]), Y_r [M x N/R] bf16,
  *                    optional G_r [M x K] bf16 (the gathered X)
- *   FO_OP_DP_GRAD_RS X_r [K x M], dY_r [K x N] (K = tokens), dW_r [M/R x N] fp32
+ *   FO_OP_DP_GRAD_RS X_r [K x M], dY_r [K x N] (K = tokens), dW_r [M/R x N]
+ *                    fp32, or bf16 with out_dtype FO_BF16
+ *   FO_OP_GEMM_AR    X_r [M x K/R], W_r [K/R x N] (or [N x K/R]), Y_r [M x N] fp32
+ * With out_dtype FO_BF16 the fp32 sums are kept in the workspace and each
+ * tile is rounded once (nearest even) into Y when its R-th partial lands.
  * Row block d of an RS output (rows d*M/R .. (d+1)*M/R-1 of the sum over
  * ranks) belongs to rank d. The all-gather concatenates shards in rank order. */
 typedef struct {
@@ -121,7 +127,8 @@ typedef struct {
   int32_t R;                  /* virtual ranks, 1..16 */
   int64_t M, N, K;
   int32_t in_dtype;           /* FO_BF16; FO_F32 (tf32 MMA) for GEMM_RS only */
-  int32_t out_dtype;          /* FO_F32 for GEMM_RS / DP_GRAD_RS, FO_BF16 for AG_GEMM */
+  int32_t out_dtype;          /* GEMM_RS / DP_GRAD_RS: FO_F32 or FO_BF16; AG_GEMM: FO_BF16;
+                                 GEMM_AR: FO_F32 */
   int32_t sched;              /* fo_sched */
   int32_t ag_transport;       /* fo_ag_transport (AG_GEMM only) */
   int32_t w_layout;           /* fo_w_layout (GEMM_RS and AG_GEMM) */
@@ -183,11 +190,21 @@ fo_status fo_workspace_init(fo_plan_t plan, void* ws, fo_stream_t stream);
 fo_status fo_ag_gemm(fo_plan_t plan, const void* const* X, const void* const* W,
                      void* const* Y, void* const* G, void* ws, fo_stream_t stream);
 
-/* Flash-RS: Y_d = sum_r (X_r . W_r)[rows of d], fp32 (gist.science
+/* Flash-RS: Y_d = sum_r (X_r . W_r)[rows of d], fp32 or bf16 (gist.science
  * "Technical Summary" section 2, Flash-Reduce-Scatter). Rank r's step s
  * computes the partial of chunk (r - 1 - s) mod R and adds it into that
  * owner's Y; the own chunk comes last. Y is overwritten. */
 fo_status fo_gemm_rs(fo_plan_t plan, const void* const* X, const void* const* W,
+                     void* const* Y, void* ws, fo_stream_t stream);
+
+/* All-reduce of the partial products, as reduce-scatter then all-gather
+ * (the tensor-parallel all-reduce; gist.science "Technical Summary" section 1
+ * lists it beside RS and AG): Y_q = sum_r X_r . W_r for every rank q, fp32
+ * [M x N]. The RS half is fo_gemm_rs into rank c's own rows of Y_c; as soon
+ * as a shard tile has all R partials, the warp that added the last one
+ * copies it into the same rows of every other rank's Y (the AG half), while
+ * the remaining partial GEMMs still run. */
+fo_status fo_gemm_ar(fo_plan_t plan, const void* const* X, const void* const* W,
                      void* const* Y, void* ws, fo_stream_t stream);
 
 /* Data-parallel weight gradient fused with its reduce-scatter:

@@ -55,8 +55,8 @@ from typing import List, Sequence, Tuple
 import numpy as np
 
 __all__ = [
-    "gemm_rs", "gemm_rs_rows", "ag_gemm", "ag_gemm_rows", "all_gather_rows",
-    "dp_grad_rs", "dp_grad_rs_rows", "reduce_scatter_rows",
+    "gemm_rs", "gemm_rs_rows", "gemm_ar", "ar_transfers", "ag_gemm", "ag_gemm_rows", "all_gather_rows",
+    "dp_grad_rs", "dp_grad_rs_rows", "reduce_scatter_rows", "weight_grads",
     "rs_chunk", "ag_source", "rs_schedule", "ag_schedule", "sliced_schedule",
     "rs_transfers", "ag_transfers", "rs_dependency_edges",
     "simulate_gemm_rs", "simulate_ag_gemm", "simulate_dp_grad_rs",
@@ -119,6 +119,20 @@ def gemm_rs_rows(X, W, d: int, rows: Sequence[int]) -> np.ndarray:
     return acc
 
 
+def gemm_ar(X: Sequence[np.ndarray], W: Sequence[np.ndarray]) -> List[np.ndarray]:
+    """AllReduce(X_r @ W_r): every rank receives the full sum over ranks.
+
+    X_r is [M, K_r], W_r is [K_r, N]; returns R copies of the [M, N] sum
+    (summed in ascending r). [GS] §1 lists all-reduce among the TP
+    collectives; the reading here is the usual all-reduce.
+    """
+    R = len(X)
+    acc = np.zeros((X[0].shape[0], W[0].shape[1]), dtype=np.float64)
+    for r in range(R):
+        acc = acc + _f64(X[r]) @ _f64(W[r])
+    return [acc.copy() for _ in range(R)]
+
+
 def all_gather_rows(X: Sequence[np.ndarray]) -> np.ndarray:
     """Literal all-gather: concatenate the R row shards in rank order."""
     return np.concatenate([_f64(x) for x in X], axis=0)
@@ -154,6 +168,13 @@ def dp_grad_rs(X: Sequence[np.ndarray], dY: Sequence[np.ndarray]) -> List[np.nda
     """
     D = [_f64(X[r]).T @ _f64(dY[r]) for r in range(len(X))]
     return reduce_scatter_rows(D)
+
+
+def weight_grads(X: Sequence[np.ndarray], dY: Sequence[np.ndarray]) -> List[np.ndarray]:
+    """Per-rank weight gradients X_r^T @ dY_r with no collective (the
+    weight-gradient GEMMs of tensor-parallel layers, whose weights are
+    sharded, not replicated)."""
+    return [_f64(X[r]).T @ _f64(dY[r]) for r in range(len(X))]
 
 
 def dp_grad_rs_rows(X, dY, d: int, rows: Sequence[int]) -> np.ndarray:
@@ -224,6 +245,12 @@ def rs_transfers(R: int, ring: bool = False, schedule=None) -> List[Tuple[int, i
             elif c != r:
                 out.append((r, c, c, s))
     return out
+
+
+def ar_transfers(R: int) -> List[Tuple[int, int, int, int]]:
+    """All-reduce as reduce-scatter then all-gather: the direct RS messages,
+    then owner c sends its finished shard to every other rank (step R)."""
+    return rs_transfers(R) + [(c, q, c, R) for c in range(R) for q in range(R) if q != c]
 
 
 def ag_transfers(R: int) -> List[Tuple[int, int, int, int]]:

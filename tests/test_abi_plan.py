@@ -94,7 +94,8 @@ def test_dropped_transfer_is_rejected():
     (dict(op="ag_gemm", R=3, M=9, N=8, K=16), B.FO_ERR_SHAPE),          # N % R
     (dict(op="dp_grad_rs", R=2, M=8, N=8, K=16), B.FO_ERR_ALIGN),       # M/R = 4 columns
     (dict(op="ag_gemm", R=2, M=8, N=16, K=16, out_dtype="f32"), B.FO_ERR_DTYPE),
-    (dict(op="gemm_rs", R=2, M=8, N=16, K=16, out_dtype="bf16"), B.FO_ERR_DTYPE),
+    (dict(op="gemm_ar", R=2, M=8, N=16, K=16, out_dtype="bf16"), B.FO_ERR_DTYPE),
+    (dict(op="gemm_ar", R=2, M=8, N=16, K=9), B.FO_ERR_SHAPE),
     (dict(op="gemm_rs", R=2, M=8, N=16, K=16, in_dtype="f32"), B.FO_ERR_UNSUPPORTED),  # tf32 needs W as [N x K]
     (dict(op="ag_gemm", R=2, M=8, N=16, K=16, sched="sliced"), B.FO_ERR_UNSUPPORTED),
 ])
@@ -197,3 +198,21 @@ def test_copy_transport_requires_gather_buffers():
     with pytest.raises(B.FlashOverlapError) as e:
         B.fo_ag_gemm(p, fake, fake, fake, None, 4096, stream=0)
     assert e.value.code == B.FO_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
+def test_allreduce_plan_is_rs_then_allgather(R):
+    p = B.fo_plan("gemm_ar", R, 128 * R, 256, 64 * R)
+    assert B.fo_plan_table(p) == oracle.rs_schedule(R).tolist()
+    assert sorted(B.fo_plan_transfers(p)) == sorted(oracle.ar_transfers(R))
+
+
+def test_bf16_output_keeps_fp32_sums_in_the_workspace():
+    R, M, N, K = 8, 8192, 4096, 14336
+    f32 = B.fo_workspace_size(B.fo_plan("gemm_rs", R, M, N, K))
+    b16 = B.fo_workspace_size(B.fo_plan("gemm_rs", R, M, N, K, out_dtype="bf16"))
+    assert b16 - f32 >= M * N * 4
+    with pytest.raises(B.FlashOverlapError) as e:     # the allocation-free entry point keeps fp32 only
+        B.fo_gemm_rs_noalloc(B.fo_plan("gemm_rs", 2, 256, 256, 256, out_dtype="bf16"), [16, 32], [16, 32],
+                             [16, 32], stream=0)
+    assert e.value.code in (B.FO_ERR_SCRATCH_LIMIT, B.FO_ERR_DTYPE)

@@ -194,6 +194,77 @@ def test_gemm_rs_new_buffers_after_cached_call(dev):
             assert np.array_equal(_np(Y[d]), ref[d])
 
 
+# ------------------------------------------------------------------ all-reduce and bf16 output
+
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("interleave", ["lockstep", "skewed"])
+@pytest.mark.parametrize("R,M,K,N", [(4, 1024, 136, 520), (2, 600, 200, 264), (8, 2048, 64, 256)])
+def test_gemm_ar_integer_bit_exact(dev, tile, interleave, R, M, K, N):
+    # RS into each owner's rows of its full output, then every finished
+    # shard tile copied to all other ranks: every rank holds the whole sum.
+    plan = B.fo_plan("gemm_ar", R, M, N, K * R, tile_config=tile, interleave=interleave)
+    ws = _ws(plan, dev)
+    Y = Guarded(R, (M, N), torch.float32, dev)
+    for seed in (7, 8):
+        inp = gemm_rs_inputs(R, M, K, N, mode="int", seed=seed)
+        X = [x.to(dev) for x in inp["X"]]
+        W = [w.to(dev) for w in inp["W"]]
+        B.fo_gemm_ar(plan, X, W, Y.views, ws)
+        _status_ok(plan, ws)
+        ref = oracle.gemm_ar([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+        for q in range(R):
+            assert np.array_equal(_np(Y.views[q]), ref[q]), f"rank {q}"
+    Y.check()
+
+
+def test_gemm_ar_random_bf16_within_tolerance(dev):
+    R, M, K, N = 4, 1024, 512, 512
+    inp = gemm_rs_inputs(R, M, K, N, mode="randn", seed=3)
+    plan = B.fo_plan("gemm_ar", R, M, N, K * R)
+    ws = _ws(plan, dev)
+    Y = [torch.empty(M, N, device=dev) for _ in range(R)]
+    B.fo_gemm_ar(plan, [x.to(dev) for x in inp["X"]], [w.to(dev) for w in inp["W"]], Y, ws)
+    _status_ok(plan, ws)
+    ref = oracle.gemm_ar([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for q in range(R):
+        _assert_close(_np(Y[q]), ref[q])
+
+
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("mode", ["int", "randn"])
+def test_gemm_rs_bf16_output_is_rounded_once(dev, tile, mode):
+    R, M, K, N = 4, 800, 200, 328
+    plan = B.fo_plan("gemm_rs", R, M, N, K * R, out_dtype="bf16", tile_config=tile)
+    ws = _ws(plan, dev)
+    Y = Guarded(R, (M // R, N), torch.bfloat16, dev)
+    for seed in (1, 2):
+        inp = gemm_rs_inputs(R, M, K, N, mode=mode, seed=seed)
+        B.fo_gemm_rs(plan, [x.to(dev) for x in inp["X"]], [w.to(dev) for w in inp["W"]], Y.views, ws)
+        _status_ok(plan, ws)
+        ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+        for d in range(R):
+            want = oracle.round_bf16(ref[d])
+            if mode == "int":
+                assert np.array_equal(_np(Y.views[d]), want)
+            else:
+                _assert_close(_np(Y.views[d]), want)
+    Y.check()
+
+
+def test_dp_grad_rs_bf16_output(dev):
+    R, T, M, N = 4, 200, 800, 328
+    inp = dp_grad_inputs(R, T, M, N, mode="int", seed=5)
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T, out_dtype="bf16")
+    ws = _ws(plan, dev)
+    dW = Guarded(R, (M // R, N), torch.bfloat16, dev)
+    B.fo_dp_grad_rs(plan, [x.to(dev) for x in inp["X"]], [y.to(dev) for y in inp["dY"]], dW.views, ws)
+    _status_ok(plan, ws)
+    dW.check()
+    ref = oracle.dp_grad_rs([_np(x) for x in inp["X"]], [_np(y) for y in inp["dY"]])
+    for d in range(R):
+        assert np.array_equal(_np(dW.views[d]), oracle.round_bf16(ref[d]))
+
+
 # ------------------------------------------------------------------ AG-GEMM
 
 def run_ag(dev, R, M, K, N, *, mode="int", layout="kn", seed=1, tile="auto"):

@@ -58,6 +58,24 @@ def test_gemm_rs_matches_brute_force(R, M, K, N):
         assert np.array_equal(got[d], ref[d])
 
 
+@pytest.mark.parametrize("R,M,K,N", [(1, 3, 4, 5), (2, 4, 3, 2), (3, 6, 5, 4)])
+def test_gemm_ar_matches_brute_force(R, M, K, N):
+    rng = np.random.default_rng(R * 31 + M)
+    X = [_ints(rng, (M, K)) for _ in range(R)]
+    W = [_ints(rng, (K, N)) for _ in range(R)]
+    got = oracle.gemm_ar(X, W)
+    for q in range(R):
+        for i in range(M):
+            for j in range(N):
+                want = sum(int(X[r][i][k]) * int(W[r][k][j]) for r in range(R) for k in range(K))
+                assert got[q][i, j] == want
+    # all-reduce = reduce-scatter, then every rank gathers the R shards
+    rs = oracle.gemm_rs(X, W)
+    for q in range(R):
+        assert np.array_equal(got[q], np.concatenate(rs, axis=0))
+    assert len(oracle.ar_transfers(R)) == 2 * R * (R - 1)
+
+
 @pytest.mark.parametrize("R,M,K,N", [(1, 2, 3, 4), (2, 4, 3, 5), (3, 6, 2, 3)])
 def test_ag_gemm_matches_brute_force(R, M, K, N):
     rng = np.random.default_rng(7 + R)
@@ -89,6 +107,17 @@ def test_dp_grad_rs_matches_brute_force(R, T, M, N):
                 want = sum(int(X[r][t][d * rows + i]) * int(dY[r][t][j])
                            for r in range(R) for t in range(T))
                 assert got[d][i, j] == want
+
+
+def test_weight_grads_match_brute_force():
+    rng = np.random.default_rng(17)
+    X = [_ints(rng, (3, 4)) for _ in range(2)]
+    dY = [_ints(rng, (3, 2)) for _ in range(2)]
+    got = oracle.weight_grads(X, dY)
+    for r in range(2):
+        for i in range(4):
+            for j in range(2):
+                assert got[r][i, j] == sum(int(X[r][t][i]) * int(dY[r][t][j]) for t in range(3))
 
 
 def test_sampled_rows_equal_full():
