@@ -27,7 +27,7 @@ TRANSPORTS = {"peer_read": 0, "copy": 1}
 W_LAYOUTS = {"kn": 0, "nk": 1}
 INJECT = {"none": 0, "drop_transfer": 1, "skip_signal": 2}
 TILE_CONFIGS = {"auto": 0, "single": 1}
-INTERLEAVES = {"auto": 0, "lockstep": 1, "skewed": 2}
+INTERLEAVES = {"auto": 0, "lockstep": 1, "skewed": 2, "rank_major": 3}
 
 # Every symbol include/flashoverlap.h declares.
 EXPORTED = [

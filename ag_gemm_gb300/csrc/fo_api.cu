@@ -194,8 +194,10 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
     if (ar) shard = static_cast<float*>(D[r]) + (size_t)r * rpc * N;
     ok &= enc2d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, shard, N, rpc, N * 4, 32, 32);
     k->shard[r] = shard;
-    if (to_ws) k->fin_out[r] = D[r];
-    if (ar) k->ar_full[r] = static_cast<float*>(D[r]);
+    // The finisher's outputs: the bf16 shard, or every rank's full output
+    // viewed as [N, rows/R, R] so a store clips at the shard's last row.
+    if (to_ws) ok &= enc2d(&k->tmF[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D[r], N, rpc, N * 2, 64, 32);
+    if (ar) ok &= enc3d(&k->tmAR[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D[r], N, rpc, R, N * 4, rpc * N * 4, 32, 32);
   }
   if (!ok) return FO_ERR_CUDA;
   remember(p, kind, A, B, (const void* const*)D);

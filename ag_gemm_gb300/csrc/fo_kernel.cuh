@@ -98,13 +98,14 @@ struct alignas(128) FoParams {
   int64_t row_bytes;           // K * 2
   int32_t pieces;              // 32-row pieces per shard
   int32_t ag_copy;             // 1: shards reach G_r along the ring and the GEMM reads them there
-  // RS/DP completion action, run on a 32-row quarter of a shard tile by the
-  // warp that publishes its R-th partial:
+  // RS/DP completion: the owner's last partial (contribution R-1) is the
+  // finisher. It waits for the other R-1, adds their sum (read from the
+  // shard rows tmD[c] addresses) to its own partial and writes the result:
   int32_t completion;          // FO_COMPLETE_*
   int64_t n_cols;              // N: columns of a shard row
   float* shard[FO_MAX_R];      // fp32 shard rows that tmD[c] addresses
-  void* fin_out[FO_MAX_R];     // FINALIZE: bf16 shard outputs [rows/R x N]
-  float* ar_full[FO_MAX_R];    // ALLREDUCE: every rank's full fp32 output [M x N]
+  CUtensorMap tmF[FO_MAX_R];   // BF16: the bf16 shard outputs [rows/R x N] (2-D)
+  CUtensorMap tmAR[FO_MAX_R];  // ALLREDUCE: every rank's full output as [N, rows/R, R] (3-D)
 };
 
 enum Completion : int { FO_COMPLETE_NONE = 0, FO_COMPLETE_BF16 = 1, FO_COMPLETE_ALLREDUCE = 2 };
@@ -150,46 +151,19 @@ __device__ __forceinline__ bool signal_partial(uint32_t* ctr, int R) {
   return false;
 }
 
-// Completion action on the 32 x 256 quarter of shard c at (row0, n0), all
-// R partials in place (called by all 32 lanes of the publishing warp):
-//   BF16       round the fp32 sums once to bf16 into the bf16 output;
-//   ALLREDUCE  copy the finished rows into every other rank's full output
-//              (the all-gather half of reduce-scatter + all-gather).
-// 128-bit L2 loads, eight in flight per lane.
-static __device__ __noinline__ void complete_quarter(const FoParams& p, int c, int row0, int n0, int lane) {
-  const int rows = min(32, p.rows_per_chunk - row0);
-  const int cols = min(FO_BN, (int)p.n_cols - n0);
-  if (rows <= 0 || cols <= 0) return;
-  const size_t N = (size_t)p.n_cols;
-  const float* src = p.shard[c] + (size_t)row0 * N + n0;
-  for (int i0 = 0; i0 < rows; i0 += 4) {
-    float4 v[4][2];
+// Loads 32 fp32 of row `row` (columns col0..col0+31) of a shard with 128-bit
+// L2 loads; rows past the shard or columns past N read as zero.
+__device__ __forceinline__ void load_sum32(const float* shard, int row, int rows, int col0, int ncols, size_t N,
+                                           float (&s)[32]) {
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const int i = i0 + a, j = lane * 4 + b * 128;
-        if (i < rows && j < cols) v[a][b] = __ldcg(reinterpret_cast<const float4*>(src + i * N + j));
-      }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        const int i = i0 + a, j = lane * 4 + b * 128;
-        if (i >= rows || j >= cols) continue;
-        if (p.completion == FO_COMPLETE_BF16) {
-          __nv_bfloat162 lo = __floats2bfloat162_rn(v[a][b].x, v[a][b].y);
-          __nv_bfloat162 hi = __floats2bfloat162_rn(v[a][b].z, v[a][b].w);
-          uint2 w;
-          w.x = *reinterpret_cast<uint32_t*>(&lo);
-          w.y = *reinterpret_cast<uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.fin_out[c]) + (size_t)(row0 + i) * N + n0 + j) = w;
-        } else {
-          const size_t off = ((size_t)c * p.rows_per_chunk + row0 + i) * N + n0 + j;
-          for (int q = 0; q < p.R; ++q)
-            if (q != c) __stcg(reinterpret_cast<float4*>(p.ar_full[q] + off), v[a][b]);
-        }
-      }
+  for (int k = 0; k < 8; ++k) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < rows && col0 + 4 * k < ncols)
+      v = __ldcg(reinterpret_cast<const float4*>(shard + (size_t)row * N + col0 + 4 * k));
+    s[4 * k] = v.x;
+    s[4 * k + 1] = v.y;
+    s[4 * k + 2] = v.z;
+    s[4 * k + 3] = v.w;
   }
 }
 
@@ -447,22 +421,17 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
     // RS: this warp's last partial, not yet published (same in every lane).
     uint32_t* pend_ctr = nullptr;
     bool pend_skip = false;
-    int pend_c = 0, pend_row0 = 0, pend_n0 = 0;
     // Publish the deferred partial (every lane calls; lane 0 owns the bulk
     // groups): wait until its writes are performed (all groups, or all but
-    // the newest tile's), release-count it, and if it completes its tile,
-    // run the plan's completion action.
+    // the newest tile's 8) and release-count it.
     auto publish = [&](bool all) {
       if (!pend_ctr) return;
-      uint32_t done = 0;
       if (lane == 0) {
         if (all) bulk_wait<0>();
         else bulk_wait<kSubRS>();
         fence_proxy_async_global();
-        if (!pend_skip) done = signal_partial(pend_ctr, p.R) ? 1u : 0u;
+        if (!pend_skip) signal_partial(pend_ctr, p.R);
       }
-      done = __shfl_sync(0xffffffffu, done, 0);
-      if (done && p.completion != FO_COMPLETE_NONE) complete_quarter(p, pend_c, pend_row0, pend_n0, lane);
       pend_ctr = nullptr;
     };
     for (int L = unit; L < total; L += units, ++tcount) {
@@ -486,12 +455,17 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
 
       uint32_t* ctr = nullptr;
       bool ok = true;
+      // The owner's last partial finishes the tile when the plan has a
+      // completion action (all-reduce, bf16 output).
+      const bool fin = EPI == EPI_RS && p.completion != FO_COMPLETE_NONE && ti.ord == p.R - 1;
       if constexpr (EPI == EPI_RS) {
         ctr = p.counters + (((size_t)ti.c * p.ctr_tiles_m + mt128) * p.tiles_n + ti.nt) * 4 + q;
+        if (fin) publish(true);   // its groups differ from a reduce tile's 8
         if (ti.ord > 0) {
           // The shard must already hold its first (stored) partial; in
-          // deterministic mode, every partial that comes before this one.
-          const uint32_t need = p.deterministic ? (uint32_t)ti.ord : 1u;
+          // deterministic mode every partial before this one; the finisher
+          // needs all R-1 others.
+          const uint32_t need = fin ? (uint32_t)(p.R - 1) : (p.deterministic ? (uint32_t)ti.ord : 1u);
           const uint32_t have = __shfl_sync(0xffffffffu, lane == 0 ? ld_acquire_u32(ctr) : 0u, 0);
           int good = 1;
           if (have < need) {
@@ -509,7 +483,89 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
         }
       }
 
-      if constexpr (EPI == EPI_AG) {
+      const size_t ncols = (size_t)p.n_cols;
+      const float* shard = EPI == EPI_RS ? p.shard[ti.c] : nullptr;
+      if (EPI == EPI_RS && fin && p.completion == FO_COMPLETE_BF16) {
+        // Finisher, bf16 output: 4 sub-tiles of 32 rows x 64 columns; own
+        // partial + the other R-1 partials' sum, rounded once.
+#pragma unroll 1
+        for (int j = 0; j < FO_BN / 64; ++j) {
+          uint32_t v0[32], v1[32], w[32];
+          float s0[32], s1[32];
+          tmem_ld32(tbase + j * 64, v0);
+          tmem_ld32(tbase + j * 64 + 32, v1);
+          load_sum32(shard, row0 + lane, p.rows_per_chunk, n0 + j * 64, (int)ncols, ncols, s0);
+          load_sum32(shard, row0 + lane, p.rows_per_chunk, n0 + j * 64 + 32, (int)ncols, ncols, s1);
+          tmem_ld_wait();
+          reg_fence(v0);
+          reg_fence(v1);
+          if (j == FO_BN / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (PAIR) mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+              else mbar_arrive(tempty_bar(acc));
+            }
+          }
+          if (!ok) continue;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(v0[2 * i]) + s0[2 * i],
+                                                      __uint_as_float(v0[2 * i + 1]) + s0[2 * i + 1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(v1[2 * i]) + s1[2 * i],
+                                                      __uint_as_float(v1[2 * i + 1]) + s1[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t*>(&h0);
+            w[16 + i] = *reinterpret_cast<uint32_t*>(&h1);
+          }
+          const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          stage_row_sw128(buf, lane, w);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.tmF[ti.c], buf, n0 + j * 64, row0);
+            bulk_commit();
+          }
+        }
+        if (ok && lane == 0) atomicExch(ctr, 0u);   // every partial is in: ready for the next call
+      } else if (EPI == EPI_RS && fin) {
+        // Finisher, all-reduce: 8 sub-tiles of 32 rows x 32 fp32 columns;
+        // own partial + the other R-1 partials' sum, stored to the same rows
+        // of every rank's full output (the all-gather half).
+        constexpr int kSub = FO_BN / 32;
+#pragma unroll 1
+        for (int j = 0; j < kSub; ++j) {
+          uint32_t v[32];
+          float sum[32];
+          tmem_ld32(tbase + j * 32, v);
+          load_sum32(shard, row0 + lane, p.rows_per_chunk, n0 + j * 32, (int)ncols, ncols, sum);
+          tmem_ld_wait();
+          reg_fence(v);
+          if (j == kSub - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (PAIR) mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+              else mbar_arrive(tempty_bar(acc));
+            }
+          }
+          if (!ok) continue;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + sum[i]);
+          const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+          stage_row_sw128(buf, lane, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int qq = 0; qq < p.R; ++qq) tma_store_3d(&p.tmAR[qq], buf, n0 + j * 32, row0, ti.c);
+            bulk_commit();
+          }
+        }
+        if (ok && lane == 0) atomicExch(ctr, 0u);   // every partial is in: ready for the next call
+      } else if constexpr (EPI == EPI_AG) {
         // 4 sub-tiles of 32 rows x 64 bf16 columns.
 #pragma unroll 1
         for (int j = 0; j < FO_BN / 64; ++j) {
@@ -595,9 +651,9 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
             pend_ctr = ctr;
             pend_skip = p.fault_inject == FO_INJECT_SKIP_SIGNAL && ti.c == 0 && mt128 == 0 && ti.nt == 0 &&
                         q == 0 && ti.ord == 0;
-            pend_c = ti.c;
-            pend_row0 = row0;
-            pend_n0 = n0;
+            // With a finisher waiting for every other partial of the tile,
+            // publishing late would stall it: publish this one now.
+            if (p.completion != FO_COMPLETE_NONE) publish(true);
           }
         }
       }

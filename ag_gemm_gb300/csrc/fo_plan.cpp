@@ -47,9 +47,17 @@ void build_table(fo_plan_s* p) {
     }
   // The kernel's task order.
   int skew = p->d.interleave;
-  if (skew == FO_INTERLEAVE_AUTO) skew = ag ? FO_INTERLEAVE_LOCKSTEP : FO_INTERLEAVE_SKEWED;
+  if (skew == FO_INTERLEAVE_AUTO)
+    skew = (ag || p->d.op == FO_OP_DP_GRAD_RS) ? FO_INTERLEAVE_RANK_MAJOR : FO_INTERLEAVE_SKEWED;
   int n = 0;
-  if (skew == FO_INTERLEAVE_SKEWED) {
+  if (skew == FO_INTERLEAVE_RANK_MAJOR) {
+    for (int r = 0; r < R; ++r)
+      for (int s = 0; s < R; ++s) {
+        p->task_r[n] = r;
+        p->task_s[n] = s;
+        ++n;
+      }
+  } else if (skew == FO_INTERLEAVE_SKEWED) {
     // Slot t = s - r (rank r runs r steps behind rank 0); inside a slot by
     // ascending step, so every shard receives its partials in step order.
     for (int t = -(R - 1); t <= R - 1; ++t)
@@ -204,7 +212,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (d->w_layout != FO_W_KN && d->w_layout != FO_W_NK) return FO_ERR_INVALID_ARG;
   if (d->fault_inject < FO_INJECT_NONE || d->fault_inject > FO_INJECT_SKIP_SIGNAL) return FO_ERR_INVALID_ARG;
   if (d->tile_config != FO_TILE_AUTO && d->tile_config != FO_TILE_SINGLE) return FO_ERR_INVALID_ARG;
-  if (d->interleave < FO_INTERLEAVE_AUTO || d->interleave > FO_INTERLEAVE_SKEWED) return FO_ERR_INVALID_ARG;
+  if (d->interleave < FO_INTERLEAVE_AUTO || d->interleave > FO_INTERLEAVE_RANK_MAJOR) return FO_ERR_INVALID_ARG;
   for (int i = 0; i < 5; ++i)
     if (d->reserved[i]) return FO_ERR_INVALID_ARG;
   if (d->M <= 0 || d->N <= 0 || d->K <= 0) return FO_ERR_SHAPE;
@@ -229,6 +237,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
       if (((K / R) * eb) % 16) return FO_ERR_ALIGN;   // rows of X_r (and of W_r if NK)
       if ((N * eb) % 16) return FO_ERR_ALIGN;         // rows of W_r (KN)
       if ((N * 4) % 16) return FO_ERR_ALIGN;          // rows of Y
+      if (d->out_dtype == FO_BF16 && (N * 2) % 16) return FO_ERR_ALIGN;   // rows of a bf16 Y
       break;
     case FO_OP_AG_GEMM:
       if (N % R) return FO_ERR_SHAPE;
@@ -244,6 +253,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
       // contiguous dimension, so it must fall on a 16-byte boundary.
       if (((M / R) * 2) % 16) return FO_ERR_ALIGN;
       if ((M * 2) % 16 || (N * 2) % 16) return FO_ERR_ALIGN;
+      if ((N * 4) % 16) return FO_ERR_ALIGN;
       break;
   }
 
@@ -260,7 +270,9 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
     case FO_OP_AG_GEMM: p->k_red = K; p->n_out = N / R; break;
     default: p->k_red = K; p->n_out = N; break;
   }
-  p->pair = eb == 2 && d->tile_config == FO_TILE_AUTO;
+  // AUTO: CTA-pair tiles for bf16 unless a shard holds 128 rows or fewer,
+  // where a 256-row pair tile would be mostly padding.
+  p->pair = eb == 2 && d->tile_config == FO_TILE_AUTO && M / R > FO_BM;
   p->tiles_m = (int)cdiv(p->rows_per_chunk, p->pair ? 2 * FO_BM : FO_BM);
   p->ctr_tiles_m = 2 * (int)cdiv(p->rows_per_chunk, 2 * FO_BM);
   p->pieces = (int)cdiv(p->rows_per_chunk, 32);

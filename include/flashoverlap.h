@@ -107,8 +107,17 @@ typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
  *           rank-adaptive RS order every partial of one slot is bound for the
  *           same owner, so that owner's shard stays in L2 while its partials
  *           are added.
- * AUTO:     SKEWED for GEMM_RS / DP_GRAD_RS, LOCKSTEP for AG_GEMM. */
-typedef enum { FO_INTERLEAVE_AUTO = 0, FO_INTERLEAVE_LOCKSTEP = 1, FO_INTERLEAVE_SKEWED = 2 } fo_interleave;
+ * RANK_MAJOR: all of rank 0's steps, then rank 1's, ...: one rank's
+ *           weights (AG) or upstream gradient (DP) stay in L2 across its
+ *           steps.
+ * AUTO:     SKEWED for GEMM_RS / GEMM_AR, RANK_MAJOR for AG_GEMM and
+ *           DP_GRAD_RS (the fastest of the three on GB300 for each op). */
+typedef enum {
+  FO_INTERLEAVE_AUTO = 0,
+  FO_INTERLEAVE_LOCKSTEP = 1,
+  FO_INTERLEAVE_SKEWED = 2,
+  FO_INTERLEAVE_RANK_MAJOR = 3
+} fo_interleave;
 
 /* Global GEMM sizes (M, N, K); the per-rank operands are, for each op:
  *   FO_OP_GEMM_RS    X_r [M x K/R], W_r [K/R x N] (or [N x K/R]), Y_r [M/R x N]

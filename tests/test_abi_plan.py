@@ -156,7 +156,7 @@ def test_workspace_counts_pair_tiles():
 
 @pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("op", ["gemm_rs", "ag_gemm", "dp_grad_rs"])
-@pytest.mark.parametrize("interleave", ["auto", "lockstep", "skewed"])
+@pytest.mark.parametrize("interleave", ["auto", "lockstep", "skewed", "rank_major"])
 def test_task_order_keeps_every_ranks_schedule_order(R, op, interleave):
     dims = {"gemm_rs": (128 * R, 256, 64 * R), "ag_gemm": (128 * R, 64 * R, 256), "dp_grad_rs": (8 * R, 256, 64)}[op]
     p = B.fo_plan(op, R, *dims, interleave=interleave)
@@ -184,12 +184,18 @@ def test_skewed_order_groups_partials_by_owner_in_step_order(R):
         assert steps == sorted(steps) == list(range(R))
 
 
-def test_auto_interleave_is_skewed_for_rs_and_lockstep_for_ag():
+def test_auto_interleave_is_skewed_for_rs_and_rank_major_for_ag_and_dp():
     R = 4
     rs = B.fo_plan_task_order(B.fo_plan("gemm_rs", R, 512, 256, 256))
     assert rs == B.fo_plan_task_order(B.fo_plan("gemm_rs", R, 512, 256, 256, interleave="skewed"))
+    ar = B.fo_plan_task_order(B.fo_plan("gemm_ar", R, 512, 256, 256))
+    assert ar == rs
     ag = B.fo_plan_task_order(B.fo_plan("ag_gemm", R, 512, 256, 256))
-    assert ag == [(r, s) for s in range(R) for r in range(R)]
+    assert ag == [(r, s) for r in range(R) for s in range(R)]
+    dp = B.fo_plan_task_order(B.fo_plan("dp_grad_rs", R, 512, 256, 256))
+    assert dp == [(r, s) for r in range(R) for s in range(R)]
+    lock = B.fo_plan_task_order(B.fo_plan("ag_gemm", R, 512, 256, 256, interleave="lockstep"))
+    assert lock == [(r, s) for s in range(R) for r in range(R)]
 
 
 def test_copy_transport_requires_gather_buffers():

@@ -140,7 +140,7 @@ def test_gemm_rs_deterministic_mode_is_bitwise_repeatable(dev):
 
 
 @pytest.mark.parametrize("tile", TILES)
-@pytest.mark.parametrize("interleave", ["lockstep", "skewed"])
+@pytest.mark.parametrize("interleave", ["lockstep", "skewed", "rank_major"])
 @pytest.mark.parametrize("det", [False, True])
 def test_gemm_rs_every_interleave_bit_exact(dev, tile, interleave, det):
     outs, ref = run_gemm_rs(dev, 8, 2048, 136, 776, tile=tile, interleave=interleave, deterministic=det, repeat=2)
@@ -267,9 +267,9 @@ def test_dp_grad_rs_bf16_output(dev):
 
 # ------------------------------------------------------------------ AG-GEMM
 
-def run_ag(dev, R, M, K, N, *, mode="int", layout="kn", seed=1, tile="auto"):
+def run_ag(dev, R, M, K, N, *, mode="int", layout="kn", seed=1, tile="auto", interleave="auto"):
     inp = ag_gemm_inputs(R, M, K, N // R, mode=mode, seed=seed)
-    plan = B.fo_plan("ag_gemm", R, M, N, K, w_layout=layout, tile_config=tile)
+    plan = B.fo_plan("ag_gemm", R, M, N, K, w_layout=layout, tile_config=tile, interleave=interleave)
     X = [x.to(dev) for x in inp["X"]]
     W = [(w if layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
     Y = Guarded(R, (M, N // R), torch.bfloat16, dev)
@@ -349,6 +349,13 @@ def test_ag_copy_missing_ready_flag_times_out(dev):
         assert np.array_equal(Y[r], oracle.round_bf16(ref[r]))
 
 
+@pytest.mark.parametrize("interleave", ["skewed", "rank_major"])
+def test_ag_gemm_interleaves_bit_exact(dev, interleave):
+    got, ref = run_ag(dev, 4, 1024, 136, 1056, interleave=interleave)
+    for r in range(4):
+        assert np.array_equal(got[r], oracle.round_bf16(ref[r]))
+
+
 @pytest.mark.parametrize("R,M,K,N", [(4, 1024, 512, 1024), (2, 400, 200, 336)])
 def test_ag_gemm_random_bf16_within_tolerance(dev, R, M, K, N):
     got, ref = run_ag(dev, R, M, K, N, mode="randn")
@@ -380,7 +387,7 @@ def test_dp_grad_rs_integer_bit_exact(dev, R, T, M, N, tile):
         assert np.array_equal(got[d], ref[d]), f"shard {d}"
 
 
-@pytest.mark.parametrize("interleave", ["lockstep", "skewed"])
+@pytest.mark.parametrize("interleave", ["lockstep", "skewed", "rank_major"])
 def test_dp_grad_rs_interleaves_bit_exact(dev, interleave):
     got, ref = run_dp(dev, 4, 200, 800, 328, interleave=interleave)
     for d in range(4):
