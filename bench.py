@@ -283,7 +283,7 @@ def run_ours(args):
         return run_layer(args, dev, world, rank)
     w = WORKLOADS[args.workload]
     if w.op != "gemm_rs":
-        raise SystemExit("bench.py times gemm_rs workloads")
+        return run_other_op(args, w, dev, world, rank)
     R, M, K, N = w.R, w.dims["M"], w.dims["K"], w.dims["N"]
     flops = w.flops()
     peaks, peak_src = load_peaks()
@@ -441,6 +441,79 @@ def run_ours(args):
 
 
 LAYER_WORKLOAD = "tpsp_layer_r8_t8192_h4096_f14336"
+
+
+def run_other_op(args, w, dev, world, rank):
+    """Timed loop of the AG-GEMM or DP-grad-RS workloads (same timing rules
+    as the default line; no comparison legs)."""
+    import torch
+    import torch.distributed as dist
+
+    from ag_gemm_gb300 import binding as B
+    d = w.dims
+    inp = w.make()
+    if w.op == "ag_gemm":
+        R, M, K, Nr = w.R, d["M"], d["K"], d["N"]
+        A = [x.to(dev) for x in inp["X"]]
+        Bm = [x.to(dev) for x in inp["W"]]
+        Y = [torch.empty(M, Nr, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        plan = B.fo_plan("ag_gemm", R, M, Nr * R, K)
+    else:
+        R, T, M, N = w.R, d["T"], d["M"], d["N"]
+        A = [x.to(dev) for x in inp["X"]]
+        Bm = [x.to(dev) for x in inp["dY"]]
+        Y = [torch.empty(M // R, N, dtype=torch.float32, device=dev) for _ in range(R)]
+        plan = B.fo_plan("dp_grad_rs", R, M, N, T)
+    ws = torch.empty(B.fo_workspace_size(plan), dtype=torch.uint8, device=dev)
+    B.fo_workspace_init(plan, ws)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if w.op == "ag_gemm":
+            B.fo_ag_gemm(plan, A, Bm, Y, None, ws, stream)
+        else:
+            B.fo_dp_grad_rs(plan, A, Bm, Y, ws, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(_smi_id(dev)) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        clk.mark("t0")
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark("t1")
+    code, info = B.fo_status_query(plan, ws, stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} {info}")
+    elapsed_ms = ev[0][0].elapsed_time(ev[-1][1])
+    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    flops = w.flops()
+    peaks, peak_src = load_peaks()
+    sustained = elapsed_ms >= 250.0
+    peak = float(peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"])
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "R": w.R, **d, "l2": "no flush: a step's operands exceed the 129 MB L2"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                     "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)") + ", " + peak_src},
+        "gpu_launches": args.steps * B.fo_plan_last_launches(plan),
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
 
 
 def run_layer(args, dev, world, rank):
