@@ -47,6 +47,18 @@ namespace fo {
 
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBuf = 32 * 128;              // 32 rows x 128 bytes
+// Staging buffers per epilogue warp and pipeline depths (overridable at
+// build time; the defaults fill the 227 KB of shared memory).
+#ifndef FO_EPI_BUFS
+#define FO_EPI_BUFS 2
+#endif
+#ifndef FO_PAIR_STAGES
+#define FO_PAIR_STAGES 6
+#endif
+#ifndef FO_SINGLE_STAGES
+#define FO_SINGLE_STAGES 4
+#endif
+constexpr int kEpiBufs = FO_EPI_BUFS;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 // AG variants that also move X shards into the gather buffers G_r carry four
 // more warps; a piece is 32 rows of one shard.
@@ -59,13 +71,14 @@ constexpr uint64_t kMbarLimitNs = 2000000000ull;
 
 template <bool PAIR>
 struct Cfg {
-  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kStages = PAIR ? FO_PAIR_STAGES : FO_SINGLE_STAGES;
   static constexpr int kAStage = FO_BM * FO_BK_BYTES;                       // 16 KB
   static constexpr int kBRows = PAIR ? FO_BN / 2 : FO_BN;                   // B rows (N) in this CTA
   static constexpr int kBStage = kBRows * FO_BK_BYTES;                      // 16 or 32 KB
   static constexpr int kStageBytes = kAStage + kBStage;
   static constexpr int kTileM = PAIR ? 2 * FO_BM : FO_BM;                   // rows of one tile
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * 2 * kEpiBuf + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiWarps * kEpiBufs * kEpiBuf + kBarBytes;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 enum Epi : int { EPI_RS = 0, EPI_AG = 1, EPI_PARTIAL = 2 };
@@ -221,7 +234,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sStage = base;
   const uint32_t sEpi = base + kStages * C::kStageBytes;
-  const uint32_t sBar = sEpi + kEpiWarps * 2 * kEpiBuf;
+  const uint32_t sBar = sEpi + kEpiWarps * kEpiBufs * kEpiBuf;
   auto full_bar = [&](int i) { return sBar + 8u * i; };
   auto empty_bar = [&](int i) { return sBar + 8u * (kStages + i); };
   auto tfull_bar = [&](int a) { return sBar + 8u * (2 * kStages + a); };
@@ -517,8 +530,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
             w[i] = *reinterpret_cast<uint32_t*>(&h0);
             w[16 + i] = *reinterpret_cast<uint32_t*>(&h1);
           }
-          const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
-          if (lane == 0) bulk_wait_read<1>();
+          const uint32_t buf = sEpi + (uint32_t)((e * kEpiBufs + (j % kEpiBufs)) * kEpiBuf);
+          if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
           __syncwarp();
           stage_row_sw128(buf, lane, w);
           fence_proxy_async_smem();
@@ -553,8 +566,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           if (!ok) continue;
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + sum[i]);
-          const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
-          if (lane == 0) bulk_wait_read<1>();
+          const uint32_t buf = sEpi + (uint32_t)((e * kEpiBufs + (j % kEpiBufs)) * kEpiBuf);
+          if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
           __syncwarp();
           stage_row_sw128(buf, lane, v);
           fence_proxy_async_smem();
@@ -592,8 +605,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
             w[i] = *reinterpret_cast<uint32_t*>(&h0);
             w[16 + i] = *reinterpret_cast<uint32_t*>(&h1);
           }
-          const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
-          if (lane == 0) bulk_wait_read<1>();
+          const uint32_t buf = sEpi + (uint32_t)((e * kEpiBufs + (j % kEpiBufs)) * kEpiBuf);
+          if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
           __syncwarp();
           stage_row_sw128(buf, lane, w);
           fence_proxy_async_smem();
@@ -626,8 +639,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
             }
           }
           if (!ok) continue;
-          const uint32_t buf = sEpi + (uint32_t)((e * 2 + (j & 1)) * kEpiBuf);
-          if (lane == 0) bulk_wait_read<1>();
+          const uint32_t buf = sEpi + (uint32_t)((e * kEpiBufs + (j % kEpiBufs)) * kEpiBuf);
+          if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
           __syncwarp();
           stage_row_sw128(buf, lane, v[j & 1]);
           fence_proxy_async_smem();
