@@ -28,6 +28,7 @@ W_LAYOUTS = {"kn": 0, "nk": 1}
 INJECT = {"none": 0, "drop_transfer": 1, "skip_signal": 2}
 TILE_CONFIGS = {"auto": 0, "single": 1}
 INTERLEAVES = {"auto": 0, "lockstep": 1, "skewed": 2, "rank_major": 3}
+RS_ALGOS = {"direct": 0, "ring": 1}
 
 # Every symbol include/flashoverlap.h declares.
 EXPORTED = [
@@ -54,7 +55,8 @@ class PlanDesc(ctypes.Structure):
         ("op", c_int32), ("R", c_int32), ("M", c_int64), ("N", c_int64), ("K", c_int64),
         ("in_dtype", c_int32), ("out_dtype", c_int32), ("sched", c_int32), ("ag_transport", c_int32),
         ("w_layout", c_int32), ("deterministic", c_int32), ("timeout_ns", c_uint64),
-        ("fault_inject", c_int32), ("tile_config", c_int32), ("interleave", c_int32), ("reserved", c_int32 * 5),
+        ("fault_inject", c_int32), ("tile_config", c_int32), ("interleave", c_int32), ("rs_algo", c_int32),
+        ("reserved", c_int32 * 4),
     ]
 
 
@@ -165,7 +167,8 @@ class Plan:
 
 def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dtype=None,
             sched="rank_adaptive", ag_transport="peer_read", w_layout="kn", deterministic=False,
-            timeout_ns=0, fault_inject="none", tile_config="auto", interleave="auto") -> Plan:
+            timeout_ns=0, fault_inject="none", tile_config="auto", interleave="auto",
+            rs_algo="direct") -> Plan:
     lib = load()
     if out_dtype is None:
         out_dtype = "bf16" if op == "ag_gemm" else "f32"
@@ -183,6 +186,7 @@ def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dty
     d.fault_inject = INJECT[fault_inject]
     d.tile_config = TILE_CONFIGS[tile_config]
     d.interleave = INTERLEAVES[interleave]
+    d.rs_algo = RS_ALGOS[rs_algo]
     h = c_void_p()
     _check(lib.fo_plan(ctypes.byref(d), ctypes.byref(h)), "fo_plan")
     return Plan(h.value, d)

@@ -155,14 +155,18 @@ fo_status check_ptrs(int R, const void* const* a) {
 // Encode the operand maps of a GEMM-RS / DP-grad-RS / GEMM-AR / pure-control
 // call. The fp32 destination of the partials is: Y_c (RS/DP with fp32 out),
 // the workspace's shard sums (bf16 out), rank c's own rows of its full
-// output (AR), or the computing rank's own buffer (partials control).
+// output (AR), or the computing rank's own buffer (partials control). Under
+// the ring RS the forwards go to the receivers' buffers in the workspace and
+// only the last hop writes Y_c.
 fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A, const void* const* B,
                         void* const* D, void* ws, fo::FoParams** out) {
   const int kind = partial ? KIND_PART : (dp ? KIND_DP : KIND_RS);
-  const bool to_ws = !partial && p->d.out_dtype == FO_BF16;
+  const bool ring = !partial && p->ring;
+  const bool bf16_out = !partial && p->d.out_dtype == FO_BF16;
+  const bool to_ws = bf16_out && !ring;
   const bool ar = !partial && p->d.op == FO_OP_GEMM_AR;
   fo::FoParams* k = cached_params(p, kind, A, B, (const void* const*)D);
-  if (k && (!to_ws || p->param_cache_ws == ws)) {
+  if (k && ((!to_ws && !ring) || p->param_cache_ws == ws)) {
     fill_common(p, k, ws);
     *out = k;
     return FO_OK;
@@ -192,19 +196,28 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
     float* shard = static_cast<float*>(D[r]);
     if (to_ws) shard = reinterpret_cast<float*>(static_cast<char*>(ws) + p->ws_shard_off + r * p->ws_shard_stride);
     if (ar) shard = static_cast<float*>(D[r]) + (size_t)r * rpc * N;
-    ok &= enc2d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, shard, N, rpc, N * 4, 32, 32);
+    if (ring && bf16_out) shard = nullptr;   // the last hop writes the bf16 output directly
+    if (shard) ok &= enc2d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, shard, N, rpc, N * 4, 32, 32);
     k->shard[r] = shard;
     // The finisher's outputs: the bf16 shard, or every rank's full output
     // viewed as [N, rows/R, R] so a store clips at the shard's last row.
-    if (to_ws) ok &= enc2d(&k->tmF[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D[r], N, rpc, N * 2, 64, 32);
+    if (bf16_out) ok &= enc2d(&k->tmF[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D[r], N, rpc, N * 2, 64, 32);
     if (ar) ok &= enc3d(&k->tmAR[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D[r], N, rpc, R, N * 4, rpc * N * 4, 32, 32);
+    if (ring) {
+      // Rank r's receive buffer: chunk c's rows at c * rows/R, viewed as
+      // [N, rows/R, R] like an all-reduce output.
+      float* inbox = reinterpret_cast<float*>(static_cast<char*>(ws) + p->ws_ring_off + r * p->ws_ring_stride);
+      k->inbox[r] = inbox;
+      ok &= enc3d(&k->tmAR[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, inbox, N, rpc, R, N * 4, rpc * N * 4, 32, 32);
+    }
   }
   if (!ok) return FO_ERR_CUDA;
   remember(p, kind, A, B, (const void* const*)D);
   p->param_cache_ws = ws;
   fill_common(p, k, ws);
   k->completion = partial ? fo::FO_COMPLETE_NONE
-                          : (to_ws ? fo::FO_COMPLETE_BF16 : (ar ? fo::FO_COMPLETE_ALLREDUCE : fo::FO_COMPLETE_NONE));
+                          : (bf16_out ? fo::FO_COMPLETE_BF16 : (ar ? fo::FO_COMPLETE_ALLREDUCE : fo::FO_COMPLETE_NONE));
+  k->ring = ring ? 1 : 0;
   *out = k;
   return FO_OK;
 }
@@ -346,6 +359,7 @@ fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const
                                         void* const* Y, void* scratch, fo::FoParams* k, int* variant,
                                         int* grid) {
   if (p->d.op != FO_OP_GEMM_RS || p->d.out_dtype != FO_F32) return FO_ERR_DTYPE;
+  if (p->ring) return FO_ERR_UNSUPPORTED;   // the ring's receive buffers do not fit the static scratch
   DevInfo di;
   fo_status st = preflight(p, &di);
   if (st != FO_OK) return st;

@@ -55,6 +55,9 @@ struct fo_plan_s {
   size_t ws_flags_off;     // AG copy transport: uint32 [R][R][pieces]
   size_t ws_shard_off;     // bf16 output: fp32 shard sums, R x align256(rows/R * N * 4)
   size_t ws_shard_stride;
+  size_t ws_ring_off;      // ring RS: rank q's fp32 receive buffer [M x N] at off + q * stride
+  size_t ws_ring_stride;
+  bool ring;               // d.rs_algo == FO_RS_RING
 
   int32_t last_launches;
   void* param_cache;       // host copy of the last kernel parameter block

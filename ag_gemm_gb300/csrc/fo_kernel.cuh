@@ -118,7 +118,14 @@ struct alignas(128) FoParams {
   int64_t n_cols;              // N: columns of a shard row
   float* shard[FO_MAX_R];      // fp32 shard rows that tmD[c] addresses
   CUtensorMap tmF[FO_MAX_R];   // BF16: the bf16 shard outputs [rows/R x N] (2-D)
-  CUtensorMap tmAR[FO_MAX_R];  // ALLREDUCE: every rank's full output as [N, rows/R, R] (3-D)
+  CUtensorMap tmAR[FO_MAX_R];  // ALLREDUCE: every rank's full output as [N, rows/R, R] (3-D);
+                               // ring RS: every rank's receive buffer, same shape
+  // Ring RS: the partial of hop s > 0 (the s-th rank of chunk c's chain) is
+  // added to the running sum its predecessor left in inbox[r] (chunk c's
+  // rows) and forwarded into inbox[r+1], or, at the last hop (the owner),
+  // written to the output.
+  int32_t ring;
+  float* inbox[FO_MAX_R];      // rank q's receive buffer [M x N] fp32 (chunk-major rows)
 };
 
 enum Completion : int { FO_COMPLETE_NONE = 0, FO_COMPLETE_BF16 = 1, FO_COMPLETE_ALLREDUCE = 2 };
@@ -165,13 +172,13 @@ __device__ __forceinline__ bool signal_partial(uint32_t* ctr, int R) {
 }
 
 // Loads 32 fp32 of row `row` (columns col0..col0+31) of a shard with 128-bit
-// L2 loads; rows past the shard or columns past N read as zero.
+// L2 loads; rows past the shard, columns past N or a null shard read as zero.
 __device__ __forceinline__ void load_sum32(const float* shard, int row, int rows, int col0, int ncols, size_t N,
                                            float (&s)[32]) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row < rows && col0 + 4 * k < ncols)
+    if (shard && row < rows && col0 + 4 * k < ncols)
       v = __ldcg(reinterpret_cast<const float4*>(shard + (size_t)row * N + col0 + 4 * k));
     s[4 * k] = v.x;
     s[4 * k + 1] = v.y;
@@ -453,6 +460,16 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1u;
       if constexpr (EPI == EPI_RS) {
+        if (p.ring && ti.ord > 0) {
+          // Ring hop: warm L2 with the running sum this warp will read once
+          // the accumulator is ready (each lane one row of its quarter).
+          const int row = (ti.mt * (PAIR ? 2 : 1) + (int)prank) * FO_BM + q * 32 + lane;
+          const int ncol = min(FO_BN, (int)p.n_cols - ti.nt * FO_BN);
+          if (row < p.rows_per_chunk && ncol > 0)
+            prefetch_l2_bulk(p.inbox[ti.r] + ((size_t)ti.c * p.rows_per_chunk + row) * (size_t)p.n_cols +
+                                 (size_t)ti.nt * FO_BN,
+                             (uint32_t)ncol * 4u);
+        }
         // About to block until the next accumulator is ready: publish the
         // deferred partial first (a warp never holds one while it waits, so
         // a waiter elsewhere always sees it eventually).
@@ -469,16 +486,27 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       uint32_t* ctr = nullptr;
       bool ok = true;
       // The owner's last partial finishes the tile when the plan has a
-      // completion action (all-reduce, bf16 output).
-      const bool fin = EPI == EPI_RS && p.completion != FO_COMPLETE_NONE && ti.ord == p.R - 1;
+      // completion action (all-reduce, bf16 output). Under the ring RS every
+      // later hop of a chain is a finisher too: it adds the running sum its
+      // predecessor forwarded and passes the result on.
+      const bool last = ti.ord == p.R - 1;
+      const bool ring = EPI == EPI_RS && p.ring != 0;
+      const bool hop = ring && ti.ord > 0;
+      const bool fin = EPI == EPI_RS && ((p.completion != FO_COMPLETE_NONE && last) || hop);
       if constexpr (EPI == EPI_RS) {
         ctr = p.counters + (((size_t)ti.c * p.ctr_tiles_m + mt128) * p.tiles_n + ti.nt) * 4 + q;
-        if (fin) publish(true);   // its groups differ from a reduce tile's 8
+        // A bf16 finisher commits 4 bulk groups per tile, not a reduce
+        // tile's 8: release the pending partial before it. A ring hop
+        // releases its predecessor tile's forward here too: the next hop
+        // of that chain may be only a tile behind.
+        if (fin && (hop || (last && p.completion == FO_COMPLETE_BF16))) publish(true);
         if (ti.ord > 0) {
           // The shard must already hold its first (stored) partial; in
           // deterministic mode every partial before this one; the finisher
-          // needs all R-1 others.
-          const uint32_t need = fin ? (uint32_t)(p.R - 1) : (p.deterministic ? (uint32_t)ti.ord : 1u);
+          // needs all R-1 others; a ring hop needs its predecessor's forward
+          // (hop ord-1, the ord-th signal of the tile).
+          const uint32_t need =
+              hop ? (uint32_t)ti.ord : (fin ? (uint32_t)(p.R - 1) : (p.deterministic ? (uint32_t)ti.ord : 1u));
           const uint32_t have = __shfl_sync(0xffffffffu, lane == 0 ? ld_acquire_u32(ctr) : 0u, 0);
           int good = 1;
           if (have < need) {
@@ -497,8 +525,13 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       }
 
       const size_t ncols = (size_t)p.n_cols;
-      const float* shard = EPI == EPI_RS ? p.shard[ti.c] : nullptr;
-      if (EPI == EPI_RS && fin && p.completion == FO_COMPLETE_BF16) {
+      // Where a finisher reads the sum of the partials before its own: the
+      // shard the others added into, or (ring) chunk c's rows of this rank's
+      // receive buffer. The first partial of a tile has nothing to read.
+      const float* sum_src = nullptr;
+      if (EPI == EPI_RS && ti.ord > 0)
+        sum_src = ring ? p.inbox[ti.r] + (size_t)ti.c * p.rows_per_chunk * ncols : p.shard[ti.c];
+      if (EPI == EPI_RS && fin && last && p.completion == FO_COMPLETE_BF16) {
         // Finisher, bf16 output: 4 sub-tiles of 32 rows x 64 columns; own
         // partial + the other R-1 partials' sum, rounded once.
 #pragma unroll 1
@@ -507,8 +540,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           float s0[32], s1[32];
           tmem_ld32(tbase + j * 64, v0);
           tmem_ld32(tbase + j * 64 + 32, v1);
-          load_sum32(shard, row0 + lane, p.rows_per_chunk, n0 + j * 64, (int)ncols, ncols, s0);
-          load_sum32(shard, row0 + lane, p.rows_per_chunk, n0 + j * 64 + 32, (int)ncols, ncols, s1);
+          load_sum32(sum_src, row0 + lane, p.rows_per_chunk, n0 + j * 64, (int)ncols, ncols, s0);
+          load_sum32(sum_src, row0 + lane, p.rows_per_chunk, n0 + j * 64 + 32, (int)ncols, ncols, s1);
           tmem_ld_wait();
           reg_fence(v0);
           reg_fence(v1);
@@ -546,13 +579,20 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
         // Finisher, all-reduce: 8 sub-tiles of 32 rows x 32 fp32 columns;
         // own partial + the other R-1 partials' sum, stored to the same rows
         // of every rank's full output (the all-gather half).
+        // Ring hop, fp32: own partial + the running sum from the receive
+        // buffer, forwarded into the next rank's receive buffer, or (last
+        // hop) stored to the owner's output.
+        // The sum of sub-tile j+1 is loaded while sub-tile j is processed.
         constexpr int kSub = FO_BN / 32;
-#pragma unroll 1
+        float sum[2][32];
+        load_sum32(sum_src, row0 + lane, p.rows_per_chunk, n0, (int)ncols, ncols, sum[0]);
+#pragma unroll
         for (int j = 0; j < kSub; ++j) {
           uint32_t v[32];
-          float sum[32];
           tmem_ld32(tbase + j * 32, v);
-          load_sum32(shard, row0 + lane, p.rows_per_chunk, n0 + j * 32, (int)ncols, ncols, sum);
+          if (j + 1 < kSub)
+            load_sum32(sum_src, row0 + lane, p.rows_per_chunk, n0 + (j + 1) * 32, (int)ncols, ncols,
+                       sum[(j + 1) & 1]);
           tmem_ld_wait();
           reg_fence(v);
           if (j == kSub - 1) {
@@ -565,7 +605,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           }
           if (!ok) continue;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + sum[i]);
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + sum[j & 1][i]);
           const uint32_t buf = sEpi + (uint32_t)((e * kEpiBufs + (j % kEpiBufs)) * kEpiBuf);
           if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
           __syncwarp();
@@ -573,11 +613,25 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            for (int qq = 0; qq < p.R; ++qq) tma_store_3d(&p.tmAR[qq], buf, n0 + j * 32, row0, ti.c);
+            if (!ring)
+              for (int qq = 0; qq < p.R; ++qq) tma_store_3d(&p.tmAR[qq], buf, n0 + j * 32, row0, ti.c);
+            else if (last)
+              tma_store_2d(&p.tmD[ti.c], buf, n0 + j * 32, row0);
+            else
+              tma_store_3d(&p.tmAR[(ti.r + 1) % p.R], buf, n0 + j * 32, row0, ti.c);
             bulk_commit();
           }
         }
-        if (ok && lane == 0) atomicExch(ctr, 0u);   // every partial is in: ready for the next call
+        if (ok && last && lane == 0) atomicExch(ctr, 0u);   // every partial is in: ready for the next call
+        if (ok && !last) {
+          // Ring: the forward is in the next rank's buffer once its stores
+          // are performed. Like a reduce tile's partial, it is released
+          // after the next tile's stores are issued (or before this warp
+          // blocks), so the warp does not wait for its own latest writes.
+          publish(false);
+          pend_ctr = ctr;
+          pend_skip = false;
+        }
       } else if constexpr (EPI == EPI_AG) {
         // 4 sub-tiles of 32 rows x 64 bf16 columns.
 #pragma unroll 1
@@ -649,8 +703,9 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
             if constexpr (EPI == EPI_PARTIAL) {
               tma_store_3d(&p.tmD[ti.r], buf, n0 + j * 32, row0, ti.c);
             } else {
-              if (ti.ord == 0) tma_store_2d(&p.tmD[ti.c], buf, n0 + j * 32, row0);
-              else tma_reduce_add_2d(&p.tmD[ti.c], buf, n0 + j * 32, row0);
+              if (ti.ord != 0) tma_reduce_add_2d(&p.tmD[ti.c], buf, n0 + j * 32, row0);
+              else if (ring && !last) tma_store_3d(&p.tmAR[(ti.r + 1) % p.R], buf, n0 + j * 32, row0, ti.c);
+              else tma_store_2d(&p.tmD[ti.c], buf, n0 + j * 32, row0);
             }
             bulk_commit();
           }

@@ -47,6 +47,7 @@ fo_status scratch_on_current_device(void** out) {
 extern "C" fo_status fo_gemm_rs_noalloc(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y,
                                         fo_stream_t stream) {
   if (!p || p->d.op != FO_OP_GEMM_RS) return FO_ERR_INVALID_ARG;
+  if (p->ring) return FO_ERR_UNSUPPORTED;   // the ring's receive buffers are workspace-sized
   fo_status st;
   if ((st = fo_internal_check_ptrs(p->R, X)) || (st = fo_internal_check_ptrs(p->R, W)) ||
       (st = fo_internal_check_ptrs(p->R, (const void* const*)Y)))

@@ -13,6 +13,8 @@
 // the ring reduce-scatter order, chunk (r - 1 - s) mod R at step s, so that
 // every owner receives exactly one partial per step; AG consumes the shard of
 // rank (r - s) mod R, which its ring predecessor forwarded one step earlier.
+// Under the ring RS algorithm the same order makes rank r's chunk at step s
+// the one rank r-1 handled at step s-1, so the running sum can be forwarded.
 #include <stdlib.h>
 #include <string.h>
 
@@ -47,8 +49,10 @@ void build_table(fo_plan_s* p) {
     }
   // The kernel's task order.
   int skew = p->d.interleave;
-  if (skew == FO_INTERLEAVE_AUTO)
-    skew = (ag || p->d.op == FO_OP_DP_GRAD_RS) ? FO_INTERLEAVE_RANK_MAJOR : FO_INTERLEAVE_SKEWED;
+  if (skew == FO_INTERLEAVE_AUTO) {
+    if (p->ring) skew = FO_INTERLEAVE_LOCKSTEP;   // a chain's hops a whole step apart: no hop waits
+    else skew = (ag || p->d.op == FO_OP_DP_GRAD_RS) ? FO_INTERLEAVE_RANK_MAJOR : FO_INTERLEAVE_SKEWED;
+  }
   int n = 0;
   if (skew == FO_INTERLEAVE_RANK_MAJOR) {
     for (int r = 0; r < R; ++r)
@@ -99,9 +103,10 @@ void build_transfers_and_edges(fo_plan_s* p) {
   p->edges.clear();
   for (int r = 0; r < R; ++r)
     for (int s = 0; s + 1 < R; ++s) p->edges.push_back({r, s, r, s + 1});
-  if (p->d.op == FO_OP_AG_GEMM) {
-    // Ring: after using shard table[r][s], rank r forwards it to r+1, which
-    // consumes it at step s+1. Nothing is forwarded after the last step.
+  if (p->d.op == FO_OP_AG_GEMM || p->ring) {
+    // Ring: after using shard table[r][s] (AG), or adding its partial to the
+    // running sum of chunk table[r][s] (ring RS), rank r forwards it to r+1,
+    // which consumes it at step s+1. Nothing is forwarded after the last step.
     for (int s = 0; s + 1 < R; ++s)
       for (int r = 0; r < R; ++r) p->transfers.push_back({r, (r + 1) % R, p->table[r][s], s});
     for (const fo_transfer& t : p->transfers) p->edges.push_back({t.src, t.step, t.dst, t.step + 1});
@@ -172,7 +177,25 @@ fo_status validate(const fo_plan_s* p) {
     if (t.step >= R - 1) return FO_ERR_PLAN_INVARIANT;                           // no tail send
   for (int s = 0; s < R; ++s)
     if (!is_perm(&p->table[0][s], R, FO_MAX_R)) return FO_ERR_PLAN_INVARIANT;   // (iii)
-  if (ag) {
+  if (p->ring) {
+    // Ring RS: every forward carries the chunk its sender handled at that
+    // step to the next rank, which handles the same chunk one step later;
+    // every rank receives R-1 forwards, all from its ring predecessor.
+    int recv[FO_MAX_R] = {0};
+    for (const fo_transfer& t : p->transfers) {
+      if (t.dst != (t.src + 1) % R || t.step < 0 || t.step + 1 >= R) return FO_ERR_PLAN_INVARIANT;
+      if (p->table[t.src][t.step] != t.chunk || p->table[t.dst][t.step + 1] != t.chunk)
+        return FO_ERR_PLAN_INVARIANT;
+      ++recv[t.dst];
+    }
+    for (int r = 0; r < R; ++r)
+      if (recv[r] != R - 1) return FO_ERR_PLAN_INVARIANT;
+    // The kernel adds each chunk's partials in the order it runs them: that
+    // order must be the chain's (hop s = step s).
+    for (int r = 0; r < R; ++r)
+      for (int s = 0; s < R; ++s)
+        if (p->ord[r][s] != s) return FO_ERR_UNSUPPORTED;
+  } else if (ag) {
     // Every shard a rank consumes after step 0 arrives by a transfer of that
     // shard to that rank at an earlier step.
     for (int r = 0; r < R; ++r)
@@ -213,8 +236,17 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (d->fault_inject < FO_INJECT_NONE || d->fault_inject > FO_INJECT_SKIP_SIGNAL) return FO_ERR_INVALID_ARG;
   if (d->tile_config != FO_TILE_AUTO && d->tile_config != FO_TILE_SINGLE) return FO_ERR_INVALID_ARG;
   if (d->interleave < FO_INTERLEAVE_AUTO || d->interleave > FO_INTERLEAVE_RANK_MAJOR) return FO_ERR_INVALID_ARG;
-  for (int i = 0; i < 5; ++i)
+  if (d->rs_algo != FO_RS_DIRECT && d->rs_algo != FO_RS_RING) return FO_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
     if (d->reserved[i]) return FO_ERR_INVALID_ARG;
+  if (d->rs_algo == FO_RS_RING) {
+    // The ring forwards a running sum, which needs the rank-adaptive order
+    // (rank r's chunk at step s is r-1's at step s-1) and a kernel order that
+    // runs every chunk's hops in step order.
+    if (d->op == FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
+    if (d->op == FO_OP_GEMM_AR || d->sched != FO_SCHED_RANK_ADAPTIVE) return FO_ERR_UNSUPPORTED;
+    if (d->interleave == FO_INTERLEAVE_RANK_MAJOR) return FO_ERR_UNSUPPORTED;
+  }
   if (d->M <= 0 || d->N <= 0 || d->K <= 0) return FO_ERR_SHAPE;
   const int R = d->R;
   const int64_t M = d->M, N = d->N, K = d->K;
@@ -262,6 +294,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   p->d = *d;
   if (!p->d.timeout_ns) p->d.timeout_ns = 1000000000ull;
   p->R = R;
+  p->ring = d->rs_algo == FO_RS_RING;
   p->elem_bytes = eb;
   p->rows_per_chunk = M / R;
   switch (d->op) {
@@ -300,9 +333,18 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   }
   p->ws_shard_off = off;
   p->ws_shard_stride = 0;
-  if (d->op != FO_OP_AG_GEMM && d->out_dtype == FO_BF16) {
+  if (d->op != FO_OP_AG_GEMM && d->out_dtype == FO_BF16 && !p->ring) {
     p->ws_shard_stride = align_up((size_t)p->rows_per_chunk * p->n_out * 4, 256);
     off += (size_t)R * p->ws_shard_stride;
+  }
+  // Ring RS: each rank's receive buffer holds one fp32 chunk per sender
+  // step; a rank receives each chunk at most once per call, so a chunk-
+  // indexed buffer of all M rows needs no reuse within a call.
+  p->ws_ring_off = off;
+  p->ws_ring_stride = 0;
+  if (p->ring) {
+    p->ws_ring_stride = align_up((size_t)p->rows_per_chunk * R * p->n_out * 4, 256);
+    off += (size_t)R * p->ws_ring_stride;
   }
   p->ws_bytes = off;
   p->last_launches = 0;

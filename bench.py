@@ -693,7 +693,21 @@ def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
     one_plan = B.fo_plan("gemm_rs", R, M, N, X[0].shape[1] * R, tile_config="single")
     one_ws = torch.zeros(B.fo_workspace_size(one_plan), dtype=torch.uint8, device=dev)
     single = _time(lambda: B.fo_gemm_rs(one_plan, X, W, Y, one_ws, stream), stream)
+    del one_ws, sl_ws
+    # The ring reduce-scatter (running sums forwarded rank to rank) and the
+    # direct algorithm's in-order (deterministic) adds, same kernel order.
+    ring_plan = B.fo_plan("gemm_rs", R, M, N, X[0].shape[1] * R, rs_algo="ring")
+    ring_ws = torch.zeros(B.fo_workspace_size(ring_plan), dtype=torch.uint8, device=dev)
+    ring = _time(lambda: B.fo_gemm_rs(ring_plan, X, W, Y, ring_ws, stream), stream)
+    del ring_ws
+    det_plan = B.fo_plan("gemm_rs", R, M, N, X[0].shape[1] * R, deterministic=True)
+    det_ws = torch.zeros(B.fo_workspace_size(det_plan), dtype=torch.uint8, device=dev)
+    det = _time(lambda: B.fo_gemm_rs(det_plan, X, W, Y, det_ws, stream), stream)
+    del det_ws
+    torch.cuda.empty_cache()
     return {
+        "ring_rs_ms": ring, "ring_rs_tflops": flops / ring / 1e9,
+        "direct_in_order_adds_ms": det, "direct_in_order_adds_tflops": flops / det / 1e9,
         "sliced_schedule_ms": sliced, "sliced_schedule_tflops": flops / sliced / 1e9,
         "single_cta_tiles_ms": single, "single_cta_tiles_tflops": flops / single / 1e9,
         "fused_ms": fused, "fused_tflops": flops / fused / 1e9,

@@ -83,6 +83,22 @@ typedef enum { FO_SCHED_RANK_ADAPTIVE = 0, FO_SCHED_SLICED = 1 } fo_sched;
  *       128-bit copies, and the GEMM waits for a per-block ready flag. */
 typedef enum { FO_AG_PEER_READ = 0, FO_AG_COPY = 1 } fo_ag_transport;
 
+/* Reduce-scatter algorithm of GEMM_RS and DP_GRAD_RS (both are readings of
+ * the decomposition into directed P2P chunk transfers, euno.news
+ * "Methodology" item 1; the pages name a ring only for the all-gather).
+ * DIRECT: each non-own partial goes straight to its owner, which adds it
+ *         into its shard on arrival.
+ * RING:   the running sum of chunk c travels along the ring: at step s rank
+ *         r adds its partial of chunk (r - 1 - s) mod R to the sum it
+ *         received from r-1 at step s-1 and forwards the result to r+1; the
+ *         owner, last in the chain, adds its own partial and keeps the sum.
+ *         Every forward lands in the receiver's fp32 buffer in the workspace.
+ *         The additions run in step order, so the result is bitwise
+ *         reproducible. Needs the rank-adaptive schedule and an interleave
+ *         that runs each chunk's hops in step order: AUTO (= LOCKSTEP),
+ *         LOCKSTEP or SKEWED. Not available for GEMM_AR. */
+typedef enum { FO_RS_DIRECT = 0, FO_RS_RING = 1 } fo_rs_algo;
+
 /* Storage of each W_r: KN = [K_r x N_r] row-major (default); NK = [N_r x K_r]
  * row-major (the nn.Linear weight layout, i.e. W_r transposed). */
 typedef enum { FO_W_KN = 0, FO_W_NK = 1 } fo_w_layout;
@@ -111,7 +127,8 @@ typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
  *           weights (AG) or upstream gradient (DP) stay in L2 across its
  *           steps.
  * AUTO:     SKEWED for GEMM_RS / GEMM_AR, RANK_MAJOR for AG_GEMM and
- *           DP_GRAD_RS (the fastest of the three on GB300 for each op). */
+ *           DP_GRAD_RS (the fastest of the three on GB300 for each op);
+ *           LOCKSTEP under the ring reduce-scatter. */
 typedef enum {
   FO_INTERLEAVE_AUTO = 0,
   FO_INTERLEAVE_LOCKSTEP = 1,
@@ -148,7 +165,8 @@ typedef struct {
   int32_t fault_inject;       /* fo_inject (tests only) */
   int32_t tile_config;        /* fo_tile_config */
   int32_t interleave;         /* fo_interleave */
-  int32_t reserved[5];        /* must be zero */
+  int32_t rs_algo;            /* fo_rs_algo (GEMM_RS and DP_GRAD_RS; else DIRECT) */
+  int32_t reserved[4];        /* must be zero */
 } fo_plan_desc;
 
 typedef struct fo_plan_s* fo_plan_t;
@@ -184,7 +202,9 @@ fo_status fo_plan_edges(fo_plan_t plan, int32_t* out, int32_t cap, int32_t* n);
 fo_status fo_plan_task_order(fo_plan_t plan, int32_t* order);
 
 /* Bytes of device workspace the launching calls need (readiness counters,
- * flags and the device status word). Never zero. */
+ * flags and the device status word; fp32 shard sums for a bf16 output;
+ * under FO_RS_RING every rank's fp32 receive buffer, R x M x N x 4 bytes).
+ * Never zero. */
 fo_status fo_workspace_size(fo_plan_t plan, size_t* bytes);
 
 /* Zero the workspace on `stream`. Required once before the first call that
@@ -202,7 +222,9 @@ fo_status fo_ag_gemm(fo_plan_t plan, const void* const* X, const void* const* W,
 /* Flash-RS: Y_d = sum_r (X_r . W_r)[rows of d], fp32 or bf16 (gist.science
  * "Technical Summary" section 2, Flash-Reduce-Scatter). Rank r's step s
  * computes the partial of chunk (r - 1 - s) mod R and adds it into that
- * owner's Y; the own chunk comes last. Y is overwritten. */
+ * owner's Y (FO_RS_DIRECT), or adds it to the running sum received from r-1
+ * and forwards that to r+1 (FO_RS_RING); the own chunk comes last. Y is
+ * overwritten. */
 fo_status fo_gemm_rs(fo_plan_t plan, const void* const* X, const void* const* W,
                      void* const* Y, void* ws, fo_stream_t stream);
 
@@ -219,7 +241,7 @@ fo_status fo_gemm_ar(fo_plan_t plan, const void* const* X, const void* const* W,
 /* Data-parallel weight gradient fused with its reduce-scatter:
  * dW_d = sum_r (X_r^T . dY_r)[rows of d], fp32 (gist.science "Technical
  * Summary" section 1: data parallelism needs a reduce-scatter). Same
- * schedule as fo_gemm_rs. dW is overwritten. */
+ * schedule and reduce-scatter algorithms as fo_gemm_rs. dW is overwritten. */
 fo_status fo_dp_grad_rs(fo_plan_t plan, const void* const* X, const void* const* dY,
                         void* const* dW, void* ws, fo_stream_t stream);
 
@@ -259,7 +281,10 @@ fo_status fo_status_query(fo_plan_t plan, void* ws, fo_stream_t stream, int32_t 
  *     caller, e.g. by issuing them on one stream.
  *   - A device-side wait that runs out is recorded in the array and cleared
  *     by the next call; it is not reported. Use fo_gemm_rs with a workspace
- *     and fo_status_query where that report is needed. */
+ *     and fo_status_query where that report is needed.
+ *   - Plans with a bf16 output return FO_ERR_DTYPE (or FO_ERR_SCRATCH_LIMIT
+ *     when their shard sums exceed the array); plans with the ring
+ *     reduce-scatter (FO_RS_RING) return FO_ERR_UNSUPPORTED. */
 #define FO_NOALLOC_SCRATCH_BYTES (64 * 1024)
 fo_status fo_gemm_rs_noalloc(fo_plan_t plan, const void* const* X, const void* const* W,
                              void* const* Y, fo_stream_t stream);

@@ -196,6 +196,10 @@ def test_auto_interleave_is_skewed_for_rs_and_rank_major_for_ag_and_dp():
     assert dp == [(r, s) for r in range(R) for s in range(R)]
     lock = B.fo_plan_task_order(B.fo_plan("ag_gemm", R, 512, 256, 256, interleave="lockstep"))
     assert lock == [(r, s) for s in range(R) for r in range(R)]
+    # the ring reduce-scatter runs lockstep: a chain's hops a whole step apart
+    for op in ("gemm_rs", "dp_grad_rs"):
+        ring = B.fo_plan_task_order(B.fo_plan(op, R, 512, 256, 256, rs_algo="ring"))
+        assert ring == B.fo_plan_task_order(B.fo_plan(op, R, 512, 256, 256, rs_algo="ring", interleave="lockstep"))
 
 
 def test_copy_transport_requires_gather_buffers():
@@ -222,3 +226,74 @@ def test_bf16_output_keeps_fp32_sums_in_the_workspace():
         B.fo_gemm_rs_noalloc(B.fo_plan("gemm_rs", 2, 256, 256, 256, out_dtype="bf16"), [16, 32], [16, 32],
                              [16, 32], stream=0)
     assert e.value.code in (B.FO_ERR_SCRATCH_LIMIT, B.FO_ERR_DTYPE)
+
+
+# ------------------------------------------------------------------ ring reduce-scatter
+
+def _ring_plan(op, R, **kw):
+    if op == "gemm_rs":
+        return B.fo_plan("gemm_rs", R, 128 * R, 256, 64 * R, rs_algo="ring", **kw)
+    return B.fo_plan("dp_grad_rs", R, 8 * R, 256, 64, rs_algo="ring", **kw)
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("op", ["gemm_rs", "dp_grad_rs"])
+def test_ring_plan_transfers_match_oracle(R, op):
+    p = _ring_plan(op, R)
+    assert B.fo_plan_table(p) == oracle.rs_schedule(R).tolist()
+    assert sorted(B.fo_plan_transfers(p)) == sorted(oracle.rs_transfers(R, ring=True))
+
+
+@pytest.mark.parametrize("R", [2, 3, 5, 8])
+def test_ring_plan_edges_are_program_order_and_forwards(R):
+    p = _ring_plan("gemm_rs", R)
+    table = B.fo_plan_table(p)
+    want = [(r, s, r, s + 1) for r in range(R) for s in range(R - 1)]
+    want += [(r, s, (r + 1) % R, s + 1) for s in range(R - 1) for r in range(R)]
+    assert sorted(B.fo_plan_edges(p)) == sorted(want)
+    # every forward reaches the rank that handles the same chunk next
+    for (src, dst, c, s) in B.fo_plan_transfers(p):
+        assert table[src][s] == c and table[dst][s + 1] == c
+
+
+@pytest.mark.parametrize("R", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("op", ["gemm_rs", "dp_grad_rs"])
+@pytest.mark.parametrize("interleave", ["auto", "lockstep", "skewed"])
+def test_ring_kernel_order_runs_every_chain_in_hop_order(R, op, interleave):
+    # The kernel adds a chunk's partials in the order it runs them, and a
+    # hop waits for its predecessor: each chain must run in hop order, or a
+    # wait could target a task that has not started.
+    p = _ring_plan(op, R, interleave=interleave)
+    table = B.fo_plan_table(p)
+    pos = {rs: i for i, rs in enumerate(B.fo_plan_task_order(p))}
+    for c in range(R):
+        chain = [((c + 1 + s) % R, s) for s in range(R)]
+        assert all(table[r][s] == c for r, s in chain)
+        assert [pos[t] for t in chain] == sorted(pos[t] for t in chain)
+
+
+@pytest.mark.parametrize("op,kw,code", [
+    ("gemm_rs", dict(interleave="rank_major"), B.FO_ERR_UNSUPPORTED),   # chains out of hop order
+    ("dp_grad_rs", dict(interleave="rank_major"), B.FO_ERR_UNSUPPORTED),
+    ("gemm_rs", dict(sched="sliced"), B.FO_ERR_UNSUPPORTED),             # no chunk passes along the ring
+    ("gemm_ar", {}, B.FO_ERR_UNSUPPORTED),
+    ("ag_gemm", {}, B.FO_ERR_INVALID_ARG),
+    ("gemm_rs", dict(fault_inject="drop_transfer"), B.FO_ERR_PLAN_INVARIANT),
+])
+def test_ring_plan_rejections(op, kw, code):
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_plan(op, 4, 512, 256, 256, rs_algo="ring", **kw)
+    assert e.value.code == code
+
+
+def test_ring_workspace_holds_every_ranks_receive_buffer():
+    R, M, N, K = 8, 8192, 4096, 14336
+    direct = B.fo_workspace_size(B.fo_plan("gemm_rs", R, M, N, K))
+    ring = B.fo_workspace_size(B.fo_plan("gemm_rs", R, M, N, K, rs_algo="ring"))
+    assert ring - direct >= R * M * N * 4
+    # a bf16 ring output needs no separate fp32 shard sums
+    assert B.fo_workspace_size(B.fo_plan("gemm_rs", R, M, N, K, rs_algo="ring", out_dtype="bf16")) == ring
+    with pytest.raises(B.FlashOverlapError) as e:     # the allocation-free entry point is direct-only
+        B.fo_gemm_rs_noalloc(B.fo_plan("gemm_rs", 2, 256, 256, 256, rs_algo="ring"), [16, 32], [16, 32],
+                             [16, 32], stream=0)
+    assert e.value.code == B.FO_ERR_UNSUPPORTED
