@@ -171,22 +171,6 @@ __device__ __forceinline__ bool signal_partial(uint32_t* ctr, int R) {
   return false;
 }
 
-// Loads 32 fp32 of row `row` (columns col0..col0+31) of a shard with 128-bit
-// L2 loads; rows past the shard, columns past N or a null shard read as zero.
-__device__ __forceinline__ void load_sum32(const float* shard, int row, int rows, int col0, int ncols, size_t N,
-                                           float (&s)[32]) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (shard && row < rows && col0 + 4 * k < ncols)
-      v = __ldcg(reinterpret_cast<const float4*>(shard + (size_t)row * N + col0 + 4 * k));
-    s[4 * k] = v.x;
-    s[4 * k + 1] = v.y;
-    s[4 * k + 2] = v.z;
-    s[4 * k + 3] = v.w;
-  }
-}
-
 // Copy n16 16-byte words with nthr threads (thread tid handles words tid,
 // tid + nthr, ...), eight loads in flight per thread; L2-only caching.
 __device__ __forceinline__ void copy16(const uint8_t* from, uint8_t* to, size_t n16, int tid, int nthr) {
@@ -218,6 +202,55 @@ __device__ __forceinline__ void stage_row_sw128(uint32_t buf, int lane, const ui
     const uint32_t addr = row + ((uint32_t)(j ^ (lane & 7)) << 4);
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * j]), "r"(w[4 * j + 1]),
                  "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
+                 : "memory");
+  }
+}
+
+// Coalesced loads of the 32 x 32 fp32 block at (row0, col0) of a [rows x
+// ncols] row-major matrix with leading dimension ld: lane l loads the
+// 16-byte chunk l % 8 of rows row0 + l / 8 + 4 i (i = 0..7), four whole
+// 128-byte rows per instruction. Rows past `rows`, columns past `ncols` or
+// a null matrix read as zero.
+__device__ __forceinline__ void load_block32_coalesced(const float* src, int row0, int rows, int col0, int ncols,
+                                                       size_t ld, int lane, float4 (&sv)[8]) {
+  const int crow = lane >> 3, col = col0 + (lane & 7) * 4;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = row0 + 4 * i + crow;
+    sv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (src && row < rows && col < ncols) sv[i] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)row * ld + col));
+  }
+}
+
+// Adds a block loaded by load_block32_coalesced into a 32 x 128 B fp32
+// staging buffer in the 128B-swizzle layout (stage_row_sw128).
+__device__ __forceinline__ void add_block32_sw128(uint32_t buf, int lane, const float4 (&sv)[8]) {
+  const int crow = lane >> 3, cch = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rr = 4 * i + crow;
+    const uint32_t a = buf + (uint32_t)rr * 128u + ((uint32_t)(cch ^ (rr & 7)) << 4);
+    float4 x;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                 : "r"(a)
+                 : "memory");
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(x.x + sv[i].x), "f"(x.y + sv[i].y),
+                 "f"(x.z + sv[i].z), "f"(x.w + sv[i].w)
+                 : "memory");
+  }
+}
+
+// Reads row `lane` (32 fp32) back from a staging buffer in the 128B-swizzle
+// layout.
+__device__ __forceinline__ void read_row_sw128(uint32_t buf, int lane, float (&f)[32]) {
+  const uint32_t row = buf + (uint32_t)lane * 128u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t a = row + ((uint32_t)(j ^ (lane & 7)) << 4);
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(f[4 * j]), "=f"(f[4 * j + 1]), "=f"(f[4 * j + 2]), "=f"(f[4 * j + 3])
+                 : "r"(a)
                  : "memory");
   }
 }
@@ -532,67 +565,27 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       if (EPI == EPI_RS && ti.ord > 0)
         sum_src = ring ? p.inbox[ti.r] + (size_t)ti.c * p.rows_per_chunk * ncols : p.shard[ti.c];
       if (EPI == EPI_RS && fin && last && p.completion == FO_COMPLETE_BF16) {
-        // Finisher, bf16 output: 4 sub-tiles of 32 rows x 64 columns; own
-        // partial + the other R-1 partials' sum, rounded once.
-#pragma unroll 1
-        for (int j = 0; j < FO_BN / 64; ++j) {
-          uint32_t v0[32], v1[32], w[32];
-          float s0[32], s1[32];
-          tmem_ld32(tbase + j * 64, v0);
-          tmem_ld32(tbase + j * 64 + 32, v1);
-          load_sum32(sum_src, row0 + lane, p.rows_per_chunk, n0 + j * 64, (int)ncols, ncols, s0);
-          load_sum32(sum_src, row0 + lane, p.rows_per_chunk, n0 + j * 64 + 32, (int)ncols, ncols, s1);
-          tmem_ld_wait();
-          reg_fence(v0);
-          reg_fence(v1);
-          if (j == FO_BN / 64 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-              if constexpr (PAIR) mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
-              else mbar_arrive(tempty_bar(acc));
-            }
-          }
-          if (!ok) continue;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(v0[2 * i]) + s0[2 * i],
-                                                      __uint_as_float(v0[2 * i + 1]) + s0[2 * i + 1]);
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(v1[2 * i]) + s1[2 * i],
-                                                      __uint_as_float(v1[2 * i + 1]) + s1[2 * i + 1]);
-            w[i] = *reinterpret_cast<uint32_t*>(&h0);
-            w[16 + i] = *reinterpret_cast<uint32_t*>(&h1);
-          }
-          const uint32_t buf = sEpi + (uint32_t)((e * kEpiBufs + (j % kEpiBufs)) * kEpiBuf);
-          if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
-          __syncwarp();
-          stage_row_sw128(buf, lane, w);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&p.tmF[ti.c], buf, n0 + j * 64, row0);
-            bulk_commit();
-          }
-        }
-        if (ok && lane == 0) atomicExch(ctr, 0u);   // every partial is in: ready for the next call
-      } else if (EPI == EPI_RS && fin) {
-        // Finisher, all-reduce: 8 sub-tiles of 32 rows x 32 fp32 columns;
-        // own partial + the other R-1 partials' sum, stored to the same rows
-        // of every rank's full output (the all-gather half).
-        // Ring hop, fp32: own partial + the running sum from the receive
-        // buffer, forwarded into the next rank's receive buffer, or (last
-        // hop) stored to the owner's output.
-        // The sum of sub-tile j+1 is loaded while sub-tile j is processed.
+        // Finisher, bf16 output: 8 sub-tiles of 32 rows x 32 columns. The own
+        // partial is staged fp32 in the warp's last buffer, the other R-1
+        // partials' sum is added there with coalesced loads, and every pair
+        // of sub-tiles is rounded once into 64-column bf16 rows, stored from
+        // the other buffers. The sums of sub-tile j+1 are in flight while
+        // sub-tile j is processed.
+        static_assert(kEpiBufs >= 2, "the bf16 finisher needs two staging buffers per warp");
         constexpr int kSub = FO_BN / 32;
-        float sum[2][32];
-        load_sum32(sum_src, row0 + lane, p.rows_per_chunk, n0, (int)ncols, ncols, sum[0]);
+        const uint32_t addbuf = sEpi + (uint32_t)((e * kEpiBufs + kEpiBufs - 1) * kEpiBuf);
+        float4 sum[2][8];
+        uint32_t w[32];
+        load_block32_coalesced(sum_src, row0, p.rows_per_chunk, n0, (int)ncols, ncols, lane, sum[0]);
+        if (lane == 0) bulk_wait_read<0>();   // no store still reads a staging buffer
+        __syncwarp();
 #pragma unroll
         for (int j = 0; j < kSub; ++j) {
           uint32_t v[32];
           tmem_ld32(tbase + j * 32, v);
           if (j + 1 < kSub)
-            load_sum32(sum_src, row0 + lane, p.rows_per_chunk, n0 + (j + 1) * 32, (int)ncols, ncols,
-                       sum[(j + 1) & 1]);
+            load_block32_coalesced(sum_src, row0, p.rows_per_chunk, n0 + (j + 1) * 32, (int)ncols, ncols, lane,
+                                   sum[(j + 1) & 1]);
           tmem_ld_wait();
           reg_fence(v);
           if (j == kSub - 1) {
@@ -604,12 +597,68 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
             }
           }
           if (!ok) continue;
+          stage_row_sw128(addbuf, lane, v);
+          __syncwarp();
+          add_block32_sw128(addbuf, lane, sum[j & 1]);
+          __syncwarp();
+          float f[32];
+          read_row_sw128(addbuf, lane, f);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + sum[j & 1][i]);
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[(j & 1) * 16 + i] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          if (j & 1) {
+            const uint32_t buf = sEpi + (uint32_t)((e * kEpiBufs + (j >> 1) % (kEpiBufs - 1)) * kEpiBuf);
+            if (lane == 0) bulk_wait_read<kEpiBufs - 2>();
+            __syncwarp();
+            stage_row_sw128(buf, lane, w);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.tmF[ti.c], buf, n0 + (j - 1) * 32, row0);
+              bulk_commit();
+            }
+          }
+        }
+        if (ok && lane == 0) atomicExch(ctr, 0u);   // every partial is in: ready for the next call
+      } else if (EPI == EPI_RS && fin) {
+        // Finisher, all-reduce: 8 sub-tiles of 32 rows x 32 fp32 columns;
+        // own partial + the other R-1 partials' sum, stored to the same rows
+        // of every rank's full output (the all-gather half).
+        // Ring hop, fp32: own partial + the running sum from the receive
+        // buffer, forwarded into the next rank's receive buffer, or (last
+        // hop) stored to the owner's output.
+        // The own partial is staged row-per-lane (as it comes out of TMEM)
+        // and the sum is added there with coalesced loads. The sums of
+        // sub-tile j+1 are in flight while sub-tile j is processed.
+        constexpr int kSub = FO_BN / 32;
+        float4 sum[2][8];
+        load_block32_coalesced(sum_src, row0, p.rows_per_chunk, n0, (int)ncols, ncols, lane, sum[0]);
+#pragma unroll
+        for (int j = 0; j < kSub; ++j) {
+          uint32_t v[32];
+          tmem_ld32(tbase + j * 32, v);
+          if (j + 1 < kSub)
+            load_block32_coalesced(sum_src, row0, p.rows_per_chunk, n0 + (j + 1) * 32, (int)ncols, ncols, lane,
+                                   sum[(j + 1) & 1]);
+          tmem_ld_wait();
+          reg_fence(v);
+          if (j == kSub - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+              if constexpr (PAIR) mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+              else mbar_arrive(tempty_bar(acc));
+            }
+          }
+          if (!ok) continue;
           const uint32_t buf = sEpi + (uint32_t)((e * kEpiBufs + (j % kEpiBufs)) * kEpiBuf);
           if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
           __syncwarp();
           stage_row_sw128(buf, lane, v);
+          __syncwarp();
+          add_block32_sw128(buf, lane, sum[j & 1]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
