@@ -25,7 +25,9 @@ DTYPES = {"bf16": 0, "f32": 1}
 SCHEDS = {"rank_adaptive": 0, "sliced": 1}
 TRANSPORTS = {"peer_read": 0, "copy": 1}
 W_LAYOUTS = {"kn": 0, "nk": 1}
-INJECT = {"none": 0, "drop_transfer": 1, "skip_signal": 2}
+INJECT = {"none": 0, "drop_transfer": 1, "skip_signal": 2, "delay_first_task": 3}
+FO_TRACE_STAMPS = 8
+FO_TRACE_MAX_CTAS = 1024
 TILE_CONFIGS = {"auto": 0, "single": 1}
 INTERLEAVES = {"auto": 0, "lockstep": 1, "skewed": 2, "rank_major": 3}
 RS_ALGOS = {"direct": 0, "ring": 1}
@@ -36,7 +38,7 @@ EXPORTED = [
     "fo_workspace_size", "fo_workspace_init", "fo_ag_gemm", "fo_gemm_rs", "fo_dp_grad_rs",
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
     "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc", "fo_plan_task_order",
-    "fo_gemm_ar",
+    "fo_gemm_ar", "fo_trace_query",
 ]
 
 
@@ -56,7 +58,7 @@ class PlanDesc(ctypes.Structure):
         ("in_dtype", c_int32), ("out_dtype", c_int32), ("sched", c_int32), ("ag_transport", c_int32),
         ("w_layout", c_int32), ("deterministic", c_int32), ("timeout_ns", c_uint64),
         ("fault_inject", c_int32), ("tile_config", c_int32), ("interleave", c_int32), ("rs_algo", c_int32),
-        ("reserved", c_int32 * 4),
+        ("trace", c_int32), ("inject_delay_us", c_int32), ("reserved", c_int32 * 2),
     ]
 
 
@@ -90,6 +92,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_gemm_rs_noalloc": ([P, PP, PP, PP, P], c_int32),
         "fo_gemm_ar": ([P, PP, PP, PP, P, P], c_int32),
         "fo_status_query": ([P, P, P, POINTER(c_int32)], c_int32),
+        "fo_trace_query": ([P, P, P, POINTER(ctypes.c_uint64), c_int32, POINTER(c_int32)], c_int32),
         "fo_gemm_partials": ([P, PP, PP, PP, P, P], c_int32),
         "fo_reduce_scatter_f32": ([P, PP, PP, P], c_int32),
         "fo_all_gather_copy": ([P, PP, PP, P], c_int32),
@@ -168,7 +171,7 @@ class Plan:
 def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dtype=None,
             sched="rank_adaptive", ag_transport="peer_read", w_layout="kn", deterministic=False,
             timeout_ns=0, fault_inject="none", tile_config="auto", interleave="auto",
-            rs_algo="direct") -> Plan:
+            rs_algo="direct", trace=False, inject_delay_us=0) -> Plan:
     lib = load()
     if out_dtype is None:
         out_dtype = "bf16" if op == "ag_gemm" else "f32"
@@ -187,6 +190,8 @@ def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dty
     d.tile_config = TILE_CONFIGS[tile_config]
     d.interleave = INTERLEAVES[interleave]
     d.rs_algo = RS_ALGOS[rs_algo]
+    d.trace = 1 if trace else 0
+    d.inject_delay_us = inject_delay_us
     h = c_void_p()
     _check(lib.fo_plan(ctypes.byref(d), ctypes.byref(h)), "fo_plan")
     return Plan(h.value, d)
@@ -285,6 +290,29 @@ def fo_status_query(plan: Plan, ws, stream=None):
     info = (c_int32 * 4)()
     code = load().fo_status_query(plan, _ptr(ws), _stream(stream), info)
     return code, list(info)
+
+
+def fo_trace_query(plan: Plan, ws, stream=None):
+    """Per-CTA timestamps of the last traced launch: a list with one row of
+    FO_TRACE_STAMPS ints (ns) per CTA."""
+    cap = FO_TRACE_MAX_CTAS
+    buf = (ctypes.c_uint64 * (cap * FO_TRACE_STAMPS))()
+    n = c_int32()
+    _check(load().fo_trace_query(plan, _ptr(ws), _stream(stream), buf, cap, ctypes.byref(n)), "fo_trace_query")
+    m = min(n.value, cap)
+    return [[buf[i * FO_TRACE_STAMPS + j] for j in range(FO_TRACE_STAMPS)] for i in range(m)]
+
+
+def trace_summary(stamps):
+    """Launch span, end of the math and exposed tail (all ns) from
+    fo_trace_query's rows: the tail is the time the last transfer was still
+    running after the last MMA had completed."""
+    start = min(r[0] for r in stamps)
+    mma_end = max(r[1] for r in stamps)
+    xfer_end = max(max(r[2:6]) for r in stamps)
+    end = max(r[6] for r in stamps)
+    return {"span_ns": end - start, "mma_end_ns": mma_end - start, "transfers_end_ns": xfer_end - start,
+            "exposed_tail_ns": max(0, xfer_end - mma_end)}
 
 
 def fo_plan_last_launches(plan: Plan) -> int:

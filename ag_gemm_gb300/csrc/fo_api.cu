@@ -2,6 +2,7 @@
 // launches of the persistent chunk-GEMM kernel and of the two auxiliary
 // kernels used by the unfused baselines, and the device status query.
 #include <cudaTypedefs.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -141,6 +142,8 @@ void fill_common(fo_plan_t p, fo::FoParams* k, void* ws) {
   k->row_bytes = p->d.K * 2;
   k->ag_copy = p->d.op == FO_OP_AG_GEMM && p->d.ag_transport == FO_AG_COPY ? 1 : 0;
   k->n_cols = p->n_out;
+  k->trace = p->d.trace ? reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + p->ws_trace_off) : nullptr;
+  k->delay_ns = p->d.fault_inject == FO_INJECT_DELAY_FIRST_TASK ? (uint64_t)p->d.inject_delay_us * 1000ull : 0ull;
 }
 
 fo_status check_ptrs(int R, const void* const* a) {
@@ -303,11 +306,15 @@ fo_status run_chunk_gemm(fo_plan_t p, int variant, const fo::FoParams* k, const 
   fo_status st = launch_grid(p, variant, di, &grid);
   if (st != FO_OK) return st;
   cudaError_t e = fo_launch_variant(variant, p->pair, *k, grid, s);
+  if (fo_log_enabled())
+    fprintf(stderr, "[flashoverlap] launch variant %d, %d CTAs (%s), stream %p: %s\n", variant, grid,
+            p->pair ? "CTA pairs" : "single CTAs", (void*)s, cudaGetErrorString(e));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FO_ERR_CUDA;
   }
   p->last_launches = 1;
+  p->last_grid = grid;
   return FO_OK;
 }
 
@@ -386,6 +393,25 @@ fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const
 fo_status fo_internal_check_ptrs(int R, const void* const* a) { return check_ptrs(R, a); }
 
 extern "C" {
+
+fo_status fo_trace_query(fo_plan_t p, const void* ws, fo_stream_t stream, uint64_t* stamps, int32_t cap,
+                         int32_t* n_ctas) {
+  if (!p || !ws || !n_ctas || cap < 0 || (cap > 0 && !stamps)) return FO_ERR_INVALID_ARG;
+  if (!p->d.trace || p->last_grid <= 0) return FO_ERR_INVALID_ARG;
+  *n_ctas = p->last_grid;
+  int m = p->last_grid < FO_TRACE_MAX_CTAS ? p->last_grid : FO_TRACE_MAX_CTAS;
+  if (m > cap) m = cap;
+  if (m > 0) {
+    const char* src = static_cast<const char*>(ws) + p->ws_trace_off;
+    if (cudaMemcpyAsync(stamps, src, (size_t)m * FO_TRACE_STAMPS * sizeof(uint64_t), cudaMemcpyDeviceToHost,
+                        (cudaStream_t)stream) != cudaSuccess ||
+        cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) {
+      cudaGetLastError();
+      return FO_ERR_CUDA;
+    }
+  }
+  return FO_OK;
+}
 
 fo_status fo_workspace_init(fo_plan_t p, void* ws, fo_stream_t stream) {
   if (!p || !ws) return FO_ERR_INVALID_ARG;

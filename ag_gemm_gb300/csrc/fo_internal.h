@@ -58,6 +58,8 @@ struct fo_plan_s {
   size_t ws_ring_off;      // ring RS: rank q's fp32 receive buffer [M x N] at off + q * stride
   size_t ws_ring_stride;
   bool ring;               // d.rs_algo == FO_RS_RING
+  size_t ws_trace_off;     // trace = 1: uint64 [FO_TRACE_MAX_CTAS][FO_TRACE_STAMPS]
+  int32_t last_grid;       // CTAs of the last fused-kernel launch (0 = none yet)
 
   int32_t last_launches;
   void* param_cache;       // host copy of the last kernel parameter block
@@ -82,3 +84,6 @@ fo_status fo_internal_check_ptrs(int R, const void* const* a);
 fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const void* const* W,
                                         void* const* Y, void* scratch, fo::FoParams* k, int* variant,
                                         int* grid);
+
+// Host logging (FO_LOG=1 in the environment): plan summaries and launches.
+bool fo_log_enabled();

@@ -126,6 +126,11 @@ struct alignas(128) FoParams {
   // written to the output.
   int32_t ring;
   float* inbox[FO_MAX_R];      // rank q's receive buffer [M x N] fp32 (chunk-major rows)
+  // Tracing: FO_TRACE_STAMPS %globaltimer stamps per CTA (null: off).
+  uint64_t* trace;
+  // Fault injection: tiles of the first task wait this long after their
+  // CTA started before their operands are loaded (0: off).
+  uint64_t delay_ns;
 };
 
 enum Completion : int { FO_COMPLETE_NONE = 0, FO_COMPLETE_BF16 = 1, FO_COMPLETE_ALLREDUCE = 2 };
@@ -311,6 +316,13 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
     fence_mbar_init();
     fence_proxy_async_smem();
   }
+  const uint64_t t_start = globaltimer();
+  uint64_t* const trace = (p.trace && blockIdx.x < FO_TRACE_MAX_CTAS) ? p.trace + (size_t)blockIdx.x * FO_TRACE_STAMPS
+                                                                       : nullptr;
+  if (trace && threadIdx.x == 0) {
+    trace[0] = t_start;
+    for (int i = 1; i < FO_TRACE_STAMPS; ++i) trace[i] = 0;
+  }
   if (warp == 1) {
     __syncwarp();
     tmem_alloc<CG>(sTmemSlot, kTmemCols);
@@ -332,6 +344,11 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
         if (*gstatus) *abort_flag = 1;
         if (*abort_flag) break;
         const Tile ti = decode_tile(p, L);
+        if (p.delay_ns && L < p.tiles_m * p.tiles_n) {
+          // Fault injection: hold the first task's tiles (bounded by the
+          // delay itself; an abort ends it early).
+          while (globaltimer() - t_start < p.delay_ns && !*abort_flag && !*gstatus) __nanosleep(2000);
+        }
         const CUtensorMap* mA = EPI == EPI_AG ? &p.tmA[ti.c] : &p.tmA[ti.r];
         const CUtensorMap* mB = &p.tmB[ti.r];
         // Row (or column, for MN-major A) where this CTA's A block starts,
@@ -464,6 +481,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       tc_commit<CG>(mma_done_bar);
       volatile int never = 0;
       mbar_wait(mma_done_bar, 0, &never, 100000000ull);
+      if (trace) trace[1] = globaltimer();
     }
   } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
@@ -780,6 +798,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       if (!aborted) publish(true);
     }
     if (lane == 0) bulk_wait<0>();
+    if (trace && lane == 0) trace[2 + e] = globaltimer();
     __syncwarp();
   }
 
@@ -830,6 +849,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
     __syncwarp();
     tmem_dealloc<CG>(tmem_base, kTmemCols);
   }
+  if (trace && threadIdx.x == 0) trace[6] = globaltimer();
   if constexpr (MOV) {
     // The last CTA of the launch advances the flag epoch for the next call.
     if (threadIdx.x == 0 && p.ag_copy) {

@@ -15,6 +15,7 @@
 // rank (r - s) mod R, which its ring predecessor forwarded one step earlier.
 // Under the ring RS algorithm the same order makes rank r's chunk at step s
 // the one rank r-1 handled at step s-1, so the running sum can be forwarded.
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -26,6 +27,19 @@
 namespace {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+// Host logging to stderr when the environment has FO_LOG=1 (read once).
+bool fo_log_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("FO_LOG");
+    return v && v[0] == '1' && v[1] == 0;
+  }();
+  return on;
+}
+
+namespace {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool is_perm(const int32_t* v, int n, int stride) {
@@ -233,11 +247,14 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (d->sched != FO_SCHED_RANK_ADAPTIVE && d->sched != FO_SCHED_SLICED) return FO_ERR_INVALID_ARG;
   if (d->ag_transport != FO_AG_PEER_READ && d->ag_transport != FO_AG_COPY) return FO_ERR_INVALID_ARG;
   if (d->w_layout != FO_W_KN && d->w_layout != FO_W_NK) return FO_ERR_INVALID_ARG;
-  if (d->fault_inject < FO_INJECT_NONE || d->fault_inject > FO_INJECT_SKIP_SIGNAL) return FO_ERR_INVALID_ARG;
+  if (d->fault_inject < FO_INJECT_NONE || d->fault_inject > FO_INJECT_DELAY_FIRST_TASK) return FO_ERR_INVALID_ARG;
+  if (d->inject_delay_us < 0 || d->inject_delay_us > 1000000) return FO_ERR_INVALID_ARG;
+  if (d->inject_delay_us && d->fault_inject != FO_INJECT_DELAY_FIRST_TASK) return FO_ERR_INVALID_ARG;
+  if (d->trace != 0 && d->trace != 1) return FO_ERR_INVALID_ARG;
   if (d->tile_config != FO_TILE_AUTO && d->tile_config != FO_TILE_SINGLE) return FO_ERR_INVALID_ARG;
   if (d->interleave < FO_INTERLEAVE_AUTO || d->interleave > FO_INTERLEAVE_RANK_MAJOR) return FO_ERR_INVALID_ARG;
   if (d->rs_algo != FO_RS_DIRECT && d->rs_algo != FO_RS_RING) return FO_ERR_INVALID_ARG;
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 2; ++i)
     if (d->reserved[i]) return FO_ERR_INVALID_ARG;
   if (d->rs_algo == FO_RS_RING) {
     // The ring forwards a running sum, which needs the rank-adaptive order
@@ -346,9 +363,21 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
     p->ws_ring_stride = align_up((size_t)p->rows_per_chunk * R * p->n_out * 4, 256);
     off += (size_t)R * p->ws_ring_stride;
   }
+  p->ws_trace_off = off;
+  if (d->trace) off += align_up((size_t)FO_TRACE_MAX_CTAS * FO_TRACE_STAMPS * sizeof(uint64_t), 256);
   p->ws_bytes = off;
   p->last_launches = 0;
+  p->last_grid = 0;
   p->param_cache = nullptr;
+  if (fo_log_enabled()) {
+    static const char* ops[] = {"ag_gemm", "gemm_rs", "dp_grad_rs", "gemm_ar"};
+    fprintf(stderr,
+            "[flashoverlap] plan %s R=%d M=%lld N=%lld K=%lld %s tiles %dx%d of %s, %d k-blocks, %s%s, "
+            "workspace %zu B\n",
+            ops[d->op], R, (long long)M, (long long)N, (long long)K, eb == 4 ? "tf32" : "bf16", p->tiles_m,
+            p->tiles_n, p->pair ? "256x256 (CTA pair)" : "128x256", p->num_kb,
+            d->sched == FO_SCHED_SLICED ? "sliced" : "rank-adaptive", p->ring ? ", ring RS" : "", p->ws_bytes);
+  }
   *out = p;
   return FO_OK;
 }

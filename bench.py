@@ -660,6 +660,26 @@ def _time(fn, stream, iters=10, warm=2):
     return a.elapsed_time(b) / iters
 
 
+def traced_tail_us(B, desc, call, stream, dev, reps=5):
+    """Median over `reps` traced launches of the exposed tail (time the last
+    transfer ran past the last MMA) and of the launch span, in us, from the
+    kernel's own %globaltimer stamps."""
+    import torch
+    desc = dict(desc)
+    op, R, M, N, K = (desc.pop(k) for k in ("op", "R", "M", "N", "K"))
+    plan = B.fo_plan(op, R, M, N, K, trace=True, **desc)
+    ws = torch.zeros(B.fo_workspace_size(plan), dtype=torch.uint8, device=dev)
+    call(plan, ws)
+    tails, spans = [], []
+    for _ in range(reps):
+        call(plan, ws)
+        s = B.trace_summary(B.fo_trace_query(plan, ws, stream))
+        tails.append(s["exposed_tail_ns"] / 1e3)
+        spans.append(s["span_ns"] / 1e3)
+    del ws
+    return {"tail_us": sorted(tails)[reps // 2], "span_us": sorted(spans)[reps // 2]}
+
+
 def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
     """Same-GPU comparisons: pure-GEMM control (no transfer), unfused
     (GEMM to per-rank partials, then a separate reduce kernel), cuBLAS."""
@@ -705,7 +725,12 @@ def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
     det = _time(lambda: B.fo_gemm_rs(det_plan, X, W, Y, det_ws, stream), stream)
     del det_ws
     torch.cuda.empty_cache()
+    tails = {}
+    for name, kw in (("rank_adaptive", {}), ("sliced", dict(sched="sliced"))):
+        tails[name] = traced_tail_us(B, dict(op="gemm_rs", R=R, M=M, N=N, K=X[0].shape[1] * R, **kw),
+                                     lambda p, w: B.fo_gemm_rs(p, X, W, Y, w, stream), stream, dev)
     return {
+        "exposed_tail_us": tails,
         "ring_rs_ms": ring, "ring_rs_tflops": flops / ring / 1e9,
         "direct_in_order_adds_ms": det, "direct_in_order_adds_tflops": flops / det / 1e9,
         "sliced_schedule_ms": sliced, "sliced_schedule_tflops": flops / sliced / 1e9,

@@ -105,8 +105,18 @@ typedef enum { FO_W_KN = 0, FO_W_NK = 1 } fo_w_layout;
 
 /* Test hooks. DROP_TRANSFER makes fo_plan omit one transfer (the validator
  * must reject the plan). SKIP_SIGNAL makes the kernel omit the readiness
- * signal of one tile, so that a bounded wait runs out on the device. */
-typedef enum { FO_INJECT_NONE = 0, FO_INJECT_DROP_TRANSFER = 1, FO_INJECT_SKIP_SIGNAL = 2 } fo_inject;
+ * signal of one tile, so that a bounded wait runs out on the device.
+ * DELAY_FIRST_TASK holds every tile of the first chunk task in the kernel's
+ * order until inject_delay_us microseconds after its CTA started, before
+ * its operands are loaded: the partials (RS/DP) or the tiles (AG) of that
+ * task arrive late, and every wait for them must hold; results must not
+ * change unless the delay exceeds timeout_ns. */
+typedef enum {
+  FO_INJECT_NONE = 0,
+  FO_INJECT_DROP_TRANSFER = 1,
+  FO_INJECT_SKIP_SIGNAL = 2,
+  FO_INJECT_DELAY_FIRST_TASK = 3
+} fo_inject;
 
 /* Output tile of the fused kernel. AUTO: a pair of CTAs on two SMs shares
  * one 256 x 256 tile (tcgen05 cta_group::2) for bf16 inputs; fp32 inputs use
@@ -166,7 +176,10 @@ typedef struct {
   int32_t tile_config;        /* fo_tile_config */
   int32_t interleave;         /* fo_interleave */
   int32_t rs_algo;            /* fo_rs_algo (GEMM_RS and DP_GRAD_RS; else DIRECT) */
-  int32_t reserved[4];        /* must be zero */
+  int32_t trace;              /* 1: every launch records per-CTA timestamps in the
+                                 workspace (fo_trace_query); 0: off */
+  int32_t inject_delay_us;    /* FO_INJECT_DELAY_FIRST_TASK: 0..10^6 microseconds */
+  int32_t reserved[2];        /* must be zero */
 } fo_plan_desc;
 
 typedef struct fo_plan_s* fo_plan_t;
@@ -203,7 +216,8 @@ fo_status fo_plan_task_order(fo_plan_t plan, int32_t* order);
 
 /* Bytes of device workspace the launching calls need (readiness counters,
  * flags and the device status word; fp32 shard sums for a bf16 output;
- * under FO_RS_RING every rank's fp32 receive buffer, R x M x N x 4 bytes).
+ * under FO_RS_RING every rank's fp32 receive buffer, R x M x N x 4 bytes;
+ * with trace = 1, FO_TRACE_MAX_CTAS x FO_TRACE_STAMPS timestamps).
  * Never zero. */
 fo_status fo_workspace_size(fo_plan_t plan, size_t* bytes);
 
@@ -284,10 +298,33 @@ fo_status fo_status_query(fo_plan_t plan, void* ws, fo_stream_t stream, int32_t 
  *     and fo_status_query where that report is needed.
  *   - Plans with a bf16 output return FO_ERR_DTYPE (or FO_ERR_SCRATCH_LIMIT
  *     when their shard sums exceed the array); plans with the ring
- *     reduce-scatter (FO_RS_RING) return FO_ERR_UNSUPPORTED. */
+ *     reduce-scatter (FO_RS_RING) return FO_ERR_UNSUPPORTED; plans with
+ *     trace = 1 return FO_ERR_SCRATCH_LIMIT (their timestamps alone fill
+ *     the array). */
 #define FO_NOALLOC_SCRATCH_BYTES (64 * 1024)
 fo_status fo_gemm_rs_noalloc(fo_plan_t plan, const void* const* X, const void* const* W,
                              void* const* Y, fo_stream_t stream);
+
+/* ---- tracing ------------------------------------------------------------ */
+
+/* Timestamps (%globaltimer, ns) of the last fused-kernel launch that used
+ * `ws`, for plans built with trace = 1. Per CTA, FO_TRACE_STAMPS values:
+ *   [0] the CTA starts;
+ *   [1] every MMA it issued has completed (leader CTAs; 0 on a pair's peer);
+ *   [2..5] epilogue warp 0..3 has seen all of its stores and adds performed
+ *          and released its last partial;
+ *   [6] the CTA leaves;
+ *   [7] 0.
+ * The exposed tail of a launch, the time its transfers run past its math,
+ * is max over CTAs of [2..5] minus max over CTAs of [1].
+ * Copies min(cap, launched CTAs) CTAs' stamps into `stamps` (host memory,
+ * cap * FO_TRACE_STAMPS values) and the launch's CTA count into *n_ctas
+ * (at most FO_TRACE_MAX_CTAS CTAs are recorded). Synchronises `stream`.
+ * FO_ERR_INVALID_ARG for a plan built without trace or before any launch. */
+#define FO_TRACE_STAMPS 8
+#define FO_TRACE_MAX_CTAS 1024
+fo_status fo_trace_query(fo_plan_t plan, const void* ws, fo_stream_t stream, uint64_t* stamps, int32_t cap,
+                         int32_t* n_ctas);
 
 /* ---- measurement controls (not part of the method) --------------------- */
 

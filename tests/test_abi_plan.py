@@ -297,3 +297,54 @@ def test_ring_workspace_holds_every_ranks_receive_buffer():
         B.fo_gemm_rs_noalloc(B.fo_plan("gemm_rs", 2, 256, 256, 256, rs_algo="ring"), [16, 32], [16, 32],
                              [16, 32], stream=0)
     assert e.value.code == B.FO_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ tracing, delay injection, logging
+
+def test_trace_plan_reserves_timestamps_in_the_workspace():
+    R, M, N, K = 8, 8192, 4096, 14336
+    plain = B.fo_workspace_size(B.fo_plan("gemm_rs", R, M, N, K))
+    traced = B.fo_plan("gemm_rs", R, M, N, K, trace=True)
+    assert B.fo_workspace_size(traced) - plain >= B.FO_TRACE_MAX_CTAS * B.FO_TRACE_STAMPS * 8
+    with pytest.raises(B.FlashOverlapError) as e:        # nothing launched yet
+        B.fo_trace_query(traced, 4096)
+    assert e.value.code == B.FO_ERR_INVALID_ARG
+    with pytest.raises(B.FlashOverlapError) as e:        # plan built without trace
+        B.fo_trace_query(B.fo_plan("gemm_rs", R, M, N, K), 4096)
+    assert e.value.code == B.FO_ERR_INVALID_ARG
+    with pytest.raises(B.FlashOverlapError) as e:        # the timestamps alone fill the static scratch
+        B.fo_gemm_rs_noalloc(B.fo_plan("gemm_rs", 2, 256, 256, 256, trace=True), [16, 32], [16, 32], [16, 32],
+                             stream=0)
+    assert e.value.code == B.FO_ERR_SCRATCH_LIMIT
+
+
+@pytest.mark.parametrize("kw", [
+    dict(inject_delay_us=100),                                         # a delay without its hook
+    dict(fault_inject="delay_first_task", inject_delay_us=-1),
+    dict(fault_inject="delay_first_task", inject_delay_us=1_000_001),
+])
+def test_delay_injection_arguments_are_checked(kw):
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_plan("gemm_rs", 4, 512, 256, 256, **kw)
+    assert e.value.code == B.FO_ERR_INVALID_ARG
+
+
+def test_trace_summary_reads_the_tail_off_the_stamps():
+    rows = [[100, 900, 950, 990, 940, 960, 1000, 0],   # leader: MMAs done at 900, last transfer 990
+            [105, 0, 930, 935, 1020, 925, 1030, 0]]    # peer: its epilogue finishes last
+    s = B.trace_summary(rows)
+    assert s == {"span_ns": 930, "mma_end_ns": 800, "transfers_end_ns": 920, "exposed_tail_ns": 120}
+
+
+def test_fo_log_prints_plans_to_stderr():
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, '.'); from ag_gemm_gb300 import binding as B; "
+            "B.fo_plan('gemm_rs', 4, 1024, 512, 256, rs_algo='ring')")
+    env = dict(os.environ, FO_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert "[flashoverlap] plan gemm_rs R=4 M=1024 N=512 K=256" in r.stderr and "ring RS" in r.stderr
+    env["FO_LOG"] = "0"
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert "[flashoverlap]" not in r.stderr
