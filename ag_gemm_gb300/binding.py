@@ -31,6 +31,7 @@ FO_TRACE_MAX_CTAS = 1024
 TILE_CONFIGS = {"auto": 0, "single": 1}
 INTERLEAVES = {"auto": 0, "lockstep": 1, "skewed": 2, "rank_major": 3}
 RS_ALGOS = {"direct": 0, "ring": 1}
+TAIL_SPLITS = {"auto": 0, "off": 1, "on": 2}
 
 # Every symbol include/flashoverlap.h declares.
 EXPORTED = [
@@ -38,7 +39,7 @@ EXPORTED = [
     "fo_workspace_size", "fo_workspace_init", "fo_ag_gemm", "fo_gemm_rs", "fo_dp_grad_rs",
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
     "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc", "fo_plan_task_order",
-    "fo_gemm_ar", "fo_trace_query",
+    "fo_gemm_ar", "fo_trace_query", "fo_plan_last_split_tiles",
 ]
 
 
@@ -58,7 +59,8 @@ class PlanDesc(ctypes.Structure):
         ("in_dtype", c_int32), ("out_dtype", c_int32), ("sched", c_int32), ("ag_transport", c_int32),
         ("w_layout", c_int32), ("deterministic", c_int32), ("timeout_ns", c_uint64),
         ("fault_inject", c_int32), ("tile_config", c_int32), ("interleave", c_int32), ("rs_algo", c_int32),
-        ("trace", c_int32), ("inject_delay_us", c_int32), ("reserved", c_int32 * 2),
+        ("trace", c_int32), ("inject_delay_us", c_int32), ("tail_split", c_int32),
+        ("reserved", c_int32 * 1),
     ]
 
 
@@ -97,6 +99,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_reduce_scatter_f32": ([P, PP, PP, P], c_int32),
         "fo_all_gather_copy": ([P, PP, PP, P], c_int32),
         "fo_plan_last_launches": ([P], c_int32),
+        "fo_plan_last_split_tiles": ([P], c_int32),
         "fo_status_string": ([c_int32], ctypes.c_char_p),
         "fo_version": ([], c_int32),
     }
@@ -171,7 +174,7 @@ class Plan:
 def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dtype=None,
             sched="rank_adaptive", ag_transport="peer_read", w_layout="kn", deterministic=False,
             timeout_ns=0, fault_inject="none", tile_config="auto", interleave="auto",
-            rs_algo="direct", trace=False, inject_delay_us=0) -> Plan:
+            rs_algo="direct", trace=False, inject_delay_us=0, tail_split="auto") -> Plan:
     lib = load()
     if out_dtype is None:
         out_dtype = "bf16" if op == "ag_gemm" else "f32"
@@ -192,6 +195,7 @@ def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dty
     d.rs_algo = RS_ALGOS[rs_algo]
     d.trace = 1 if trace else 0
     d.inject_delay_us = inject_delay_us
+    d.tail_split = TAIL_SPLITS[tail_split]
     h = c_void_p()
     _check(lib.fo_plan(ctypes.byref(d), ctypes.byref(h)), "fo_plan")
     return Plan(h.value, d)
@@ -317,6 +321,10 @@ def trace_summary(stamps):
 
 def fo_plan_last_launches(plan: Plan) -> int:
     return load().fo_plan_last_launches(plan)
+
+
+def fo_plan_last_split_tiles(plan: Plan) -> int:
+    return load().fo_plan_last_split_tiles(plan)
 
 
 def fo_version() -> int:

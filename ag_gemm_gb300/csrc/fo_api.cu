@@ -143,6 +143,17 @@ void fill_common(fo_plan_t p, fo::FoParams* k, void* ws) {
   k->ag_copy = p->d.op == FO_OP_AG_GEMM && p->d.ag_transport == FO_AG_COPY ? 1 : 0;
   k->n_cols = p->n_out;
   k->trace = p->d.trace ? reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + p->ws_trace_off) : nullptr;
+  // Tail split: decided per launch (run_chunk_gemm) once the grid is known.
+  k->sk_tiles = 0;
+  if (p->sk_cap) {
+    float* buf = reinterpret_cast<float*>(static_cast<char*>(ws) + p->ws_split_off);
+    if (k->sk_buf != buf) {
+      const uint64_t rows = (uint64_t)p->sk_cap * (p->pair ? 2 * FO_BM : FO_BM);
+      if (!enc2d(&k->tmSK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, buf, FO_BN, rows, FO_BN * 4, 32, 32)) buf = nullptr;
+    }
+    k->sk_buf = buf;
+    k->sk_ctr = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + p->ws_split_ctr_off);
+  }
   k->delay_ns = p->d.fault_inject == FO_INJECT_DELAY_FIRST_TASK ? (uint64_t)p->d.inject_delay_us * 1000ull : 0ull;
 }
 
@@ -301,20 +312,27 @@ fo_status launch_grid(fo_plan_t p, int variant, const DevInfo& di, int* grid) {
   return *grid > 0 ? FO_OK : FO_ERR_CUDA;
 }
 
-fo_status run_chunk_gemm(fo_plan_t p, int variant, const fo::FoParams* k, const DevInfo& di, cudaStream_t s) {
+fo_status run_chunk_gemm(fo_plan_t p, int variant, fo::FoParams* k, const DevInfo& di, cudaStream_t s) {
   int grid = 0;
   fo_status st = launch_grid(p, variant, di, &grid);
   if (st != FO_OK) return st;
+  // Tail split for this launch's units, when the workspace has room for it.
+  k->sk_tiles = 0;
+  if (p->sk_cap && k->sk_buf) {
+    const int sk = fo_tail_split_tiles((int64_t)p->R * p->R * p->tiles_m * p->tiles_n, p->pair ? grid / 2 : grid);
+    if (sk <= p->sk_cap) k->sk_tiles = sk;
+  }
   cudaError_t e = fo_launch_variant(variant, p->pair, *k, grid, s);
   if (fo_log_enabled())
-    fprintf(stderr, "[flashoverlap] launch variant %d, %d CTAs (%s), stream %p: %s\n", variant, grid,
-            p->pair ? "CTA pairs" : "single CTAs", (void*)s, cudaGetErrorString(e));
+    fprintf(stderr, "[flashoverlap] launch variant %d, %d CTAs (%s), %d tiles split, stream %p: %s\n", variant,
+            grid, p->pair ? "CTA pairs" : "single CTAs", k->sk_tiles, (void*)s, cudaGetErrorString(e));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FO_ERR_CUDA;
   }
   p->last_launches = 1;
   p->last_grid = grid;
+  p->last_split_tiles = k->sk_tiles;
   return FO_OK;
 }
 
@@ -386,6 +404,9 @@ fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const
   }
   if (!ok) return FO_ERR_CUDA;
   fill_common(p, k, scratch);
+  k->sk_tiles = 0;   // no tail split: its buffers are not in the static scratch
+  k->sk_buf = nullptr;
+  k->sk_ctr = nullptr;
   *variant = es == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
   return launch_grid(p, *variant, di, grid);
 }

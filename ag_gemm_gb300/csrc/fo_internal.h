@@ -60,6 +60,13 @@ struct fo_plan_s {
   bool ring;               // d.rs_algo == FO_RS_RING
   size_t ws_trace_off;     // trace = 1: uint64 [FO_TRACE_MAX_CTAS][FO_TRACE_STAMPS]
   int32_t last_grid;       // CTAs of the last fused-kernel launch (0 = none yet)
+  // Tail split: room for sk_cap split tiles (0 = none reserved): their fp32
+  // partials at ws_split_off (sk_cap x tile rows x FO_BN) and their release
+  // counters [sk_cap][2][4] at ws_split_ctr_off. The split region ends the
+  // workspace; everything else fits in the first ws_split_off bytes.
+  int32_t sk_cap;
+  size_t ws_split_off, ws_split_ctr_off;
+  int32_t last_split_tiles;
 
   int32_t last_launches;
   void* param_cache;       // host copy of the last kernel parameter block
@@ -87,3 +94,13 @@ fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const
 
 // Host logging (FO_LOG=1 in the environment): plan summaries and launches.
 bool fo_log_enabled();
+
+// Units of a GB300 (152 SMs) for a plan's tile shape: 76 CTA pairs or 152
+// CTAs. Used to size the tail split's workspace at plan time.
+#define FO_GB300_SMS 152
+
+// Tiles to cut along the reduction when `total` tiles run on `units` units:
+// the last partial wave plus two whole waves (or every tile, below two
+// waves), when the partial wave would leave more than 2% of the launch
+// idle; else 0.
+int fo_tail_split_tiles(int64_t total, int units);

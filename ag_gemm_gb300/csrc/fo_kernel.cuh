@@ -131,6 +131,16 @@ struct alignas(128) FoParams {
   // Fault injection: tiles of the first task wait this long after their
   // CTA started before their operands are loaded (0: off).
   uint64_t delay_ns;
+  // Tail split: the last sk_tiles tiles of the launch (the last partial
+  // wave plus up to two whole waves) are cut along K so that every unit gets the
+  // same number of k-blocks (0: off). A cut tile's head part leaves its fp32
+  // partial in the split buffer (tmSK / sk_buf, one kTileM x FO_BN block
+  // per split tile) and releases sk_ctr[(tile * 2 + cta) * 4 + quarter];
+  // its finishing part adds it and completes the tile as usual.
+  int32_t sk_tiles;
+  float* sk_buf;
+  uint32_t* sk_ctr;
+  CUtensorMap tmSK;
 };
 
 enum Completion : int { FO_COMPLETE_NONE = 0, FO_COMPLETE_BF16 = 1, FO_COMPLETE_ALLREDUCE = 2 };
@@ -148,6 +158,54 @@ __host__ __device__ constexpr uint32_t instr_desc() {
 struct Tile {
   int r, s, c, ord, mt, nt;    // mt: m-tile of this kernel's tile height
 };
+
+// One unit of a CTA's (or CTA pair's) work: k-blocks [kb0, kb1) of tile L.
+// FULL covers the whole reduction. Under the tail split a tile may be cut
+// once: its HEAD part (from k-block 0) leaves an fp32 partial, its FINISH
+// part (to the last k-block) adds that partial and completes the tile.
+enum WorkRole : int { WORK_FULL = 0, WORK_HEAD = 1, WORK_FINISH = 2 };
+struct Work {
+  int L, kb0, kb1, role, sk;   // sk: index among the split tiles (HEAD / FINISH)
+};
+
+// The i-th work item of `unit` (false when there is none). Without the tail
+// split, tiles go round-robin: unit, unit + units, ... With it, the first
+// total - sk_tiles tiles (whole waves) go round-robin, and the k-blocks of
+// the last sk_tiles tiles are dealt out in equal contiguous ranges, each at
+// least one tile long, so a tile is cut at most once. Every unit runs its
+// HEAD part first: a HEAD never waits, so each FINISH waits only for work
+// that runs ahead of anything it could block.
+__device__ __forceinline__ bool get_work(const FoParams& p, int total, int unit, int units, int i, Work& w) {
+  const int nkb = p.num_kb;
+  if (p.sk_tiles == 0) {
+    const int L = unit + i * units;
+    if (L >= total) return false;
+    w.L = L, w.kb0 = 0, w.kb1 = nkb, w.role = WORK_FULL, w.sk = -1;
+    return true;
+  }
+  const int first = total - p.sk_tiles;   // a whole number of waves
+  const int ndp = first / units;
+  if (i < ndp) {
+    w.L = unit + i * units, w.kb0 = 0, w.kb1 = nkb, w.role = WORK_FULL, w.sk = -1;
+    return true;
+  }
+  const int j = i - ndp;
+  const int64_t iters = (int64_t)p.sk_tiles * nkb;
+  const int64_t a = iters * unit / units, b = iters * (unit + 1) / units;
+  if (a >= b) return false;
+  const int ta = (int)(a / nkb), tb = (int)((b - 1) / nkb);
+  const int nseg = tb - ta + 1;
+  if (j >= nseg) return false;
+  const int kb1_last = (int)((b - 1) % nkb) + 1;
+  const bool head_last = nseg > 1 && kb1_last < nkb;   // the range ends inside tile tb
+  const int kseg = head_last ? (j == 0 ? nseg - 1 : j - 1) : j;
+  w.sk = ta + kseg;
+  w.L = first + w.sk;
+  w.kb0 = kseg == 0 ? (int)(a % nkb) : 0;
+  w.kb1 = kseg == nseg - 1 ? kb1_last : nkb;
+  w.role = (w.kb0 == 0 && w.kb1 == nkb) ? WORK_FULL : (w.kb0 == 0 ? WORK_HEAD : WORK_FINISH);
+  return true;
+}
 
 __device__ __forceinline__ Tile decode_tile(const FoParams& p, int L) {
   const int tpt = p.tiles_m * p.tiles_n;
@@ -340,7 +398,9 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
-      for (int L = unit; L < total; L += units) {
+      Work w;
+      for (int wi = 0; get_work(p, total, unit, units, wi, w); ++wi) {
+        const int L = w.L;
         if (*gstatus) *abort_flag = 1;
         if (*abort_flag) break;
         const Tile ti = decode_tile(p, L);
@@ -377,7 +437,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           }
         }
         bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int stage = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           if (!mbar_wait(empty_bar(stage), ph ^ 1u, abort_flag, kMbarLimitNs)) {
@@ -440,7 +500,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       uint32_t it = 0, tcount = 0;
-      for (int L = unit; L < total; L += units, ++tcount) {
+      Work w;
+      for (int wi = 0; get_work(p, total, unit, units, wi, w); ++wi, ++tcount) {
         if (*abort_flag) break;
         const int acc = tcount & 1;
         const uint32_t aph = (tcount >> 1) & 1u;
@@ -448,7 +509,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * FO_BN);
         bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int stage = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
           if (!mbar_wait(full_bar(stage), ph, abort_flag, kMbarLimitNs)) {
@@ -468,7 +529,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
                 A_MN ? smem_desc_sw128(sa + aoff, kBoxBytes, 1024) : smem_desc_sw128(sa + aoff, 16, 1024);
             const uint64_t bdesc =
                 B_MN ? smem_desc_sw128(sb + boff, kBoxBytes, 1024) : smem_desc_sw128(sb + boff, 16, 1024);
-            tc_mma<CG, TF32>(d, adesc, bdesc, kIdesc, (kb | k) != 0 ? 1u : 0u);
+            tc_mma<CG, TF32>(d, adesc, bdesc, kIdesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
           }
           if constexpr (PAIR) tc_commit_pair_multicast(empty_bar(stage), 0x3);
           else tc_commit<1>(empty_bar(stage));
@@ -505,13 +566,18 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       }
       pend_ctr = nullptr;
     };
-    for (int L = unit; L < total; L += units, ++tcount) {
+    Work w;
+    for (int wi = 0; get_work(p, total, unit, units, wi, w); ++wi, ++tcount) {
       if (*abort_flag) break;
-      const Tile ti = decode_tile(p, L);
+      const Tile ti = decode_tile(p, w.L);
       const int acc = tcount & 1;
       const uint32_t aph = (tcount >> 1) & 1u;
+      // Tiles of the split region run close together on every unit, so a
+      // partial another tile may wait for is released at once, not a tile
+      // later.
+      const bool in_split = p.sk_tiles != 0 && w.L >= total - p.sk_tiles;
       if constexpr (EPI == EPI_RS) {
-        if (p.ring && ti.ord > 0) {
+        if (p.ring && ti.ord > 0 && w.role != WORK_HEAD) {
           // Ring hop: warm L2 with the running sum this warp will read once
           // the accumulator is ready (each lane one row of its quarter).
           const int row = (ti.mt * (PAIR ? 2 : 1) + (int)prank) * FO_BM + q * 32 + lane;
@@ -533,6 +599,107 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       const int mt128 = ti.mt * (PAIR ? 2 : 1) + (int)prank;   // 128-row tile of this CTA within the chunk
       const int row0 = mt128 * FO_BM + q * 32;                   // first row of this quarter within the chunk
       const int n0 = ti.nt * FO_BN;
+
+      if (w.role != WORK_FULL) {
+        // Tail split. This warp's 32 rows of the tile in the split buffer:
+        const int srow = w.sk * C::kTileM + (int)prank * FO_BM + q * 32;
+        uint32_t* const sc = p.sk_ctr + ((size_t)w.sk * 2 + prank) * 4 + q;
+        constexpr int kSub = FO_BN / 32;
+        if (w.role == WORK_HEAD) {
+          // Head part: store the fp32 partial, free the accumulator and
+          // release the partial to the finishing part.
+          // (At most one head and one finishing part per unit and launch.
+          // The loops handle two sub-tiles per trip with fixed registers:
+          // the second's loads are in flight while the first is processed.)
+          if constexpr (EPI == EPI_RS) publish(true);
+          auto head_store = [&](int j, uint32_t(&v)[32]) {
+            const uint32_t buf = sEpi + (uint32_t)((e * kEpiBufs + (j % kEpiBufs)) * kEpiBuf);
+            if (lane == 0) bulk_wait_read<kEpiBufs - 1>();
+            __syncwarp();
+            stage_row_sw128(buf, lane, v);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.tmSK, buf, j * 32, srow);
+              bulk_commit();
+            }
+          };
+#pragma unroll 1
+          for (int j = 0; j < kSub; j += 2) {
+            uint32_t va[32], vb[32];
+            tmem_ld32(tbase + j * 32, va);
+            tmem_ld32(tbase + (j + 1) * 32, vb);
+            tmem_ld_wait();
+            reg_fence(va);
+            reg_fence(vb);
+            if (j + 2 == kSub) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                if constexpr (PAIR) mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+                else mbar_arrive(tempty_bar(acc));
+              }
+            }
+            head_store(j, va);
+            head_store(j + 1, vb);
+          }
+          if (lane == 0) {
+            bulk_wait<0>();
+            fence_proxy_async_global();
+            atom_add_release_u32(sc, 1u);
+          }
+          __syncwarp();
+          continue;
+        }
+        // Finishing part: wait for the head part's partial and add it into
+        // the accumulator; the tile then completes like any other.
+        int good = 1;
+        const uint32_t have = __shfl_sync(0xffffffffu, lane == 0 ? ld_acquire_u32(sc) : 0u, 0);
+        if (have < 1u) {
+          if constexpr (EPI == EPI_RS) publish(true);
+          if (lane == 0) {
+            good = wait_counter_geq(sc, 1u, p.timeout_ns, abort_flag, gstatus) ? 1 : 0;
+            if (!good && !*abort_flag && !*gstatus) record_error(p.status, FO_ERR_TIMEOUT, ti.r, ti.s, ti.c);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t abuf = sEpi + (uint32_t)(e * kEpiBufs * kEpiBuf);
+        const int srows = (w.sk + 1) * C::kTileM;
+        if (lane == 0) bulk_wait_read<0>();   // no store still reads the staging buffer
+        __syncwarp();
+        auto finish_add = [&](int j, const float4(&hs)[8]) {
+          uint32_t v[32];
+          tmem_ld32(tbase + j * 32, v);
+          tmem_ld_wait();
+          reg_fence(v);
+          stage_row_sw128(abuf, lane, v);
+          __syncwarp();
+          add_block32_sw128(abuf, lane, hs);
+          __syncwarp();
+          float f[32];
+          read_row_sw128(abuf, lane, f);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(f[i]);
+          tmem_st32(tbase + j * 32, v);
+          __syncwarp();   // every lane has read its row before the next sub-tile is staged
+        };
+        float4 ha[8], hb[8];
+        load_block32_coalesced(p.sk_buf, srow, srows, 0, FO_BN, FO_BN, lane, ha);
+        load_block32_coalesced(p.sk_buf, srow, srows, 32, FO_BN, FO_BN, lane, hb);
+#pragma unroll 1
+        for (int j = 0; j < kSub; j += 2) {
+          finish_add(j, ha);
+          if (j + 2 < kSub) load_block32_coalesced(p.sk_buf, srow, srows, (j + 2) * 32, FO_BN, FO_BN, lane, ha);
+          finish_add(j + 1, hb);
+          if (j + 3 < kSub) load_block32_coalesced(p.sk_buf, srow, srows, (j + 3) * 32, FO_BN, FO_BN, lane, hb);
+        }
+        tmem_st_wait();
+        if (lane == 0) atomicExch(sc, 0u);   // consumed: ready for the next launch
+        __syncwarp();
+      }
 
       uint32_t* ctr = nullptr;
       bool ok = true;
@@ -698,6 +865,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           publish(false);
           pend_ctr = ctr;
           pend_skip = false;
+          if (in_split) publish(true);
         }
       } else if constexpr (EPI == EPI_AG) {
         // 4 sub-tiles of 32 rows x 64 bf16 columns.
@@ -788,7 +956,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
                         q == 0 && ti.ord == 0;
             // With a finisher waiting for every other partial of the tile,
             // publishing late would stall it: publish this one now.
-            if (p.completion != FO_COMPLETE_NONE) publish(true);
+            if (p.completion != FO_COMPLETE_NONE || in_split) publish(true);
           }
         }
       }

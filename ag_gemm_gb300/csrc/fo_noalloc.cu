@@ -52,7 +52,9 @@ extern "C" fo_status fo_gemm_rs_noalloc(fo_plan_t p, const void* const* X, const
   if ((st = fo_internal_check_ptrs(p->R, X)) || (st = fo_internal_check_ptrs(p->R, W)) ||
       (st = fo_internal_check_ptrs(p->R, (const void* const*)Y)))
     return st;
-  if (p->ws_bytes > (size_t)FO_NOALLOC_SCRATCH_BYTES) return FO_ERR_SCRATCH_LIMIT;
+  // The tail split's buffers end the workspace; this entry point never
+  // splits, so it needs only what comes before them.
+  if (p->ws_split_off > (size_t)FO_NOALLOC_SCRATCH_BYTES) return FO_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   if ((st = scratch_on_current_device(&scratch))) return st;
   fo::FoParams params;   // on the stack: no host allocation either
@@ -60,7 +62,7 @@ extern "C" fo_status fo_gemm_rs_noalloc(fo_plan_t p, const void* const* X, const
   if ((st = fo_internal_rs_params_nocache(p, X, W, Y, scratch, &params, &variant, &grid))) return st;
   // The previous call's counters reset themselves, but a call that timed out
   // leaves them (and the status word) set: start every call from zero.
-  if (cudaMemsetAsync(scratch, 0, p->ws_bytes, (cudaStream_t)stream) != cudaSuccess) {
+  if (cudaMemsetAsync(scratch, 0, p->ws_split_off, (cudaStream_t)stream) != cudaSuccess) {
     cudaGetLastError();
     return FO_ERR_CUDA;
   }

@@ -30,6 +30,18 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
+int fo_tail_split_tiles(int64_t total, int units) {
+  if (units <= 0 || total <= units) return 0;
+  const int64_t waves = total / units, rem = total % units;
+  if (rem == 0) return 0;
+  const double idle = (double)(units - rem) / ((double)units * (double)(waves + 1));
+  if (idle <= 0.02) return 0;
+  // Two whole waves plus the partial one where there are that many, so that
+  // each unit's share (about two tiles) ends in a whole tile, whose math
+  // hides the finishing part's extra epilogue work.
+  return (int)(waves >= 2 ? 2 * units + rem : total);
+}
+
 // Host logging to stderr when the environment has FO_LOG=1 (read once).
 bool fo_log_enabled() {
   static const bool on = [] {
@@ -251,11 +263,11 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (d->inject_delay_us < 0 || d->inject_delay_us > 1000000) return FO_ERR_INVALID_ARG;
   if (d->inject_delay_us && d->fault_inject != FO_INJECT_DELAY_FIRST_TASK) return FO_ERR_INVALID_ARG;
   if (d->trace != 0 && d->trace != 1) return FO_ERR_INVALID_ARG;
+  if (d->tail_split < FO_TAIL_SPLIT_AUTO || d->tail_split > FO_TAIL_SPLIT_ON) return FO_ERR_INVALID_ARG;
   if (d->tile_config != FO_TILE_AUTO && d->tile_config != FO_TILE_SINGLE) return FO_ERR_INVALID_ARG;
   if (d->interleave < FO_INTERLEAVE_AUTO || d->interleave > FO_INTERLEAVE_RANK_MAJOR) return FO_ERR_INVALID_ARG;
   if (d->rs_algo != FO_RS_DIRECT && d->rs_algo != FO_RS_RING) return FO_ERR_INVALID_ARG;
-  for (int i = 0; i < 2; ++i)
-    if (d->reserved[i]) return FO_ERR_INVALID_ARG;
+  if (d->reserved[0]) return FO_ERR_INVALID_ARG;
   if (d->rs_algo == FO_RS_RING) {
     // The ring forwards a running sum, which needs the rank-adaptive order
     // (rank r's chunk at step s is r-1's at step s-1) and a kernel order that
@@ -365,18 +377,39 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   }
   p->ws_trace_off = off;
   if (d->trace) off += align_up((size_t)FO_TRACE_MAX_CTAS * FO_TRACE_STAMPS * sizeof(uint64_t), 256);
+  // Tail split, sized for a GB300's units (a launch on fewer or more units
+  // uses it only when its split fits).
+  p->ws_split_off = off;
+  p->sk_cap = 0;
+  {
+    const int64_t tiles = (int64_t)R * R * p->tiles_m * p->tiles_n;
+    const int units = p->pair ? FO_GB300_SMS / 2 : FO_GB300_SMS;
+    const bool on = d->tail_split == FO_TAIL_SPLIT_ON ||
+                    (d->tail_split == FO_TAIL_SPLIT_AUTO && d->op == FO_OP_AG_GEMM && p->num_kb >= 32 &&
+                     tiles >= 2 * (int64_t)units);
+    if (on) p->sk_cap = fo_tail_split_tiles(tiles, units);
+  }
+  if (p->sk_cap) {
+    off += align_up((size_t)p->sk_cap * (p->pair ? 2 * FO_BM : FO_BM) * FO_BN * 4, 256);
+    p->ws_split_ctr_off = off;
+    off += align_up((size_t)p->sk_cap * 8 * sizeof(uint32_t), 256);
+  } else {
+    p->ws_split_ctr_off = off;
+  }
   p->ws_bytes = off;
   p->last_launches = 0;
   p->last_grid = 0;
+  p->last_split_tiles = 0;
   p->param_cache = nullptr;
   if (fo_log_enabled()) {
     static const char* ops[] = {"ag_gemm", "gemm_rs", "dp_grad_rs", "gemm_ar"};
     fprintf(stderr,
             "[flashoverlap] plan %s R=%d M=%lld N=%lld K=%lld %s tiles %dx%d of %s, %d k-blocks, %s%s, "
-            "workspace %zu B\n",
+            "tail split for up to %d tiles, workspace %zu B\n",
             ops[d->op], R, (long long)M, (long long)N, (long long)K, eb == 4 ? "tf32" : "bf16", p->tiles_m,
             p->tiles_n, p->pair ? "256x256 (CTA pair)" : "128x256", p->num_kb,
-            d->sched == FO_SCHED_SLICED ? "sliced" : "rank-adaptive", p->ring ? ", ring RS" : "", p->ws_bytes);
+            d->sched == FO_SCHED_SLICED ? "sliced" : "rank-adaptive", p->ring ? ", ring RS" : "", p->sk_cap,
+            p->ws_bytes);
   }
   *out = p;
   return FO_OK;
@@ -437,6 +470,8 @@ fo_status fo_workspace_size(fo_plan_t p, size_t* bytes) {
 }
 
 int32_t fo_plan_last_launches(fo_plan_t p) { return p ? p->last_launches : -1; }
+
+int32_t fo_plan_last_split_tiles(fo_plan_t p) { return p ? p->last_split_tiles : -1; }
 
 const char* fo_status_string(fo_status s) {
   switch (s) {

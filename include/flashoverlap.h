@@ -139,6 +139,24 @@ typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
  * AUTO:     SKEWED for GEMM_RS / GEMM_AR, RANK_MAJOR for AG_GEMM and
  *           DP_GRAD_RS (the fastest of the three on GB300 for each op);
  *           LOCKSTEP under the ring reduce-scatter. */
+/* Balancing of the launch's last waves. The persistent kernel deals whole
+ * tiles to its units (CTA pairs or CTAs) round-robin; when the tile count is
+ * not a multiple of the units, the last wave leaves most of them idle.
+ * ON:   when that idle share would exceed 2% of the launch, the last
+ *       partial wave plus up to two whole waves of tiles are instead cut
+ *       along the reduction into equal ranges of k-blocks, one per unit; a
+ *       tile cut in two is completed by the unit holding its last k-block,
+ *       which adds the other part's fp32 partial (kept in the workspace).
+ *       Results agree with OFF up to fp32 re-association of that tile's
+ *       reduction (bit-exact in the integer mode).
+ * AUTO: ON for AG_GEMM plans whose tiles take at least 32 k-blocks and
+ *       whose launch spans two or more whole waves; OFF otherwise. (Cutting
+ *       costs each unit one extra store and reload of a tile; reduce-scatter
+ *       tiles cut this way also wait on one another's partials, which on
+ *       GB300 cost more than the balance gains.)
+ * OFF:  whole tiles only. */
+typedef enum { FO_TAIL_SPLIT_AUTO = 0, FO_TAIL_SPLIT_OFF = 1, FO_TAIL_SPLIT_ON = 2 } fo_tail_split;
+
 typedef enum {
   FO_INTERLEAVE_AUTO = 0,
   FO_INTERLEAVE_LOCKSTEP = 1,
@@ -179,7 +197,8 @@ typedef struct {
   int32_t trace;              /* 1: every launch records per-CTA timestamps in the
                                  workspace (fo_trace_query); 0: off */
   int32_t inject_delay_us;    /* FO_INJECT_DELAY_FIRST_TASK: 0..10^6 microseconds */
-  int32_t reserved[2];        /* must be zero */
+  int32_t tail_split;         /* fo_tail_split */
+  int32_t reserved[1];        /* must be zero */
 } fo_plan_desc;
 
 typedef struct fo_plan_s* fo_plan_t;
@@ -210,6 +229,10 @@ fo_status fo_plan_transfers(fo_plan_t plan, int32_t* out, int32_t cap, int32_t* 
  * may complete. `cap` in edges; *n gets the count. */
 fo_status fo_plan_edges(fo_plan_t plan, int32_t* out, int32_t cap, int32_t* n);
 
+/* Tiles the last launch with this plan cut along the reduction (the tail
+ * split; 0 = none, or no launch yet). -1 for a null plan. */
+int32_t fo_plan_last_split_tiles(fo_plan_t plan);
+
 /* Copy out the order in which the kernel runs the R*R chunk tasks:
  * order[2*i] = rank, order[2*i+1] = step of the i-th task. */
 fo_status fo_plan_task_order(fo_plan_t plan, int32_t* order);
@@ -217,8 +240,9 @@ fo_status fo_plan_task_order(fo_plan_t plan, int32_t* order);
 /* Bytes of device workspace the launching calls need (readiness counters,
  * flags and the device status word; fp32 shard sums for a bf16 output;
  * under FO_RS_RING every rank's fp32 receive buffer, R x M x N x 4 bytes;
- * with trace = 1, FO_TRACE_MAX_CTAS x FO_TRACE_STAMPS timestamps).
- * Never zero. */
+ * with trace = 1, FO_TRACE_MAX_CTAS x FO_TRACE_STAMPS timestamps; when the
+ * tail split applies, one fp32 tile per split tile, sized for the 152 SMs
+ * of a GB300). Never zero. */
 fo_status fo_workspace_size(fo_plan_t plan, size_t* bytes);
 
 /* Zero the workspace on `stream`. Required once before the first call that
