@@ -53,6 +53,37 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def algorithmic_bytes(w) -> float:
+    """DRAM bytes a launch must move at least: operands read once, the
+    output written once, and for a reduce-scatter (R-1)/R of every rank's
+    fp32 partial written to its owner and read back; peer-read all-gather
+    moves no extra bytes."""
+    d, R = w.dims, w.R
+    if w.op == "gemm_rs":
+        M, K, N = d["M"], d["K"], d["N"]
+        eb = 4 if w.dtype == "f32" else 2
+        return R * (M * K + K * N) * eb + 2.0 * (R - 1) * M * N * 4 + M * N * 4
+    if w.op == "dp_grad_rs":
+        T, M, N = d["T"], d["M"], d["N"]
+        return R * (T * M + T * N) * 2 + 2.0 * (R - 1) * M * N * 4 + M * N * 4
+    if w.op == "ag_gemm":
+        M, K, N = d["M"], d["K"], d["N"]
+        return (M * K + R * K * N + R * M * N) * 2
+    raise ValueError(w.op)
+
+
+def hbm_summary(w, kernel_ms, traffic, peaks):
+    """Bytes per launch and GB/s against the measured copy bandwidth."""
+    alg = algorithmic_bytes(w)
+    peak = float(peaks["hbm_gbs"])
+    out = {"algorithmic_bytes": alg, "algorithmic_gbs": alg / (kernel_ms * 1e-3) / 1e9, "peak_gbs": peak,
+           "traffic_bytes": traffic, "traffic_gbs": None}
+    out["frac_algorithmic"] = out["algorithmic_gbs"] / peak
+    if traffic:
+        out["traffic_gbs"] = traffic / (kernel_ms * 1e-3) / 1e9
+    return out
+
+
 def kernel_source_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -423,6 +454,8 @@ def run_ours(args):
                      "traffic": args.traffic if args.traffic is not None else profiled_traffic(w.name),
                      "peak_source": f"{peak_name}, {peak_src}",
                      "frac_of_burst_peak": achieved / float(peaks["bf16_tflops"])},
+        "hbm": hbm_summary(w, kernel_ms, args.traffic if args.traffic is not None else profiled_traffic(w.name),
+                           peaks),
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "pipelined": "inputs of step j+1 in and shards of step j-1 out during step j"},
         "gpu_launches": launches,
@@ -508,6 +541,7 @@ def run_other_op(args, w, dev, world, rank):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)") + ", " + peak_src},
+        "hbm": hbm_summary(w, kernel_ms, profiled_traffic(w.name), peaks),
         "gpu_launches": args.steps * B.fo_plan_last_launches(plan),
         "clocks": clk.summary(),
     }

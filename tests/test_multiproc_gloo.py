@@ -60,3 +60,19 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_algorithmic_bytes_of_the_bench_workloads():
+    # Operands once, output once, (R-1)/R of every fp32 partial to its owner
+    # and back (reduce-scatter); peer-read all-gather moves nothing extra.
+    import bench
+    from ag_gemm_gb300.inputs import WORKLOADS
+    rs = WORKLOADS["gemm_rs_down_r8_t8192_k1792_n4096"]
+    x_w = 8 * (8192 * 1792 + 1792 * 4096) * 2
+    partial = 8192 * 4096 * 4
+    assert bench.algorithmic_bytes(rs) == x_w + 2 * 7 * partial + partial
+    ag = WORKLOADS["ag_gemm_qkv_r4_s4096_h4096_n3072"]
+    assert bench.algorithmic_bytes(ag) == (4096 * 4096 + 4 * 4096 * 3072 + 4 * 4096 * 3072) * 2
+    s = bench.hbm_summary(rs, 0.5, 1.0e9, {"hbm_gbs": 6000.0})
+    assert abs(s["algorithmic_gbs"] - bench.algorithmic_bytes(rs) / 0.5e-3 / 1e9) < 1e-6
+    assert abs(s["traffic_gbs"] - 2000.0) < 1e-9 and abs(s["frac_algorithmic"] - s["algorithmic_gbs"] / 6000.0) < 1e-12
