@@ -198,7 +198,7 @@ def test_gemm_rs_new_buffers_after_cached_call(dev):
 
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("interleave", ["lockstep", "skewed"])
-@pytest.mark.parametrize("R,M,K,N", [(4, 1024, 136, 520), (2, 600, 200, 264), (8, 2048, 64, 256)])
+@pytest.mark.parametrize("R,M,K,N", [(4, 1024, 136, 520), (2, 600, 200, 264), (8, 2048, 64, 256), (1, 256, 128, 256)])
 def test_gemm_ar_integer_bit_exact(dev, tile, interleave, R, M, K, N):
     # RS into each owner's rows of its full output, then every finished
     # shard tile copied to all other ranks: every rank holds the whole sum.
@@ -380,7 +380,7 @@ def run_dp(dev, R, T, M, N, *, mode="int", seed=3, tile="auto", interleave="auto
 
 
 @pytest.mark.parametrize("tile", TILES)
-@pytest.mark.parametrize("R,T,M,N", [(2, 256, 256, 256), (4, 200, 800, 328), (8, 128, 1024, 256)])
+@pytest.mark.parametrize("R,T,M,N", [(1, 128, 256, 256), (2, 256, 256, 256), (4, 200, 800, 328), (8, 128, 1024, 256)])
 def test_dp_grad_rs_integer_bit_exact(dev, R, T, M, N, tile):
     got, ref = run_dp(dev, R, T, M, N, tile=tile)
     for d in range(R):
