@@ -29,7 +29,7 @@ INJECT = {"none": 0, "drop_transfer": 1, "skip_signal": 2, "delay_first_task": 3
 FO_TRACE_STAMPS = 8
 FO_TRACE_MAX_CTAS = 1024
 TILE_CONFIGS = {"auto": 0, "single": 1}
-INTERLEAVES = {"auto": 0, "lockstep": 1, "skewed": 2, "rank_major": 3}
+INTERLEAVES = {"auto": 0, "lockstep": 1, "skewed": 2, "rank_major": 3, "skewed_pairs": 4}
 RS_ALGOS = {"direct": 0, "ring": 1}
 TAIL_SPLITS = {"auto": 0, "off": 1, "on": 2}
 

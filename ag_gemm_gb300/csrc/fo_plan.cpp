@@ -77,7 +77,7 @@ void build_table(fo_plan_s* p) {
   int skew = p->d.interleave;
   if (skew == FO_INTERLEAVE_AUTO) {
     if (p->ring) skew = FO_INTERLEAVE_LOCKSTEP;   // a chain's hops a whole step apart: no hop waits
-    else skew = (ag || p->d.op == FO_OP_DP_GRAD_RS) ? FO_INTERLEAVE_RANK_MAJOR : FO_INTERLEAVE_SKEWED;
+    else skew = (ag || p->d.op == FO_OP_DP_GRAD_RS) ? FO_INTERLEAVE_RANK_MAJOR : FO_INTERLEAVE_SKEWED_PAIRS;
   }
   int n = 0;
   if (skew == FO_INTERLEAVE_RANK_MAJOR) {
@@ -87,6 +87,18 @@ void build_table(fo_plan_s* p) {
         p->task_s[n] = s;
         ++n;
       }
+  } else if (skew == FO_INTERLEAVE_SKEWED_PAIRS) {
+    // Slots t and t + 1 together: rank r runs its steps t + r and t + 1 + r
+    // back to back (ranks in ascending order, as in a single slot).
+    for (int t = -(R - 1); t <= R - 1; t += 2)
+      for (int r = 0; r < R; ++r)
+        for (int dt = 0; dt < 2 && t + dt <= R - 1; ++dt) {
+          const int s = t + dt + r;
+          if (s < 0 || s >= R) continue;
+          p->task_r[n] = r;
+          p->task_s[n] = s;
+          ++n;
+        }
   } else if (skew == FO_INTERLEAVE_SKEWED) {
     // Slot t = s - r (rank r runs r steps behind rank 0); inside a slot by
     // ascending step, so every shard receives its partials in step order.
@@ -265,7 +277,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (d->trace != 0 && d->trace != 1) return FO_ERR_INVALID_ARG;
   if (d->tail_split < FO_TAIL_SPLIT_AUTO || d->tail_split > FO_TAIL_SPLIT_ON) return FO_ERR_INVALID_ARG;
   if (d->tile_config != FO_TILE_AUTO && d->tile_config != FO_TILE_SINGLE) return FO_ERR_INVALID_ARG;
-  if (d->interleave < FO_INTERLEAVE_AUTO || d->interleave > FO_INTERLEAVE_RANK_MAJOR) return FO_ERR_INVALID_ARG;
+  if (d->interleave < FO_INTERLEAVE_AUTO || d->interleave > FO_INTERLEAVE_SKEWED_PAIRS) return FO_ERR_INVALID_ARG;
   if (d->rs_algo != FO_RS_DIRECT && d->rs_algo != FO_RS_RING) return FO_ERR_INVALID_ARG;
   if (d->reserved[0]) return FO_ERR_INVALID_ARG;
   if (d->rs_algo == FO_RS_RING) {

@@ -87,7 +87,7 @@ def hbm_summary(w, kernel_ms, traffic, peaks):
 def kernel_source_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("fo_device.cuh", "fo_kernel.cuh"):
+    for f in ("fo_device.cuh", "fo_kernel.cuh", "fo_plan.cpp"):
         with open(os.path.join(ROOT, "ag_gemm_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()

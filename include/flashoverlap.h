@@ -136,8 +136,11 @@ typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
  * RANK_MAJOR: all of rank 0's steps, then rank 1's, ...: one rank's
  *           weights (AG) or upstream gradient (DP) stay in L2 across its
  *           steps.
- * AUTO:     SKEWED for GEMM_RS / GEMM_AR, RANK_MAJOR for AG_GEMM and
- *           DP_GRAD_RS (the fastest of the three on GB300 for each op);
+ * SKEWED_PAIRS: SKEWED taken two slots at a time, each rank running its
+ *           two steps of the pair back to back: its weights are read once
+ *           per pair, while the two owners' shards stay in L2.
+ * AUTO:     SKEWED_PAIRS for GEMM_RS / GEMM_AR, RANK_MAJOR for AG_GEMM and
+ *           DP_GRAD_RS (the fastest choices on GB300 for each op);
  *           LOCKSTEP under the ring reduce-scatter. */
 /* Balancing of the launch's last waves. The persistent kernel deals whole
  * tiles to its units (CTA pairs or CTAs) round-robin; when the tile count is
@@ -161,7 +164,8 @@ typedef enum {
   FO_INTERLEAVE_AUTO = 0,
   FO_INTERLEAVE_LOCKSTEP = 1,
   FO_INTERLEAVE_SKEWED = 2,
-  FO_INTERLEAVE_RANK_MAJOR = 3
+  FO_INTERLEAVE_RANK_MAJOR = 3,
+  FO_INTERLEAVE_SKEWED_PAIRS = 4
 } fo_interleave;
 
 /* Global GEMM sizes (M, N, K); the per-rank operands are, for each op:

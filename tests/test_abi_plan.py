@@ -156,7 +156,7 @@ def test_workspace_counts_pair_tiles():
 
 @pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("op", ["gemm_rs", "ag_gemm", "dp_grad_rs"])
-@pytest.mark.parametrize("interleave", ["auto", "lockstep", "skewed", "rank_major"])
+@pytest.mark.parametrize("interleave", ["auto", "lockstep", "skewed", "rank_major", "skewed_pairs"])
 def test_task_order_keeps_every_ranks_schedule_order(R, op, interleave):
     dims = {"gemm_rs": (128 * R, 256, 64 * R), "ag_gemm": (128 * R, 64 * R, 256), "dp_grad_rs": (8 * R, 256, 64)}[op]
     p = B.fo_plan(op, R, *dims, interleave=interleave)
@@ -184,10 +184,34 @@ def test_skewed_order_groups_partials_by_owner_in_step_order(R):
         assert steps == sorted(steps) == list(range(R))
 
 
-def test_auto_interleave_is_skewed_for_rs_and_rank_major_for_ag_and_dp():
+@pytest.mark.parametrize("R", [2, 3, 4, 5, 8, 16])
+def test_skewed_pairs_run_each_ranks_two_steps_of_a_slot_pair_together(R):
+    p = B.fo_plan("gemm_rs", R, 128 * R, 256, 64 * R, interleave="skewed_pairs")
+    order = B.fo_plan_task_order(p)
+    assert sorted(order) == [(r, s) for r in range(R) for s in range(R)]
+    table = oracle.rs_schedule(R)
+    # slots t = s - r, taken in pairs (-(R-1), -(R-2)), (-(R-3), -(R-4)), ...
+    pair_of = lambda r, s: (s - r + R - 1) // 2
+    pairs = [pair_of(r, s) for (r, s) in order]
+    assert pairs == sorted(pairs)
+    for k in set(pairs):
+        tasks = [(r, s) for (r, s) in order if pair_of(r, s) == k]
+        # at most two owners per slot pair, and a rank's tasks of the pair adjacent and in step order
+        assert len({int(table[r, s]) for (r, s) in tasks}) <= 2
+        for r in {r for (r, _) in tasks}:
+            idx = [i for i, (rr, _) in enumerate(tasks) if rr == r]
+            assert idx == list(range(idx[0], idx[0] + len(idx)))
+            assert [tasks[i][1] for i in idx] == sorted(tasks[i][1] for i in idx)
+    # every owner still gets its partials in step order
+    for c in range(R):
+        steps = [s for (r, s) in order if int(table[r, s]) == c]
+        assert steps == list(range(R))
+
+
+def test_auto_interleave_is_skewed_pairs_for_rs_and_rank_major_for_ag_and_dp():
     R = 4
     rs = B.fo_plan_task_order(B.fo_plan("gemm_rs", R, 512, 256, 256))
-    assert rs == B.fo_plan_task_order(B.fo_plan("gemm_rs", R, 512, 256, 256, interleave="skewed"))
+    assert rs == B.fo_plan_task_order(B.fo_plan("gemm_rs", R, 512, 256, 256, interleave="skewed_pairs"))
     ar = B.fo_plan_task_order(B.fo_plan("gemm_ar", R, 512, 256, 256))
     assert ar == rs
     ag = B.fo_plan_task_order(B.fo_plan("ag_gemm", R, 512, 256, 256))
@@ -258,7 +282,7 @@ def test_ring_plan_edges_are_program_order_and_forwards(R):
 
 @pytest.mark.parametrize("R", [2, 3, 4, 8, 16])
 @pytest.mark.parametrize("op", ["gemm_rs", "dp_grad_rs"])
-@pytest.mark.parametrize("interleave", ["auto", "lockstep", "skewed"])
+@pytest.mark.parametrize("interleave", ["auto", "lockstep", "skewed", "skewed_pairs"])
 def test_ring_kernel_order_runs_every_chain_in_hop_order(R, op, interleave):
     # The kernel adds a chunk's partials in the order it runs them, and a
     # hop waits for its predecessor: each chain must run in hop order, or a

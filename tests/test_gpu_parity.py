@@ -140,7 +140,7 @@ def test_gemm_rs_deterministic_mode_is_bitwise_repeatable(dev):
 
 
 @pytest.mark.parametrize("tile", TILES)
-@pytest.mark.parametrize("interleave", ["lockstep", "skewed", "rank_major"])
+@pytest.mark.parametrize("interleave", ["lockstep", "skewed", "rank_major", "skewed_pairs"])
 @pytest.mark.parametrize("det", [False, True])
 def test_gemm_rs_every_interleave_bit_exact(dev, tile, interleave, det):
     outs, ref = run_gemm_rs(dev, 8, 2048, 136, 776, tile=tile, interleave=interleave, deterministic=det, repeat=2)
@@ -197,7 +197,7 @@ def test_gemm_rs_new_buffers_after_cached_call(dev):
 # ------------------------------------------------------------------ all-reduce and bf16 output
 
 @pytest.mark.parametrize("tile", TILES)
-@pytest.mark.parametrize("interleave", ["lockstep", "skewed"])
+@pytest.mark.parametrize("interleave", ["lockstep", "skewed", "skewed_pairs"])
 @pytest.mark.parametrize("R,M,K,N", [(4, 1024, 136, 520), (2, 600, 200, 264), (8, 2048, 64, 256), (1, 256, 128, 256)])
 def test_gemm_ar_integer_bit_exact(dev, tile, interleave, R, M, K, N):
     # RS into each owner's rows of its full output, then every finished
