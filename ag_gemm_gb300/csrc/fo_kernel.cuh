@@ -235,11 +235,13 @@ __device__ __forceinline__ bool signal_partial(uint32_t* ctr, int R) {
 }
 
 // Copy n16 16-byte words with nthr threads (thread tid handles words tid,
-// tid + nthr, ...), eight loads in flight per thread; L2-only caching.
+// tid + nthr, ...), sixteen loads in flight per thread (the four mover warps
+// of a CTA keep 32 KB in flight; eight loads left the gather copies
+// latency-bound); L2-only caching.
 __device__ __forceinline__ void copy16(const uint8_t* from, uint8_t* to, size_t n16, int tid, int nthr) {
   const uint4* s = reinterpret_cast<const uint4*>(from);
   uint4* d = reinterpret_cast<uint4*>(to);
-  constexpr int U = 8;
+  constexpr int U = 16;
   size_t i = (size_t)tid;
   for (; i + (size_t)(U - 1) * nthr < n16; i += (size_t)U * nthr) {
     uint4 v[U];

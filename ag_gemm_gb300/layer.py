@@ -19,6 +19,11 @@ backward (the usual TP-SP duals; the pages do not spell them out)
     column-parallel AG-GEMM Y_r = AllGather(X) . W_r:
         dX   = RS(dY_r . W_r^T)               GEMM-RS, W read as [N x K]
         dW_r = AllGather(X)^T . dY_r          per-rank weight GEMM (partials)
+The weight gradients of the row-parallel projections (o, down) are produced
+transposed, as AllGather(dY)^T . X_r, i.e. in the nn.Linear layout
+[out x in] = [H x H/R] and [H x F/R]: the per-rank GEMM then splits H rows
+into R chunks of H/R rows instead of H/R or F/R rows into R chunks (64 or
+224 rows for the default shape, which fill 128- and 256-row tiles poorly).
 
 The attention core, the SwiGLU and the norms are not part of the path: their
 outputs (attn_r, act_r) and upstream gradients are fixed synthetic tensors.
@@ -99,7 +104,7 @@ class TpspLayerProjections:
         self.G_dy, self.G_dh = per_rank((T, H)), per_rank((T, H))
         self.d_act, self.d_attn = per_rank((T, F // R)), per_rank((T, H // R))
         self.d_h_from_ug, self.d_x = per_rank((T // R, H)), per_rank((T // R, H))
-        self.dWd, self.dWo = per_rank((F // R, H), f32), per_rank((H // R, H), f32)
+        self.dWd, self.dWo = per_rank((H, F // R), f32), per_rank((H, H // R), f32)   # [out x in]
         self.dWug, self.dWqkv = per_rank((H, 2 * F // R), f32), per_rank((H, 3 * H // R), f32)
 
         P = {}
@@ -114,9 +119,9 @@ class TpspLayerProjections:
         P["o_dx"] = B.fo_plan("ag_gemm", R, T, H, H, w_layout="nk")
         P["qkv_dx"] = B.fo_plan("gemm_rs", R, T, H, 3 * H, w_layout="nk", out_dtype="bf16")
         # backward: weight gradients (per-rank GEMMs, no collective)
-        P["down_dw"] = B.fo_plan("dp_grad_rs", R, F // R, H, T)
+        P["down_dw"] = B.fo_plan("dp_grad_rs", R, H, F // R, T)
         P["ug_dw"] = B.fo_plan("dp_grad_rs", R, H, 2 * F // R, T)
-        P["o_dw"] = B.fo_plan("dp_grad_rs", R, H // R, H, T)
+        P["o_dw"] = B.fo_plan("dp_grad_rs", R, H, H // R, T)
         P["qkv_dw"] = B.fo_plan("dp_grad_rs", R, H, 3 * H // R, T)
         self.plans = P
         self.ws = {}
@@ -135,15 +140,15 @@ class TpspLayerProjections:
 
     def backward(self, stream=None):
         P, ws = self.plans, self.ws
-        # down (row-parallel): dAct = AG(dy) . Wd^T, dWd = act^T . AG(dy)
+        # down (row-parallel): dAct = AG(dy) . Wd^T, dWd^T = AG(dy)^T . act
         B.fo_ag_gemm(P["down_dx"], self.dy, self.Wd, self.d_act, self.G_dy, ws["down_dx"], stream)
-        B.fo_gemm_partials(P["down_dw"], self.act, self.G_dy, self.dWd, ws["down_dw"], stream)
+        B.fo_gemm_partials(P["down_dw"], self.G_dy, self.act, self.dWd, ws["down_dw"], stream)
         # up|gate (column-parallel): dh = RS(dug . Wug^T), dWug = Gh^T . dug
         B.fo_gemm_rs(P["ug_dx"], self.dug, self.Wug, self.d_h_from_ug, ws["ug_dx"], stream)
         B.fo_gemm_partials(P["ug_dw"], self.Gh, self.dug, self.dWug, ws["ug_dw"], stream)
-        # o (row-parallel): dAttn = AG(dh) . Wo^T, dWo = attn^T . AG(dh)
+        # o (row-parallel): dAttn = AG(dh) . Wo^T, dWo^T = AG(dh)^T . attn
         B.fo_ag_gemm(P["o_dx"], self.dh, self.Wo, self.d_attn, self.G_dh, ws["o_dx"], stream)
-        B.fo_gemm_partials(P["o_dw"], self.attn, self.G_dh, self.dWo, ws["o_dw"], stream)
+        B.fo_gemm_partials(P["o_dw"], self.G_dh, self.attn, self.dWo, ws["o_dw"], stream)
         # QKV (column-parallel): dx = RS(dqkv . Wqkv^T), dWqkv = Gx^T . dqkv
         B.fo_gemm_rs(P["qkv_dx"], self.dqkv, self.Wqkv, self.d_x, ws["qkv_dx"], stream)
         B.fo_gemm_partials(P["qkv_dw"], self.Gx, self.dqkv, self.dWqkv, ws["qkv_dw"], stream)

@@ -74,7 +74,7 @@ def test_backward_projections(layer):
         assert np.array_equal(_np(L.G_dy[r]), G_dy)
         assert np.array_equal(_np(L.d_h_from_ug[r]), oracle.round_bf16(d_h[r]))
         assert np.array_equal(_np(L.d_x[r]), oracle.round_bf16(d_x[r]))
-        assert np.array_equal(_np(L.dWd[r]), dWd[r])
-        assert np.array_equal(_np(L.dWo[r]), dWo[r])
+        assert np.array_equal(_np(L.dWd[r]), dWd[r].T)      # row-parallel grads in [out x in]
+        assert np.array_equal(_np(L.dWo[r]), dWo[r].T)
         assert np.array_equal(_np(L.dWug[r]), dWug[r])
         assert np.array_equal(_np(L.dWqkv[r]), dWqkv[r])
