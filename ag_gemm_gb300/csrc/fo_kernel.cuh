@@ -1,10 +1,14 @@
 // The persistent chunk-GEMM kernel of FlashOverlap on sm_103a.
 //
-// Persistent CTAs walk a static list of output tiles in step-major order:
-// all tiles of step 0 (every rank's first chunk task), then step 1, and so
-// on. This is the rank-adaptive order of Flash-RS / Flash-AG (gist.science,
-// "Technical Summary" section 2): for reduce-scatter each rank's own chunk is
-// its last task, for all-gather its first.
+// Every rank's chunk tasks run in that rank's schedule order, the
+// rank-adaptive order of Flash-RS / Flash-AG (gist.science, "Technical
+// Summary" section 2): for reduce-scatter each rank's own chunk is its last
+// task, for all-gather its first. How the R ranks' sequences interleave on
+// the one GPU (lockstep, skewed, skewed in slot pairs, rank-major) is the
+// plan's choice; the kernel walks the plan's task list. The tiles of that
+// list go to the persistent units (CTAs or CTA pairs) round-robin; under the
+// tail split the last waves are dealt out as equal k-block ranges instead
+// (get_work).
 //
 // Two tile configurations:
 //   PAIR = false  one CTA per SM owns a 128 x 256 fp32 accumulator; the MMA
@@ -16,7 +20,7 @@
 //                 its 128 rows x 256 columns. Operand traffic into each SM
 //                 is 2/3 of the single-CTA tile's.
 //
-// Warp roles (192 threads per CTA):
+// Warp roles (192 threads per CTA; 320 with movers):
 //   warp 0     TMA producer: 128-byte-wide K slices of both operands into a
 //              shared-memory ring (128B swizzle); 4 stages of 48 KB, or 6 of
 //              32 KB per CTA in the pair.
@@ -29,15 +33,25 @@
 //                       first partial of a shard tile is stored, later ones
 //                       are added (TMA reduce-add, fp32, at L2) once the
 //                       per-tile counter says the shard holds the first. This
-//                       accumulate is the P2P transfer.
+//                       accumulate is the P2P transfer. With a completion
+//                       action (bf16 output, all-reduce) the owner's last
+//                       partial finishes the tile; under the ring RS each
+//                       later hop adds the running sum its predecessor
+//                       forwarded and passes the result on.
 //                AG     bf16 store into rank r's output rows of the source
 //                       shard; the A operand was read straight from the
-//                       source rank's buffer (the transfer is the read).
+//                       source rank's buffer (the transfer is the read), or
+//                       from r's gather buffer under the copy transport.
 //                PARTIAL fp32 store into the computing rank's own buffer
 //                       (pure-GEMM control, no transfer).
+//   warps 6-9  (MOV) movers: 128-bit copies of 32-row shard pieces into the
+//              gather buffers, ring-forwarded behind ready flags (copy
+//              transport) or as a side output (peer read).
 // Synchronisation (shd-paper.top, 方法详解 "key design" paragraph, item 3):
-// mbarriers inside the CTA / pair, acquire/release counters in global memory
-// across CTAs; every wait is bounded and failures land in a status word.
+// mbarriers inside the CTA / pair, acquire/release counters and flags in
+// global memory across CTAs; every wait is bounded and failures land in a
+// status word. Optional %globaltimer stamps per CTA record when its math and
+// its transfers ended.
 #pragma once
 
 #include "fo_device.cuh"

@@ -85,11 +85,19 @@ def hbm_summary(w, kernel_ms, traffic, peaks):
 
 
 def kernel_source_sha256() -> str:
+    """sha256 of the kernel and plan sources with comments and blank lines
+    removed, so that a profile stays tied to the code it measured and not to
+    its comments."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("fo_device.cuh", "fo_kernel.cuh", "fo_plan.cpp"):
-        with open(os.path.join(ROOT, "ag_gemm_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "ag_gemm_gb300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        src = "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+        h.update(src.encode("utf-8"))
     return h.hexdigest()
 
 
