@@ -236,6 +236,18 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
   return FO_OK;
 }
 
+// How an AG call under peer read fills the gather buffers G_r. The mover
+// warps copy R*R shards (R*M*K*2 bytes) while the GEMM runs; they keep up
+// only while the GEMM is long enough, i.e. for wide outputs. For narrow ones
+// (N/R <= 1024 columns) the producer writes each A stage it loaded for the
+// first column block into G_r: no extra reads, at the cost of a wait for each
+// store before its stage is refilled. Measured on GB300 (R = 8, 8192 x 4096
+// gathered): N/R = 512: movers 392 us, stores 282 us (GEMM alone 159 us);
+// N/R = 1536: movers 500 us, stores 610 us (GEMM alone 438 us).
+bool gather_by_stores(fo_plan_t p) {
+  return p->d.ag_transport == FO_AG_PEER_READ && p->n_out <= 1024;
+}
+
 fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* const* G,
                    void* ws, fo::FoParams** out) {
   fo::FoParams* k = cached_params(p, KIND_AG, X, W, (const void* const*)Y, (const void* const*)G);
@@ -256,7 +268,11 @@ fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void
     if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, W[r], nr, K, nr * 2, 64, 64);
     else ok &= enc2d(&k->tmB[r], dt, W[r], K, nr, K * 2, 64, p->pair ? FO_BN / 2 : FO_BN);
     ok &= enc3d(&k->tmD[r], dt, Y[r], nr, rpc, R, nr * 2, rpc * nr * 2, 64, 32);
-    if (G) {
+    if (G && gather_by_stores(p)) {
+      // G_r is written from the A stages the GEMM loads, viewed as
+      // [K, rows/R, R] so that a store clips at the shard's last row.
+      ok &= enc3d(&k->tmG[r], dt, G[r], K, rpc, R, K * 2, rpc * K * 2, 64, FO_BM);
+    } else if (G) {
       ok &= enc2d(&k->tmG[r], dt, G[r], K, M, K * 2, 64, FO_BM);
       k->xsrc[r] = X[r];
       k->gdst[r] = G[r];
@@ -505,8 +521,10 @@ fo_status fo_ag_gemm(fo_plan_t p, const void* const* X, const void* const* W, vo
   fo::FoParams* k = nullptr;
   if ((st = build_ag(p, X, W, Y, G, ws, &k))) return st;
   int v;
-  if (G) v = p->d.w_layout == FO_W_KN ? FO_V_AG_BF16_KN_MOV : FO_V_AG_BF16_NK_MOV;
-  else v = p->d.w_layout == FO_W_KN ? FO_V_AG_BF16_KN : FO_V_AG_BF16_NK;
+  const bool kn = p->d.w_layout == FO_W_KN;
+  if (G && gather_by_stores(p)) v = kn ? FO_V_AG_BF16_KN_GST : FO_V_AG_BF16_NK_GST;
+  else if (G) v = kn ? FO_V_AG_BF16_KN_MOV : FO_V_AG_BF16_NK_MOV;
+  else v = kn ? FO_V_AG_BF16_KN : FO_V_AG_BF16_NK;
   return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
 }
 
@@ -608,7 +626,9 @@ static cudaError_t fo_variant_call(int v, bool pair, const fo::FoParams* p, int 
     case FO_V_AG_BF16_KN:
     case FO_V_AG_BF16_NK:
     case FO_V_AG_BF16_KN_MOV:
-    case FO_V_AG_BF16_NK_MOV: return fo_variant_ag(v, pair, p, grid, s, ctas);
+    case FO_V_AG_BF16_NK_MOV:
+    case FO_V_AG_BF16_KN_GST:
+    case FO_V_AG_BF16_NK_GST: return fo_variant_ag(v, pair, p, grid, s, ctas);
     case FO_V_PART_BF16_KN:
     case FO_V_PART_BF16_NK:
     case FO_V_PART_TF32_NK: return fo_variant_part(v, pair, p, grid, s, ctas);

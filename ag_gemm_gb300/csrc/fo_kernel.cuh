@@ -46,7 +46,9 @@
 //                       (pure-GEMM control, no transfer).
 //   warps 6-9  (MOV) movers: 128-bit copies of 32-row shard pieces into the
 //              gather buffers, ring-forwarded behind ready flags (copy
-//              transport) or as a side output (peer read).
+//              transport) or as a side output (peer read, wide outputs).
+//              With narrow outputs under peer read, the producer instead
+//              stores the A stages it loaded into the gather buffers.
 // Synchronisation (shd-paper.top, 方法详解 "key design" paragraph, item 3):
 // mbarriers inside the CTA / pair, acquire/release counters and flags in
 // global memory across CTAs; every wait is bounded and failures land in a
@@ -125,6 +127,7 @@ struct alignas(128) FoParams {
   int64_t row_bytes;           // K * 2
   int32_t pieces;              // 32-row pieces per shard
   int32_t ag_copy;             // 1: shards reach G_r along the ring and the GEMM reads them there
+  // (GST kernels: tmG views G_r as [K, rows/R, R], the map of the stores.)
   // RS/DP completion: the owner's last partial (contribution R-1) is the
   // finisher. It waits for the other R-1, adds their sum (read from the
   // shard rows tmD[c] addresses) to its own partial and writes the result:
@@ -334,9 +337,13 @@ __device__ __forceinline__ void read_row_sw128(uint32_t buf, int lane, float (&f
   }
 }
 
-template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false>
+// GST: peer-read all-gather with a gather buffer and narrow outputs: the
+// producer writes every A stage it loaded for a tile of the first column
+// block back out to G_r, instead of mover warps copying the shards.
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false, bool GST = false>
 __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(const __grid_constant__ FoParams p) {
   static_assert(!MOV || EPI == EPI_AG, "movers belong to the all-gather kernel");
+  static_assert(!GST || (EPI == EPI_AG && !MOV), "gather stores replace the movers of the all-gather kernel");
   using C = Cfg<PAIR>;
   constexpr int CG = PAIR ? 2 : 1;
   constexpr int kStages = C::kStages;
@@ -414,6 +421,23 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
+      // Gather stores still owed per stage: the A block a stage holds goes to
+      // G_r once the MMA has read it and before the stage is refilled.
+      constexpr int kG = GST ? kStages : 1;
+      int g_r[kG], g_c[kG], g_row[kG], g_k[kG];
+      uint32_t g_it[kG];
+#pragma unroll
+      for (int i = 0; i < kG; ++i) g_r[i] = -1;
+      auto g_flush = [&](int st) {
+        if constexpr (GST) {
+          if (g_r[st] >= 0) {
+            tma_store_3d(&p.tmG[g_r[st]], sStage + st * C::kStageBytes, g_k[st], g_row[st], g_c[st]);
+            bulk_commit();
+            bulk_wait_read<0>();   // the stage may be refilled once the store has read it
+            g_r[st] = -1;
+          }
+        }
+      };
       Work w;
       for (int wi = 0; get_work(p, total, unit, units, wi, w); ++wi) {
         const int L = w.L;
@@ -460,9 +484,15 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
             ok = false;
             break;
           }
+          g_flush(stage);
           const uint32_t sa = sStage + stage * C::kStageBytes;
           const uint32_t sb = sa + C::kAStage;
           const int k0 = kb * kBK;
+          if constexpr (GST) {
+            if (ti.nt == 0) {
+              g_r[stage] = ti.r, g_c[stage] = ti.c, g_row[stage] = a_mn0, g_k[stage] = k0, g_it[stage] = it;
+            }
+          }
           if constexpr (PAIR) {
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxBytes);
@@ -497,6 +527,18 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           }
         }
         if (!ok) break;
+      }
+      // Gather stores still owed: each waits until the MMA has read its stage.
+      if constexpr (GST) {
+        if (!*abort_flag) {
+#pragma unroll 1
+          for (int st = 0; st < kStages; ++st) {
+            if (g_r[st] < 0) continue;
+            if (!mbar_wait(empty_bar(st), (g_it[st] / kStages) & 1u, abort_flag, kMbarLimitNs)) break;
+            g_flush(st);
+          }
+        }
+        bulk_wait<0>();
       }
       // Drain: every load still in flight lands before the CTA may exit.
       // The pair's loads complete on the leader's barriers, which count both
@@ -1064,6 +1106,8 @@ enum fo_variant {
   FO_V_PART_DP,
   FO_V_AG_BF16_KN_MOV,
   FO_V_AG_BF16_NK_MOV,
+  FO_V_AG_BF16_KN_GST,
+  FO_V_AG_BF16_NK_GST,
   FO_V_COUNT
 };
 

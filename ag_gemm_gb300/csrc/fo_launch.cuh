@@ -3,9 +3,9 @@
 
 #include "fo_kernel.cuh"
 
-template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false>
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false, bool GST = false>
 cudaError_t fo_launch_one(const fo::FoParams& p, int grid, cudaStream_t stream) {
-  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV>;
+  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV, GST>;
   constexpr int smem = fo::Cfg<PAIR>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -34,9 +34,9 @@ cudaError_t fo_launch_one(const fo::FoParams& p, int grid, cudaStream_t stream) 
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false>
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false, bool GST = false>
 cudaError_t fo_max_ctas_one(int* ctas) {
-  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV>;
+  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV, GST>;
   constexpr int smem = fo::Cfg<PAIR>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -82,3 +82,8 @@ cudaError_t fo_max_ctas_one(int* ctas) {
                 : fo_launch_one<EPI, A_MN, B_MN, TF32, true, true>(*p, grid, s))               \
         : (ctas ? fo_max_ctas_one<EPI, A_MN, B_MN, TF32, false, true>(ctas)                   \
                 : fo_launch_one<EPI, A_MN, B_MN, TF32, false, true>(*p, grid, s)))
+#define FO_DISPATCH_PAIR_GST(EPI, A_MN, B_MN, TF32)                                          \
+  (pair ? (ctas ? fo_max_ctas_one<EPI, A_MN, B_MN, TF32, true, false, true>(ctas)             \
+                : fo_launch_one<EPI, A_MN, B_MN, TF32, true, false, true>(*p, grid, s))        \
+        : (ctas ? fo_max_ctas_one<EPI, A_MN, B_MN, TF32, false, false, true>(ctas)            \
+                : fo_launch_one<EPI, A_MN, B_MN, TF32, false, false, true>(*p, grid, s)))

@@ -257,7 +257,11 @@ fo_status fo_workspace_init(fo_plan_t plan, void* ws, fo_stream_t stream);
  * fp32 accumulation, rounded once (gist.science "Technical Summary" section 2,
  * Flash-All-Gather). Rank r's step s computes the rows of shard
  * (r - s) mod R. G may be NULL (no gathered copy; PEER_READ only) or an array
- * of R pointers to [M x K] bf16 buffers that receive the gathered X. */
+ * of R pointers to [M x K] bf16 buffers that receive the gathered X. Under
+ * COPY, G_r is the ring-forwarded buffer the GEMM reads from. Under
+ * PEER_READ it is a side output: copied by mover warps next to the GEMM, or,
+ * for outputs of at most 1024 columns per rank, written from the X tiles the
+ * GEMM already loads. */
 fo_status fo_ag_gemm(fo_plan_t plan, const void* const* X, const void* const* W,
                      void* const* Y, void* const* G, void* ws, fo_stream_t stream);
 

@@ -321,11 +321,14 @@ def run_ag_gather(dev, R, M, K, N, *, transport, tile="auto", layout="kn", seeds
 @pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("transport", ["copy", "peer_read"])
 @pytest.mark.parametrize("R,M,K,N,layout", [(4, 1024, 256, 512, "kn"), (2, 400, 200, 336, "nk"),
-                                             (3, 600, 136, 768, "kn")])
+                                             (3, 600, 136, 768, "kn"),
+                                             (2, 400, 136, 2560, "kn"), (4, 1000, 200, 5120, "nk")])
 def test_ag_gemm_gather_buffers_bit_exact(dev, tile, transport, R, M, K, N, layout):
     # copy: shards travel the ring into G_r and the GEMM of steps >= 1 reads
-    # them there; peer_read: G_r is a side output. Either way Y_r and G_r are
-    # exact; two calls in a row with new inputs on one workspace.
+    # them there; peer_read: G_r is a side output, written from the GEMM's
+    # loaded X tiles (outputs of <= 1024 columns per rank) or by mover warps
+    # (the last two shapes). Either way Y_r and G_r are exact; two calls in a
+    # row with new inputs on one workspace.
     for code, info, Y, G, inp in run_ag_gather(dev, R, M, K, N, transport=transport, tile=tile, layout=layout,
                                                seeds=(1, 2)):
         assert code == 0, info

@@ -145,10 +145,12 @@ def test_split_gemm_ar_integer_bit_exact(dev):
         assert np.array_equal(_np(Y[q]), ref[q])
 
 
+# 80 pair tiles (N_r = 1280: G by movers); 128 pair tiles (N_r = 1024: G from the loaded stages)
+@pytest.mark.parametrize("M,N", [(1024, 5120), (2048, 4096)])
 @pytest.mark.parametrize("transport", ["peer_read", "copy"])
 @pytest.mark.parametrize("mode", ["int", "randn"])
-def test_split_ag_gemm(dev, transport, mode):
-    R, M, K, N = 4, 1024, 320, 5120          # 80 pair tiles (N_r = 1280)
+def test_split_ag_gemm(dev, transport, mode, M, N):
+    R, K = 4, 320
     inp = ag_gemm_inputs(R, M, K, N // R, mode=mode, seed=1)
     plan = B.fo_plan("ag_gemm", R, M, N, K, ag_transport=transport, tail_split="on")
     bufs, Y = _guarded(R, (M, N // R), torch.bfloat16, dev)
