@@ -15,8 +15,9 @@ The JSON line reports whole-job TFLOP/s, the roofline fraction of the fused
 kernel against the measured bf16 dense peak, the same metric end to end with
 host buffers (host->device inputs and device->host outputs inside the timed
 region), the CPU oracle timed on a bounded sample, and, next to them, the
-pure-GEMM control, the unfused baseline (our GEMM + a separate reduce kernel)
-and cuBLAS through torch.matmul.
+pure-GEMM control, the unfused baseline (our GEMM + a separate reduce kernel),
+the data-slicing baseline over chunk counts 1 to 16, and cuBLAS through
+torch.matmul.
 
 With --gpus N > 1 (launched by torchrun) every rank runs an independent
 replica on its own GPU (the method here needs no cross-GPU exchange: the R
@@ -722,6 +723,71 @@ def traced_tail_us(B, desc, call, stream, dev, reps=5):
     return {"tail_us": sorted(tails)[reps // 2], "span_us": sorted(spans)[reps // 2]}
 
 
+class DataSlicing:
+    """The data-slicing baseline of the pages ([GS] "Technical Summary" §1,
+    Existing Solutions): the GEMM-RS cut into S row slices of M/S rows. Each
+    slice's GEMM (all R ranks' rows of that slice, one launch, fp32 partials)
+    runs on the launching stream; that slice's reduce-scatter (a separate
+    kernel) runs on a side stream once the slice's GEMM is done, overlapping
+    the next slice's GEMM. The last slice's reduce-scatter has no compute
+    left to hide behind: it is the tail. Rank d's output holds, for each
+    slice j in order, its M/(S*R) rows of that slice (slicing changes which
+    rows a rank owns; the sums are the same)."""
+
+    def __init__(self, B, R, M, N, Kr, S, dev):
+        import torch
+        if M % (S * R):
+            raise ValueError("M must split into S slices of R chunks")
+        self.B, self.R, self.S, self.Ms = B, R, S, M // S
+        tile = "auto" if self.Ms // R >= 256 else "single"
+        # One plan per slice: each keeps its own cached launch parameters.
+        self.plans = [B.fo_plan("gemm_rs", R, self.Ms, N, Kr * R, tile_config=tile) for _ in range(S)]
+        self.ws = [torch.zeros(B.fo_workspace_size(p), dtype=torch.uint8, device=dev) for p in self.plans]
+        self.P = [torch.empty(M, N, dtype=torch.float32, device=dev) for _ in range(R)]
+        self.side = torch.cuda.Stream(dev)
+
+    def __call__(self, X, W, Y, stream):
+        import torch
+        B, R, Ms = self.B, self.R, self.Ms
+        start = torch.cuda.Event()
+        start.record(stream)
+        self.side.wait_event(start)       # the previous call's readers of P are done
+        for j, plan in enumerate(self.plans):
+            Ps = [p[j * Ms:(j + 1) * Ms] for p in self.P]
+            B.fo_gemm_partials(plan, [x[j * Ms:(j + 1) * Ms] for x in X], W, Ps, self.ws[j], stream)
+            ready = torch.cuda.Event()
+            ready.record(stream)
+            self.side.wait_event(ready)
+            B.fo_reduce_scatter_f32(plan, Ps, [y[j * Ms // R:(j + 1) * Ms // R] for y in Y], self.side)
+        done = torch.cuda.Event()
+        done.record(self.side)
+        stream.wait_event(done)
+
+
+def slicing_sweep(B, X, W, Y, stream, dev, fused, pure, unfused, counts=(1, 2, 4, 8, 16)):
+    """Data slicing over chunk counts against the fused launch, with the
+    pages' measure ([GS] §4): the share of the serial path's communication
+    overhead (unfused minus the pure GEMM) that a method removes."""
+    import torch
+    R, (M, Kr), N = len(X), X[0].shape, W[0].shape[1]
+    overhead = unfused - pure
+
+    def reduction(t):
+        return 100.0 * (1.0 - (t - pure) / overhead) if overhead > 0 else None
+
+    rows = []
+    for S in counts:
+        if M % (S * R):
+            continue
+        ds = DataSlicing(B, R, M, N, Kr, S, dev)
+        t = _time(lambda: ds(X, W, Y, stream), stream)
+        rows.append({"chunks": S, "ms": t, "overhead_reduction_pct": reduction(t)})
+        del ds
+        torch.cuda.empty_cache()
+    return {"rows": rows, "fused_overhead_reduction_pct": reduction(fused),
+            "pure_gemm_ms": pure, "unfused_serial_ms": unfused}
+
+
 def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
     """Same-GPU comparisons: pure-GEMM control (no transfer), unfused
     (GEMM to per-rank partials, then a separate reduce kernel), cuBLAS."""
@@ -771,7 +837,9 @@ def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
     for name, kw in (("rank_adaptive", {}), ("sliced", dict(sched="sliced"))):
         tails[name] = traced_tail_us(B, dict(op="gemm_rs", R=R, M=M, N=N, K=X[0].shape[1] * R, **kw),
                                      lambda p, w: B.fo_gemm_rs(p, X, W, Y, w, stream), stream, dev)
+    slicing = slicing_sweep(B, X, W, Y, stream, dev, fused, pure, unf)
     return {
+        "data_slicing": slicing,
         "exposed_tail_us": tails,
         "ring_rs_ms": ring, "ring_rs_tflops": flops / ring / 1e9,
         "direct_in_order_adds_ms": det, "direct_in_order_adds_tflops": flops / det / 1e9,
