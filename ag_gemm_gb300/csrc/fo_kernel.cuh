@@ -424,8 +424,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       // Gather stores still owed per stage: the A block a stage holds goes to
       // G_r once the MMA has read it and before the stage is refilled.
       constexpr int kG = GST ? kStages : 1;
-      int g_r[kG], g_c[kG], g_row[kG], g_k[kG];
-      uint32_t g_it[kG];
+      int g_r[kG], g_c[kG] = {}, g_row[kG] = {}, g_k[kG] = {};
+      uint32_t g_it[kG] = {};
 #pragma unroll
       for (int i = 0; i < kG; ++i) g_r[i] = -1;
       auto g_flush = [&](int st) {
@@ -439,10 +439,15 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
         }
       };
       Work w;
+      // Another CTA's recorded failure ends this one's work. The status word
+      // is read at a tile's start and tested at the next one's, so its
+      // global round trip never holds up the tile's first loads.
+      int32_t gs = 0;
       for (int wi = 0; get_work(p, total, unit, units, wi, w); ++wi) {
         const int L = w.L;
-        if (*gstatus) *abort_flag = 1;
+        if (gs) *abort_flag = 1;
         if (*abort_flag) break;
+        gs = *gstatus;
         const Tile ti = decode_tile(p, L);
         if (p.delay_ns && L < p.tiles_m * p.tiles_n) {
           // Fault injection: hold the first task's tiles (bounded by the
