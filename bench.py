@@ -270,6 +270,18 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def workload_config(w, world: int) -> dict:
+    """The `config` object of a bench line, the same for both arms."""
+    dims = dict(w.dims)
+    if w.op == "gemm_rs":
+        dims = {"M": dims["M"], "K_per_rank": dims["K"], "N": dims["N"]}
+        l2 = "no flush: inputs (352 MB) and output (134 MB) of a step exceed the 129 MB L2"
+    else:
+        l2 = "no flush: a step's operands exceed the 129 MB L2"
+    return {"workload": w.name, "R": w.R, **dims, "l2": l2,
+            "parallelism": "replicas" if world > 1 else f"single GPU, {w.R} virtual ranks"}
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -292,7 +304,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / len(per),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "R": w.R, **w.dims, "parallelism": "replicas"},
+        "config": workload_config(w, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -454,9 +466,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "R": R, "M": M, "K_per_rank": K, "N": N,
-                   "l2": "no flush: inputs (352 MB) and output (134 MB) of a step exceed the 129 MB L2",
-                   "parallelism": "replicas" if world > 1 else "single GPU, 8 virtual ranks"},
+        "config": workload_config(w, world),
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
@@ -546,7 +556,7 @@ def run_other_op(args, w, dev, world, rank):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "R": w.R, **d, "l2": "no flush: a step's operands exceed the 129 MB L2"},
+        "config": workload_config(w, world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)") + ", " + peak_src},

@@ -76,3 +76,16 @@ def test_algorithmic_bytes_of_the_bench_workloads():
     s = bench.hbm_summary(rs, 0.5, 1.0e9, {"hbm_gbs": 6000.0})
     assert abs(s["algorithmic_gbs"] - bench.algorithmic_bytes(rs) / 0.5e-3 / 1e9) < 1e-6
     assert abs(s["traffic_gbs"] - 2000.0) < 1e-9 and abs(s["frac_algorithmic"] - s["algorithmic_gbs"] / 6000.0) < 1e-12
+
+
+def test_both_arms_describe_the_workload_alike():
+    # The reference arm and the GPU arm print the same `config` object.
+    import bench
+    from ag_gemm_gb300.inputs import WORKLOADS
+    rs = WORKLOADS[bench.DEFAULT_WORKLOAD]
+    c = bench.workload_config(rs, 1)
+    assert c["workload"] == rs.name and (c["R"], c["M"], c["K_per_rank"], c["N"]) == (8, 8192, 1792, 4096)
+    assert c["parallelism"] == "single GPU, 8 virtual ranks" and "l2" in c
+    assert bench.workload_config(rs, 4)["parallelism"] == "replicas"
+    ag = WORKLOADS["ag_gemm_qkv_r4_s4096_h4096_n3072"]
+    assert bench.workload_config(ag, 1)["parallelism"] == "single GPU, 4 virtual ranks"
