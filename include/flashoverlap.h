@@ -362,7 +362,11 @@ fo_status fo_trace_query(fo_plan_t plan, const void* ws, fo_stream_t stream, uin
 
 /* Pure-GEMM control for GEMM_RS / DP_GRAD_RS plans: the same chunk GEMM
  * tasks in the same order, but every partial is stored into its own rank's
- * [M x N] fp32 buffer P_r (no transfer, no accumulate). */
+ * [M x N] fp32 buffer P_r (no transfer, no accumulate). It doubles as the
+ * per-rank GEMM where no collective follows: in a TP-SP layer each rank's
+ * weight gradient (gathered activations^T . its upstream gradient) stays on
+ * that rank, and a DP_GRAD_RS plan run through this call computes all R of
+ * them in one launch. */
 fo_status fo_gemm_partials(fo_plan_t plan, const void* const* A, const void* const* B,
                            void* const* P, void* ws, fo_stream_t stream);
 
