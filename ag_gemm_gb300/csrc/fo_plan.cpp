@@ -76,7 +76,9 @@ void build_table(fo_plan_s* p) {
   // The kernel's task order.
   int skew = p->d.interleave;
   if (skew == FO_INTERLEAVE_AUTO) {
-    if (p->ring) skew = FO_INTERLEAVE_LOCKSTEP;   // a chain's hops a whole step apart: no hop waits
+    // Ring reduce-scatter and ring-forwarded all-gather: a chain's hops run
+    // a whole step apart, so no hop waits for the one before.
+    if (p->ring || (ag && p->d.ag_transport == FO_AG_COPY)) skew = FO_INTERLEAVE_LOCKSTEP;
     else skew = (ag || p->d.op == FO_OP_DP_GRAD_RS) ? FO_INTERLEAVE_RANK_MAJOR : FO_INTERLEAVE_SKEWED_PAIRS;
   }
   int n = 0;

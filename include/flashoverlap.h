@@ -139,9 +139,10 @@ typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
  * SKEWED_PAIRS: SKEWED taken two slots at a time, each rank running its
  *           two steps of the pair back to back: its weights are read once
  *           per pair, while the two owners' shards stay in L2.
- * AUTO:     SKEWED_PAIRS for GEMM_RS / GEMM_AR, RANK_MAJOR for AG_GEMM and
- *           DP_GRAD_RS (the fastest choices on GB300 for each op);
- *           LOCKSTEP under the ring reduce-scatter. */
+ * AUTO:     SKEWED_PAIRS for GEMM_RS / GEMM_AR, RANK_MAJOR for AG_GEMM
+ *           (peer read) and DP_GRAD_RS (the fastest choices on GB300 for
+ *           each op); LOCKSTEP under the ring reduce-scatter and the copy
+ *           transport, whose ring hops then run a whole step apart. */
 /* Balancing of the launch's last waves. The persistent kernel deals whole
  * tiles to its units (CTA pairs or CTAs) round-robin; when the tile count is
  * not a multiple of the units, the last wave leaves most of them idle.

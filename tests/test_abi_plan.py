@@ -208,7 +208,7 @@ def test_skewed_pairs_run_each_ranks_two_steps_of_a_slot_pair_together(R):
         assert steps == list(range(R))
 
 
-def test_auto_interleave_is_skewed_pairs_for_rs_and_rank_major_for_ag_and_dp():
+def test_auto_interleave_per_op_and_transport():
     R = 4
     rs = B.fo_plan_task_order(B.fo_plan("gemm_rs", R, 512, 256, 256))
     assert rs == B.fo_plan_task_order(B.fo_plan("gemm_rs", R, 512, 256, 256, interleave="skewed_pairs"))
@@ -224,6 +224,9 @@ def test_auto_interleave_is_skewed_pairs_for_rs_and_rank_major_for_ag_and_dp():
     for op in ("gemm_rs", "dp_grad_rs"):
         ring = B.fo_plan_task_order(B.fo_plan(op, R, 512, 256, 256, rs_algo="ring"))
         assert ring == B.fo_plan_task_order(B.fo_plan(op, R, 512, 256, 256, rs_algo="ring", interleave="lockstep"))
+    # so does the ring-forwarded all-gather (copy transport)
+    copy = B.fo_plan_task_order(B.fo_plan("ag_gemm", R, 512, 256, 256, ag_transport="copy"))
+    assert copy == lock
 
 
 def test_copy_transport_requires_gather_buffers():
