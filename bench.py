@@ -212,26 +212,39 @@ class ClockSampler:
 # ---------------------------------------------------------------- CPU oracle timing
 
 def oracle_inputs(workload):
-    """The workload's seeded inputs as the float64 arrays the oracle takes."""
-    if workload.op != "gemm_rs":
-        raise ValueError("oracle sample implemented for gemm_rs workloads")
+    """The workload's seeded inputs as the float64 arrays the oracle takes:
+    (X, W) for GEMM-RS and AG-GEMM, (X, dY) for DP-grad-RS."""
     inp = workload.make()
-    return [x.double().numpy() for x in inp["X"]], [w.double().numpy() for w in inp["W"]]
+    second = inp["dY"] if workload.op == "dp_grad_rs" else inp["W"]
+    return [x.double().numpy() for x in inp["X"]], [w.double().numpy() for w in second]
 
 
 def oracle_pass(workload, arrays, rows: int):
     """One pass of the CPU oracle over the first `rows` rows of every output
-    shard; returns (seconds, FLOPs)."""
+    shard (of every source shard of every rank's output, for AG-GEMM);
+    returns (seconds, FLOPs)."""
     import numpy as np
 
     import oracle
-    d = workload.dims
-    Xn, Wn = arrays
+    d, R = workload.dims, workload.R
+    A, Bn = arrays
     idx = np.arange(rows)
     t0 = time.perf_counter()
-    for sh in range(workload.R):
-        oracle.gemm_rs_rows(Xn, Wn, sh, idx)
-    return time.perf_counter() - t0, 2.0 * workload.R * rows * workload.R * d["K"] * d["N"]
+    if workload.op == "gemm_rs":
+        for sh in range(R):
+            oracle.gemm_rs_rows(A, Bn, sh, idx)
+        flops = 2.0 * R * rows * R * d["K"] * d["N"]
+    elif workload.op == "ag_gemm":
+        rpc = d["M"] // R
+        g = np.concatenate([src * rpc + idx for src in range(R)])
+        for r in range(R):
+            oracle.ag_gemm_rows(A, Bn, r, g)
+        flops = 2.0 * R * len(g) * d["K"] * d["N"]
+    else:
+        for sh in range(R):
+            oracle.dp_grad_rs_rows(A, Bn, sh, idx)
+        flops = 2.0 * R * rows * R * d["T"] * d["N"]
+    return time.perf_counter() - t0, flops
 
 
 def oracle_rows_for(workload, arrays, target_s: float) -> int:
@@ -258,8 +271,9 @@ def oracle_sample(workload, arrays, budget_s: float = 12.0):
         tot_t += dt
         tot_f += fl
         passes += 1
+    what = "source shards of every rank's output" if workload.op == "ag_gemm" else "output shards"
     desc = (f"{passes} pass(es) over {rows} of {workload.dims['M'] // workload.R} rows of each of the "
-            f"{workload.R} shards ({tot_f / 1e9:.0f} GFLOP fp64, {tot_t:.1f} s)")
+            f"{workload.R} {what} ({tot_f / 1e9:.0f} GFLOP fp64, {tot_t:.1f} s)")
     return tot_f / tot_t / 1e12, desc
 
 
@@ -298,7 +312,8 @@ def run_reference(args):
     tot_t = sum(p[0] for p in per)
     tot_flops = sum(p[1] for p in per)
     value = tot_flops / tot_t / 1e12
-    desc = (f"per step: {rows} of {w.dims['M'] // w.R} rows of each of the {w.R} shards "
+    what = "source shards of every rank's output" if w.op == "ag_gemm" else "output shards"
+    desc = (f"per step: {rows} of {w.dims['M'] // w.R} rows of each of the {w.R} {what} "
             f"({per[0][1] / 1e9:.0f} GFLOP fp64 numpy)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -314,6 +329,77 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- GPU arm
+
+def measure_e2e(B, mk_plan, launch, host_in, dev_in, dev_out, dev, stream, world, flops, steps):
+    """The metric end to end through the public API with host buffers. Every
+    step copies its inputs (each tensor of host_in) in from pinned host
+    memory and its outputs out to pinned host memory. Steps are pipelined
+    over two device buffer sets: step j+1's inputs stream in and step j-1's
+    outputs stream out (copy engines, two more streams) while step j
+    computes. dev_in / dev_out are the first buffer set; mk_plan() makes a
+    plan per set (each keeps its parameter block cached); launch(plan, ins,
+    outs, ws, stream) is the call."""
+    import torch
+    import torch.distributed as dist
+    hin = [[t.pin_memory() for t in group] for group in host_in]
+    hout = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in dev_out] for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for group in hin for t in group)
+    d2h = sum(t.numel() * t.element_size() for t in hout[0])
+    sets = [(dev_in, dev_out),
+            ([[torch.empty_like(t) for t in group] for group in dev_in], [torch.empty_like(o) for o in dev_out])]
+    plans = [mk_plan(), mk_plan()]
+    wss = []
+    for p in plans:
+        ws = torch.empty(B.fo_workspace_size(p), dtype=torch.uint8, device=dev)
+        B.fo_workspace_init(p, ws, stream)
+        wss.append(ws)
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+
+    def run(nsteps):
+        in_ready = [torch.cuda.Event() for _ in range(nsteps)]
+        done = [torch.cuda.Event() for _ in range(nsteps)]
+        out_done = [torch.cuda.Event() for _ in range(nsteps)]
+        for j in range(nsteps):
+            din, dout = sets[j % 2]
+            with torch.cuda.stream(s_in):
+                if j >= 2:
+                    s_in.wait_event(done[j - 2])          # set j%2's inputs no longer read
+                for dgroup, hgroup in zip(din, hin):
+                    for d_, h_ in zip(dgroup, hgroup):
+                        d_.copy_(h_, non_blocking=True)
+                in_ready[j].record(s_in)
+            stream.wait_event(in_ready[j])
+            if j >= 2:
+                stream.wait_event(out_done[j - 2])        # set j%2's outputs already copied out
+            launch(plans[j % 2], din, dout, wss[j % 2], stream)
+            done[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done[j])
+                for h_, d_ in zip(hout[j % 2], dout):
+                    h_.copy_(d_, non_blocking=True)
+                out_done[j].record(s_out)
+        stream.wait_event(out_done[nsteps - 1])
+
+    run(2)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    run(steps)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(a.elapsed_time(b), world, dev) / steps
+    for p, ws in zip(plans, wss):
+        code, info = B.fo_status_query(p, ws, stream)
+        if code != 0:
+            raise RuntimeError(f"device status {code} {info}")
+    return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "pipelined": "inputs of step j+1 in and outputs of step j-1 out during step j"}
+
 
 def run_ours(args):
     import torch
@@ -394,69 +480,9 @@ def run_ours(args):
     peak = float(peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"])
     peak_name = "bf16_tflops_sustained" if sustained else "bf16_tflops (burst)"
 
-    # End to end through the public API with host buffers: every step copies
-    # its inputs (all X_r and W_r) in from pinned host memory and its shards
-    # out to pinned host memory. Steps are pipelined over two device buffer
-    # sets: step j+1's inputs stream in and step j-1's shards stream out
-    # (copy engines, two more streams) while step j computes.
-    hX = [x.pin_memory() for x in inp["X"]]
-    hW = [x.pin_memory() for x in inp["W"]]
-    hY = [[torch.empty(M // R, N, dtype=torch.float32).pin_memory() for _ in range(R)] for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in hX + hW)
-    d2h = sum(t.numel() * t.element_size() for t in hY[0])
-    sets = [(X, W, Y),
-            ([torch.empty_like(x) for x in X], [torch.empty_like(x) for x in W], [torch.empty_like(y) for y in Y])]
-    plan2 = B.fo_plan("gemm_rs", R, M, N, K * R)   # one plan per buffer set keeps both parameter blocks cached
-    plans = [plan, plan2]
-    ws2 = torch.empty_like(ws)
-    B.fo_workspace_init(plan2, ws2)
-    wss = [ws, ws2]
-    s_in = torch.cuda.Stream(dev)
-    s_out = torch.cuda.Stream(dev)
-    e2e_steps = max(4, min(args.steps, 12))
-
-    def e2e_run(nsteps):
-        in_ready = [torch.cuda.Event() for _ in range(nsteps)]
-        done = [torch.cuda.Event() for _ in range(nsteps)]
-        out_done = [torch.cuda.Event() for _ in range(nsteps)]
-        for j in range(nsteps):
-            dX, dW, dY = sets[j % 2]
-            with torch.cuda.stream(s_in):
-                if j >= 2:
-                    s_in.wait_event(done[j - 2])          # set j%2's inputs no longer read
-                for d_, h_ in zip(dX, hX):
-                    d_.copy_(h_, non_blocking=True)
-                for d_, h_ in zip(dW, hW):
-                    d_.copy_(h_, non_blocking=True)
-                in_ready[j].record(s_in)
-            stream.wait_event(in_ready[j])
-            if j >= 2:
-                stream.wait_event(out_done[j - 2])        # set j%2's shards already copied out
-            B.fo_gemm_rs(plans[j % 2], dX, dW, dY, wss[j % 2], stream)
-            done[j].record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(done[j])
-                for h_, d_ in zip(hY[j % 2], dY):
-                    h_.copy_(d_, non_blocking=True)
-                out_done[j].record(s_out)
-        stream.wait_event(out_done[nsteps - 1])
-
-    e2e_run(2)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    e2e_run(e2e_steps)
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev) / e2e_steps
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
-    code, info = B.fo_status_query(plan2, ws2, stream)
-    if code != 0:
-        raise RuntimeError(f"device status {code} {info}")
-    del sets[1]
+    e2e = measure_e2e(B, lambda: B.fo_plan("gemm_rs", R, M, N, K * R),
+                      lambda p, din, dout, ws_, s_: B.fo_gemm_rs(p, din[0], din[1], dout, ws_, s_),
+                      [inp["X"], inp["W"]], [X, W], Y, dev, stream, world, flops, max(4, min(args.steps, 12)))
 
     extras = {}
     if not args.no_extras:
@@ -475,8 +501,7 @@ def run_ours(args):
                      "frac_of_burst_peak": achieved / float(peaks["bf16_tflops"])},
         "hbm": hbm_summary(w, kernel_ms, args.traffic if args.traffic is not None else profiled_traffic(w.name),
                            peaks),
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "pipelined": "inputs of step j+1 in and shards of step j-1 out during step j"},
+        "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "baselines": extras,
@@ -544,6 +569,16 @@ def run_other_op(args, w, dev, world, rank):
     if code != 0:
         raise RuntimeError(f"device status {code} {info}")
     elapsed_ms = ev[0][0].elapsed_time(ev[-1][1])
+    if w.op == "ag_gemm":
+        e2e = measure_e2e(B, lambda: B.fo_plan("ag_gemm", R, M, Nr * R, K),
+                          lambda p, din, dout, ws_, s_: B.fo_ag_gemm(p, din[0], din[1], dout, None, ws_, s_),
+                          [inp["X"], inp["W"]], [A, Bm], Y, dev, stream, world, w.flops(),
+                          max(4, min(args.steps, 12)))
+    else:
+        e2e = measure_e2e(B, lambda: B.fo_plan("dp_grad_rs", R, M, N, T),
+                          lambda p, din, dout, ws_, s_: B.fo_dp_grad_rs(p, din[0], din[1], dout, ws_, s_),
+                          [inp["X"], inp["dY"]], [A, Bm], Y, dev, stream, world, w.flops(),
+                          max(4, min(args.steps, 12)))
     kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     flops = w.flops()
@@ -561,9 +596,14 @@ def run_other_op(args, w, dev, world, rank):
                      "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                      "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)") + ", " + peak_src},
         "hbm": hbm_summary(w, kernel_ms, profiled_traffic(w.name), peaks),
+        "e2e": e2e,
         "gpu_launches": args.steps * B.fo_plan_last_launches(plan),
         "clocks": clk.summary(),
     }
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, desc = oracle_sample(w, oracle_inputs(w))
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": desc}
     if rank == 0:
         print(json.dumps(line))
     return 0

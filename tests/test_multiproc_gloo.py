@@ -89,3 +89,27 @@ def test_both_arms_describe_the_workload_alike():
     assert bench.workload_config(rs, 4)["parallelism"] == "replicas"
     ag = WORKLOADS["ag_gemm_qkv_r4_s4096_h4096_n3072"]
     assert bench.workload_config(ag, 1)["parallelism"] == "single GPU, 4 virtual ranks"
+
+
+def test_oracle_sample_flop_counts_for_every_op():
+    # The bench's CPU baseline counts, per pass, the FLOPs of exactly the
+    # sampled output rows: R shards x rows rows x (R ranks x 2 K N) for the
+    # reduce-scatters, R ranks x (R x rows) gathered rows x 2 K N_r for AG.
+    import types
+
+    import numpy as np
+
+    import bench
+    rng = np.random.default_rng(0)
+    R, rows = 2, 3
+    rs = types.SimpleNamespace(op="gemm_rs", R=R, dims={"M": 8, "K": 4, "N": 5})
+    Xs = [rng.standard_normal((8, 4)) for _ in range(R)]
+    Ws = [rng.standard_normal((4, 5)) for _ in range(R)]
+    assert bench.oracle_pass(rs, (Xs, Ws), rows)[1] == 2.0 * R * rows * R * 4 * 5
+    ag = types.SimpleNamespace(op="ag_gemm", R=R, dims={"M": 8, "K": 4, "N": 5})
+    Xa = [rng.standard_normal((4, 4)) for _ in range(R)]
+    assert bench.oracle_pass(ag, (Xa, Ws), rows)[1] == 2.0 * R * (R * rows) * 4 * 5
+    dp = types.SimpleNamespace(op="dp_grad_rs", R=R, dims={"T": 6, "M": 8, "N": 5})
+    Xd = [rng.standard_normal((6, 8)) for _ in range(R)]
+    dY = [rng.standard_normal((6, 5)) for _ in range(R)]
+    assert bench.oracle_pass(dp, (Xd, dY), rows)[1] == 2.0 * R * rows * R * 6 * 5
