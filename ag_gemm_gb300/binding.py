@@ -39,7 +39,7 @@ EXPORTED = [
     "fo_workspace_size", "fo_workspace_init", "fo_ag_gemm", "fo_gemm_rs", "fo_dp_grad_rs",
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
     "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc", "fo_plan_task_order",
-    "fo_gemm_ar", "fo_trace_query", "fo_plan_last_split_tiles",
+    "fo_gemm_ar", "fo_trace_query", "fo_plan_last_split_tiles", "fo_check_device_pointers",
 ]
 
 
@@ -100,6 +100,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_all_gather_copy": ([P, PP, PP, P], c_int32),
         "fo_plan_last_launches": ([P], c_int32),
         "fo_plan_last_split_tiles": ([P], c_int32),
+        "fo_check_device_pointers": ([c_int32, PP, P], c_int32),
         "fo_status_string": ([c_int32], ctypes.c_char_p),
         "fo_version": ([], c_int32),
     }
@@ -131,6 +132,8 @@ def _ptr(x) -> int:
     if hasattr(x, "data_ptr"):
         if not x.is_contiguous():
             raise ValueError("tensors passed to libflashoverlap must be contiguous")
+        if not getattr(x, "is_cuda", True) and not x.is_pinned():
+            raise ValueError("tensors passed to libflashoverlap must be CUDA tensors (or pinned host memory)")
         return x.data_ptr()
     raise TypeError(f"cannot take a device pointer from {type(x)!r}")
 
@@ -278,6 +281,13 @@ def fo_dp_grad_rs(plan: Plan, X, dY, dW, ws, stream=None) -> None:
 def fo_gemm_partials(plan: Plan, A, B, P, ws, stream=None) -> None:
     _check(load().fo_gemm_partials(plan, _ptr_array(A), _ptr_array(B), _ptr_array(P), _ptr(ws),
                                    _stream(stream)), "fo_gemm_partials")
+
+
+def fo_check_device_pointers(ptrs, stream=None) -> int:
+    """Status of fo_check_device_pointers for raw addresses (ints): FO_OK
+    when the current device can use every one of them."""
+    arr = (c_void_p * len(ptrs))(*[int(p) for p in ptrs])
+    return int(load().fo_check_device_pointers(len(ptrs), arr, _stream(stream)))
 
 
 def fo_reduce_scatter_f32(plan: Plan, P, Y, stream=None) -> None:

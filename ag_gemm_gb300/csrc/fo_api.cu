@@ -166,6 +166,58 @@ fo_status check_ptrs(int R, const void* const* a) {
   return FO_OK;
 }
 
+// Every pointer must address memory the current device can read and write
+// at that same address: its own device memory, managed memory, or host
+// memory pinned or registered with CUDA (mapped into the unified address
+// space). Pageable host memory and another GPU's memory are rejected, so a
+// wrong pointer fails here instead of faulting in the kernel. The query is
+// skipped while `stream` captures a graph, and for pointers the driver cannot
+// classify.
+fo_status check_device_ptrs(int R, const void* const* a, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return FO_OK;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return FO_OK;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FO_OK;
+  }
+  for (int r = 0; r < R; ++r) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, a[r]) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    switch (at.type) {
+      case cudaMemoryTypeDevice:
+        if (at.device != dev) return FO_ERR_INVALID_ARG;
+        break;
+      case cudaMemoryTypeManaged:
+        break;
+      case cudaMemoryTypeHost:
+        if (at.devicePointer != a[r]) return FO_ERR_INVALID_ARG;
+        break;
+      default:   // pageable host memory
+        return FO_ERR_INVALID_ARG;
+    }
+  }
+  return FO_OK;
+}
+
+// The same for every pointer a call hands the kernel (G and ws may be null).
+fo_status check_call_ptrs(int R, const void* const* a, const void* const* b, const void* const* d,
+                          const void* const* g, const void* ws, cudaStream_t s) {
+  fo_status st;
+  if ((st = check_device_ptrs(R, a, s)) || (st = check_device_ptrs(R, b, s)) || (st = check_device_ptrs(R, d, s)))
+    return st;
+  if (g && (st = check_device_ptrs(R, g, s))) return st;
+  if (ws && (st = check_device_ptrs(1, &ws, s))) return st;
+  return FO_OK;
+}
+
 // Encode the operand maps of a GEMM-RS / DP-grad-RS / GEMM-AR / pure-control
 // call. The fp32 destination of the partials is: Y_c (RS/DP with fp32 out),
 // the workspace's shard sums (bf16 out), rank c's own rows of its full
@@ -173,7 +225,7 @@ fo_status check_ptrs(int R, const void* const* a) {
 // the ring RS the forwards go to the receivers' buffers in the workspace and
 // only the last hop writes Y_c.
 fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A, const void* const* B,
-                        void* const* D, void* ws, fo::FoParams** out) {
+                        void* const* D, void* ws, cudaStream_t stream, fo::FoParams** out) {
   const int kind = partial ? KIND_PART : (dp ? KIND_DP : KIND_RS);
   const bool ring = !partial && p->ring;
   const bool bf16_out = !partial && p->d.out_dtype == FO_BF16;
@@ -185,6 +237,7 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
     *out = k;
     return FO_OK;
   }
+  if (fo_status st = check_call_ptrs(p->R, A, B, (const void* const*)D, nullptr, ws, stream)) return st;
   k = fresh_params(p);
   if (!k) return FO_ERR_INVALID_ARG;
   const int R = p->R;
@@ -249,13 +302,15 @@ bool gather_by_stores(fo_plan_t p) {
 }
 
 fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* const* G,
-                   void* ws, fo::FoParams** out) {
+                   void* ws, cudaStream_t stream, fo::FoParams** out) {
   fo::FoParams* k = cached_params(p, KIND_AG, X, W, (const void* const*)Y, (const void* const*)G);
   if (k) {
     fill_common(p, k, ws);
     *out = k;
     return FO_OK;
   }
+  if (fo_status st = check_call_ptrs(p->R, X, W, (const void* const*)Y, (const void* const*)G, ws, stream))
+    return st;
   k = fresh_params(p);
   if (!k) return FO_ERR_INVALID_ARG;
   const int R = p->R;
@@ -428,8 +483,16 @@ fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const
 }
 
 fo_status fo_internal_check_ptrs(int R, const void* const* a) { return check_ptrs(R, a); }
+fo_status fo_internal_check_device_ptrs(int R, const void* const* a, fo_stream_t stream) {
+  return check_device_ptrs(R, a, (cudaStream_t)stream);
+}
 
 extern "C" {
+
+fo_status fo_check_device_pointers(int32_t n, const void* const* ptrs, fo_stream_t stream) {
+  if (n < 0 || (n > 0 && !ptrs)) return FO_ERR_INVALID_ARG;
+  return check_device_ptrs(n, ptrs, (cudaStream_t)stream);
+}
 
 fo_status fo_trace_query(fo_plan_t p, const void* ws, fo_stream_t stream, uint64_t* stamps, int32_t cap,
                          int32_t* n_ctas) {
@@ -470,7 +533,7 @@ fo_status fo_gemm_rs(fo_plan_t p, const void* const* X, const void* const* W, vo
   DevInfo di;
   if ((st = preflight(p, &di))) return st;
   fo::FoParams* k = nullptr;
-  if ((st = build_rs_like(p, false, false, X, W, Y, ws, &k))) return st;
+  if ((st = build_rs_like(p, false, false, X, W, Y, ws, (cudaStream_t)stream, &k))) return st;
   int v = p->elem_bytes == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
   return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
 }
@@ -486,7 +549,7 @@ fo_status fo_gemm_ar(fo_plan_t p, const void* const* X, const void* const* W, vo
   DevInfo di;
   if ((st = preflight(p, &di))) return st;
   fo::FoParams* k = nullptr;
-  if ((st = build_rs_like(p, false, false, X, W, Y, ws, &k))) return st;
+  if ((st = build_rs_like(p, false, false, X, W, Y, ws, (cudaStream_t)stream, &k))) return st;
   int v = p->elem_bytes == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
   return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
 }
@@ -502,7 +565,7 @@ fo_status fo_dp_grad_rs(fo_plan_t p, const void* const* X, const void* const* dY
   DevInfo di;
   if ((st = preflight(p, &di))) return st;
   fo::FoParams* k = nullptr;
-  if ((st = build_rs_like(p, true, false, X, dY, dW, ws, &k))) return st;
+  if ((st = build_rs_like(p, true, false, X, dY, dW, ws, (cudaStream_t)stream, &k))) return st;
   return run_chunk_gemm(p, FO_V_DP_BF16, k, di, (cudaStream_t)stream);
 }
 
@@ -519,7 +582,7 @@ fo_status fo_ag_gemm(fo_plan_t p, const void* const* X, const void* const* W, vo
   DevInfo di;
   if ((st = preflight(p, &di))) return st;
   fo::FoParams* k = nullptr;
-  if ((st = build_ag(p, X, W, Y, G, ws, &k))) return st;
+  if ((st = build_ag(p, X, W, Y, G, ws, (cudaStream_t)stream, &k))) return st;
   int v;
   const bool kn = p->d.w_layout == FO_W_KN;
   if (G && gather_by_stores(p)) v = kn ? FO_V_AG_BF16_KN_GST : FO_V_AG_BF16_NK_GST;
@@ -539,7 +602,7 @@ fo_status fo_gemm_partials(fo_plan_t p, const void* const* A, const void* const*
   if ((st = preflight(p, &di))) return st;
   const bool dp = p->d.op == FO_OP_DP_GRAD_RS;
   fo::FoParams* k = nullptr;
-  if ((st = build_rs_like(p, dp, true, A, B, P, ws, &k))) return st;
+  if ((st = build_rs_like(p, dp, true, A, B, P, ws, (cudaStream_t)stream, &k))) return st;
   int v = dp ? FO_V_PART_DP
              : (p->elem_bytes == 4 ? FO_V_PART_TF32_NK
                                    : (p->d.w_layout == FO_W_KN ? FO_V_PART_BF16_KN : FO_V_PART_BF16_NK));
@@ -551,6 +614,9 @@ fo_status fo_reduce_scatter_f32(fo_plan_t p, const void* const* P, void* const* 
   if (p->d.op == FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
   fo_status st;
   if ((st = check_ptrs(p->R, P)) || (st = check_ptrs(p->R, (const void* const*)Y))) return st;
+  if ((st = check_device_ptrs(p->R, P, (cudaStream_t)stream)) ||
+      (st = check_device_ptrs(p->R, (const void* const*)Y, (cudaStream_t)stream)))
+    return st;
   if (p->n_out % 4) return FO_ERR_ALIGN;
   DevInfo di;
   if ((st = device_info(&di))) return st;
@@ -572,6 +638,9 @@ fo_status fo_all_gather_copy(fo_plan_t p, const void* const* X, void* const* G, 
   if (p->d.op != FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
   fo_status st;
   if ((st = check_ptrs(p->R, X)) || (st = check_ptrs(p->R, (const void* const*)G))) return st;
+  if ((st = check_device_ptrs(p->R, X, (cudaStream_t)stream)) ||
+      (st = check_device_ptrs(p->R, (const void* const*)G, (cudaStream_t)stream)))
+    return st;
   DevInfo di;
   if ((st = device_info(&di))) return st;
   PtrArray xa = {};

@@ -88,6 +88,7 @@ struct fo_ws_header {
 // (fo_noalloc.cu). FoParams is declared in fo_kernel.cuh.
 namespace fo { struct FoParams; }
 fo_status fo_internal_check_ptrs(int R, const void* const* a);
+fo_status fo_internal_check_device_ptrs(int R, const void* const* a, fo_stream_t stream);
 fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const void* const* W,
                                         void* const* Y, void* scratch, fo::FoParams* k, int* variant,
                                         int* grid);

@@ -52,6 +52,9 @@ extern "C" fo_status fo_gemm_rs_noalloc(fo_plan_t p, const void* const* X, const
   if ((st = fo_internal_check_ptrs(p->R, X)) || (st = fo_internal_check_ptrs(p->R, W)) ||
       (st = fo_internal_check_ptrs(p->R, (const void* const*)Y)))
     return st;
+  if ((st = fo_internal_check_device_ptrs(p->R, X, stream)) || (st = fo_internal_check_device_ptrs(p->R, W, stream)) ||
+      (st = fo_internal_check_device_ptrs(p->R, (const void* const*)Y, stream)))
+    return st;
   // The tail split's buffers end the workspace; this entry point never
   // splits, so it needs only what comes before them.
   if (p->ws_split_off > (size_t)FO_NOALLOC_SCRATCH_BYTES) return FO_ERR_SCRATCH_LIMIT;

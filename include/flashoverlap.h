@@ -381,6 +381,16 @@ fo_status fo_reduce_scatter_f32(fo_plan_t plan, const void* const* P, void* cons
 fo_status fo_all_gather_copy(fo_plan_t plan, const void* const* X, void* const* G,
                              fo_stream_t stream);
 
+/* Checks that each of n pointers addresses memory the current device can
+ * use at that address: its own device memory, managed memory, or host memory
+ * pinned or registered with CUDA. FO_OK, or FO_ERR_INVALID_ARG for pageable
+ * host memory, another GPU's memory, a null array or n < 0. Pointers the
+ * driver cannot classify pass. The launching calls run the same check
+ * whenever their pointers change (not while `stream` captures a graph), so
+ * a wrong pointer fails on the host instead of faulting in a kernel. Host
+ * only; enqueues nothing. */
+fo_status fo_check_device_pointers(int32_t n, const void* const* ptrs, fo_stream_t stream);
+
 /* Number of our kernels the last launching call on this plan enqueued. */
 int32_t fo_plan_last_launches(fo_plan_t plan);
 

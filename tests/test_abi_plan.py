@@ -375,3 +375,15 @@ def test_fo_log_prints_plans_to_stderr():
     env["FO_LOG"] = "0"
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
     assert "[flashoverlap]" not in r.stderr
+
+
+def test_binding_refuses_host_tensors():
+    # A CPU tensor never reaches the library: its address would not be
+    # device memory.
+    import torch
+    p = B.fo_plan("gemm_rs", 2, 256, 256, 512)
+    host = [torch.zeros(256, 256, dtype=torch.bfloat16) for _ in range(2)]
+    with pytest.raises(ValueError):
+        B.fo_gemm_rs(p, host, host, host, 4096, stream=0)
+    assert B.fo_plan_last_launches(p) == 0
+    assert B.fo_check_device_pointers.__doc__
