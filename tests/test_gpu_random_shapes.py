@@ -1,0 +1,132 @@
+"""Seeded random shapes for every op: R from 1 to 16, ragged rows, K and N,
+either tile configuration, any interleave, both weight layouts and output
+dtypes. Integer inputs, so every result must equal the oracle bit for bit
+(bf16 outputs: the oracle rounded once); guard bands around every output.
+Dimensions are multiples of 8 so that every row of every operand starts on
+a 16-byte boundary, as the library requires.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ag_gemm_gb300 import binding as B
+from ag_gemm_gb300.inputs import ag_gemm_inputs, dp_grad_inputs, gemm_rs_inputs
+from test_gpu_parity import Guarded, _np, _status_ok, _ws
+
+pytestmark = pytest.mark.gpu
+
+CASES = 25
+INTERLEAVES = ["auto", "lockstep", "skewed", "rank_major", "skewed_pairs"]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a GB300"
+    return torch.device("cuda:0")
+
+
+def _draw(seed):
+    g = np.random.default_rng(seed)
+    R = int(g.integers(1, 17))
+    rows = 8 * int(g.integers(1, 41))          # rows per rank: 8 .. 320
+    K = 8 * int(g.integers(1, 49))             # 8 .. 384
+    N = 8 * int(g.integers(1, 65))             # 8 .. 512
+    return g, R, rows, K, N
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_gemm_rs(dev, seed):
+    g, R, rows, Kr, N = _draw(1000 + seed)
+    M = R * rows
+    layout = ["kn", "nk"][int(g.integers(2))]
+    out = ["f32", "bf16"][int(g.integers(2))]
+    tile = ["auto", "single"][int(g.integers(2))]
+    il = INTERLEAVES[int(g.integers(len(INTERLEAVES)))]
+    det = bool(g.integers(2))
+    inp = gemm_rs_inputs(R, M, Kr, N, mode="int", seed=seed)
+    plan = B.fo_plan("gemm_rs", R, M, N, Kr * R, w_layout=layout, out_dtype=out, tile_config=tile,
+                     interleave=il, deterministic=det)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [(w if layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
+    Y = Guarded(R, (rows, N), torch.float32 if out == "f32" else torch.bfloat16, dev)
+    ws = _ws(plan, dev)
+    for _ in range(2):
+        B.fo_gemm_rs(plan, X, W, Y.views, ws)
+        _status_ok(plan, ws)
+    Y.check()
+    ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for d in range(R):
+        want = ref[d] if out == "f32" else oracle.round_bf16(ref[d])
+        assert np.array_equal(_np(Y.views[d]), want), f"R={R} M={M} K={Kr} N={N} {layout} {out} {tile} {il} shard {d}"
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_ag_gemm(dev, seed):
+    g, R, rows, K, Nr = _draw(2000 + seed)
+    M = R * rows
+    layout = ["kn", "nk"][int(g.integers(2))]
+    tile = ["auto", "single"][int(g.integers(2))]
+    il = INTERLEAVES[int(g.integers(len(INTERLEAVES)))]
+    transport = ["peer_read", "copy"][int(g.integers(2))]
+    with_g = transport == "copy" or bool(g.integers(2))
+    inp = ag_gemm_inputs(R, M, K, Nr, mode="int", seed=seed)
+    plan = B.fo_plan("ag_gemm", R, M, Nr * R, K, w_layout=layout, tile_config=tile, interleave=il,
+                     ag_transport=transport)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [(w if layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
+    Y = Guarded(R, (M, Nr), torch.bfloat16, dev)
+    G = Guarded(R, (M, K), torch.bfloat16, dev) if with_g else None
+    ws = _ws(plan, dev)
+    for _ in range(2):
+        B.fo_ag_gemm(plan, X, W, Y.views, G.views if G else None, ws)
+        _status_ok(plan, ws)
+    Y.check()
+    ref, gathered = oracle.ag_gemm([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    what = f"R={R} M={M} K={K} N_r={Nr} {layout} {tile} {il} {transport} G={with_g}"
+    for r in range(R):
+        assert np.array_equal(_np(Y.views[r]), oracle.round_bf16(ref[r])), f"{what} rank {r}"
+    if G:
+        G.check()
+        for r in range(R):
+            assert np.array_equal(_np(G.views[r]), gathered), f"{what} gather buffer {r}"
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_dp_grad_rs(dev, seed):
+    g, R, rows, T, N = _draw(3000 + seed)
+    M = R * rows
+    tile = ["auto", "single"][int(g.integers(2))]
+    il = INTERLEAVES[int(g.integers(len(INTERLEAVES)))]
+    out = ["f32", "bf16"][int(g.integers(2))]
+    inp = dp_grad_inputs(R, T, M, N, mode="int", seed=seed)
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T, tile_config=tile, interleave=il, out_dtype=out)
+    dW = Guarded(R, (rows, N), torch.float32 if out == "f32" else torch.bfloat16, dev)
+    ws = _ws(plan, dev)
+    B.fo_dp_grad_rs(plan, [x.to(dev) for x in inp["X"]], [y.to(dev) for y in inp["dY"]], dW.views, ws)
+    _status_ok(plan, ws)
+    dW.check()
+    ref = oracle.dp_grad_rs([_np(x) for x in inp["X"]], [_np(y) for y in inp["dY"]])
+    for d in range(R):
+        want = ref[d] if out == "f32" else oracle.round_bf16(ref[d])
+        assert np.array_equal(_np(dW.views[d]), want), f"R={R} T={T} M={M} N={N} {tile} {il} {out} shard {d}"
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_gemm_ar(dev, seed):
+    g, R, rows, Kr, N = _draw(4000 + seed)
+    M = R * rows
+    tile = ["auto", "single"][int(g.integers(2))]
+    il = ["auto", "lockstep", "skewed", "skewed_pairs"][int(g.integers(4))]
+    inp = gemm_rs_inputs(R, M, Kr, N, mode="int", seed=seed)
+    plan = B.fo_plan("gemm_ar", R, M, N, Kr * R, tile_config=tile, interleave=il)
+    Y = Guarded(R, (M, N), torch.float32, dev)
+    ws = _ws(plan, dev)
+    B.fo_gemm_ar(plan, [x.to(dev) for x in inp["X"]], [w.to(dev) for w in inp["W"]], Y.views, ws)
+    _status_ok(plan, ws)
+    Y.check()
+    ref = oracle.gemm_ar([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for q in range(R):
+        assert np.array_equal(_np(Y.views[q]), ref[q]), f"R={R} M={M} K={Kr} N={N} {tile} {il} rank {q}"
