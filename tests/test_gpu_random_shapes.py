@@ -1,6 +1,6 @@
 """Seeded random shapes for every op: R from 1 to 16, ragged rows, K and N,
 either tile configuration, any interleave, both weight layouts and output
-dtypes. Integer inputs, so every result must equal the oracle bit for bit
+dtypes, with the tail split forced on in about half the draws. Integer inputs, so every result must equal the oracle bit for bit
 (bf16 outputs: the oracle rounded once); guard bands around every output.
 Dimensions are multiples of 8 so that every row of every operand starts on
 a 16-byte boundary, as the library requires.
@@ -18,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 CASES = 25
 INTERLEAVES = ["auto", "lockstep", "skewed", "rank_major", "skewed_pairs"]
+SPLITS = ["auto", "on"]
 
 
 @pytest.fixture(scope="module")
@@ -46,9 +47,10 @@ def test_random_gemm_rs(dev, seed):
     tile = ["auto", "single"][int(g.integers(2))]
     il = INTERLEAVES[int(g.integers(len(INTERLEAVES)))]
     det = bool(g.integers(2))
+    split = SPLITS[int(g.integers(2))]
     inp = gemm_rs_inputs(R, M, Kr, N, mode="int", seed=seed)
     plan = B.fo_plan("gemm_rs", R, M, N, Kr * R, w_layout=layout, out_dtype=out, tile_config=tile,
-                     interleave=il, deterministic=det)
+                     interleave=il, deterministic=det, tail_split=split)
     X = [x.to(dev) for x in inp["X"]]
     W = [(w if layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
     Y = Guarded(R, (rows, N), torch.float32 if out == "f32" else torch.bfloat16, dev)
@@ -60,7 +62,7 @@ def test_random_gemm_rs(dev, seed):
     ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
     for d in range(R):
         want = ref[d] if out == "f32" else oracle.round_bf16(ref[d])
-        assert np.array_equal(_np(Y.views[d]), want), f"R={R} M={M} K={Kr} N={N} {layout} {out} {tile} {il} shard {d}"
+        assert np.array_equal(_np(Y.views[d]), want), f"R={R} M={M} K={Kr} N={N} {layout} {out} {tile} {il} {split} shard {d}"
 
 
 @pytest.mark.parametrize("seed", range(CASES))
@@ -72,9 +74,10 @@ def test_random_ag_gemm(dev, seed):
     il = INTERLEAVES[int(g.integers(len(INTERLEAVES)))]
     transport = ["peer_read", "copy"][int(g.integers(2))]
     with_g = transport == "copy" or bool(g.integers(2))
+    split = SPLITS[int(g.integers(2))]
     inp = ag_gemm_inputs(R, M, K, Nr, mode="int", seed=seed)
     plan = B.fo_plan("ag_gemm", R, M, Nr * R, K, w_layout=layout, tile_config=tile, interleave=il,
-                     ag_transport=transport)
+                     ag_transport=transport, tail_split=split)
     X = [x.to(dev) for x in inp["X"]]
     W = [(w if layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
     Y = Guarded(R, (M, Nr), torch.bfloat16, dev)
@@ -85,7 +88,7 @@ def test_random_ag_gemm(dev, seed):
         _status_ok(plan, ws)
     Y.check()
     ref, gathered = oracle.ag_gemm([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
-    what = f"R={R} M={M} K={K} N_r={Nr} {layout} {tile} {il} {transport} G={with_g}"
+    what = f"R={R} M={M} K={K} N_r={Nr} {layout} {tile} {il} {transport} G={with_g} {split}"
     for r in range(R):
         assert np.array_equal(_np(Y.views[r]), oracle.round_bf16(ref[r])), f"{what} rank {r}"
     if G:
@@ -101,8 +104,9 @@ def test_random_dp_grad_rs(dev, seed):
     tile = ["auto", "single"][int(g.integers(2))]
     il = INTERLEAVES[int(g.integers(len(INTERLEAVES)))]
     out = ["f32", "bf16"][int(g.integers(2))]
+    split = SPLITS[int(g.integers(2))]
     inp = dp_grad_inputs(R, T, M, N, mode="int", seed=seed)
-    plan = B.fo_plan("dp_grad_rs", R, M, N, T, tile_config=tile, interleave=il, out_dtype=out)
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T, tile_config=tile, interleave=il, out_dtype=out, tail_split=split)
     dW = Guarded(R, (rows, N), torch.float32 if out == "f32" else torch.bfloat16, dev)
     ws = _ws(plan, dev)
     B.fo_dp_grad_rs(plan, [x.to(dev) for x in inp["X"]], [y.to(dev) for y in inp["dY"]], dW.views, ws)
@@ -111,7 +115,7 @@ def test_random_dp_grad_rs(dev, seed):
     ref = oracle.dp_grad_rs([_np(x) for x in inp["X"]], [_np(y) for y in inp["dY"]])
     for d in range(R):
         want = ref[d] if out == "f32" else oracle.round_bf16(ref[d])
-        assert np.array_equal(_np(dW.views[d]), want), f"R={R} T={T} M={M} N={N} {tile} {il} {out} shard {d}"
+        assert np.array_equal(_np(dW.views[d]), want), f"R={R} T={T} M={M} N={N} {tile} {il} {out} {split} shard {d}"
 
 
 @pytest.mark.parametrize("seed", range(CASES))
@@ -120,8 +124,9 @@ def test_random_gemm_ar(dev, seed):
     M = R * rows
     tile = ["auto", "single"][int(g.integers(2))]
     il = ["auto", "lockstep", "skewed", "skewed_pairs"][int(g.integers(4))]
+    split = SPLITS[int(g.integers(2))]
     inp = gemm_rs_inputs(R, M, Kr, N, mode="int", seed=seed)
-    plan = B.fo_plan("gemm_ar", R, M, N, Kr * R, tile_config=tile, interleave=il)
+    plan = B.fo_plan("gemm_ar", R, M, N, Kr * R, tile_config=tile, interleave=il, tail_split=split)
     Y = Guarded(R, (M, N), torch.float32, dev)
     ws = _ws(plan, dev)
     B.fo_gemm_ar(plan, [x.to(dev) for x in inp["X"]], [w.to(dev) for w in inp["W"]], Y.views, ws)
@@ -129,4 +134,4 @@ def test_random_gemm_ar(dev, seed):
     Y.check()
     ref = oracle.gemm_ar([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
     for q in range(R):
-        assert np.array_equal(_np(Y.views[q]), ref[q]), f"R={R} M={M} K={Kr} N={N} {tile} {il} rank {q}"
+        assert np.array_equal(_np(Y.views[q]), ref[q]), f"R={R} M={M} K={Kr} N={N} {tile} {il} {split} rank {q}"
