@@ -135,3 +135,71 @@ def test_random_gemm_ar(dev, seed):
     ref = oracle.gemm_ar([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
     for q in range(R):
         assert np.array_equal(_np(Y.views[q]), ref[q]), f"R={R} M={M} K={Kr} N={N} {tile} {il} {split} rank {q}"
+
+
+# ---------------------------------------------------------------- random data
+# The same draws with normal-distributed inputs, held to the stated
+# tolerances: relative Frobenius error <= 1e-3 and elementwise relative error
+# <= 2e-2 against the fp64 oracle (rounded once to bf16 for bf16 outputs).
+RANDN_CASES = 8
+FRO_TOL, MAX_TOL = 1e-3, 2e-2
+
+
+def _close(got, want, what):
+    fro, mx, _ = oracle.rel_errors(got, want)
+    assert fro <= FRO_TOL and mx <= MAX_TOL, f"{what}: rel fro {fro:.3e}, max rel {mx:.3e}"
+
+
+@pytest.mark.parametrize("seed", range(RANDN_CASES))
+def test_random_gemm_rs_randn(dev, seed):
+    g, R, rows, Kr, N = _draw(5000 + seed)
+    M = R * rows
+    out = ["f32", "bf16"][int(g.integers(2))]
+    split = SPLITS[int(g.integers(2))]
+    inp = gemm_rs_inputs(R, M, Kr, N, mode="randn", seed=seed)
+    plan = B.fo_plan("gemm_rs", R, M, N, Kr * R, out_dtype=out, tail_split=split)
+    Y = Guarded(R, (rows, N), torch.float32 if out == "f32" else torch.bfloat16, dev)
+    ws = _ws(plan, dev)
+    B.fo_gemm_rs(plan, [x.to(dev) for x in inp["X"]], [w.to(dev) for w in inp["W"]], Y.views, ws)
+    _status_ok(plan, ws)
+    Y.check()
+    ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for d in range(R):
+        want = ref[d] if out == "f32" else oracle.round_bf16(ref[d])
+        _close(_np(Y.views[d]), want, f"R={R} M={M} K={Kr} N={N} {out} {split} shard {d}")
+
+
+@pytest.mark.parametrize("seed", range(RANDN_CASES))
+def test_random_ag_gemm_randn(dev, seed):
+    g, R, rows, K, Nr = _draw(6000 + seed)
+    M = R * rows
+    split = SPLITS[int(g.integers(2))]
+    inp = ag_gemm_inputs(R, M, K, Nr, mode="randn", seed=seed)
+    plan = B.fo_plan("ag_gemm", R, M, Nr * R, K, tail_split=split)
+    Y = Guarded(R, (M, Nr), torch.bfloat16, dev)
+    ws = _ws(plan, dev)
+    B.fo_ag_gemm(plan, [x.to(dev) for x in inp["X"]], [w.to(dev) for w in inp["W"]], Y.views, None, ws)
+    _status_ok(plan, ws)
+    Y.check()
+    ref, _ = oracle.ag_gemm([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for r in range(R):
+        _close(_np(Y.views[r]), oracle.round_bf16(ref[r]), f"R={R} M={M} K={K} N_r={Nr} {split} rank {r}")
+
+
+@pytest.mark.parametrize("seed", range(RANDN_CASES))
+def test_random_dp_grad_rs_randn(dev, seed):
+    g, R, rows, T, N = _draw(7000 + seed)
+    M = R * rows
+    out = ["f32", "bf16"][int(g.integers(2))]
+    split = SPLITS[int(g.integers(2))]
+    inp = dp_grad_inputs(R, T, M, N, mode="randn", seed=seed)
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T, out_dtype=out, tail_split=split)
+    dW = Guarded(R, (rows, N), torch.float32 if out == "f32" else torch.bfloat16, dev)
+    ws = _ws(plan, dev)
+    B.fo_dp_grad_rs(plan, [x.to(dev) for x in inp["X"]], [y.to(dev) for y in inp["dY"]], dW.views, ws)
+    _status_ok(plan, ws)
+    dW.check()
+    ref = oracle.dp_grad_rs([_np(x) for x in inp["X"]], [_np(y) for y in inp["dY"]])
+    for d in range(R):
+        want = ref[d] if out == "f32" else oracle.round_bf16(ref[d])
+        _close(_np(dW.views[d]), want, f"R={R} T={T} M={M} N={N} {out} {split} shard {d}")
