@@ -729,6 +729,46 @@ def run_sweep(args):
     return 0
 
 
+def run_single_gemm(args):
+    """One rank's GEMM (8192 x 4096 x K) through the fused kernel with a
+    bf16 output (R = 1 all-gather plan) and an fp32 output (R = 1 partials
+    control), next to cuBLAS bf16 on the same operands; one JSON line of
+    TFLOP/s. The inputs stay in L2, so this isolates the kernel's main loop
+    and epilogue from HBM and from the R-rank schedule."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from ag_gemm_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    M, N = 8192, 4096
+    g = torch.Generator().manual_seed(2)
+    rows = []
+    for K in (1792, 4096):
+        X = torch.randn(M, K, generator=g).bfloat16().to(dev)
+        W = (torch.randn(K, N, generator=g) * 0.02).bfloat16().to(dev)
+        y16 = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        y32 = torch.empty(M, N, device=dev)
+        pa = B.fo_plan("ag_gemm", 1, M, N, K)
+        wa = torch.zeros(B.fo_workspace_size(pa), dtype=torch.uint8, device=dev)
+        pp = B.fo_plan("gemm_rs", 1, M, N, K)
+        wp = torch.zeros(B.fo_workspace_size(pp), dtype=torch.uint8, device=dev)
+        flops = 2.0 * M * N * K
+        t_cub = _time(lambda: torch.matmul(X, W, out=y16), stream, iters=args.steps, warm=args.warmup)
+        t_bf = _time(lambda: B.fo_ag_gemm(pa, [X], [W], [y16], None, wa, stream), stream, iters=args.steps,
+                     warm=args.warmup)
+        t_f32 = _time(lambda: B.fo_gemm_partials(pp, [X], [W], [y32], wp, stream), stream, iters=args.steps,
+                      warm=args.warmup)
+        rows.append({"K": K, "cublas_bf16_tflops": flops / t_cub / 1e9, "fused_bf16_out_tflops": flops / t_bf / 1e9,
+                     "fused_f32_out_tflops": flops / t_f32 / 1e9})
+        del X, W, y16, y32, wa, wp
+        torch.cuda.empty_cache()
+    print(json.dumps({"single_gemm": {"M": M, "N": N}, "rows": rows}))
+    return 0
+
+
 def _smi_id(dev) -> str:
     """nvidia-smi selector of a torch device (its UUID when torch exposes it)."""
     import torch
@@ -915,6 +955,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: MLP-block sweep over --sweep-seqs (one JSON line)")
     ap.add_argument("--sweep-seqs", default="128,512,1024,2048,4096,8192,16384")
+    ap.add_argument("--single-gemm", action="store_true",
+                    help="instead of the bench line: one rank's GEMM, fused kernel against cuBLAS (one JSON line)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the fused kernel from an ncu capture of this build")
     args = ap.parse_args(argv)
@@ -924,6 +966,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.single_gemm:
+        return run_single_gemm(args)
     return run_ours(args)
 
 
