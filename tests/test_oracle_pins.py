@@ -440,3 +440,176 @@ def test_rel_errors_simple_cases():
     fro, mx, _ = oracle.rel_errors(got, ref)
     assert fro == pytest.approx(0.1 / np.sqrt(21.0))
     assert mx == pytest.approx(0.1)
+
+
+# --------------------------------------------------------------------------
+# Transfer lists and dependency edges: hand-derived fixture for R = 3 and 4,
+# an execution of the message lists on data, and a reachability pin.
+# --------------------------------------------------------------------------
+
+def _read_golden_transfers():
+    """{(kind, R): [tuples]} from tests/golden/transfers_r3_r4.txt."""
+    out = {}
+    with open(os.path.join(GOLDEN, "transfers_r3_r4.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, vals = line.split(":")
+            parts = head.split()
+            kind, R = parts[0], int(parts[1])
+            key = (kind, R) if kind != "table" else (kind, R, int(parts[2]))
+            out.setdefault(key, []).append(tuple(int(v) for v in vals.split()))
+    return out
+
+
+def _fixture_edges(R):
+    return sorted(((a, b), (c, d)) for (a, b, c, d) in _read_golden_transfers()[("edge", R)])
+
+
+def _ar_fixture_ok(R, fn):
+    return sorted(fn(R)) == sorted(_read_golden_transfers()[("ar", R)])
+
+
+def _edges_fixture_ok(R, fn):
+    return sorted(fn(R)) == _fixture_edges(R)
+
+
+@pytest.mark.parametrize("R", [3, 4])
+def test_transfer_lists_match_hand_derived_fixture(R):
+    g = _read_golden_transfers()
+    assert oracle.rs_schedule(R).tolist() == [list(g[("table", R, r)][0]) for r in range(R)]
+    assert sorted(oracle.rs_transfers(R)) == sorted(g[("rs_direct", R)])
+    assert sorted(oracle.rs_transfers(R, ring=True)) == sorted(g[("rs_ring", R)])
+    assert sorted(oracle.ag_transfers(R)) == sorted(g[("ag", R)])
+    assert _ar_fixture_ok(R, oracle.ar_transfers)
+    for kind in ("rs_direct", "rs_ring", "ag", "ar"):
+        assert len(set(g[(kind, R)])) == len(g[(kind, R)])       # no duplicate message
+
+
+@pytest.mark.parametrize("R", [3, 4])
+def test_dependency_edges_match_hand_derived_fixture(R):
+    assert _edges_fixture_ok(R, oracle.rs_dependency_edges)
+
+
+def _run_ar_messages(P, msgs, sch):
+    """Execute an all-reduce message list on data (pure Python bookkeeping).
+
+    Rank r starts with its [M, N] partial P_r. A message (src, dst, c, s) with
+    s < R is a reduce-scatter partial: src must compute chunk c at step s, and
+    owner dst == c adds rows c of P_src into its shard. A message with s == R
+    is the all-gather half: src must be the owner of c, and dst receives the
+    finished shard. Returns every rank's [M, N] result, or raises on a message
+    that the schedule cannot produce.
+    """
+    R = len(P)
+    rows = P[0].shape[0] // R
+    shard = {c: P[c][c * rows:(c + 1) * rows].copy() for c in range(R)}
+    got = {(q, c): None for q in range(R) for c in range(R)}
+    for (src, dst, c, s) in sorted(msgs, key=lambda m: m[3]):
+        if s < R:
+            if int(sch[src, s]) != c or dst != c or src == c:
+                raise AssertionError(f"bad reduce-scatter message {(src, dst, c, s)}")
+            shard[c] = shard[c] + P[src][c * rows:(c + 1) * rows]
+        else:
+            if src != c or dst == c:
+                raise AssertionError(f"bad all-gather message {(src, dst, c, s)}")
+            got[(dst, c)] = shard[c].copy()
+    for c in range(R):
+        got[(c, c)] = shard[c]
+    if any(v is None for v in got.values()):
+        raise AssertionError("a rank misses a shard")
+    return [np.concatenate([got[(q, c)] for c in range(R)], axis=0) for q in range(R)]
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 6])
+def test_ar_transfers_executed_on_data_give_the_all_reduce(R):
+    rng = np.random.default_rng(60 + R)
+    M, K, N = 2 * R, 3, 2
+    X = [_ints(rng, (M, K)) for _ in range(R)]
+    W = [_ints(rng, (K, N)) for _ in range(R)]
+    P = [X[r] @ W[r] for r in range(R)]
+    got = _run_ar_messages(P, oracle.ar_transfers(R), oracle.rs_schedule(R))
+    want = oracle.gemm_ar(X, W)
+    for q in range(R):
+        assert np.array_equal(got[q], want[q])
+
+
+def _reaches(edges, a, b):
+    adj = {}
+    for u, v in edges:
+        adj.setdefault(u, []).append(v)
+    stack, seen = [a], {a}
+    while stack:
+        u = stack.pop()
+        if u == b:
+            return True
+        for v in adj.get(u, []):
+            if v not in seen:
+                seen.add(v)
+                stack.append(v)
+    return False
+
+
+def _edges_order_every_contribution_before_owner(R, edges):
+    sch = oracle.rs_schedule(R)
+    for r in range(R):
+        for s in range(R):
+            c = int(sch[r, s])
+            if c != r and not _reaches(edges, (r, s), (c, R - 1)):
+                return False
+        for s in range(R - 1):
+            if ((r, s), (r, s + 1)) not in edges:
+                return False
+    return True
+
+
+@pytest.mark.parametrize("R", [2, 3, 4, 5, 8])
+def test_dependency_edges_order_every_contribution_before_the_owners_last_task(R):
+    edges = oracle.rs_dependency_edges(R)
+    assert _edges_order_every_contribution_before_owner(R, edges)
+    # the own-chunk task is the only one that consumes a transfer
+    for (a, b) in edges:
+        if a[0] != b[0]:
+            assert b[1] == R - 1
+
+
+def test_planted_wrong_all_gather_destination_is_caught(monkeypatch):
+    real = O.ar_transfers
+
+    def wrong_chunk(R):
+        rs = O.rs_transfers(R)
+        return rs + [(c, q, q, R) for c in range(R) for q in range(R) if q != c]
+
+    monkeypatch.setattr(O, "ar_transfers", wrong_chunk)
+    for R in (3, 4):
+        assert len(O.ar_transfers(R)) == len(real(R))           # the old count pin passes
+        assert not _ar_fixture_ok(R, O.ar_transfers)
+    R = 3
+    P = [np.arange(R * 2 * 2, dtype=np.float64).reshape(R * 2, 2) + r for r in range(R)]
+    with pytest.raises(AssertionError):
+        _run_ar_messages(P, O.ar_transfers(R), O.rs_schedule(R))
+
+
+def test_planted_dropped_transfer_edges_are_caught(monkeypatch):
+    def program_order_only(R, schedule=None):
+        return [((r, s), (r, s + 1)) for r in range(R) for s in range(R - 1)]
+
+    monkeypatch.setattr(O, "rs_dependency_edges", program_order_only)
+    for R in (3, 4):
+        assert not _edges_fixture_ok(R, O.rs_dependency_edges)
+        assert not _edges_order_every_contribution_before_owner(R, O.rs_dependency_edges(R))
+
+
+def test_planted_wrong_ring_forward_is_caught(monkeypatch):
+    real = O.rs_transfers
+
+    def skip_one(R, ring=False, schedule=None):
+        out = real(R, ring=ring, schedule=schedule)
+        if ring:
+            out = [(a, (b + 1) % R, c, s) for (a, b, c, s) in out]   # forward two hops
+        return out
+
+    monkeypatch.setattr(O, "rs_transfers", skip_one)
+    g = _read_golden_transfers()
+    assert sorted(O.rs_transfers(4, ring=True)) != sorted(g[("rs_ring", 4)])
