@@ -46,18 +46,22 @@ fo_status scratch_on_current_device(void** out) {
 
 extern "C" fo_status fo_gemm_rs_noalloc(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y,
                                         fo_stream_t stream) {
+  // Checks that need only the plan come first, so a plan this entry point
+  // cannot run is refused the same way with or without a GPU.
   if (!p || p->d.op != FO_OP_GEMM_RS) return FO_ERR_INVALID_ARG;
   if (p->ring) return FO_ERR_UNSUPPORTED;   // the ring's receive buffers are workspace-sized
   fo_status st;
   if ((st = fo_internal_check_ptrs(p->R, X)) || (st = fo_internal_check_ptrs(p->R, W)) ||
       (st = fo_internal_check_ptrs(p->R, (const void* const*)Y)))
     return st;
+  // The tail split's buffers end the workspace; this entry point never
+  // splits, so it needs only what comes before them (timestamps of a traced
+  // plan included, which alone exceed the array).
+  if (p->ws_split_off > (size_t)FO_NOALLOC_SCRATCH_BYTES || p->d.trace) return FO_ERR_SCRATCH_LIMIT;
+  if (p->d.out_dtype != FO_F32) return FO_ERR_DTYPE;
   if ((st = fo_internal_check_device_ptrs(p->R, X, stream)) || (st = fo_internal_check_device_ptrs(p->R, W, stream)) ||
       (st = fo_internal_check_device_ptrs(p->R, (const void* const*)Y, stream)))
     return st;
-  // The tail split's buffers end the workspace; this entry point never
-  // splits, so it needs only what comes before them.
-  if (p->ws_split_off > (size_t)FO_NOALLOC_SCRATCH_BYTES) return FO_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   if ((st = scratch_on_current_device(&scratch))) return st;
   fo::FoParams params;   // on the stack: no host allocation either

@@ -320,7 +320,14 @@ fo_status fo_status_query(fo_plan_t plan, void* ws, fo_stream_t stream, int32_t 
  *     The caller passes inputs and outputs exactly as for fo_gemm_rs.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.
+ *     before any stream capture on the device. The address is kept for the
+ *     life of the process: cudaDeviceReset (or anything else that destroys
+ *     the device's primary context) invalidates it, so do not call this
+ *     entry point on a device after resetting it.
+ *   - Every call queries its 3R pointers (cudaPointerGetAttributes) and
+ *     encodes 3R tensor maps on the host; nothing is cached in the plan.
+ *   - Plan checks come first: a plan this entry point cannot run is refused
+ *     before any pointer is queried or anything is enqueued.
  *   - Each call first zeroes the part of the array it uses (cudaMemsetAsync
  *     on `stream`), then launches the fused kernel.
  *   - All calls share the one array: calls that can overlap on the GPU

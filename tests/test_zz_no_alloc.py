@@ -61,7 +61,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
 def test_noalloc_rejects_problems_beyond_its_scratch():
     # R = 16 with 16 x 8192 rows and N = 8192 needs 16 x (64 x 32 tiles) x
     # 16 B of counters (512 KiB): more than the 64 KiB static scratch.
-    # Rejected before any device work, so this runs without a GPU.
+    # Rejected from the plan alone, before any pointer is queried or
+    # anything is enqueued, so this runs with or without a GPU.
     import __graft_entry__
     __graft_entry__.build()
     plan = B.fo_plan("gemm_rs", 16, 16 * 8192, 8192, 16 * 256)
@@ -70,3 +71,30 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     with pytest.raises(B.FlashOverlapError) as e:
         B.fo_gemm_rs_noalloc(plan, fake, fake, fake, stream=0)
     assert e.value.code == B.FO_ERR_SCRATCH_LIMIT
+
+
+@pytest.mark.gpu
+def test_noalloc_call_after_a_timed_out_call_is_exact():
+    # A call whose device wait runs out leaves its counters and status word in
+    # the shared static array; the next call zeroes the array before it
+    # launches, so a healthy call that follows gives the exact result.
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a GB300"
+    dev = torch.device("cuda:0")
+    R, M, K, N = 2, 256, 128, 256
+    inp = gemm_rs_inputs(R, M, K, N, mode="int", seed=0)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [w.to(dev) for w in inp["W"]]
+    Y = [torch.empty(M // R, N, device=dev) for _ in range(R)]
+    bad = B.fo_plan("gemm_rs", R, M, N, K * R, fault_inject="skip_signal", timeout_ns=20_000_000)
+    B.fo_gemm_rs_noalloc(bad, X, W, Y)       # one counter signal is never given: the wait runs out
+    torch.cuda.synchronize()
+    good = B.fo_plan("gemm_rs", R, M, N, K * R)
+    want = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for call in range(2):
+        Y = [torch.full((M // R, N), float("nan"), device=dev) for _ in range(R)]
+        B.fo_gemm_rs_noalloc(good, X, W, Y)
+        torch.cuda.synchronize()
+        for d in range(R):
+            assert np.array_equal(_np(Y[d]), want[d]), f"call {call} shard {d}"
