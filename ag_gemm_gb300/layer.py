@@ -28,8 +28,9 @@ into R chunks of H/R rows instead of H/R or F/R rows into R chunks (64 or
 The attention core, the SwiGLU and the norms are not part of the path: their
 outputs (attn_r, act_r) and upstream gradients are fixed synthetic tensors.
 Every GEMM runs in the library's kernels; this module only allocates
-buffers and issues the calls (16 launches per forward + backward: 4 + 4 + 4
-weight-gradient GEMMs + 4 more collective GEMMs).
+buffers and issues the calls: 12 launches per forward + backward (4
+forward collective GEMMs, 4 backward data-gradient collective GEMMs and 4
+per-rank weight-gradient GEMMs).
 """
 from __future__ import annotations
 

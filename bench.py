@@ -485,8 +485,10 @@ def run_ours(args):
                       [inp["X"], inp["W"]], [X, W], Y, dev, stream, world, flops, max(4, min(args.steps, 12)))
 
     extras = {}
+    others = None
     if not args.no_extras:
         extras = measure_extras(B, plan, X, W, Y, ws, stream, flops, dev)
+        others = measure_other_workloads(B, dev, stream)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -505,6 +507,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "baselines": extras,
+        "other_workloads": others,
     }
     if rank == 0 and not args.no_cpu_baseline:
         tf, desc = oracle_sample(w, oracle_inputs(w))
@@ -520,13 +523,10 @@ def run_ours(args):
 LAYER_WORKLOAD = "tpsp_layer_r8_t8192_h4096_f14336"
 
 
-def run_other_op(args, w, dev, world, rank):
-    """Timed loop of the AG-GEMM or DP-grad-RS workloads (same timing rules
-    as the default line; no comparison legs)."""
+def _op_setup(B, w, dev):
+    """Device inputs, outputs, plan and workspace of an AG-GEMM or DP-grad-RS
+    workload: (inp, A, Bm, Y, plan, ws, launch(stream))."""
     import torch
-    import torch.distributed as dist
-
-    from ag_gemm_gb300 import binding as B
     d = w.dims
     inp = w.make()
     if w.op == "ag_gemm":
@@ -543,13 +543,98 @@ def run_other_op(args, w, dev, world, rank):
         plan = B.fo_plan("dp_grad_rs", R, M, N, T)
     ws = torch.empty(B.fo_workspace_size(plan), dtype=torch.uint8, device=dev)
     B.fo_workspace_init(plan, ws)
-    stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def launch(stream):
         if w.op == "ag_gemm":
             B.fo_ag_gemm(plan, A, Bm, Y, None, ws, stream)
         else:
             B.fo_dp_grad_rs(plan, A, Bm, Y, ws, stream)
+
+    return inp, A, Bm, Y, plan, ws, launch
+
+
+def measure_other_workloads(B, dev, stream, iters=20):
+    """Short timed loops of the all-gather GEMM (QKV, R = 4), the DP
+    gradient (R = 8) and the TP-SP layer (R = 8, forward + backward), on the
+    device that times the default line: per workload the mean CUDA-event
+    time per launch (per step for the layer), TFLOP/s, the fraction of the
+    measured burst bf16 peak (each loop lasts well under a quarter second),
+    algorithmic HBM bytes and GB/s, and the ncu DRAM traffic per launch when
+    the committed capture matches the kernel source."""
+    import torch
+
+    from ag_gemm_gb300.inputs import WORKLOADS
+    from ag_gemm_gb300.layer import LayerShape, TpspLayerProjections
+    peaks, peak_src = load_peaks()
+    burst = float(peaks["bf16_tflops"])
+    out = {}
+    for name in ("ag_gemm_qkv_r4_s4096_h4096_n3072", "dp_grad_rs_r8_t4096_4096x4096"):
+        w = WORKLOADS[name]
+        inp, A, Bm, Y, plan, ws, launch = _op_setup(B, w, dev)
+        for _ in range(5):
+            launch(stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        torch.cuda.synchronize(dev)
+        for a, b in ev:
+            a.record(stream)
+            launch(stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        code, info = B.fo_status_query(plan, ws, stream)
+        if code != 0:
+            raise RuntimeError(f"device status {code} {info} ({name})")
+        ms = sum(a.elapsed_time(b) for a, b in ev) / iters
+        tf = w.flops() / (ms * 1e-3) / 1e12
+        traffic = profiled_traffic(name)
+        out[name] = {"ms": ms, "tflops": tf, "frac_of_burst_peak": tf / burst, "launches": iters,
+                     "traffic": traffic, "hbm": hbm_summary(w, ms, traffic, peaks)}
+        del inp, A, Bm, Y, ws
+        torch.cuda.empty_cache()
+    shape = LayerShape(R=8, T=8192, H=4096, F=14336)
+    L = TpspLayerProjections(shape, device=dev, seed=4)
+    for _ in range(3):
+        L.forward(stream)
+        L.backward(stream)
+    steps = 5
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    L.launches = 0
+    a.record(stream)
+    for _ in range(steps):
+        L.forward(stream)
+        L.backward(stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    if any(L.status()):
+        raise RuntimeError(f"device status {L.status()} (layer)")
+    ms = a.elapsed_time(b) / steps
+    tf = shape.flops()["total"] / (ms * 1e-3) / 1e12
+    out[LAYER_WORKLOAD] = {"ms": ms, "tflops": tf, "frac_of_burst_peak": tf / burst,
+                           "launches": L.launches, "steps": steps, "traffic": None}
+    del L
+    torch.cuda.empty_cache()
+    out["peak_source"] = f"bf16_tflops (burst), {peak_src}"
+    return out
+
+
+def run_other_op(args, w, dev, world, rank):
+    """Timed loop of the AG-GEMM or DP-grad-RS workloads (same timing rules
+    as the default line; no comparison legs)."""
+    import torch
+    import torch.distributed as dist
+
+    from ag_gemm_gb300 import binding as B
+    d = w.dims
+    stream = torch.cuda.current_stream(dev)
+    inp, A, Bm, Y, plan, ws, launch = _op_setup(B, w, dev)
+    if w.op == "ag_gemm":
+        R, M, K, Nr = w.R, d["M"], d["K"], d["N"]
+    else:
+        R, T, M, N = w.R, d["T"], d["M"], d["N"]
+
+    def step():
+        launch(stream)
 
     for _ in range(max(args.warmup, 3)):
         step()

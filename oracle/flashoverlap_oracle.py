@@ -43,6 +43,12 @@ Readings where the pages are silent (each is listed in the design notes):
   ``(r - 1 - s) mod R`` (ring reduce-scatter order, own chunk at s = R-1);
   AG rank r at step s consumes the shard of rank ``(r - s) mod R`` (own
   shard at s = 0, then what arrives from its ring predecessor).
+* Flash All-to-All ([GS] §2 names it as the extension for Ulysses
+  parallelism, without detail): rank r's projection X_r @ W_r is cut into R
+  column blocks (head groups); block c goes to rank c, which stacks the
+  blocks of all ranks in rank order. Rank r computes block
+  ``(r - 1 - s) mod R`` at step s, the Flash-RS order: the block that stays
+  on the rank last, one incoming block per rank and step.
 * Outputs of the RS ops are fp32 in the library; the oracle returns fp64.
   The AG output is bf16 in the library; ``round_bf16`` gives the oracle's
   value at that precision (round to nearest, ties to even, once).
@@ -56,7 +62,8 @@ import numpy as np
 
 __all__ = [
     "gemm_rs", "gemm_rs_rows", "gemm_ar", "ar_transfers", "ag_gemm", "ag_gemm_rows", "all_gather_rows",
-    "dp_grad_rs", "dp_grad_rs_rows", "reduce_scatter_rows", "weight_grads",
+    "dp_grad_rs", "dp_grad_rs_rows", "reduce_scatter_rows", "weight_grads", "weight_grads_rows",
+    "all_to_all_blocks", "gemm_a2a", "gemm_a2a_rows", "a2a_transfers", "simulate_gemm_a2a",
     "rs_chunk", "ag_source", "rs_schedule", "ag_schedule", "sliced_schedule",
     "rs_transfers", "ag_transfers", "rs_dependency_edges",
     "simulate_gemm_rs", "simulate_ag_gemm", "simulate_dp_grad_rs",
@@ -177,6 +184,54 @@ def weight_grads(X: Sequence[np.ndarray], dY: Sequence[np.ndarray]) -> List[np.n
     return [_f64(X[r]).T @ _f64(dY[r]) for r in range(len(X))]
 
 
+def weight_grads_rows(X, dY, r: int, rows: Sequence[int]) -> np.ndarray:
+    """Selected rows of rank r's weight gradient X_r^T @ dY_r (no collective):
+    row i is X_r[:, i]^T @ dY_r (same definition, restricted to a few rows)."""
+    idx = np.asarray(rows)
+    return _f64(X[r][:, idx]).T @ _f64(dY[r])
+
+
+def all_to_all_blocks(P: Sequence[np.ndarray]) -> List[np.ndarray]:
+    """Literal all-to-all of R equally shaped [M/R, N] arrays by column blocks.
+
+    Rank c receives, from every rank r in rank order, the column block c of
+    P_r (columns [c*N/R, (c+1)*N/R)): Y_c = concat_r P_r[:, c block] along
+    rows, so rank r's rows land at [r*M/R, (r+1)*M/R). [GS] §1: Ulysses
+    parallelism needs an all-to-all; the block ownership is this module's
+    reading (head group c lives on rank c).
+    """
+    R = len(P)
+    N = P[0].shape[1]
+    if N % R:
+        raise ValueError("N must be divisible by R")
+    nc = N // R
+    return [np.concatenate([_f64(P[r])[:, c * nc:(c + 1) * nc] for r in range(R)], axis=0) for c in range(R)]
+
+
+def gemm_a2a(X: Sequence[np.ndarray], W: Sequence[np.ndarray]) -> List[np.ndarray]:
+    """AllToAll(X_r @ W_r): the Ulysses projection whose all-to-all Flash
+    All-to-All overlaps ([GS] §2 "Architectural Versatility").
+
+    X_r is [M/R, K] (rank r's tokens), W_r is [K, N] (the full projection,
+    one copy per rank); returns R arrays [M, N/R]: every token's columns of
+    head group c on rank c.
+    """
+    return all_to_all_blocks([_f64(X[r]) @ _f64(W[r]) for r in range(len(X))])
+
+
+def gemm_a2a_rows(X, W, c: int, rows: Sequence[int]) -> np.ndarray:
+    """Selected rows (global token index) of rank c's output of ``gemm_a2a``:
+    row g = r*M/R + i is X_r[i] @ W_r[:, c block]."""
+    R = len(X)
+    rpc = X[0].shape[0]
+    nc = W[0].shape[1] // R
+    out = np.empty((len(rows), nc), dtype=np.float64)
+    for j, g in enumerate(rows):
+        r, i = divmod(int(g), rpc)
+        out[j] = _f64(X[r][i]) @ _f64(W[r])[:, c * nc:(c + 1) * nc]
+    return out
+
+
 def dp_grad_rs_rows(X, dY, d: int, rows: Sequence[int]) -> np.ndarray:
     """Selected rows of shard d of ``dp_grad_rs``."""
     R = len(X)
@@ -260,6 +315,16 @@ def ag_transfers(R: int) -> List[Tuple[int, int, int, int]]:
     return [(r, (r + 1) % R, int(sch[r, s]), s) for s in range(R - 1) for r in range(R)]
 
 
+def a2a_transfers(R: int, schedule=None) -> List[Tuple[int, int, int, int]]:
+    """Directed P2P messages (src_rank, dst_rank, block, step) of Flash
+    All-to-All: at step s rank r computes column block c = schedule[r, s] of
+    its projection and, unless c == r, sends it to rank c. Same order as
+    Flash-RS (the block that stays is computed last); the pages name the
+    extension only ([GS] §2), so the order is this module's reading."""
+    sch = rs_schedule(R) if schedule is None else np.asarray(schedule)
+    return [(r, int(sch[r, s]), int(sch[r, s]), s) for s in range(R) for r in range(R) if int(sch[r, s]) != r]
+
+
 def rs_dependency_edges(R: int, schedule=None) -> List[Tuple[Tuple[int, int], Tuple[int, int]]]:
     """Edges of the task/transfer DAG of Flash-RS (direct), as
     ((rank, step) -> (rank, step)) pairs: program order on every rank, and
@@ -316,6 +381,28 @@ def simulate_gemm_rs(X, W, schedule=None, ring: bool = False) -> List[np.ndarray
             else:
                 nxt[(r + 1) % R] = part
         inbox = nxt
+    return Y
+
+
+def simulate_gemm_a2a(X, W, schedule=None) -> List[np.ndarray]:
+    """Execute Flash All-to-All literally: at step s rank r computes
+    X_r @ W_r[:, c block] for c = schedule[r, s] and places it in rank c's
+    output at rank r's rows. A block written twice or never raises."""
+    R = len(X)
+    rpc = X[0].shape[0]
+    nc = W[0].shape[1] // R
+    sch = rs_schedule(R) if schedule is None else np.asarray(schedule)
+    Y = [np.full((rpc * R, nc), np.nan) for _ in range(R)]
+    written = set()
+    for s in range(R):
+        for r in range(R):
+            c = int(sch[r, s])
+            if (r, c) in written:
+                raise AssertionError(f"block ({r}, {c}) computed twice")
+            written.add((r, c))
+            Y[c][r * rpc:(r + 1) * rpc] = _f64(X[r]) @ _f64(W[r])[:, c * nc:(c + 1) * nc]
+    if len(written) != R * R:
+        raise AssertionError("a block was never computed")
     return Y
 
 
@@ -435,11 +522,11 @@ def round_bf16(x) -> np.ndarray:
     return np.ldexp(q / 256.0, e)
 
 
-def rel_errors(got, ref) -> Tuple[float, float, int]:
+def rel_errors(got, ref, floor_rel: float = 1e-3) -> Tuple[float, float, int]:
     """(relative Frobenius error, max elementwise relative error, clamped count).
 
-    Elementwise denominators are max(|ref|, 1e-3 * rms(ref)); the count is
-    the number of elements whose denominator was clamped.
+    Elementwise denominators are max(|ref|, floor_rel * rms(ref)); the count
+    is the number of elements whose denominator was clamped.
     """
     got = _f64(got)
     ref = _f64(ref)
@@ -447,7 +534,7 @@ def rel_errors(got, ref) -> Tuple[float, float, int]:
     nref = np.linalg.norm(ref)
     fro = float(np.linalg.norm(diff) / nref) if nref > 0 else float(np.linalg.norm(diff))
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
-    floor = 1e-3 * rms
+    floor = floor_rel * rms
     den = np.maximum(np.abs(ref), floor)
     clamped = int(np.count_nonzero(np.abs(ref) < floor))
     with np.errstate(divide="ignore", invalid="ignore"):

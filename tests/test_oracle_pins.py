@@ -137,6 +137,9 @@ def test_sampled_rows_equal_full():
     D = oracle.dp_grad_rs(Xd, dY)
     for d in range(R):
         assert np.array_equal(oracle.dp_grad_rs_rows(Xd, dY, d, [2, 0]), D[d][[2, 0]])
+    G = oracle.weight_grads(Xd, dY)
+    for r in range(R):
+        assert np.array_equal(oracle.weight_grads_rows(Xd, dY, r, [3, 0, 15]), G[r][[3, 0, 15]])
 
 
 # --------------------------------------------------------------------------
@@ -440,6 +443,11 @@ def test_rel_errors_simple_cases():
     fro, mx, _ = oracle.rel_errors(got, ref)
     assert fro == pytest.approx(0.1 / np.sqrt(21.0))
     assert mx == pytest.approx(0.1)
+    # the denominator floor: rms(ref) = sqrt(21/4); an error on the zero element
+    near0 = ref + np.array([0.0, 0.0, 1e-3, 0.0])
+    rms = np.sqrt(21.0 / 4.0)
+    assert oracle.rel_errors(near0, ref)[1] == pytest.approx(1e-3 / (1e-3 * rms))
+    assert oracle.rel_errors(near0, ref, 1e-2)[1] == pytest.approx(1e-3 / (1e-2 * rms))
 
 
 # --------------------------------------------------------------------------
