@@ -621,3 +621,95 @@ def test_planted_wrong_ring_forward_is_caught(monkeypatch):
     monkeypatch.setattr(O, "rs_transfers", skip_one)
     g = _read_golden_transfers()
     assert sorted(O.rs_transfers(4, ring=True)) != sorted(g[("rs_ring", 4)])
+
+
+# --------------------------------------------------------------------------
+# Flash All-to-All (the Ulysses projection): brute force, a closed-form
+# probe, decomposed == collective, the hand-derived message list.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R,M,K,N", [(1, 2, 3, 4), (2, 4, 3, 6), (3, 6, 2, 3), (4, 8, 3, 8)])
+def test_gemm_a2a_matches_brute_force(R, M, K, N):
+    rng = np.random.default_rng(70 + R)
+    rows = M // R
+    X = [_ints(rng, (rows, K)) for _ in range(R)]
+    W = [_ints(rng, (K, N)) for _ in range(R)]
+    Y = oracle.gemm_a2a(X, W)
+    nc = N // R
+    for c in range(R):
+        assert Y[c].shape == (M, nc)
+        for g in range(M):
+            r, i = divmod(g, rows)
+            for j in range(nc):
+                want = sum(int(X[r][i][k]) * int(W[r][k][c * nc + j]) for k in range(K))
+                assert Y[c][g, j] == want
+        assert np.array_equal(oracle.gemm_a2a_rows(X, W, c, [M - 1, 0]), Y[c][[M - 1, 0]])
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8])
+def test_a2a_identity_weight_moves_column_blocks(R):
+    # W = I: the projection is X itself, so rank c must hold column block c
+    # of every rank's tokens, stacked in rank order.
+    rows, K = 3, 2 * R
+    X = [np.arange(rows * K, dtype=np.float64).reshape(rows, K) + 1000 * r for r in range(R)]
+    W = [np.eye(K) for _ in range(R)]
+    for f in (oracle.gemm_a2a, oracle.simulate_gemm_a2a):
+        Y = f(X, W)
+        for c in range(R):
+            for r in range(R):
+                assert np.array_equal(Y[c][r * rows:(r + 1) * rows], X[r][:, 2 * c:2 * c + 2])
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 6, 8])
+def test_decomposed_a2a_equals_collective(R):
+    rng = np.random.default_rng(80 + R)
+    X = [_ints(rng, (2, 5)) for _ in range(R)]
+    W = [_ints(rng, (5, 2 * R)) for _ in range(R)]
+    ref = oracle.gemm_a2a(X, W)
+    for sch in (None, oracle.sliced_schedule(R)):
+        got = oracle.simulate_gemm_a2a(X, W, schedule=sch)
+        for c in range(R):
+            assert np.array_equal(got[c], ref[c])
+
+
+def test_a2a_simulator_rejects_a_schedule_that_repeats_a_block():
+    R = 3
+    X = [np.ones((1, 2)) for _ in range(R)]
+    W = [np.ones((2, 3)) for _ in range(R)]
+    bad = oracle.rs_schedule(R).copy()
+    bad[0, 1] = bad[0, 0]
+    with pytest.raises(AssertionError):
+        oracle.simulate_gemm_a2a(X, W, schedule=bad)
+
+
+@pytest.mark.parametrize("R", [3, 4])
+def test_a2a_transfers_match_hand_derived_fixture(R):
+    g = _read_golden_transfers()
+    assert sorted(oracle.a2a_transfers(R)) == sorted(g[("a2a", R)])
+
+
+@pytest.mark.parametrize("R", list(range(1, 17)))
+def test_a2a_transfer_invariants(R):
+    tr = oracle.a2a_transfers(R)
+    assert len(tr) == R * (R - 1)                                   # every (src, dst != src) once
+    assert sorted((a, b) for (a, b, _, _) in tr) == [(a, b) for a in range(R) for b in range(R) if a != b]
+    assert all(c == d for (_, d, c, _) in tr)                        # block c goes to rank c
+    assert all(s < R - 1 for (_, _, _, s) in tr)                     # the last step sends nothing
+    for s in range(R - 1):                                           # one incoming block per rank and step
+        assert sorted(d for (_, d, _, st) in tr if st == s) == list(range(R))
+
+
+def test_planted_swapped_a2a_roles_are_caught(monkeypatch):
+    def swapped(P):
+        R = len(P)
+        nc = P[0].shape[1] // R
+        return [np.concatenate([P[c][:, r * nc:(r + 1) * nc] for r in range(R)], axis=0) for c in range(R)]
+
+    monkeypatch.setattr(O, "all_to_all_blocks", swapped)
+    R, rows, K = 3, 2, 6
+    X = [np.arange(rows * K, dtype=np.float64).reshape(rows, K) + 1000 * r for r in range(R)]
+    W = [np.eye(K) for _ in range(R)]
+    Y = O.gemm_a2a(X, W)
+    ok = all(np.array_equal(Y[c][r * rows:(r + 1) * rows], X[r][:, 2 * c:2 * c + 2])
+             for c in range(R) for r in range(R))
+    assert not ok
