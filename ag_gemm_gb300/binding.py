@@ -20,7 +20,7 @@ FO_OK, FO_ERR_INVALID_ARG, FO_ERR_SHAPE, FO_ERR_DTYPE, FO_ERR_ALIGN = 0, 1, 2, 3
 FO_ERR_UNSUPPORTED, FO_ERR_CUDA, FO_ERR_TIMEOUT, FO_ERR_PLAN_INVARIANT = 5, 6, 7, 8
 FO_ERR_SCRATCH_LIMIT = 9
 FO_NOALLOC_SCRATCH_BYTES = 64 * 1024
-OPS = {"ag_gemm": 0, "gemm_rs": 1, "dp_grad_rs": 2, "gemm_ar": 3}
+OPS = {"ag_gemm": 0, "gemm_rs": 1, "dp_grad_rs": 2, "gemm_ar": 3, "gemm_a2a": 4}
 DTYPES = {"bf16": 0, "f32": 1}
 SCHEDS = {"rank_adaptive": 0, "sliced": 1}
 TRANSPORTS = {"peer_read": 0, "copy": 1}
@@ -40,6 +40,7 @@ EXPORTED = [
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
     "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc", "fo_plan_task_order",
     "fo_gemm_ar", "fo_trace_query", "fo_plan_last_split_tiles", "fo_check_device_pointers",
+    "fo_gemm_a2a", "fo_all_to_all_copy",
 ]
 
 
@@ -93,6 +94,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_dp_grad_rs": ([P, PP, PP, PP, P, P], c_int32),
         "fo_gemm_rs_noalloc": ([P, PP, PP, PP, P], c_int32),
         "fo_gemm_ar": ([P, PP, PP, PP, P, P], c_int32),
+        "fo_gemm_a2a": ([P, PP, PP, PP, P, P], c_int32),
+        "fo_all_to_all_copy": ([P, PP, PP, P], c_int32),
         "fo_status_query": ([P, P, P, POINTER(c_int32)], c_int32),
         "fo_trace_query": ([P, P, P, POINTER(ctypes.c_uint64), c_int32, POINTER(c_int32)], c_int32),
         "fo_gemm_partials": ([P, PP, PP, PP, P, P], c_int32),
@@ -180,7 +183,7 @@ def fo_plan(op: str, R: int, M: int, N: int, K: int, *, in_dtype="bf16", out_dty
             rs_algo="direct", trace=False, inject_delay_us=0, tail_split="auto") -> Plan:
     lib = load()
     if out_dtype is None:
-        out_dtype = "bf16" if op == "ag_gemm" else "f32"
+        out_dtype = "bf16" if op in ("ag_gemm", "gemm_a2a") else "f32"
     d = PlanDesc()
     d.op = OPS[op]
     d.R = R
@@ -260,6 +263,15 @@ def fo_gemm_rs(plan: Plan, X, W, Y, ws, stream=None) -> None:
 def fo_gemm_ar(plan: Plan, X, W, Y, ws, stream=None) -> None:
     _check(load().fo_gemm_ar(plan, _ptr_array(X), _ptr_array(W), _ptr_array(Y), _ptr(ws), _stream(stream)),
            "fo_gemm_ar")
+
+
+def fo_gemm_a2a(plan: Plan, X, W, Y, ws, stream=None) -> None:
+    _check(load().fo_gemm_a2a(plan, _ptr_array(X), _ptr_array(W), _ptr_array(Y), _ptr(ws), _stream(stream)),
+           "fo_gemm_a2a")
+
+
+def fo_all_to_all_copy(plan: Plan, P, Y, stream=None) -> None:
+    _check(load().fo_all_to_all_copy(plan, _ptr_array(P), _ptr_array(Y), _stream(stream)), "fo_all_to_all_copy")
 
 
 def fo_ag_gemm(plan: Plan, X, W, Y, G=None, ws=None, stream=None) -> None:

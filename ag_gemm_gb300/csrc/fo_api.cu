@@ -84,7 +84,7 @@ bool enc3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t d0,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-enum CallKind { KIND_NONE = 0, KIND_RS = 1, KIND_DP = 2, KIND_AG = 3, KIND_PART = 4 };
+enum CallKind { KIND_NONE = 0, KIND_RS = 1, KIND_DP = 2, KIND_AG = 3, KIND_PART = 4, KIND_A2A = 5 };
 
 // Returns the cached parameter block when the same call kind is made with
 // the same pointers again, else nullptr.
@@ -141,6 +141,7 @@ void fill_common(fo_plan_t p, fo::FoParams* k, void* ws) {
   k->pieces = p->pieces;
   k->row_bytes = p->d.K * 2;
   k->ag_copy = p->d.op == FO_OP_AG_GEMM && p->d.ag_transport == FO_AG_COPY ? 1 : 0;
+  k->a2a = p->d.op == FO_OP_GEMM_A2A ? 1 : 0;
   k->n_cols = p->n_out;
   k->trace = p->d.trace ? reinterpret_cast<uint64_t*>(static_cast<char*>(ws) + p->ws_trace_off) : nullptr;
   // Tail split: decided per launch (run_chunk_gemm) once the grid is known.
@@ -340,6 +341,39 @@ fo_status build_ag(fo_plan_t p, const void* const* X, const void* const* W, void
   return FO_OK;
 }
 
+// All-to-all: X_r [M/R x K] as the A operand (like an all-gather shard), the
+// whole W_r [K x N] (or [N x K]) as B, read at column block c of each task,
+// and each Y_c [M x N/R] viewed [N/R, M/R, R] so that a store of rank r's
+// rows clips at its block's last row and column.
+fo_status build_a2a(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* ws,
+                    cudaStream_t stream, fo::FoParams** out) {
+  fo::FoParams* k = cached_params(p, KIND_A2A, X, W, (const void* const*)Y);
+  if (k) {
+    fill_common(p, k, ws);
+    *out = k;
+    return FO_OK;
+  }
+  if (fo_status st = check_call_ptrs(p->R, X, W, (const void* const*)Y, nullptr, ws, stream)) return st;
+  k = fresh_params(p);
+  if (!k) return FO_ERR_INVALID_ARG;
+  const int R = p->R;
+  const uint64_t K = (uint64_t)p->d.K, N = (uint64_t)p->d.N, nc = (uint64_t)p->n_out;
+  const uint64_t rpc = (uint64_t)p->rows_per_chunk;
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok = true;
+  for (int r = 0; r < R && ok; ++r) {
+    ok &= enc2d(&k->tmA[r], dt, X[r], K, rpc, K * 2, 64, FO_BM);
+    if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, W[r], N, K, N * 2, 64, 64);
+    else ok &= enc2d(&k->tmB[r], dt, W[r], K, N, K * 2, 64, p->pair ? FO_BN / 2 : FO_BN);
+    ok &= enc3d(&k->tmD[r], dt, Y[r], nc, rpc, R, nc * 2, rpc * nc * 2, 64, 32);
+  }
+  if (!ok) return FO_ERR_CUDA;
+  remember(p, KIND_A2A, X, W, (const void* const*)Y);
+  fill_common(p, k, ws);
+  *out = k;
+  return FO_OK;
+}
+
 fo_status preflight(fo_plan_t p, DevInfo* di) {
   if (!load_encode()) return FO_ERR_CUDA;
   fo_status st = device_info(di);
@@ -443,6 +477,22 @@ __global__ void all_gather_copy_kernel(PtrArray X, MutPtrArray G, int R, int64_t
     const int r = (int)(pair / R), src = (int)(pair - (int64_t)r * R);
     const int4 v = reinterpret_cast<const int4*>(X.p[src])[j];
     reinterpret_cast<int4*>(G.p[r])[(int64_t)src * shard_vec16 + j] = v;
+  }
+}
+
+// Y_c[r * rows + i, :] = P_r[i, c block] for every (c, r, i): 16-byte copies,
+// one per thread and loop trip (P_r [rows x R * nc16 * 8], Y_c [R * rows x
+// nc16 * 8], bf16).
+__global__ void all_to_all_copy_kernel(PtrArray P, MutPtrArray Y, int R, int64_t rows, int64_t nc16) {
+  const int64_t per_block = rows * nc16;   // one (c, r) block
+  const int64_t total = per_block * R * R;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t blk = i / per_block;
+    const int64_t w = i - blk * per_block;
+    const int c = (int)(blk / R), r = (int)(blk - (int64_t)c * R);
+    const int64_t row = w / nc16, v = w - row * nc16;
+    const int4 x = reinterpret_cast<const int4*>(P.p[r])[row * nc16 * R + (int64_t)c * nc16 + v];
+    reinterpret_cast<int4*>(Y.p[c])[((int64_t)r * rows + row) * nc16 + v] = x;
   }
 }
 
@@ -591,10 +641,26 @@ fo_status fo_ag_gemm(fo_plan_t p, const void* const* X, const void* const* W, vo
   return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
 }
 
+fo_status fo_gemm_a2a(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* ws,
+                      fo_stream_t stream) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (p->d.op != FO_OP_GEMM_A2A) return FO_ERR_INVALID_ARG;
+  fo_status st;
+  if ((st = check_ptrs(p->R, X)) || (st = check_ptrs(p->R, W)) || (st = check_ptrs(p->R, (const void* const*)Y)))
+    return st;
+  if (!aligned16(ws)) return FO_ERR_ALIGN;
+  DevInfo di;
+  if ((st = preflight(p, &di))) return st;
+  fo::FoParams* k = nullptr;
+  if ((st = build_a2a(p, X, W, Y, ws, (cudaStream_t)stream, &k))) return st;
+  return run_chunk_gemm(p, p->d.w_layout == FO_W_KN ? FO_V_AG_BF16_KN : FO_V_AG_BF16_NK, k, di,
+                        (cudaStream_t)stream);
+}
+
 fo_status fo_gemm_partials(fo_plan_t p, const void* const* A, const void* const* B, void* const* P, void* ws,
                            fo_stream_t stream) {
   if (!p || !ws) return FO_ERR_INVALID_ARG;
-  if (p->d.op == FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
+  if (p->d.op == FO_OP_AG_GEMM || p->d.op == FO_OP_GEMM_A2A) return FO_ERR_INVALID_ARG;
   fo_status st;
   if ((st = check_ptrs(p->R, A)) || (st = check_ptrs(p->R, B)) || (st = check_ptrs(p->R, (const void* const*)P)))
     return st;
@@ -611,7 +677,7 @@ fo_status fo_gemm_partials(fo_plan_t p, const void* const* A, const void* const*
 
 fo_status fo_reduce_scatter_f32(fo_plan_t p, const void* const* P, void* const* Y, fo_stream_t stream) {
   if (!p) return FO_ERR_INVALID_ARG;
-  if (p->d.op == FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
+  if (p->d.op == FO_OP_AG_GEMM || p->d.op == FO_OP_GEMM_A2A) return FO_ERR_INVALID_ARG;
   fo_status st;
   if ((st = check_ptrs(p->R, P)) || (st = check_ptrs(p->R, (const void* const*)Y))) return st;
   if ((st = check_device_ptrs(p->R, P, (cudaStream_t)stream)) ||
@@ -651,6 +717,30 @@ fo_status fo_all_gather_copy(fo_plan_t p, const void* const* X, void* const* G, 
   }
   const int64_t shard_vec16 = p->rows_per_chunk * p->d.K * 2 / 16;
   all_gather_copy_kernel<<<di.sms * 4, 256, 0, (cudaStream_t)stream>>>(xa, ga, p->R, shard_vec16);
+  if (cudaGetLastError() != cudaSuccess) return FO_ERR_CUDA;
+  p->last_launches = 1;
+  return FO_OK;
+}
+
+fo_status fo_all_to_all_copy(fo_plan_t p, const void* const* P, void* const* Y, fo_stream_t stream) {
+  if (!p) return FO_ERR_INVALID_ARG;
+  if (p->d.op != FO_OP_GEMM_A2A) return FO_ERR_INVALID_ARG;
+  fo_status st;
+  if ((st = check_ptrs(p->R, P)) || (st = check_ptrs(p->R, (const void* const*)Y))) return st;
+  if ((st = check_device_ptrs(p->R, P, (cudaStream_t)stream)) ||
+      (st = check_device_ptrs(p->R, (const void* const*)Y, (cudaStream_t)stream)))
+    return st;
+  DevInfo di;
+  if ((st = device_info(&di))) return st;
+  PtrArray pa = {};
+  MutPtrArray ya = {};
+  for (int r = 0; r < p->R; ++r) {
+    pa.p[r] = P[r];
+    ya.p[r] = Y[r];
+  }
+  // n_out * 2 bytes is a multiple of 16 (checked by fo_plan).
+  all_to_all_copy_kernel<<<di.sms * 4, 256, 0, (cudaStream_t)stream>>>(pa, ya, p->R, p->rows_per_chunk,
+                                                                        p->n_out * 2 / 16);
   if (cudaGetLastError() != cudaSuccess) return FO_ERR_CUDA;
   p->last_launches = 1;
   return FO_OK;

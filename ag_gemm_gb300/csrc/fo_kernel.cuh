@@ -42,6 +42,9 @@
 //                       shard; the A operand was read straight from the
 //                       source rank's buffer (the transfer is the read), or
 //                       from r's gather buffer under the copy transport.
+//                       All-to-all (same kernel): X_r times W_r's column
+//                       block c, stored into rank c's output at rank r's
+//                       rows (the transfer is the store).
 //                PARTIAL fp32 store into the computing rank's own buffer
 //                       (pure-GEMM control, no transfer).
 //   warps 6-9  (MOV) movers: 128-bit copies of 32-row shard pieces into the
@@ -127,6 +130,10 @@ struct alignas(128) FoParams {
   int64_t row_bytes;           // K * 2
   int32_t pieces;              // 32-row pieces per shard
   int32_t ag_copy;             // 1: shards reach G_r along the ring and the GEMM reads them there
+  // All-to-all (EPI_AG kernels): task (r, s) multiplies X_r by column block
+  // c = table[r][s] of W_r (columns c * n_cols ...) and stores the bf16 tile
+  // into rank c's output at rank r's rows (tmD[c] viewed [n_cols, rows/R, R]).
+  int32_t a2a;
   // (GST kernels: tmG views G_r as [K, rows/R, R], the map of the stores.)
   // RS/DP completion: the owner's last partial (contribution R-1) is the
   // finisher. It waits for the other R-1, adds their sum (read from the
@@ -454,12 +461,13 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           // delay itself; an abort ends it early).
           while (globaltimer() - t_start < p.delay_ns && !*abort_flag && !*gstatus) __nanosleep(2000);
         }
-        const CUtensorMap* mA = EPI == EPI_AG ? &p.tmA[ti.c] : &p.tmA[ti.r];
+        const CUtensorMap* mA = EPI == EPI_AG ? &p.tmA[p.a2a ? ti.r : ti.c] : &p.tmA[ti.r];
         const CUtensorMap* mB = &p.tmB[ti.r];
         // Row (or column, for MN-major A) where this CTA's A block starts,
-        // and the first output column of its B block.
+        // and the first output column of its B block (in the all-to-all,
+        // within W_r's column block c).
         int a_mn0 = (EPI == EPI_AG ? 0 : ti.c * p.rows_per_chunk) + ti.mt * C::kTileM + (int)prank * FO_BM;
-        const int b_n0 = ti.nt * FO_BN + (int)prank * C::kBRows;
+        const int b_n0 = (EPI == EPI_AG && p.a2a ? ti.c * (int)p.n_cols : 0) + ti.nt * FO_BN + (int)prank * C::kBRows;
         if constexpr (MOV) {
           if (p.ag_copy && ti.s > 0) {
             // Copy transport: this shard reached G_r along the ring. Wait
@@ -964,7 +972,10 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&p.tmD[ti.r], buf, n0 + j * 64, row0, ti.c);
+            // All-gather: rank r's rows of shard c; all-to-all: rank c's
+            // output at the rows of rank r.
+            if (p.a2a) tma_store_3d(&p.tmD[ti.c], buf, n0 + j * 64, row0, ti.r);
+            else tma_store_3d(&p.tmD[ti.r], buf, n0 + j * 64, row0, ti.c);
             bulk_commit();
           }
         }

@@ -15,6 +15,10 @@
 // rank (r - s) mod R, which its ring predecessor forwarded one step earlier.
 // Under the ring RS algorithm the same order makes rank r's chunk at step s
 // the one rank r-1 handled at step s-1, so the running sum can be forwarded.
+// Flash All-to-All (gist.science, "Technical Summary" section 2, named for
+// Ulysses parallelism) takes the RS table too: rank r computes the column
+// block of rank (r - 1 - s) mod R at step s and sends it straight there, the
+// block that stays last; its transfers and edges are those of the direct RS.
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
@@ -79,7 +83,8 @@ void build_table(fo_plan_s* p) {
     // Ring reduce-scatter and ring-forwarded all-gather: a chain's hops run
     // a whole step apart, so no hop waits for the one before.
     if (p->ring || (ag && p->d.ag_transport == FO_AG_COPY)) skew = FO_INTERLEAVE_LOCKSTEP;
-    else skew = (ag || p->d.op == FO_OP_DP_GRAD_RS) ? FO_INTERLEAVE_RANK_MAJOR : FO_INTERLEAVE_SKEWED_PAIRS;
+    else skew = (ag || p->d.op == FO_OP_DP_GRAD_RS || p->d.op == FO_OP_GEMM_A2A) ? FO_INTERLEAVE_RANK_MAJOR
+                                                                                  : FO_INTERLEAVE_SKEWED_PAIRS;
   }
   int n = 0;
   if (skew == FO_INTERLEAVE_RANK_MAJOR) {
@@ -268,7 +273,7 @@ extern "C" {
 fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (!d || !out) return FO_ERR_INVALID_ARG;
   *out = nullptr;
-  if (d->op < FO_OP_AG_GEMM || d->op > FO_OP_GEMM_AR) return FO_ERR_INVALID_ARG;
+  if (d->op < FO_OP_AG_GEMM || d->op > FO_OP_GEMM_A2A) return FO_ERR_INVALID_ARG;
   if (d->R < 1 || d->R > FO_MAX_R) return FO_ERR_INVALID_ARG;
   if (d->sched != FO_SCHED_RANK_ADAPTIVE && d->sched != FO_SCHED_SLICED) return FO_ERR_INVALID_ARG;
   if (d->ag_transport != FO_AG_PEER_READ && d->ag_transport != FO_AG_COPY) return FO_ERR_INVALID_ARG;
@@ -286,7 +291,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
     // The ring forwards a running sum, which needs the rank-adaptive order
     // (rank r's chunk at step s is r-1's at step s-1) and a kernel order that
     // runs every chunk's hops in step order.
-    if (d->op == FO_OP_AG_GEMM) return FO_ERR_INVALID_ARG;
+    if (d->op == FO_OP_AG_GEMM || d->op == FO_OP_GEMM_A2A) return FO_ERR_INVALID_ARG;
     if (d->op == FO_OP_GEMM_AR || d->sched != FO_SCHED_RANK_ADAPTIVE) return FO_ERR_UNSUPPORTED;
     if (d->interleave == FO_INTERLEAVE_RANK_MAJOR) return FO_ERR_UNSUPPORTED;
   }
@@ -320,6 +325,15 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
       if (d->sched != FO_SCHED_RANK_ADAPTIVE) return FO_ERR_UNSUPPORTED;
       if ((K * 2) % 16 || ((N / R) * 2) % 16) return FO_ERR_ALIGN;
       break;
+    case FO_OP_GEMM_A2A:
+      // Column block c of W_r starts at column c*N/R: a TMA coordinate along
+      // the contiguous dimension of a [K x N] weight, so it falls on a
+      // 16-byte boundary only when N/R bf16 values fill whole 16 bytes.
+      if (N % R) return FO_ERR_SHAPE;
+      if (d->in_dtype != FO_BF16 || d->out_dtype != FO_BF16) return FO_ERR_DTYPE;
+      if (d->ag_transport != FO_AG_PEER_READ) return FO_ERR_INVALID_ARG;
+      if ((K * 2) % 16 || ((N / R) * 2) % 16) return FO_ERR_ALIGN;
+      break;
     case FO_OP_DP_GRAD_RS:
       if (d->in_dtype != FO_BF16) return FO_ERR_DTYPE;
       if (d->out_dtype != FO_F32 && d->out_dtype != FO_BF16) return FO_ERR_DTYPE;
@@ -343,7 +357,8 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   switch (d->op) {
     case FO_OP_GEMM_RS:
     case FO_OP_GEMM_AR: p->k_red = K / R; p->n_out = N; break;
-    case FO_OP_AG_GEMM: p->k_red = K; p->n_out = N / R; break;
+    case FO_OP_AG_GEMM:
+    case FO_OP_GEMM_A2A: p->k_red = K; p->n_out = N / R; break;
     default: p->k_red = K; p->n_out = N; break;
   }
   // AUTO: CTA-pair tiles for bf16 unless a shard holds 128 rows or fewer,
@@ -371,12 +386,12 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   p->ws_flags_off = off;
   if (d->op == FO_OP_AG_GEMM) {
     off += align_up((size_t)R * R * p->pieces * sizeof(uint32_t), 256);
-  } else {
+  } else if (d->op != FO_OP_GEMM_A2A) {   // the all-to-all's blocks are disjoint: no counters
     off += align_up((size_t)R * p->ctr_tiles_m * p->tiles_n * 4 * sizeof(uint32_t), 256);
   }
   p->ws_shard_off = off;
   p->ws_shard_stride = 0;
-  if (d->op != FO_OP_AG_GEMM && d->out_dtype == FO_BF16 && !p->ring) {
+  if (d->op != FO_OP_AG_GEMM && d->op != FO_OP_GEMM_A2A && d->out_dtype == FO_BF16 && !p->ring) {
     p->ws_shard_stride = align_up((size_t)p->rows_per_chunk * p->n_out * 4, 256);
     off += (size_t)R * p->ws_shard_stride;
   }
@@ -399,7 +414,8 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
     const int64_t tiles = (int64_t)R * R * p->tiles_m * p->tiles_n;
     const int units = p->pair ? FO_GB300_SMS / 2 : FO_GB300_SMS;
     const bool on = d->tail_split == FO_TAIL_SPLIT_ON ||
-                    (d->tail_split == FO_TAIL_SPLIT_AUTO && d->op == FO_OP_AG_GEMM && p->num_kb >= 32 &&
+                    (d->tail_split == FO_TAIL_SPLIT_AUTO &&
+                     (d->op == FO_OP_AG_GEMM || d->op == FO_OP_GEMM_A2A) && p->num_kb >= 32 &&
                      tiles >= 2 * (int64_t)units);
     if (on) p->sk_cap = fo_tail_split_tiles(tiles, units);
   }
@@ -416,7 +432,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   p->last_split_tiles = 0;
   p->param_cache = nullptr;
   if (fo_log_enabled()) {
-    static const char* ops[] = {"ag_gemm", "gemm_rs", "dp_grad_rs", "gemm_ar"};
+    static const char* ops[] = {"ag_gemm", "gemm_rs", "dp_grad_rs", "gemm_ar", "gemm_a2a"};
     fprintf(stderr,
             "[flashoverlap] plan %s R=%d M=%lld N=%lld K=%lld %s tiles %dx%d of %s, %d k-blocks, %s%s, "
             "tail split for up to %d tiles, workspace %zu B\n",

@@ -69,7 +69,7 @@ def dp_grad_inputs(R: int, T: int, M: int, N: int, *, dtype="bf16", mode="randn"
 class Workload:
     """One named workload: the op, the virtual rank count and the global sizes."""
     name: str
-    op: str            # "gemm_rs" | "ag_gemm" | "dp_grad_rs"
+    op: str            # "gemm_rs" | "ag_gemm" | "dp_grad_rs" | "gemm_a2a"
     R: int
     dims: Dict[str, int] = field(default_factory=dict)
     dtype: str = "bf16"
@@ -82,6 +82,8 @@ class Workload:
             return 2.0 * self.R * d["M"] * d["N"] * d["K"]
         if self.op == "ag_gemm":
             return 2.0 * self.R * d["M"] * d["N"] * d["K"]
+        if self.op == "gemm_a2a":
+            return 2.0 * d["M"] * d["N"] * d["K"]
         if self.op == "dp_grad_rs":
             return 2.0 * self.R * d["M"] * d["N"] * d["T"]
         raise ValueError(self.op)
@@ -91,7 +93,7 @@ class Workload:
         if self.op == "gemm_rs":
             return gemm_rs_inputs(self.R, d["M"], d["K"], d["N"], dtype=self.dtype,
                                   mode=self.mode, seed=self.seed, **kw)
-        if self.op == "ag_gemm":
+        if self.op in ("ag_gemm", "gemm_a2a"):
             return ag_gemm_inputs(self.R, d["M"], d["K"], d["N"], dtype=self.dtype,
                                   mode=self.mode, seed=self.seed, **kw)
         if self.op == "dp_grad_rs":
@@ -101,8 +103,10 @@ class Workload:
 
 
 # The named workloads. Sizes are global: M rows of the RS output / gathered
-# sequence, K the per-rank reduction size (RS) or hidden size (AG), N the
-# output width per rank (AG) or total (RS), T tokens (DP grad).
+# sequence, K the per-rank reduction size (RS) or hidden size (AG, A2A), N the
+# output width per rank (AG) or total (RS, A2A: all R head groups), T tokens
+# (DP grad). The all-to-all draws its inputs like the all-gather: X_r
+# [M/R x K], then W_r [K x N] (the whole projection on every rank).
 WORKLOADS = {
     "gemm_rs_int_r2_256x512x512": Workload("gemm_rs_int_r2_256x512x512", "gemm_rs", 2,
                                            {"M": 256, "K": 512, "N": 512}, "f32", "int", 0),
@@ -112,4 +116,9 @@ WORKLOADS = {
                                                   {"M": 8192, "K": 1792, "N": 4096}, "bf16", "randn", 2),
     "dp_grad_rs_r8_t4096_4096x4096": Workload("dp_grad_rs_r8_t4096_4096x4096", "dp_grad_rs", 8,
                                               {"T": 4096, "M": 4096, "N": 4096}, "bf16", "randn", 3),
+    # Ulysses QKV projection of the Llama-like layer's shape: 8192 tokens
+    # over R = 8, hidden 4096, Q|K|V of 32 heads (12288 columns, 4 heads of
+    # 128 per rank after the all-to-all).
+    "gemm_a2a_qkv_r8_t8192_h4096_n12288": Workload("gemm_a2a_qkv_r8_t8192_h4096_n12288", "gemm_a2a", 8,
+                                                   {"M": 8192, "K": 4096, "N": 12288}, "bf16", "randn", 5),
 }

@@ -12,7 +12,9 @@ Inputs are seeded synthetic tensors (X ~ N(0,1), W ~ N(0,0.02)) already
 resident in HBM; together they exceed L2, so no L2 flush runs between steps.
 
 The JSON line reports whole-job TFLOP/s, the roofline fraction of the fused
-kernel against the measured bf16 dense peak, the same metric end to end with
+kernel against the measured bf16 dense peak, short timed loops of the other
+fused ops (all-gather QKV projection, DP gradient, all-to-all projection,
+the TP-SP layer's forward and backward) on the same device, the same metric end to end with
 host buffers (host->device inputs and device->host outputs inside the timed
 region), the CPU oracle timed on a bounded sample, and, next to them, the
 pure-GEMM control, the unfused baseline (our GEMM + a separate reduce kernel),
@@ -70,6 +72,11 @@ def algorithmic_bytes(w) -> float:
     if w.op == "ag_gemm":
         M, K, N = d["M"], d["K"], d["N"]
         return (M * K + R * K * N + R * M * N) * 2
+    if w.op == "gemm_a2a":
+        # X once, every rank's whole W_r once, Y once; the all-to-all's
+        # transfer is the output store itself.
+        M, K, N = d["M"], d["K"], d["N"]
+        return (M * K + R * K * N + M * N) * 2
     raise ValueError(w.op)
 
 
@@ -240,6 +247,12 @@ def oracle_pass(workload, arrays, rows: int):
         for r in range(R):
             oracle.ag_gemm_rows(A, Bn, r, g)
         flops = 2.0 * R * len(g) * d["K"] * d["N"]
+    elif workload.op == "gemm_a2a":
+        rpc = d["M"] // R
+        g = np.concatenate([src * rpc + idx for src in range(R)])
+        for c in range(R):
+            oracle.gemm_a2a_rows(A, Bn, c, g)
+        flops = 2.0 * R * len(g) * d["K"] * (d["N"] // R)
     else:
         for sh in range(R):
             oracle.dp_grad_rs_rows(A, Bn, sh, idx)
@@ -271,7 +284,8 @@ def oracle_sample(workload, arrays, budget_s: float = 12.0):
         tot_t += dt
         tot_f += fl
         passes += 1
-    what = "source shards of every rank's output" if workload.op == "ag_gemm" else "output shards"
+    what = {"ag_gemm": "source shards of every rank's output",
+            "gemm_a2a": "source ranks' row blocks of every rank's output"}.get(workload.op, "output shards")
     desc = (f"{passes} pass(es) over {rows} of {workload.dims['M'] // workload.R} rows of each of the "
             f"{workload.R} {what} ({tot_f / 1e9:.0f} GFLOP fp64, {tot_t:.1f} s)")
     return tot_f / tot_t / 1e12, desc
@@ -312,7 +326,8 @@ def run_reference(args):
     tot_t = sum(p[0] for p in per)
     tot_flops = sum(p[1] for p in per)
     value = tot_flops / tot_t / 1e12
-    what = "source shards of every rank's output" if w.op == "ag_gemm" else "output shards"
+    what = {"ag_gemm": "source shards of every rank's output",
+            "gemm_a2a": "source ranks' row blocks of every rank's output"}.get(w.op, "output shards")
     desc = (f"per step: {rows} of {w.dims['M'] // w.R} rows of each of the {w.R} {what} "
             f"({per[0][1] / 1e9:.0f} GFLOP fp64 numpy)")
     line = {
@@ -524,12 +539,18 @@ LAYER_WORKLOAD = "tpsp_layer_r8_t8192_h4096_f14336"
 
 
 def _op_setup(B, w, dev):
-    """Device inputs, outputs, plan and workspace of an AG-GEMM or DP-grad-RS
-    workload: (inp, A, Bm, Y, plan, ws, launch(stream))."""
+    """Device inputs, outputs, plan and workspace of an AG-GEMM, A2A or
+    DP-grad-RS workload: (inp, A, Bm, Y, plan, ws, launch(stream))."""
     import torch
     d = w.dims
     inp = w.make()
-    if w.op == "ag_gemm":
+    if w.op == "gemm_a2a":
+        R, M, K, N = w.R, d["M"], d["K"], d["N"]
+        A = [x.to(dev) for x in inp["X"]]
+        Bm = [x.to(dev) for x in inp["W"]]
+        Y = [torch.empty(M, N // R, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        plan = B.fo_plan("gemm_a2a", R, M, N, K)
+    elif w.op == "ag_gemm":
         R, M, K, Nr = w.R, d["M"], d["K"], d["N"]
         A = [x.to(dev) for x in inp["X"]]
         Bm = [x.to(dev) for x in inp["W"]]
@@ -545,7 +566,9 @@ def _op_setup(B, w, dev):
     B.fo_workspace_init(plan, ws)
 
     def launch(stream):
-        if w.op == "ag_gemm":
+        if w.op == "gemm_a2a":
+            B.fo_gemm_a2a(plan, A, Bm, Y, ws, stream)
+        elif w.op == "ag_gemm":
             B.fo_ag_gemm(plan, A, Bm, Y, None, ws, stream)
         else:
             B.fo_dp_grad_rs(plan, A, Bm, Y, ws, stream)
@@ -568,7 +591,8 @@ def measure_other_workloads(B, dev, stream, iters=20):
     peaks, peak_src = load_peaks()
     burst = float(peaks["bf16_tflops"])
     out = {}
-    for name in ("ag_gemm_qkv_r4_s4096_h4096_n3072", "dp_grad_rs_r8_t4096_4096x4096"):
+    for name in ("ag_gemm_qkv_r4_s4096_h4096_n3072", "dp_grad_rs_r8_t4096_4096x4096",
+                 "gemm_a2a_qkv_r8_t8192_h4096_n12288"):
         w = WORKLOADS[name]
         inp, A, Bm, Y, plan, ws, launch = _op_setup(B, w, dev)
         for _ in range(5):
@@ -588,6 +612,8 @@ def measure_other_workloads(B, dev, stream, iters=20):
         traffic = profiled_traffic(name)
         out[name] = {"ms": ms, "tflops": tf, "frac_of_burst_peak": tf / burst, "launches": iters,
                      "traffic": traffic, "hbm": hbm_summary(w, ms, traffic, peaks)}
+        if w.op == "gemm_a2a":
+            out[name].update(a2a_baselines(B, plan, A, Bm, Y, stream, dev, w.flops(), ms))
         del inp, A, Bm, Y, ws
         torch.cuda.empty_cache()
     shape = LayerShape(R=8, T=8192, H=4096, F=14336)
@@ -618,9 +644,35 @@ def measure_other_workloads(B, dev, stream, iters=20):
     return out
 
 
+def a2a_baselines(B, plan, X, W, Y, stream, dev, flops, fused_ms):
+    """Same-GPU comparisons of the fused all-to-all projection: each rank's
+    whole projection by cuBLAS (torch.matmul, bf16 out), and the unfused
+    path (those GEMMs, then the separate all-to-all copy kernel)."""
+    import torch
+    R = len(X)
+    P = [torch.empty(X[0].shape[0], W[0].shape[1], dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+    def cublas():
+        for r in range(R):
+            torch.matmul(X[r], W[r], out=P[r])
+
+    def unfused():
+        cublas()
+        B.fo_all_to_all_copy(plan, P, Y, stream)
+
+    cub = _time(cublas, stream)
+    unf = _time(unfused, stream)
+    copy = _time(lambda: B.fo_all_to_all_copy(plan, P, Y, stream), stream)
+    del P
+    torch.cuda.empty_cache()
+    return {"cublas_matmul_ms": cub, "cublas_matmul_tflops": flops / cub / 1e9,
+            "unfused_ms": unf, "unfused_tflops": flops / unf / 1e9, "unfused_copy_kernel_ms": copy,
+            "latency_reduction_vs_unfused_pct": 100.0 * (1.0 - fused_ms / unf)}
+
+
 def run_other_op(args, w, dev, world, rank):
-    """Timed loop of the AG-GEMM or DP-grad-RS workloads (same timing rules
-    as the default line; no comparison legs)."""
+    """Timed loop of the AG-GEMM, A2A or DP-grad-RS workloads (same timing
+    rules as the default line; no comparison legs)."""
     import torch
     import torch.distributed as dist
 
@@ -628,7 +680,7 @@ def run_other_op(args, w, dev, world, rank):
     d = w.dims
     stream = torch.cuda.current_stream(dev)
     inp, A, Bm, Y, plan, ws, launch = _op_setup(B, w, dev)
-    if w.op == "ag_gemm":
+    if w.op in ("ag_gemm", "gemm_a2a"):
         R, M, K, Nr = w.R, d["M"], d["K"], d["N"]
     else:
         R, T, M, N = w.R, d["T"], d["M"], d["N"]
@@ -654,7 +706,12 @@ def run_other_op(args, w, dev, world, rank):
     if code != 0:
         raise RuntimeError(f"device status {code} {info}")
     elapsed_ms = ev[0][0].elapsed_time(ev[-1][1])
-    if w.op == "ag_gemm":
+    if w.op == "gemm_a2a":
+        e2e = measure_e2e(B, lambda: B.fo_plan("gemm_a2a", R, M, Nr, K),
+                          lambda p, din, dout, ws_, s_: B.fo_gemm_a2a(p, din[0], din[1], dout, ws_, s_),
+                          [inp["X"], inp["W"]], [A, Bm], Y, dev, stream, world, w.flops(),
+                          max(4, min(args.steps, 12)))
+    elif w.op == "ag_gemm":
         e2e = measure_e2e(B, lambda: B.fo_plan("ag_gemm", R, M, Nr * R, K),
                           lambda p, din, dout, ws_, s_: B.fo_ag_gemm(p, din[0], din[1], dout, None, ws_, s_),
                           [inp["X"], inp["W"]], [A, Bm], Y, dev, stream, world, w.flops(),

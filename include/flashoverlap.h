@@ -67,7 +67,8 @@ typedef enum {
   FO_OP_AG_GEMM = 0,          /* Y_r = AllGather(X) . W_r           */
   FO_OP_GEMM_RS = 1,          /* Y   = ReduceScatter(X_r . W_r)     */
   FO_OP_DP_GRAD_RS = 2,       /* dW  = ReduceScatter(X_r^T . dY_r)  */
-  FO_OP_GEMM_AR = 3           /* Y_r = AllReduce(X_q . W_q) = RS then AG */
+  FO_OP_GEMM_AR = 3,          /* Y_r = AllReduce(X_q . W_q) = RS then AG */
+  FO_OP_GEMM_A2A = 4          /* Y_c = AllToAll(X_r . W_r): block c of every rank */
 } fo_op;
 
 typedef enum { FO_BF16 = 0, FO_F32 = 1 } fo_dtype;
@@ -140,8 +141,9 @@ typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
  *           two steps of the pair back to back: its weights are read once
  *           per pair, while the two owners' shards stay in L2.
  * AUTO:     SKEWED_PAIRS for GEMM_RS / GEMM_AR, RANK_MAJOR for AG_GEMM
- *           (peer read) and DP_GRAD_RS (the fastest choices on GB300 for
- *           each op); LOCKSTEP under the ring reduce-scatter and the copy
+ *           (peer read), DP_GRAD_RS and GEMM_A2A (the fastest choices on
+ *           GB300 for each op; an all-to-all rank reads one X_r and one W_r
+ *           for all of its steps); LOCKSTEP under the ring reduce-scatter and the copy
  *           transport, whose ring hops then run a whole step apart. */
 /* Balancing of the launch's last waves. The persistent kernel deals whole
  * tiles to its units (CTA pairs or CTAs) round-robin; when the tile count is
@@ -153,7 +155,7 @@ typedef enum { FO_TILE_AUTO = 0, FO_TILE_SINGLE = 1 } fo_tile_config;
  *       which adds the other part's fp32 partial (kept in the workspace).
  *       Results agree with OFF up to fp32 re-association of that tile's
  *       reduction (bit-exact in the integer mode).
- * AUTO: ON for AG_GEMM plans whose tiles take at least 32 k-blocks and
+ * AUTO: ON for AG_GEMM and GEMM_A2A plans whose tiles take at least 32 k-blocks and
  *       whose launch spans two or more whole waves; OFF otherwise. (Cutting
  *       costs each unit one extra store and reload of a tile; reduce-scatter
  *       tiles cut this way also wait on one another's partials, which on
@@ -177,20 +179,24 @@ typedef enum {
  *   FO_OP_DP_GRAD_RS X_r [K x M], dY_r [K x N] (K = tokens), dW_r [M/R x N]
  *                    fp32, or bf16 with out_dtype FO_BF16
  *   FO_OP_GEMM_AR    X_r [M x K/R], W_r [K/R x N] (or [N x K/R]), Y_r [M x N] fp32
+ *   FO_OP_GEMM_A2A   X_r [M/R x K], W_r [K x N] (or [N x K]), Y_c [M x N/R] bf16:
+ *                    rows r*M/R .. (r+1)*M/R-1 of Y_c are X_r . W_r's columns
+ *                    c*N/R .. (c+1)*N/R-1 (column block c = head group c)
  * With out_dtype FO_BF16 the fp32 sums are kept in the workspace and each
  * tile is rounded once (nearest even) into Y when its R-th partial lands.
  * Row block d of an RS output (rows d*M/R .. (d+1)*M/R-1 of the sum over
- * ranks) belongs to rank d. The all-gather concatenates shards in rank order. */
+ * ranks) belongs to rank d. The all-gather concatenates shards in rank order.
+ * GEMM_A2A uses the RS step table (the block that stays is computed last). */
 typedef struct {
   int32_t op;                 /* fo_op */
   int32_t R;                  /* virtual ranks, 1..16 */
   int64_t M, N, K;
   int32_t in_dtype;           /* FO_BF16; FO_F32 (tf32 MMA) for GEMM_RS only */
-  int32_t out_dtype;          /* GEMM_RS / DP_GRAD_RS: FO_F32 or FO_BF16; AG_GEMM: FO_BF16;
-                                 GEMM_AR: FO_F32 */
+  int32_t out_dtype;          /* GEMM_RS / DP_GRAD_RS: FO_F32 or FO_BF16; AG_GEMM and
+                                 GEMM_A2A: FO_BF16; GEMM_AR: FO_F32 */
   int32_t sched;              /* fo_sched */
   int32_t ag_transport;       /* fo_ag_transport (AG_GEMM only) */
-  int32_t w_layout;           /* fo_w_layout (GEMM_RS and AG_GEMM) */
+  int32_t w_layout;           /* fo_w_layout (GEMM_RS, GEMM_AR, AG_GEMM and GEMM_A2A) */
   int32_t deterministic;      /* RS: 1 = partials are added in step order (bitwise
                                  reproducible); 0 = each add may start once the
                                  shard's first partial is stored */
@@ -284,6 +290,23 @@ fo_status fo_gemm_rs(fo_plan_t plan, const void* const* X, const void* const* W,
  * the remaining partial GEMMs still run. */
 fo_status fo_gemm_ar(fo_plan_t plan, const void* const* X, const void* const* W,
                      void* const* Y, void* ws, fo_stream_t stream);
+
+/* Flash All-to-All: the projection of Ulysses (sequence) parallelism fused
+ * with its all-to-all (gist.science "Technical Summary" section 1: Ulysses
+ * parallelism needs an all-to-all; section 2, "Architectural Versatility":
+ * Flash All-to-All extends the method to it). Rank r holds its M/R tokens
+ * X_r [M/R x K] and the whole projection W_r [K x N] ([N x K] for
+ * FO_W_NK); column block c (N/R columns, head group c) of X_r . W_r belongs
+ * to rank c, which stacks the blocks of all ranks in rank order:
+ * Y_c [M x N/R] bf16, rows r*M/R .. (r+1)*M/R-1 from rank r (fp32
+ * accumulation, rounded once). Rank r's step s computes block
+ * (r - 1 - s) mod R and writes it straight into rank c's Y_c (the P2P
+ * transfer); the block that stays on the rank is computed last, as in
+ * Flash-RS, so no transfer trails the last compute. The blocks are
+ * disjoint, so no tile waits for another. Y is overwritten. The workspace
+ * holds only the status word (and the tail split's buffers). */
+fo_status fo_gemm_a2a(fo_plan_t plan, const void* const* X, const void* const* W,
+                      void* const* Y, void* ws, fo_stream_t stream);
 
 /* Data-parallel weight gradient fused with its reduce-scatter:
  * dW_d = sum_r (X_r^T . dY_r)[rows of d], fp32 (gist.science "Technical
@@ -386,6 +409,12 @@ fo_status fo_reduce_scatter_f32(fo_plan_t plan, const void* const* P, void* cons
 /* Unfused all-gather baseline: G_r = concat(X_0..X_{R-1}) for every r, by
  * 128-bit copies (X_r [M/R x K] bf16, G_r [M x K]). */
 fo_status fo_all_gather_copy(fo_plan_t plan, const void* const* X, void* const* G,
+                             fo_stream_t stream);
+
+/* Unfused all-to-all baseline for GEMM_A2A plans: Y_c[rows of r] =
+ * P_r[:, column block c] for every (r, c), by 128-bit copies (P_r [M/R x N]
+ * bf16, the whole projection of rank r; Y_c [M x N/R] bf16). */
+fo_status fo_all_to_all_copy(fo_plan_t plan, const void* const* P, void* const* Y,
                              fo_stream_t stream);
 
 /* Checks that each of n pointers addresses memory the current device can

@@ -387,3 +387,64 @@ def test_binding_refuses_host_tensors():
         B.fo_gemm_rs(p, host, host, host, 4096, stream=0)
     assert B.fo_plan_last_launches(p) == 0
     assert B.fo_check_device_pointers.__doc__
+
+
+# ------------------------------------------------------------------ all-to-all (Ulysses projection)
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
+def test_a2a_plan_matches_the_oracle(R):
+    p = B.fo_plan("gemm_a2a", R, 128 * R, 64 * R, 256)
+    assert B.fo_plan_table(p) == oracle.rs_schedule(R).tolist()          # the block that stays comes last
+    assert sorted(B.fo_plan_transfers(p)) == sorted(oracle.a2a_transfers(R))
+    got = sorted((a, b, c, d) for (a, b, c, d) in B.fo_plan_edges(p))
+    want = sorted((a[0], a[1], b[0], b[1]) for a, b in oracle.rs_dependency_edges(R))
+    assert got == want
+    assert B.fo_plan_task_order(p) == [(r, s) for r in range(R) for s in range(R)]   # AUTO: rank-major
+
+
+def test_a2a_plan_options_and_workspace():
+    R = 8
+    p = B.fo_plan("gemm_a2a", R, 8192, 12288, 4096)
+    sl = B.fo_plan("gemm_a2a", R, 8192, 12288, 4096, sched="sliced")
+    assert B.fo_plan_table(sl) == oracle.sliced_schedule(R).tolist()
+    # no readiness counters: the header, plus the tail split's buffers when the
+    # launch's last wave would idle most units
+    small = B.fo_plan("gemm_a2a", 2, 512, 512, 256, tail_split="off")
+    assert B.fo_workspace_size(small) == 256
+    assert B.fo_workspace_size(p) > 256
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(R=2, M=8, N=15, K=16), B.FO_ERR_SHAPE),                        # N not divisible by R
+    (dict(R=2, M=8, N=12, K=16), B.FO_ERR_ALIGN),                        # N/R = 6 columns: not 16 bytes
+    (dict(R=2, M=8, N=16, K=12), B.FO_ERR_ALIGN),                        # rows of X_r not 16 bytes
+    (dict(R=2, M=8, N=16, K=16, out_dtype="f32"), B.FO_ERR_DTYPE),
+    (dict(R=2, M=8, N=16, K=16, in_dtype="f32"), B.FO_ERR_DTYPE),
+    (dict(R=2, M=8, N=16, K=16, rs_algo="ring"), B.FO_ERR_INVALID_ARG),
+    (dict(R=2, M=8, N=16, K=16, ag_transport="copy"), B.FO_ERR_INVALID_ARG),
+    (dict(R=2, M=9, N=16, K=16), B.FO_ERR_SHAPE),
+])
+def test_a2a_plan_rejections(kw, code):
+    kw = dict(kw)
+    R, M, N, K = kw.pop("R"), kw.pop("M"), kw.pop("N"), kw.pop("K")
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_plan("gemm_a2a", R, M, N, K, **kw)
+    assert e.value.code == code
+
+
+def test_a2a_plan_refuses_the_reduce_scatter_calls():
+    p = B.fo_plan("gemm_a2a", 2, 256, 512, 256)
+    fake = [16 * (i + 1) for i in range(2)]
+    for call in (lambda: B.fo_gemm_rs(p, fake, fake, fake, 4096, stream=0),
+                 lambda: B.fo_gemm_partials(p, fake, fake, fake, 4096, stream=0),
+                 lambda: B.fo_reduce_scatter_f32(p, fake, fake, stream=0),
+                 lambda: B.fo_all_gather_copy(p, fake, fake, stream=0)):
+        with pytest.raises(B.FlashOverlapError) as e:
+            call()
+        assert e.value.code == B.FO_ERR_INVALID_ARG
+    rs = B.fo_plan("gemm_rs", 2, 256, 512, 256)
+    for call in (lambda: B.fo_gemm_a2a(rs, fake, fake, fake, 4096, stream=0),
+                 lambda: B.fo_all_to_all_copy(rs, fake, fake, stream=0)):
+        with pytest.raises(B.FlashOverlapError) as e:
+            call()
+        assert e.value.code == B.FO_ERR_INVALID_ARG
