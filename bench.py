@@ -822,6 +822,8 @@ def run_sweep(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     R, H, F = 4, 4096, 14336
+    peaks, _ = load_peaks()
+    burst, hbm_peak = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
     seqs = [int(x) for x in args.sweep_seqs.split(",")]
     g = torch.Generator().manual_seed(6)
     rows = []
@@ -861,8 +863,22 @@ def run_sweep(args):
 
         flops = 2.0 * T * H * 2 * F + 2.0 * T * F * H
         t_f, t_s, t_u = _time(fused, stream), _time(sliced, stream), _time(unfused, stream)
+        # HBM roofline of the fused pair: bytes each launch must move at
+        # least (operands once, outputs once, the RS partials to their owners
+        # and back), and the operand bytes the per-chunk decomposition pulls
+        # from L2 into the SMs (every chunk task reads all of its rank's
+        # weight, so the weights cross R times; the X chunks once each).
+        w_ug, w_d = H * 2 * F * 2.0, F * H * 2.0                  # all ranks' weights
+        hbm_bytes = (T * H * 2.0 + w_ug + T * 2 * F * 2.0) + \
+                    (T * F * 2.0 + w_d + 2.0 * (R - 1) * T * H * 4 + T * H * 4.0)
+        l2_operand_bytes = R * (w_ug + w_d) + R * T * H * 2.0 + T * F * 2.0
         rows.append({"seq": T, "fused_ms": t_f, "sliced_ms": t_s, "unfused_ms": t_u,
                      "fused_tflops": flops / t_f / 1e9,
+                     "frac_of_burst_peak": flops / t_f / 1e9 / burst,
+                     "hbm_algorithmic_bytes": hbm_bytes,
+                     "hbm_frac": hbm_bytes / (t_f * 1e-3) / 1e9 / hbm_peak,
+                     "l2_operand_bytes": l2_operand_bytes,
+                     "l2_operand_gbs": l2_operand_bytes / (t_f * 1e-3) / 1e9,
                      "latency_reduction_vs_unfused_pct": 100.0 * (t_u - t_f) / t_u,
                      "sliced_reduction_vs_unfused_pct": 100.0 * (t_u - t_s) / t_u})
         del x, Wug, act, Wd, y_ug, y, G, P, ws, ws1
