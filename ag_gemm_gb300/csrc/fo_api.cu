@@ -84,6 +84,21 @@ bool enc3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t d0,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Kernel variant of a GEMM-RS / GEMM-AR plan: bf16 operands with W as
+// [K x N] (B MN-major) or [N x K] (B K-major); tf32 operands always with B
+// K-major (a W given as [K x N] is first transposed into the workspace).
+int rs_variant(fo_plan_t p) {
+  if (p->elem_bytes == 4) return FO_V_RS_TF32_NK;
+  return p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK;
+}
+
+// fp32 W_r given as [K_r x N]: the tf32 MMA takes both operands K-major,
+// so every call first writes W_r^T [N x K_r] into the workspace.
+bool tf32_kn(fo_plan_t p) { return p->elem_bytes == 4 && p->d.w_layout == FO_W_KN; }
+float* wt_copy(fo_plan_t p, void* ws, int r) {
+  return reinterpret_cast<float*>(static_cast<char*>(ws) + p->ws_wt_off + (size_t)r * p->ws_wt_stride);
+}
+
 enum CallKind { KIND_NONE = 0, KIND_RS = 1, KIND_DP = 2, KIND_AG = 3, KIND_PART = 4, KIND_A2A = 5 };
 
 // Returns the cached parameter block when the same call kind is made with
@@ -232,8 +247,9 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
   const bool bf16_out = !partial && p->d.out_dtype == FO_BF16;
   const bool to_ws = bf16_out && !ring;
   const bool ar = !partial && p->d.op == FO_OP_GEMM_AR;
+  const bool wt = !dp && tf32_kn(p);
   fo::FoParams* k = cached_params(p, kind, A, B, (const void* const*)D);
-  if (k && ((!to_ws && !ring) || p->param_cache_ws == ws)) {
+  if (k && ((!to_ws && !ring && !wt) || p->param_cache_ws == ws)) {
     fill_common(p, k, ws);
     *out = k;
     return FO_OK;
@@ -251,7 +267,8 @@ fo_status build_rs_like(fo_plan_t p, bool dp, bool partial, const void* const* A
   for (int r = 0; r < R && ok; ++r) {
     if (!dp) {
       ok &= enc2d(&k->tmA[r], dt, A[r], kr, M, kr * es, bk, FO_BM);
-      if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, B[r], N, kr, N * es, bk, bk);
+      if (wt) ok &= enc2d(&k->tmB[r], dt, wt_copy(p, ws, r), kr, N, kr * es, bk, p->pair ? FO_BN / 2 : FO_BN);
+      else if (p->d.w_layout == FO_W_KN) ok &= enc2d(&k->tmB[r], dt, B[r], N, kr, N * es, bk, bk);
       else ok &= enc2d(&k->tmB[r], dt, B[r], kr, N, kr * es, bk, p->pair ? FO_BN / 2 : FO_BN);
     } else {
       ok &= enc2d(&k->tmA[r], dt, A[r], M, kr, M * es, bk, bk);
@@ -441,6 +458,20 @@ fo_status run_chunk_gemm(fo_plan_t p, int variant, fo::FoParams* k, const DevInf
   return FO_OK;
 }
 
+fo_status transpose_w(fo_plan_t p, const void* const* W, void* ws, cudaStream_t s);
+
+// GEMM-RS-like launch; with fp32 W_r given as [K x N], the transpose into the
+// workspace goes first on the same stream (two launches).
+fo_status run_rs_chunk_gemm(fo_plan_t p, const void* const* W, void* ws, int variant, fo::FoParams* k,
+                            const DevInfo& di, cudaStream_t s) {
+  if (tf32_kn(p)) {
+    if (fo_status st = transpose_w(p, W, ws, s)) return st;
+  }
+  fo_status st = run_chunk_gemm(p, variant, k, di, s);
+  if (st == FO_OK && tf32_kn(p)) p->last_launches = 2;
+  return st;
+}
+
 // ---------------------------------------------------------------- aux kernels
 
 struct PtrArray {
@@ -496,6 +527,45 @@ __global__ void all_to_all_copy_kernel(PtrArray P, MutPtrArray Y, int R, int64_t
   }
 }
 
+// Wt_r = W_r^T for every rank r (blockIdx.z): W_r [K x N] fp32 row-major,
+// Wt_r [N x K]; 32 x 32 tiles through shared memory so that both the reads
+// and the writes are coalesced.
+__global__ void transpose_f32_kernel(PtrArray W, MutPtrArray Wt, int64_t K, int64_t N) {
+  __shared__ float tile[32][33];
+  const float* src = static_cast<const float*>(W.p[blockIdx.z]);
+  float* dst = static_cast<float*>(Wt.p[blockIdx.z]);
+  const int64_t n0 = (int64_t)blockIdx.x * 32;
+  for (int64_t k0 = (int64_t)blockIdx.y * 32; k0 < K; k0 += (int64_t)gridDim.y * 32) {
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+      const int64_t k = k0 + i, n = n0 + threadIdx.x;
+      tile[i][threadIdx.x] = (k < K && n < N) ? src[k * N + n] : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+      const int64_t n = n0 + i, k = k0 + threadIdx.x;
+      if (n < N && k < K) dst[n * K + k] = tile[threadIdx.x][i];
+    }
+    __syncthreads();
+  }
+}
+
+// Launch the transpose of every rank's fp32 W_r into the workspace (plans
+// with fp32 inputs and W as [K x N] only).
+fo_status transpose_w(fo_plan_t p, const void* const* W, void* ws, cudaStream_t s) {
+  PtrArray wa = {};
+  MutPtrArray ta = {};
+  for (int r = 0; r < p->R; ++r) {
+    wa.p[r] = W[r];
+    ta.p[r] = wt_copy(p, ws, r);
+  }
+  const int64_t K = p->k_red, N = p->n_out;
+  const int64_t ky = (K + 31) / 32;
+  dim3 grid((unsigned)((N + 31) / 32), (unsigned)(ky < 65535 ? ky : 65535), (unsigned)p->R);
+  transpose_f32_kernel<<<grid, dim3(32, 8), 0, s>>>(wa, ta, K, N);
+  if (cudaGetLastError() != cudaSuccess) return FO_ERR_CUDA;
+  return FO_OK;
+}
+
 }  // namespace
 
 // Parameters of one fo_gemm_rs launch built into caller storage (no plan
@@ -506,6 +576,7 @@ fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const
                                         int* grid) {
   if (p->d.op != FO_OP_GEMM_RS || p->d.out_dtype != FO_F32) return FO_ERR_DTYPE;
   if (p->ring) return FO_ERR_UNSUPPORTED;   // the ring's receive buffers do not fit the static scratch
+  if (tf32_kn(p)) return FO_ERR_UNSUPPORTED;   // W_r^T would have to live in the static scratch
   DevInfo di;
   fo_status st = preflight(p, &di);
   if (st != FO_OK) return st;
@@ -528,7 +599,7 @@ fo_status fo_internal_rs_params_nocache(fo_plan_t p, const void* const* X, const
   k->sk_tiles = 0;   // no tail split: its buffers are not in the static scratch
   k->sk_buf = nullptr;
   k->sk_ctr = nullptr;
-  *variant = es == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
+  *variant = rs_variant(p);
   return launch_grid(p, *variant, di, grid);
 }
 
@@ -584,8 +655,7 @@ fo_status fo_gemm_rs(fo_plan_t p, const void* const* X, const void* const* W, vo
   if ((st = preflight(p, &di))) return st;
   fo::FoParams* k = nullptr;
   if ((st = build_rs_like(p, false, false, X, W, Y, ws, (cudaStream_t)stream, &k))) return st;
-  int v = p->elem_bytes == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
-  return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
+  return run_rs_chunk_gemm(p, W, ws, rs_variant(p), k, di, (cudaStream_t)stream);
 }
 
 fo_status fo_gemm_ar(fo_plan_t p, const void* const* X, const void* const* W, void* const* Y, void* ws,
@@ -600,8 +670,7 @@ fo_status fo_gemm_ar(fo_plan_t p, const void* const* X, const void* const* W, vo
   if ((st = preflight(p, &di))) return st;
   fo::FoParams* k = nullptr;
   if ((st = build_rs_like(p, false, false, X, W, Y, ws, (cudaStream_t)stream, &k))) return st;
-  int v = p->elem_bytes == 4 ? FO_V_RS_TF32_NK : (p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK);
-  return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
+  return run_rs_chunk_gemm(p, W, ws, rs_variant(p), k, di, (cudaStream_t)stream);
 }
 
 fo_status fo_dp_grad_rs(fo_plan_t p, const void* const* X, const void* const* dY, void* const* dW, void* ws,
@@ -672,7 +741,8 @@ fo_status fo_gemm_partials(fo_plan_t p, const void* const* A, const void* const*
   int v = dp ? FO_V_PART_DP
              : (p->elem_bytes == 4 ? FO_V_PART_TF32_NK
                                    : (p->d.w_layout == FO_W_KN ? FO_V_PART_BF16_KN : FO_V_PART_BF16_NK));
-  return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
+  if (dp) return run_chunk_gemm(p, v, k, di, (cudaStream_t)stream);
+  return run_rs_chunk_gemm(p, B, ws, v, k, di, (cudaStream_t)stream);
 }
 
 fo_status fo_reduce_scatter_f32(fo_plan_t p, const void* const* P, void* const* Y, fo_stream_t stream) {

@@ -58,6 +58,8 @@ struct fo_plan_s {
   size_t ws_ring_off;      // ring RS: rank q's fp32 receive buffer [M x N] at off + q * stride
   size_t ws_ring_stride;
   bool ring;               // d.rs_algo == FO_RS_RING
+  size_t ws_wt_off;        // fp32 inputs with W as [K x N]: W_r^T [N x K_r] fp32 at off + r * stride
+  size_t ws_wt_stride;
   size_t ws_trace_off;     // trace = 1: uint64 [FO_TRACE_MAX_CTAS][FO_TRACE_STAMPS]
   int32_t last_grid;       // CTAs of the last fused-kernel launch (0 = none yet)
   // Tail split: room for sk_cap split tiles (0 = none reserved): their fp32

@@ -59,6 +59,9 @@ extern "C" fo_status fo_gemm_rs_noalloc(fo_plan_t p, const void* const* X, const
   // plan included, which alone exceed the array).
   if (p->ws_split_off > (size_t)FO_NOALLOC_SCRATCH_BYTES || p->d.trace) return FO_ERR_SCRATCH_LIMIT;
   if (p->d.out_dtype != FO_F32) return FO_ERR_DTYPE;
+  // fp32 W given as [K x N] is transposed into the workspace before the
+  // fused launch; this entry point has no room for that copy.
+  if (p->elem_bytes == 4 && p->d.w_layout == FO_W_KN) return FO_ERR_UNSUPPORTED;
   if ((st = fo_internal_check_device_ptrs(p->R, X, stream)) || (st = fo_internal_check_device_ptrs(p->R, W, stream)) ||
       (st = fo_internal_check_device_ptrs(p->R, (const void* const*)Y, stream)))
     return st;

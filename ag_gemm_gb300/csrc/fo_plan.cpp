@@ -308,9 +308,7 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
       if (K % R) return FO_ERR_SHAPE;
       if (d->out_dtype != FO_F32 && !(d->op == FO_OP_GEMM_RS && d->out_dtype == FO_BF16)) return FO_ERR_DTYPE;
       if (d->in_dtype == FO_F32) {
-        eb = 4;
-        // fp32 operands feed the tf32 MMA only with both operands K-major.
-        if (d->w_layout != FO_W_NK) return FO_ERR_UNSUPPORTED;
+        eb = 4;   // fp32 operands feed the tf32 MMA (a [K x N] W is transposed first)
       } else if (d->in_dtype != FO_BF16) {
         return FO_ERR_DTYPE;
       }
@@ -403,6 +401,14 @@ fo_status fo_plan(const fo_plan_desc* d, fo_plan_t* out) {
   if (p->ring) {
     p->ws_ring_stride = align_up((size_t)p->rows_per_chunk * R * p->n_out * 4, 256);
     off += (size_t)R * p->ws_ring_stride;
+  }
+  // fp32 inputs with W as [K x N]: the tf32 MMA reads B K-major only, so
+  // each call transposes W_r into this region first.
+  p->ws_wt_off = off;
+  p->ws_wt_stride = 0;
+  if (eb == 4 && d->w_layout == FO_W_KN) {
+    p->ws_wt_stride = align_up((size_t)p->k_red * p->n_out * 4, 256);
+    off += (size_t)R * p->ws_wt_stride;
   }
   p->ws_trace_off = off;
   if (d->trace) off += align_up((size_t)FO_TRACE_MAX_CTAS * FO_TRACE_STAMPS * sizeof(uint64_t), 256);

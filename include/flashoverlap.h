@@ -191,7 +191,7 @@ typedef struct {
   int32_t op;                 /* fo_op */
   int32_t R;                  /* virtual ranks, 1..16 */
   int64_t M, N, K;
-  int32_t in_dtype;           /* FO_BF16; FO_F32 (tf32 MMA) for GEMM_RS only */
+  int32_t in_dtype;           /* FO_BF16; FO_F32 (tf32 MMA) for GEMM_RS and GEMM_AR */
   int32_t out_dtype;          /* GEMM_RS / DP_GRAD_RS: FO_F32 or FO_BF16; AG_GEMM and
                                  GEMM_A2A: FO_BF16; GEMM_AR: FO_F32 */
   int32_t sched;              /* fo_sched */
@@ -250,6 +250,7 @@ fo_status fo_plan_task_order(fo_plan_t plan, int32_t* order);
 
 /* Bytes of device workspace the launching calls need (readiness counters,
  * flags and the device status word; fp32 shard sums for a bf16 output;
+ * for fp32 inputs with W as [K x N], every rank's transposed W_r;
  * under FO_RS_RING every rank's fp32 receive buffer, R x M x N x 4 bytes;
  * with trace = 1, FO_TRACE_MAX_CTAS x FO_TRACE_STAMPS timestamps; when the
  * tail split applies, one fp32 tile per split tile, sized for the 152 SMs
@@ -277,7 +278,10 @@ fo_status fo_ag_gemm(fo_plan_t plan, const void* const* X, const void* const* W,
  * computes the partial of chunk (r - 1 - s) mod R and adds it into that
  * owner's Y (FO_RS_DIRECT), or adds it to the running sum received from r-1
  * and forwards that to r+1 (FO_RS_RING); the own chunk comes last. Y is
- * overwritten. */
+ * overwritten. fp32 inputs run on the tf32 MMA, which reads its operands
+ * K-major only: with W_r given as [K/R x N] (FO_W_KN) the call first
+ * transposes every W_r into the workspace (a second launch on `stream`,
+ * before the fused kernel); with [N x K/R] (FO_W_NK) it reads W_r as is. */
 fo_status fo_gemm_rs(fo_plan_t plan, const void* const* X, const void* const* W,
                      void* const* Y, void* ws, fo_stream_t stream);
 
@@ -361,7 +365,9 @@ fo_status fo_status_query(fo_plan_t plan, void* ws, fo_stream_t stream, int32_t 
  *     and fo_status_query where that report is needed.
  *   - Plans with a bf16 output return FO_ERR_DTYPE (or FO_ERR_SCRATCH_LIMIT
  *     when their shard sums exceed the array); plans with the ring
- *     reduce-scatter (FO_RS_RING) return FO_ERR_UNSUPPORTED; plans with
+ *     reduce-scatter (FO_RS_RING), and plans with fp32 inputs and W as
+ *     [K x N] (whose transposed W would need the array), return
+ *     FO_ERR_UNSUPPORTED (or FO_ERR_SCRATCH_LIMIT); plans with
  *     trace = 1 return FO_ERR_SCRATCH_LIMIT (their timestamps alone fill
  *     the array). */
 #define FO_NOALLOC_SCRATCH_BYTES (64 * 1024)

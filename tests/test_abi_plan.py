@@ -96,7 +96,7 @@ def test_dropped_transfer_is_rejected():
     (dict(op="ag_gemm", R=2, M=8, N=16, K=16, out_dtype="f32"), B.FO_ERR_DTYPE),
     (dict(op="gemm_ar", R=2, M=8, N=16, K=16, out_dtype="bf16"), B.FO_ERR_DTYPE),
     (dict(op="gemm_ar", R=2, M=8, N=16, K=9), B.FO_ERR_SHAPE),
-    (dict(op="gemm_rs", R=2, M=8, N=16, K=16, in_dtype="f32"), B.FO_ERR_UNSUPPORTED),  # tf32 needs W as [N x K]
+    (dict(op="gemm_rs", R=2, M=8, N=6, K=16, in_dtype="f32"), B.FO_ERR_ALIGN),   # fp32 rows of 24 bytes
     (dict(op="ag_gemm", R=2, M=8, N=16, K=16, sched="sliced"), B.FO_ERR_UNSUPPORTED),
 ])
 def test_plan_rejects_bad_descriptors(kw, code):
@@ -448,3 +448,11 @@ def test_a2a_plan_refuses_the_reduce_scatter_calls():
         with pytest.raises(B.FlashOverlapError) as e:
             call()
         assert e.value.code == B.FO_ERR_INVALID_ARG
+
+
+def test_fp32_inputs_take_either_weight_layout():
+    # The 256 x 512 x 512 R = 2 integer workload as stated: fp32 X_r [256 x 512]
+    # and W_r [512 x 512] in the [K x N] layout (tf32 MMA, B operand MN-major).
+    for layout in ("kn", "nk"):
+        p = B.fo_plan("gemm_rs", 2, 256, 512, 1024, in_dtype="f32", w_layout=layout)
+        assert B.fo_plan_table(p) == oracle.rs_schedule(2).tolist()

@@ -34,13 +34,16 @@ def _ws(plan, dev):
     return ws
 
 
-@pytest.mark.parametrize("tile", ["auto", "single"])
-def test_gemm_rs_replays_from_a_cuda_graph(dev, tile):
+@pytest.mark.parametrize("tile,dtype", [("auto", "bf16"), ("single", "bf16"), ("auto", "f32")])
+def test_gemm_rs_replays_from_a_cuda_graph(dev, tile, dtype):
+    # (fp32 inputs with W as [K x N]: the graph holds the transpose of W into
+    # the workspace and the fused launch.)
     R, M, K, N = 4, 1024, 256, 512
-    plan = B.fo_plan("gemm_rs", R, M, N, K * R, tile_config=tile)
+    plan = B.fo_plan("gemm_rs", R, M, N, K * R, tile_config=tile, in_dtype=dtype)
     ws = _ws(plan, dev)
-    X = [torch.empty(M, K, dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    W = [torch.empty(K, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    X = [torch.empty(M, K, dtype=tdt, device=dev) for _ in range(R)]
+    W = [torch.empty(K, N, dtype=tdt, device=dev) for _ in range(R)]
     Y = [torch.empty(M // R, N, device=dev) for _ in range(R)]
     for t in X + W:
         t.zero_()
@@ -50,7 +53,7 @@ def test_gemm_rs_replays_from_a_cuda_graph(dev, tile):
     with torch.cuda.graph(g):
         B.fo_gemm_rs(plan, X, W, Y, ws)
     for seed in (1, 2, 3):
-        inp = gemm_rs_inputs(R, M, K, N, mode="int", seed=seed)
+        inp = gemm_rs_inputs(R, M, K, N, mode="int", seed=seed, dtype=dtype)
         for r in range(R):
             X[r].copy_(inp["X"][r])
             W[r].copy_(inp["W"][r])

@@ -84,7 +84,8 @@ def run_gemm_rs(dev, R, M, K, N, *, dtype="bf16", mode="int", w_layout="kn", see
         _status_ok(plan, ws)
         outs.append([_np(y) for y in Y.views])
     Y.check()
-    assert B.fo_plan_last_launches(plan) == 1
+    # fp32 W as [K x N] is transposed into the workspace first: two launches
+    assert B.fo_plan_last_launches(plan) == (2 if dtype == "f32" and w_layout == "kn" else 1)
     ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
     return outs, ref
 
@@ -115,9 +116,10 @@ def test_gemm_rs_integer_bit_exact(dev, R, M, K, N, layout, tile):
         assert np.array_equal(outs[0][d], ref[d]), f"shard {d}"
 
 
-@pytest.mark.parametrize("R,M,K,N", [(2, 256, 512, 512), (3, 600, 100, 132)])
-def test_gemm_rs_fp32_inputs_tf32_bit_exact(dev, R, M, K, N):
-    outs, ref = run_gemm_rs(dev, R, M, K, N, dtype="f32", w_layout="nk")
+@pytest.mark.parametrize("layout", ["nk", "kn"])   # W as [N x K] (B K-major) or [K x N] (B MN-major)
+@pytest.mark.parametrize("R,M,K,N", [(2, 256, 512, 512), (3, 600, 100, 132), (4, 1024, 96, 800)])
+def test_gemm_rs_fp32_inputs_tf32_bit_exact(dev, R, M, K, N, layout):
+    outs, ref = run_gemm_rs(dev, R, M, K, N, dtype="f32", w_layout=layout)
     for d in range(R):
         assert np.array_equal(outs[0][d], ref[d]), f"shard {d}"
 

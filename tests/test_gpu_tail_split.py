@@ -103,8 +103,9 @@ def test_split_gemm_rs_integer_bit_exact(dev, R, M, K, N, tile, kw):
         assert np.array_equal(off[d], ref[d])
 
 
-def test_split_gemm_rs_tf32_bit_exact(dev):
-    outs, ref = run_rs(dev, 2, 512, 256, 5120, dtype="f32", layout="nk")   # 160 single-CTA tiles
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+def test_split_gemm_rs_tf32_bit_exact(dev, layout):
+    outs, ref = run_rs(dev, 2, 512, 256, 5120, dtype="f32", layout=layout)   # 160 single-CTA tiles
     assert outs["on"][1] > 0
     for d in range(2):
         assert np.array_equal(outs["on"][0][d], ref[d])

@@ -98,3 +98,16 @@ def test_noalloc_call_after_a_timed_out_call_is_exact():
         torch.cuda.synchronize()
         for d in range(R):
             assert np.array_equal(_np(Y[d]), want[d]), f"call {call} shard {d}"
+
+
+def test_noalloc_refuses_fp32_inputs_with_w_as_k_by_n():
+    # Such plans transpose W into the workspace first; the allocation-free
+    # entry point has no room for that copy. Refused from the plan alone.
+    import __graft_entry__
+    __graft_entry__.build()
+    plan = B.fo_plan("gemm_rs", 2, 64, 16, 16, in_dtype="f32")      # tiny: fits the scratch otherwise
+    assert B.fo_workspace_size(plan) <= B.FO_NOALLOC_SCRATCH_BYTES
+    fake = [16 * (i + 1) for i in range(2)]
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_gemm_rs_noalloc(plan, fake, fake, fake, stream=0)
+    assert e.value.code == B.FO_ERR_UNSUPPORTED
