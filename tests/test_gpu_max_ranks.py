@@ -1,6 +1,7 @@
-"""GPU parity at the largest rank count a plan accepts (R = 16): every op, a
-ragged case, both tile configurations, the bf16 output, the ring
-reduce-scatter and both all-gather transports with gather buffers. Integer
+"""GPU parity at the largest rank count a plan accepts (R = 16): every op (the
+all-to-all included), a ragged case, both tile configurations, the bf16
+output, the ring reduce-scatter and both all-gather transports with gather
+buffers. Integer
 inputs, so every result must match the oracle bit for bit; guard bands
 around every output catch stray writes.
 """
@@ -99,3 +100,15 @@ def test_dp_grad_rs_sixteen_ranks(dev, tile):
     got, ref = run_dp(dev, R, 128, 4096, 256, tile=tile)
     for d in range(R):
         assert np.array_equal(got[d], ref[d]), f"shard {d}"
+
+
+@pytest.mark.parametrize("tile", ["auto", "single"])
+@pytest.mark.parametrize("M,K,N,layout", [
+    (4096, 128, 4096, "kn"),     # 256 tokens per rank, blocks of 256 columns
+    (1600, 72, 1664, "nk"),      # ragged: 100 tokens per rank, blocks of 104 columns
+])
+def test_a2a_sixteen_ranks(dev, tile, M, K, N, layout):
+    from test_gpu_a2a import run_a2a
+    outs, ref, _ = run_a2a(dev, R, M, K, N, layout=layout, tile=tile)
+    for c in range(R):
+        assert np.array_equal(outs[0][c], oracle.round_bf16(ref[c])), f"rank {c}"

@@ -1,4 +1,5 @@
-"""Seeded random shapes for every op: R from 1 to 16, ragged rows, K and N,
+"""Seeded random shapes for every op (reduce-scatter with bf16 and fp32
+inputs, all-gather, DP gradient, all-reduce, all-to-all): R from 1 to 16, ragged rows, K and N,
 either tile configuration, any interleave, both weight layouts and output
 dtypes, with the tail split forced on in about half the draws. Integer inputs, so every result must equal the oracle bit for bit
 (bf16 outputs: the oracle rounded once); guard bands around every output.
@@ -137,6 +138,56 @@ def test_random_gemm_ar(dev, seed):
         assert np.array_equal(_np(Y.views[q]), ref[q]), f"R={R} M={M} K={Kr} N={N} {tile} {il} {split} rank {q}"
 
 
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_gemm_a2a(dev, seed):
+    g, R, rows, K, Nc = _draw(8000 + seed)       # Nc: columns of one block (head group)
+    M, N = R * rows, R * Nc
+    layout = ["kn", "nk"][int(g.integers(2))]
+    tile = ["auto", "single"][int(g.integers(2))]
+    il = INTERLEAVES[int(g.integers(len(INTERLEAVES)))]
+    sched = ["rank_adaptive", "sliced"][int(g.integers(2))]
+    split = SPLITS[int(g.integers(2))]
+    inp = ag_gemm_inputs(R, M, K, N, mode="int", seed=seed)
+    plan = B.fo_plan("gemm_a2a", R, M, N, K, w_layout=layout, tile_config=tile, interleave=il, sched=sched,
+                     tail_split=split)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [(w if layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
+    Y = Guarded(R, (M, Nc), torch.bfloat16, dev)
+    ws = _ws(plan, dev)
+    for _ in range(2):
+        B.fo_gemm_a2a(plan, X, W, Y.views, ws)
+        _status_ok(plan, ws)
+    Y.check()
+    ref = oracle.gemm_a2a([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    what = f"R={R} M={M} K={K} N={N} {layout} {tile} {il} {sched} {split}"
+    for c in range(R):
+        assert np.array_equal(_np(Y.views[c]), oracle.round_bf16(ref[c])), f"{what} rank {c}"
+
+
+@pytest.mark.parametrize("seed", range(CASES // 2))
+def test_random_gemm_rs_fp32_inputs(dev, seed):
+    # fp32 inputs on the tf32 MMA, W in either layout ([K x N] is transposed
+    # into the workspace first); K and N multiples of 4 keep fp32 rows on
+    # 16-byte boundaries.
+    g, R, rows, Kr, N = _draw(9000 + seed)
+    M = R * rows
+    layout = ["kn", "nk"][int(g.integers(2))]
+    split = SPLITS[int(g.integers(2))]
+    inp = gemm_rs_inputs(R, M, Kr, N, dtype="f32", mode="int", seed=seed)
+    plan = B.fo_plan("gemm_rs", R, M, N, Kr * R, in_dtype="f32", w_layout=layout, tail_split=split)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [(w if layout == "kn" else w.t().contiguous()).to(dev) for w in inp["W"]]
+    Y = Guarded(R, (rows, N), torch.float32, dev)
+    ws = _ws(plan, dev)
+    for _ in range(2):
+        B.fo_gemm_rs(plan, X, W, Y.views, ws)
+        _status_ok(plan, ws)
+    Y.check()
+    ref = oracle.gemm_rs([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for d in range(R):
+        assert np.array_equal(_np(Y.views[d]), ref[d]), f"R={R} M={M} K={Kr} N={N} {layout} {split} shard {d}"
+
+
 # ---------------------------------------------------------------- random data
 # The same draws with normal-distributed inputs, held to the stated
 # tolerances: relative Frobenius error <= 1e-3 and elementwise relative error
@@ -203,3 +254,20 @@ def test_random_dp_grad_rs_randn(dev, seed):
     for d in range(R):
         want = ref[d] if out == "f32" else oracle.round_bf16(ref[d])
         _close(_np(dW.views[d]), want, f"R={R} T={T} M={M} N={N} {out} {split} shard {d}")
+
+
+@pytest.mark.parametrize("seed", range(RANDN_CASES))
+def test_random_gemm_a2a_randn(dev, seed):
+    g, R, rows, K, Nc = _draw(10000 + seed)
+    M, N = R * rows, R * Nc
+    split = SPLITS[int(g.integers(2))]
+    inp = ag_gemm_inputs(R, M, K, N, mode="randn", seed=seed)
+    plan = B.fo_plan("gemm_a2a", R, M, N, K, tail_split=split)
+    Y = Guarded(R, (M, Nc), torch.bfloat16, dev)
+    ws = _ws(plan, dev)
+    B.fo_gemm_a2a(plan, [x.to(dev) for x in inp["X"]], [w.to(dev) for w in inp["W"]], Y.views, ws)
+    _status_ok(plan, ws)
+    Y.check()
+    ref = oracle.gemm_a2a([_np(x) for x in inp["X"]], [_np(w) for w in inp["W"]])
+    for c in range(R):
+        _close(_np(Y.views[c]), oracle.round_bf16(ref[c]), f"R={R} M={M} K={K} N={N} {split} rank {c}")
