@@ -64,6 +64,7 @@ __all__ = [
     "gemm_rs", "gemm_rs_rows", "gemm_ar", "ar_transfers", "ag_gemm", "ag_gemm_rows", "all_gather_rows",
     "dp_grad_rs", "dp_grad_rs_rows", "reduce_scatter_rows", "weight_grads", "weight_grads_rows",
     "all_to_all_blocks", "gemm_a2a", "gemm_a2a_rows", "a2a_transfers", "simulate_gemm_a2a",
+    "attention", "attn_rs", "simulate_query_split",
     "rs_chunk", "ag_source", "rs_schedule", "ag_schedule", "sliced_schedule",
     "rs_transfers", "ag_transfers", "rs_dependency_edges",
     "simulate_gemm_rs", "simulate_ag_gemm", "simulate_dp_grad_rs",
@@ -241,6 +242,78 @@ def dp_grad_rs_rows(X, dY, d: int, rows: Sequence[int]) -> np.ndarray:
     for r in range(R):
         acc = acc + _f64(X[r][:, idx]).T @ _f64(dY[r])
     return acc
+
+
+def attention(Q, K, V, heads: int, causal: bool) -> np.ndarray:
+    """Scaled dot-product attention of every head, in fp64.
+
+    Q, K, V are [T, heads*d] (head h in columns h*d .. (h+1)*d-1). For
+    head h: O_h = softmax(Q_h K_h^T / sqrt(d) + mask) V_h, the softmax taken
+    over keys for every query row; with ``causal`` the mask allows key j for
+    query i only when j <= i. Returns O [T, heads*d]. This is the attention
+    core that query-split attention decomposes ([GS] §2 "Architectural
+    Versatility": scores, softmax, weighted sum).
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    T = Q.shape[0]
+    d = Q.shape[1] // heads
+    O = np.empty((T, heads * d), dtype=np.float64)
+    allowed = np.tril(np.ones((T, K.shape[0]), dtype=bool)) if causal else None
+    for h in range(heads):
+        cols = slice(h * d, (h + 1) * d)
+        S = (Q[:, cols] @ K[:, cols].T) / np.sqrt(d)
+        if causal:
+            S = np.where(allowed, S, -np.inf)
+        S = S - S.max(axis=1, keepdims=True)
+        P = np.exp(S)
+        P = P / P.sum(axis=1, keepdims=True)
+        O[:, cols] = P @ V[:, cols]
+    return O
+
+
+def attn_rs(Q, K, V, Wo, heads: int, causal: bool, round_o: bool = False) -> List[np.ndarray]:
+    """Tensor-parallel attention with its row-parallel output projection:
+    rank r holds ``heads`` heads (Q_r, K_r, V_r [T, heads*d], every token) and
+    Wo_r [heads*d, H]; Y = sum_r attention_r @ Wo_r, reduce-scattered by token
+    rows (rank c gets rows c*T/R ..). With ``round_o`` every O_r is rounded
+    once to bf16 first (the activation the projection reads). [GS] §1: TP
+    needs a reduce-scatter; §2: query-split attention."""
+    O = [attention(Q[r], K[r], V[r], heads, causal) for r in range(len(Q))]
+    if round_o:
+        O = [round_bf16(o) for o in O]
+    return gemm_rs(O, Wo)
+
+
+def simulate_query_split(Q, K, V, Wo, heads: int, causal: bool, schedule=None) -> List[np.ndarray]:
+    """Query-split attention executed literally: at step s rank r takes query
+    block c = schedule[r, s] (rows c*T/R ..), computes the attention of those
+    queries for its heads against all of its keys (causal: keys up to each
+    query), multiplies by Wo_r and sends the partial to rank c, which adds it
+    into its shard. Reading of [GS] §2 (the attention split by queries so
+    that each query block's projection partial can be sent while the next
+    block computes; the block that stays is computed last, as in Flash-RS)."""
+    R = len(Q)
+    T = Q[0].shape[0]
+    rows = T // R
+    d = Q[0].shape[1] // heads
+    sch = rs_schedule(R) if schedule is None else np.asarray(schedule)
+    Y = [np.zeros((rows, Wo[0].shape[1]), dtype=np.float64) for _ in range(R)]
+    for s in range(R):
+        for r in range(R):
+            c = int(sch[r, s])
+            q0 = c * rows
+            Qr, Kr, Vr = _f64(Q[r]), _f64(K[r]), _f64(V[r])
+            Oc = np.empty((rows, heads * d), dtype=np.float64)
+            for h in range(heads):
+                cols = slice(h * d, (h + 1) * d)
+                S = (Qr[q0:q0 + rows, cols] @ Kr[:, cols].T) / np.sqrt(d)
+                if causal:
+                    S = np.where(np.arange(T)[None, :] <= np.arange(q0, q0 + rows)[:, None], S, -np.inf)
+                S = S - S.max(axis=1, keepdims=True)
+                P = np.exp(S)
+                Oc[:, cols] = (P / P.sum(axis=1, keepdims=True)) @ Vr[:, cols]
+            Y[c] = Y[c] + Oc @ _f64(Wo[r])
+    return Y
 
 
 # ---------------------------------------------------------------------------

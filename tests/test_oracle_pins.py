@@ -7,6 +7,7 @@ brute-force search over schedules. A few tests plant a mistake in the oracle
 (monkeypatched, on the CPU) and check that a pin catches it.
 """
 import itertools
+import math
 import os
 from fractions import Fraction
 
@@ -713,3 +714,111 @@ def test_planted_swapped_a2a_roles_are_caught(monkeypatch):
     ok = all(np.array_equal(Y[c][r * rows:(r + 1) * rows], X[r][:, 2 * c:2 * c + 2])
              for c in range(R) for r in range(R))
     assert not ok
+
+
+# --------------------------------------------------------------------------
+# Query-split attention (the attention core and its row-parallel output
+# projection): brute force, closed forms, decomposed == whole.
+# --------------------------------------------------------------------------
+
+
+def _bf_attention(Q, K, V, heads, causal):
+    """Pure-Python softmax attention, one query row and one head at a time."""
+    T, D = len(Q), len(Q[0])
+    d = D // heads
+    out = [[0.0] * D for _ in range(T)]
+    for h in range(heads):
+        for i in range(T):
+            keys = range(i + 1) if causal else range(len(K))
+            sc = {j: sum(Q[i][h * d + t] * K[j][h * d + t] for t in range(d)) / math.sqrt(d) for j in keys}
+            m = max(sc.values())
+            w = {j: math.exp(v - m) for j, v in sc.items()}
+            z = sum(w.values())
+            for t in range(d):
+                out[i][h * d + t] = sum(w[j] * V[j][h * d + t] for j in keys) / z
+    return np.array(out)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("T,heads,d", [(1, 1, 1), (4, 1, 3), (6, 2, 2), (5, 3, 4)])
+def test_attention_matches_brute_force(T, heads, d, causal):
+    rng = np.random.default_rng(T * 10 + heads)
+    Q, K, V = (rng.standard_normal((T, heads * d)) for _ in range(3))
+    got = oracle.attention(Q, K, V, heads, causal)
+    assert np.allclose(got, _bf_attention(Q.tolist(), K.tolist(), V.tolist(), heads, causal), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(1)
+    T, heads, d = 7, 2, 3
+    K, V = rng.standard_normal((T, heads * d)), rng.standard_normal((T, heads * d))
+    Q0 = np.zeros((T, heads * d))
+    # zero queries: every score is equal, so each output row is a plain mean
+    assert np.allclose(oracle.attention(Q0, K, V, heads, False), np.repeat(V.mean(axis=0, keepdims=True), T, 0))
+    prefix = np.cumsum(V, axis=0) / np.arange(1, T + 1)[:, None]
+    assert np.allclose(oracle.attention(Q0, K, V, heads, True), prefix)
+    # causal: the first query sees only the first key
+    Q = rng.standard_normal((T, heads * d))
+    assert np.allclose(oracle.attention(Q, K, V, heads, True)[0], V[0])
+    # non-causal: permuting keys and values together changes nothing
+    perm = rng.permutation(T)
+    assert np.allclose(oracle.attention(Q, K[perm], V[perm], heads, False), oracle.attention(Q, K, V, heads, False))
+
+
+def test_attn_rs_is_attention_then_the_projection_reduce_scattered():
+    rng = np.random.default_rng(2)
+    R, T, heads, d, H = 2, 4, 1, 2, 3
+    Q, K, V = ([rng.standard_normal((T, heads * d)) for _ in range(R)] for _ in range(3))
+    Wo = [rng.standard_normal((heads * d, H)) for _ in range(R)]
+    Y = oracle.attn_rs(Q, K, V, Wo, heads, True)
+    rows = T // R
+    for c in range(R):
+        for i in range(rows):
+            for j in range(H):
+                want = 0.0
+                for r in range(R):
+                    o = _bf_attention(Q[r].tolist(), K[r].tolist(), V[r].tolist(), heads, True)[c * rows + i]
+                    want += sum(o[t] * Wo[r][t, j] for t in range(heads * d))
+                assert Y[c][i, j] == pytest.approx(want, rel=1e-12, abs=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("R", [1, 2, 3, 4])
+def test_query_split_equals_whole_attention(R, causal):
+    rng = np.random.default_rng(90 + R)
+    T, heads, d, H = 3 * R, 2, 2, 5
+    Q, K, V = ([rng.standard_normal((T, heads * d)) for _ in range(R)] for _ in range(3))
+    Wo = [rng.standard_normal((heads * d, H)) for _ in range(R)]
+    ref = oracle.attn_rs(Q, K, V, Wo, heads, causal)
+    for sch in (None, oracle.sliced_schedule(R)):
+        got = oracle.simulate_query_split(Q, K, V, Wo, heads, causal, schedule=sch)
+        for c in range(R):
+            assert np.allclose(got[c], ref[c], rtol=1e-12, atol=1e-12)
+
+
+def test_planted_attention_mistakes_are_caught(monkeypatch):
+    rng = np.random.default_rng(3)
+    T, heads, d = 5, 1, 4
+    Q, K, V = (rng.standard_normal((T, heads * d)) for _ in range(3))
+    want = _bf_attention(Q.tolist(), K.tolist(), V.tolist(), heads, True)
+    real_sqrt = np.sqrt
+
+    class NoScale:
+        def __getattr__(self, name):
+            return (lambda x: 1.0) if name == "sqrt" else getattr(np, name)
+
+    monkeypatch.setattr(O, "np", NoScale())          # the 1/sqrt(d) scale dropped
+    assert not np.allclose(O.attention(Q, K, V, heads, True), want)
+    monkeypatch.undo()
+    assert real_sqrt is np.sqrt
+
+    def off_by_one(Q_, K_, V_, heads_, causal_):
+        # a causal mask that also hides the diagonal key (row 0 then sees nothing)
+        Qf, Kf, Vf = (np.asarray(a, dtype=np.float64) for a in (Q_, K_, V_))
+        S = Qf @ Kf.T / np.sqrt(d)
+        S = np.where(np.tril(np.ones((T, T), dtype=bool), -1), S, -1e300)
+        P = np.exp(S - S.max(axis=1, keepdims=True))
+        return (P / P.sum(axis=1, keepdims=True)) @ Vf
+
+    monkeypatch.setattr(O, "attention", off_by_one)
+    assert not np.allclose(O.attention(Q, K, V, heads, True), want)
