@@ -40,7 +40,7 @@ EXPORTED = [
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
     "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc", "fo_plan_task_order",
     "fo_gemm_ar", "fo_trace_query", "fo_plan_last_split_tiles", "fo_check_device_pointers",
-    "fo_gemm_a2a", "fo_all_to_all_copy",
+    "fo_gemm_a2a", "fo_all_to_all_copy", "fo_attn_rs",
 ]
 
 
@@ -96,6 +96,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_gemm_ar": ([P, PP, PP, PP, P, P], c_int32),
         "fo_gemm_a2a": ([P, PP, PP, PP, P, P], c_int32),
         "fo_all_to_all_copy": ([P, PP, PP, P], c_int32),
+        "fo_attn_rs": ([P, PP, PP, PP, PP, PP, PP, c_int32, c_int32, P, P], c_int32),
         "fo_status_query": ([P, P, P, POINTER(c_int32)], c_int32),
         "fo_trace_query": ([P, P, P, POINTER(ctypes.c_uint64), c_int32, POINTER(c_int32)], c_int32),
         "fo_gemm_partials": ([P, PP, PP, PP, P, P], c_int32),
@@ -272,6 +273,12 @@ def fo_gemm_a2a(plan: Plan, X, W, Y, ws, stream=None) -> None:
 
 def fo_all_to_all_copy(plan: Plan, P, Y, stream=None) -> None:
     _check(load().fo_all_to_all_copy(plan, _ptr_array(P), _ptr_array(Y), _stream(stream)), "fo_all_to_all_copy")
+
+
+def fo_attn_rs(plan: Plan, Q, K, V, Wo, O, Y, heads: int, causal: bool, ws, stream=None) -> None:
+    _check(load().fo_attn_rs(plan, _ptr_array(Q), _ptr_array(K), _ptr_array(V), _ptr_array(Wo), _ptr_array(O),
+                             _ptr_array(Y), int(heads), 1 if causal else 0, _ptr(ws), _stream(stream)),
+           "fo_attn_rs")
 
 
 def fo_ag_gemm(plan: Plan, X, W, Y, G=None, ws=None, stream=None) -> None:

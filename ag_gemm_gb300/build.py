@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libflashoverlap.so")
 
 SOURCES = ["fo_plan.cpp", "fo_api.cu", "fo_kern_rs.cu", "fo_kern_dp.cu", "fo_kern_ag.cu", "fo_kern_part.cu",
-           "fo_noalloc.cu"]
+           "fo_noalloc.cu", "fo_attn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

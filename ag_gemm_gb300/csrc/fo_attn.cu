@@ -1,0 +1,509 @@
+// Query-split attention with its row-parallel output projection on sm_103a.
+//
+// Tensor-parallel attention: rank r holds `heads` heads of dimension 128,
+// Q_r, K_r, V_r [T x heads*128] bf16 for every token, and its slice Wo_r of
+// the output projection. Query-split attention (gist.science, "Technical
+// Summary" section 2, "Architectural Versatility": scores, softmax and the
+// weighted sum decomposed so that more compute overlaps the communication)
+// splits the queries into R blocks; rank r's step s takes query block
+// c = (r - 1 - s) mod R, the Flash-RS order, so the block that stays on the
+// rank comes last. Block c's attention output rows are the rows of chunk c
+// of the projection's reduce-scatter.
+//
+// fo_attn_rs runs two launches on one stream:
+//   1. fo_attn_kernel: the attention of every (rank, step, head, 128-query
+//      tile) in the plan's task order, O_r = softmax(Q K^T / sqrt(128) +
+//      mask) V, written bf16 into the caller's O_r;
+//   2. the fused GEMM + reduce-scatter (fo_gemm_rs) of O_r . Wo_r.
+// On one GPU the reduce-scatter's transfers are the second launch's L2
+// reduce-adds, already overlapped with its own math; the first launch
+// computes the attention in the same query-block order.
+//
+// fo_attn_kernel, one CTA per SM, persistent over work items:
+//   warp 0     TMA producer: the item's Q tile (128 x 128) once, then K and
+//              V blocks of 128 keys into a two-stage ring;
+//   warp 1     TMEM allocation; MMA issue: S_j = Q K_j^T into one of two
+//              TMEM score buffers, then O += P_{j-1} V_{j-1} once the softmax
+//              warps have written P_{j-1}, so S_j overlaps softmax(j-1);
+//   warps 2-5  softmax, one query row per thread: the row's 128 scores from
+//              TMEM, the running maximum and sum (online softmax), P in bf16
+//              into shared memory as the next MMA's A operand, and the
+//              rescale of the TMEM output row when the maximum grows by more
+//              than 8 in log2 units (a smaller growth keeps the old maximum:
+//              the weights then stay below 2^8 and the final division by the
+//              sum cancels the choice); the sum takes the weights as rounded
+//              to bf16; at the item's end O / sum, bf16, TMA store.
+// Every wait is bounded; a wait that runs out raises the CTA's abort flag and
+// records FO_ERR_TIMEOUT in the workspace status word.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "fo_device.cuh"
+#include "fo_internal.h"
+
+namespace fo_attn {
+
+using namespace fo;
+
+constexpr int kHeadDim = 128;
+constexpr int kTile = 128;                       // query rows per item, keys per block
+constexpr int kThreads = 192;
+constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;   // 32 KB of bf16
+constexpr uint32_t kHalf = kTileBytes / 2;              // one 64-column half: 128 rows x 128 B
+constexpr int kStages = 2;
+// Shared memory, from a 1024-byte aligned base: Q, two K/V stages, two P
+// buffers, barriers.
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kOffQ + kTileBytes;
+constexpr uint32_t kOffP = kOffKV + kStages * 2 * kTileBytes;
+constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
+constexpr int kSmemBytes = 1024 + (int)kOffBar + 256;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kRescaleLog2 = 8.0f;
+
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, A
+// K-major, B K-major (scores) or MN-major (weighted sum), M = N = 128.
+__host__ __device__ constexpr uint32_t idesc(bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(kTile >> 3) << 17) |
+         ((uint32_t)(kTile >> 4) << 24);
+}
+
+struct AttnParams {
+  CUtensorMap tmQ[FO_MAX_R];   // Q_r [T x heads*128], box 64 x 128
+  CUtensorMap tmK[FO_MAX_R];   // K_r, box 64 x 128
+  CUtensorMap tmV[FO_MAX_R];   // V_r, box 64 x 64
+  CUtensorMap tmO[FO_MAX_R];   // O_r, box 64 x 32 (stores)
+  int32_t table[FO_MAX_R][FO_MAX_R];
+  int32_t task_r[FO_MAX_R * FO_MAX_R];
+  int32_t task_s[FO_MAX_R * FO_MAX_R];
+  int32_t R, T, heads, causal, qtiles;   // qtiles: 128-row query tiles per block of T/R rows
+  float scale_log2;                      // log2(e) / sqrt(128)
+  int32_t* status;
+};
+
+struct Item {
+  int r, s, c, h, q0, nkb;
+};
+
+__device__ __forceinline__ Item decode(const AttnParams& p, int L) {
+  const int per_task = p.heads * p.qtiles;
+  const int task = L / per_task;
+  const int rem = L - task * per_task;
+  Item it;
+  it.r = p.task_r[task];
+  it.s = p.task_s[task];
+  it.c = p.table[it.r][it.s];
+  it.h = rem / p.qtiles;
+  const int qt = rem - it.h * p.qtiles;
+  it.q0 = it.c * (p.T / p.R) + qt * kTile;
+  it.nkb = p.causal ? it.q0 / kTile + 1 : p.T / kTile;
+  return it;
+}
+
+// Row `row` (one per thread) of a 128-row, 64-column bf16 half in the
+// 128B-swizzle layout: 16-byte chunk j of the row sits at chunk j ^ (row % 8).
+__device__ __forceinline__ void store_row_half(uint32_t half_base, int row, const uint32_t (&w)[32], int w0) {
+  const uint32_t rb = half_base + (uint32_t)row * 128u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t a = rb + ((uint32_t)(j ^ (row & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[w0 + 4 * j]), "r"(w[w0 + 4 * j + 1]),
+                 "r"(w[w0 + 4 * j + 2]), "r"(w[w0 + 4 * j + 3])
+                 : "memory");
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + kOffQ, sKV = base + kOffKV, sP = base + kOffP, sBar = base + kOffBar;
+  auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
+  const uint32_t q_full = bar(0), q_empty = bar(1), o_free = bar(2);
+  auto kv_full = [&](int st) { return bar(3 + st); };
+  auto kv_empty = [&](int st) { return bar(5 + st); };
+  auto s_full = [&](int b) { return bar(7 + b); };
+  auto s_free = [&](int b) { return bar(9 + b); };
+  auto p_full = [&](int b) { return bar(11 + b); };
+  auto pv_done = [&](int b) { return bar(13 + b); };
+  const uint32_t sSlot = bar(15);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + (sSlot - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (sSlot - base) + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = p.R * p.R * p.heads * p.qtiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(o_free, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(kv_full(i), 1);
+      mbar_init(kv_empty(i), 1);
+      mbar_init(s_full(i), 1);
+      mbar_init(s_free(i), 4);
+      mbar_init(p_full(i), 4);
+      mbar_init(pv_done(i), 1);
+    }
+    mbar_init(bar(16), 1);   // every MMA issued has completed (before TMEM is freed)
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc<1>(sSlot, 512);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;   // S buffers at columns 0 and 128, O at 256
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t g = 0;
+      int n = 0;
+      bool ok = true;
+      for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++n) {
+        const Item it = decode(p, L);
+        const int col = it.h * kHeadDim;
+        if (!mbar_wait(q_empty, (uint32_t)(n & 1) ^ 1u, abort_flag, kWaitNs)) break;
+        mbar_arrive_expect_tx(q_full, kTileBytes);
+        tma_load_2d(sQ, &p.tmQ[it.r], q_full, col, it.q0);
+        tma_load_2d(sQ + kHalf, &p.tmQ[it.r], q_full, col + 64, it.q0);
+        for (int j = 0; j < it.nkb; ++j, ++g) {
+          const int st = (int)(g & 1u);
+          if (!mbar_wait(kv_empty(st), ((g >> 1) & 1u) ^ 1u, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sk = sKV + (uint32_t)st * 2u * kTileBytes, sv = sk + kTileBytes;
+          mbar_arrive_expect_tx(kv_full(st), 2u * kTileBytes);
+          tma_load_2d(sk, &p.tmK[it.r], kv_full(st), col, j * kTile);
+          tma_load_2d(sk + kHalf, &p.tmK[it.r], kv_full(st), col + 64, j * kTile);
+          // V as the MN-major B operand: per 64 keys, two 64-column boxes.
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+            for (int dh = 0; dh < 2; ++dh)
+              tma_load_2d(sv + (uint32_t)kh * kHalf + (uint32_t)dh * (kHalf / 2), &p.tmV[it.r], kv_full(st),
+                          col + dh * 64, j * kTile + kh * 64);
+        }
+      }
+      // Loads still in flight land before the CTA may exit.
+      volatile int never = 0;
+      const uint32_t first = g > 2u ? g - 2u : 0u;
+      for (uint32_t k = first; k < g; ++k) mbar_wait(kv_full((int)(k & 1u)), (k >> 1) & 1u, &never, 100000000ull);
+      if (n > 0) mbar_wait(q_full, (uint32_t)((n - 1) & 1), &never, 100000000ull);
+      if (*abort_flag) record_error(p.status, FO_ERR_TIMEOUT, -1, -1, 0);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t g = 0;
+      int n = 0;
+      bool ok = true;
+      auto pv = [&](uint32_t gp, bool first) -> bool {
+        const int b = (int)(gp & 1u);
+        if (!mbar_wait(p_full(b), (gp >> 1) & 1u, abort_flag, kWaitNs)) return false;
+        if (first && !mbar_wait(o_free, (uint32_t)(n & 1) ^ 1u, abort_flag, kWaitNs)) return false;
+        tc_fence_after();
+        const uint32_t pa = sP + (uint32_t)b * kTileBytes;
+        const uint32_t vb = sKV + (uint32_t)b * 2u * kTileBytes + kTileBytes;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+          const uint64_t ad = smem_desc_sw128(pa + kh * kHalf + kk * 32u, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(vb + kh * kHalf + kk * 2048u, kHalf / 2, 1024);
+          tc_mma<1, false>(tmem + 256u, ad, bd, idesc(true), (!first || k > 0) ? 1u : 0u);
+        }
+        tc_commit<1>(pv_done(b));
+        tc_commit<1>(kv_empty(b));
+        return true;
+      };
+      for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++n) {
+        const Item it = decode(p, L);
+        if (!mbar_wait(q_full, (uint32_t)(n & 1), abort_flag, kWaitNs)) break;
+        tc_fence_after();
+        for (int j = 0; j < it.nkb; ++j, ++g) {
+          const int st = (int)(g & 1u);
+          const uint32_t ph = (g >> 1) & 1u;
+          if (!mbar_wait(kv_full(st), ph, abort_flag, kWaitNs) || !mbar_wait(s_free(st), ph ^ 1u, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kb = sKV + (uint32_t)st * 2u * kTileBytes;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+            const uint64_t ad = smem_desc_sw128(sQ + kh * kHalf + kk * 32u, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kb + kh * kHalf + kk * 32u, 16, 1024);
+            tc_mma<1, false>(tmem + (uint32_t)st * 128u, ad, bd, idesc(false), k > 0 ? 1u : 0u);
+          }
+          tc_commit<1>(s_full(st));
+          if (j == it.nkb - 1) tc_commit<1>(q_empty);
+          if (j > 0 && !pv(g - 1, j == 1)) {
+            ok = false;
+            break;
+          }
+        }
+        if (ok && !pv(g - 1, it.nkb == 1)) ok = false;
+      }
+      // Every issued MMA completes before TMEM is released.
+      tc_commit<1>(bar(16));
+      volatile int never = 0;
+      mbar_wait(bar(16), 0, &never, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int row = q * 32 + lane;          // query row within the tile
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    uint32_t g = 0;
+    int n = 0;
+    for (int L = blockIdx.x; L < total; L += gridDim.x, ++n) {
+      const Item it = decode(p, L);
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < it.nkb; ++j, ++g) {
+        const int b = (int)(g & 1u);
+        const uint32_t ph = (g >> 1) & 1u;
+        if (!mbar_wait(s_full(b), ph, abort_flag, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float x[128];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + (uint32_t)b * 128u + (uint32_t)cc * 32u, v);
+          tmem_ld_wait();
+          reg_fence(v);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) x[cc * 32 + t] = __uint_as_float(v[t]) * p.scale_log2;
+        }
+        // The scores are in registers: the buffer may take the next block.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free(b));
+        const bool diag = p.causal && j == it.nkb - 1;   // the block holding this tile's own keys
+        float mx = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < 128; ++t) {
+          if (diag && t > row) x[t] = -INFINITY;
+          mx = fmaxf(mx, x[t]);
+        }
+        const float m_use = (j == 0 || mx > m + kRescaleLog2) ? fmaxf(m, mx) : m;
+        const float alpha = j == 0 ? 0.f : exp2f(m - m_use);
+        // P in bf16 into buffer b once the weighted sum two blocks back has
+        // read it (and this warp's last output store has read it).
+        if (!mbar_wait(pv_done(b), ph ^ 1u, abort_flag, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        float sum = 0.f;
+        const uint32_t pb = sP + (uint32_t)b * kTileBytes;
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh) {
+          uint32_t w[32];
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            const float e0 = exp2f(x[kh * 64 + 2 * t] - m_use), e1 = exp2f(x[kh * 64 + 2 * t + 1] - m_use);
+            __nv_bfloat162 h = __floats2bfloat162_rn(e0, e1);
+            // The sum takes the rounded weights the weighted sum uses, so the
+            // output stays a convex combination of the rows of V.
+            sum += __low2float(h) + __high2float(h);
+            w[t] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          store_row_half(pb + (uint32_t)kh * kHalf, row, w, 0);
+        }
+        l = l * alpha + sum;
+        m = m_use;
+        fence_proxy_async_smem();
+        // Rescale this row of O when its maximum moved (after the weighted
+        // sum of the previous block has completed).
+        const bool need = j > 0 && alpha < 1.f;
+        if (__any_sync(0xffffffffu, need)) {
+          const uint32_t gq = g - 1u;
+          if (!mbar_wait(pv_done((int)(gq & 1u)), (gq >> 1) & 1u, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float a = need ? alpha : 1.f;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + 256u + (uint32_t)cc * 32u, v);
+            tmem_ld_wait();
+            reg_fence(v);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a);
+            tmem_st32(tmem + lane_off + 256u + (uint32_t)cc * 32u, v);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(b));
+      }
+      if (!ok) break;
+      // The item's output: O / l in bf16, staged in this warp's own rows of
+      // the P buffer the last weighted sum read (the rows this warp alone
+      // writes), then TMA-stored, 64 columns x 32 rows per op.
+      const uint32_t gl = g - 1u;
+      if (!mbar_wait(pv_done((int)(gl & 1u)), (gl >> 1) & 1u, abort_flag, kWaitNs)) break;
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const uint32_t stage = sP + (uint32_t)(gl & 1u) * kTileBytes + (uint32_t)q * 4096u;
+#pragma unroll
+      for (int dh = 0; dh < 2; ++dh) {
+        uint32_t w[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + 256u + (uint32_t)(dh * 64 + cc * 32), v);
+          tmem_ld_wait();
+          reg_fence(v);
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            w[cc * 16 + t] = pack_bf16(__uint_as_float(v[2 * t]) * inv, __uint_as_float(v[2 * t + 1]) * inv);
+        }
+        // 32 rows x 128 B per box, rows indexed by lane: the half dh of the
+        // P buffer, this warp's 32 rows.
+        const uint32_t rb = stage + (uint32_t)dh * kHalf + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + ((uint32_t)(j ^ (lane & 7)) << 4)),
+                       "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
+                       : "memory");
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(o_free);
+        tma_store_2d(&p.tmO[it.r], stage, it.h * kHeadDim, it.q0 + q * 32);
+        tma_store_2d(&p.tmO[it.r], stage + kHalf, it.h * kHeadDim + 64, it.q0 + q * 32);
+        bulk_commit();
+      }
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    __syncwarp();
+    tmem_dealloc<1>(tmem, 512);
+  }
+}
+
+}  // namespace fo_attn
+
+namespace {
+
+bool enc(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_c, uint32_t box_r) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_c, box_r};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" fo_status fo_attn_rs(fo_plan_t p, const void* const* Q, const void* const* K, const void* const* V,
+                                const void* const* Wo, void* const* O, void* const* Y, int32_t heads,
+                                int32_t causal, void* ws, fo_stream_t stream) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (p->d.op != FO_OP_GEMM_RS || p->elem_bytes != 2) return FO_ERR_INVALID_ARG;
+  if (heads < 1 || (causal != 0 && causal != 1)) return FO_ERR_INVALID_ARG;
+  const int R = p->R;
+  const int64_t T = p->d.M, width = (int64_t)heads * fo_attn::kHeadDim;
+  if (p->k_red != width) return FO_ERR_SHAPE;            // the projection reads heads * 128 columns per rank
+  if ((T / R) % fo_attn::kTile) return FO_ERR_SHAPE;      // whole 128-row query tiles per block
+  fo_status st;
+  if ((st = fo_internal_check_ptrs(R, Q)) || (st = fo_internal_check_ptrs(R, K)) ||
+      (st = fo_internal_check_ptrs(R, V)) || (st = fo_internal_check_ptrs(R, Wo)) ||
+      (st = fo_internal_check_ptrs(R, (const void* const*)O)) || (st = fo_internal_check_ptrs(R, (const void* const*)Y)))
+    return st;
+  if ((st = fo_internal_check_device_ptrs(R, Q, stream)) || (st = fo_internal_check_device_ptrs(R, K, stream)) ||
+      (st = fo_internal_check_device_ptrs(R, V, stream)) ||
+      (st = fo_internal_check_device_ptrs(R, (const void* const*)O, stream)))
+    return st;
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return FO_ERR_UNSUPPORTED;
+  static_assert(sizeof(fo_attn::AttnParams) <= 32764, "kernel parameters");
+  fo_attn::AttnParams k;
+  memset(static_cast<void*>(&k), 0, sizeof(k));
+  bool ok = true;
+  for (int r = 0; r < R && ok; ++r) {
+    ok &= enc(&k.tmQ[r], Q[r], (uint64_t)width, (uint64_t)T, 64, 128);
+    ok &= enc(&k.tmK[r], K[r], (uint64_t)width, (uint64_t)T, 64, 128);
+    ok &= enc(&k.tmV[r], V[r], (uint64_t)width, (uint64_t)T, 64, 64);
+    ok &= enc(&k.tmO[r], O[r], (uint64_t)width, (uint64_t)T, 64, 32);
+  }
+  if (!ok) return FO_ERR_CUDA;
+  memcpy(k.table, p->table, sizeof(k.table));
+  memcpy(k.task_r, p->task_r, sizeof(k.task_r));
+  memcpy(k.task_s, p->task_s, sizeof(k.task_s));
+  k.R = R;
+  k.T = (int32_t)T;
+  k.heads = heads;
+  k.causal = causal;
+  k.qtiles = (int32_t)(T / R / fo_attn::kTile);
+  k.scale_log2 = (float)(1.4426950408889634 / sqrt((double)fo_attn::kHeadDim));
+  k.status = static_cast<int32_t*>(ws);
+  const int total = R * R * heads * k.qtiles;
+  const int grid = total < sms ? total : sms;
+  auto kern = fo_attn::fo_attn_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fo_attn::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return FO_ERR_CUDA;
+  }
+  kern<<<grid, fo_attn::kThreads, fo_attn::kSmemBytes, (cudaStream_t)stream>>>(k);
+  if (cudaGetLastError() != cudaSuccess) return FO_ERR_CUDA;
+  if (fo_log_enabled())
+    fprintf(stderr, "[flashoverlap] attention R=%d T=%lld heads=%d causal=%d: %d items on %d CTAs\n", R,
+            (long long)T, heads, causal, total, grid);
+  // The projection's fused GEMM + reduce-scatter of O_r . Wo_r.
+  if ((st = fo_gemm_rs(p, (const void* const*)O, Wo, Y, ws, stream))) return st;
+  p->last_launches = 2;
+  return FO_OK;
+}

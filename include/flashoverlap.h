@@ -312,6 +312,33 @@ fo_status fo_gemm_ar(fo_plan_t plan, const void* const* X, const void* const* W,
 fo_status fo_gemm_a2a(fo_plan_t plan, const void* const* X, const void* const* W,
                       void* const* Y, void* ws, fo_stream_t stream);
 
+/* Query-split attention with the row-parallel output projection
+ * (gist.science "Technical Summary" section 2, "Architectural
+ * Versatility": the attention's scores, softmax and weighted sum are
+ * decomposed to put more compute beside the communication; section 1: the
+ * tensor-parallel projection needs a reduce-scatter).
+ * `plan`: a GEMM_RS plan with M = T tokens, N = H (the projection's output
+ * width) and K = R * heads * 128, bf16 inputs, fp32 or bf16 output.
+ * Rank r holds Q_r, K_r, V_r [T x heads*128] bf16 (its heads, every token;
+ * head h in columns h*128 .. h*128+127) and Wo_r [heads*128 x H] ([H x
+ * heads*128] with FO_W_NK); it receives O_r [T x heads*128] bf16, its
+ * attention output (overwritten; kept for a backward pass), and Y_r
+ * [T/R x H], rows r*T/R .. of sum_r O_r . Wo_r (overwritten).
+ * Per head, O = softmax(Q K^T / sqrt(128) + mask) V over the keys; with
+ * causal = 1 key j is masked for query i when j > i, with 0 nothing is.
+ * The queries split into R blocks of T/R rows; rank r's step s takes block
+ * (r - 1 - s) mod R, so the block that stays on the rank comes last.
+ * Two launches on `stream`: the attention of every (rank, step, head,
+ * 128-query tile) in the plan's task order, then fo_gemm_rs of O_r . Wo_r.
+ * The softmax weights are rounded to bf16 for the tensor cores' weighted
+ * sum, and O once to bf16. Requires heads >= 1 and T/R a multiple of 128;
+ * FO_ERR_SHAPE when K != R * heads * 128 or T/R is not; FO_ERR_INVALID_ARG
+ * for another op, fp32 inputs, heads < 1 or causal not 0 or 1. Device-side
+ * waits are bounded and report through fo_status_query like fo_gemm_rs. */
+fo_status fo_attn_rs(fo_plan_t plan, const void* const* Q, const void* const* K, const void* const* V,
+                     const void* const* Wo, void* const* O, void* const* Y, int32_t heads, int32_t causal,
+                     void* ws, fo_stream_t stream);
+
 /* Data-parallel weight gradient fused with its reduce-scatter:
  * dW_d = sum_r (X_r^T . dY_r)[rows of d], fp32 (gist.science "Technical
  * Summary" section 1: data parallelism needs a reduce-scatter). Same

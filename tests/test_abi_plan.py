@@ -456,3 +456,25 @@ def test_fp32_inputs_take_either_weight_layout():
     for layout in ("kn", "nk"):
         p = B.fo_plan("gemm_rs", 2, 256, 512, 1024, in_dtype="f32", w_layout=layout)
         assert B.fo_plan_table(p) == oracle.rs_schedule(2).tolist()
+
+
+# ------------------------------------------------------------------ query-split attention: host checks
+
+def test_attn_rs_rejects_bad_arguments_on_the_host():
+    fake = [16 * (i + 1) for i in range(2)]
+    p = B.fo_plan("gemm_rs", 2, 512, 256, 2 * 2 * 128)          # T = 512, heads = 2 per rank, H = 256
+    for heads, causal, code in ((0, 0, B.FO_ERR_INVALID_ARG), (2, 2, B.FO_ERR_INVALID_ARG),
+                                (3, 0, B.FO_ERR_SHAPE)):         # K != R * heads * 128
+        with pytest.raises(B.FlashOverlapError) as e:
+            B._check(B.load().fo_attn_rs(p, B._ptr_array(fake), B._ptr_array(fake), B._ptr_array(fake),
+                                         B._ptr_array(fake), B._ptr_array(fake), B._ptr_array(fake), heads, causal,
+                                         4096, 0), "fo_attn_rs")
+        assert e.value.code == code
+    odd = B.fo_plan("gemm_rs", 2, 384, 256, 2 * 128)              # T/R = 192: not whole 128-row tiles
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_attn_rs(odd, fake, fake, fake, fake, fake, fake, 1, False, 4096, stream=0)
+    assert e.value.code == B.FO_ERR_SHAPE
+    ag = B.fo_plan("ag_gemm", 2, 512, 256, 256)
+    with pytest.raises(B.FlashOverlapError) as e:
+        B.fo_attn_rs(ag, fake, fake, fake, fake, fake, fake, 1, False, 4096, stream=0)
+    assert e.value.code == B.FO_ERR_INVALID_ARG

@@ -1,0 +1,159 @@
+"""GPU parity of query-split attention with its row-parallel output
+projection (fo_attn_rs) against the CPU oracle, through the C ABI.
+
+Tolerances. The tensor cores take the softmax weights in bf16 (unit
+roundoff 2^-9) and the attention output O is rounded once to bf16, so O
+differs from the fp64 oracle by about 1e-3 of its rms from the weights and
+up to one bf16 step on elements whose two values round apart. O is held to
+a relative Frobenius error of 4e-3 and, elementwise, to 2e-2 of max(|ref|,
+rms(ref)). The projection is checked separately at the stated GEMM
+tolerances (relative Frobenius 1e-3, elementwise 2e-2) against the oracle's
+reduce-scatter of the O the GPU produced; end to end, Y is held to the same
+4e-3 Frobenius bound as O.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ag_gemm_gb300 import binding as B
+
+pytestmark = pytest.mark.gpu
+
+O_FRO, O_MAX = 4e-3, 2e-2
+FRO_TOL, MAX_TOL = 1e-3, 2e-2
+D = 128
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a GB300"
+    return torch.device("cuda:0")
+
+
+def _np(t):
+    return t.detach().to("cpu").double().numpy()
+
+
+def _inputs(R, T, heads, H, seed, q_scale=1.0, growing_keys=False):
+    g = torch.Generator().manual_seed(seed)
+    bf = torch.bfloat16
+    Q = [(torch.randn(T, heads * D, generator=g) * q_scale).to(bf) for _ in range(R)]
+    K = [torch.randn(T, heads * D, generator=g).to(bf) for _ in range(R)]
+    V = [torch.randn(T, heads * D, generator=g).to(bf) for _ in range(R)]
+    Wo = [(torch.randn(heads * D, H, generator=g) * 0.02).to(bf) for _ in range(R)]
+    if growing_keys:
+        # Scores that grow along the keys: each row's maximum keeps rising
+        # from one 128-key block to the next, so the output must be
+        # rescaled again and again.
+        ramp = torch.linspace(0.0, 6.0, T)[:, None]
+        for r in range(R):
+            Q[r] = (torch.ones(T, heads * D) * 0.5).to(bf)
+            K[r] = (torch.randn(T, heads * D, generator=g) * 0.1 + ramp).to(bf)
+    return Q, K, V, Wo
+
+
+def run_attn(dev, R, T, heads, H, causal, seed=0, out="f32", **kw):
+    Q, K, V, Wo = _inputs(R, T, heads, H, seed, **kw)
+    plan = B.fo_plan("gemm_rs", R, T, H, R * heads * D, out_dtype=out)
+    ws = torch.zeros(B.fo_workspace_size(plan), dtype=torch.uint8, device=dev)
+    dQ, dK, dV, dW = ([t.to(dev) for t in ts] for ts in (Q, K, V, Wo))
+    O = [torch.full((T, heads * D), float("nan"), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    Y = [torch.full((T // R, H), float("nan"), dtype=torch.float32 if out == "f32" else torch.bfloat16,
+                    device=dev) for _ in range(R)]
+    B.fo_attn_rs(plan, dQ, dK, dV, dW, O, Y, heads, causal, ws)
+    code, info = B.fo_status_query(plan, ws)
+    assert code == 0, f"device status {code} {info}"
+    assert B.fo_plan_last_launches(plan) == 2
+    return [_np(t) for t in Q], [_np(t) for t in K], [_np(t) for t in V], [_np(t) for t in Wo], \
+        [_np(o) for o in O], [_np(y) for y in Y]
+
+
+def _check_o(got, ref, what):
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    fro = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    mx = float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), rms)))
+    assert fro <= O_FRO and mx <= O_MAX, f"{what}: rel fro {fro:.3e}, max {mx:.3e}"
+
+
+def _check_all(Q, K, V, Wo, O, Y, heads, causal, out="f32"):
+    R = len(Q)
+    for r in range(R):
+        ref_o = oracle.round_bf16(oracle.attention(Q[r], K[r], V[r], heads, causal))
+        _check_o(O[r], ref_o, f"O rank {r}")
+    # the projection on the O the GPU produced: the GEMM-RS tolerances
+    proj = oracle.gemm_rs(O, Wo)
+    for d in range(R):
+        want = proj[d] if out == "f32" else oracle.round_bf16(proj[d])
+        fro, mx, _ = oracle.rel_errors(Y[d], want)
+        assert fro <= FRO_TOL and mx <= MAX_TOL, f"Y shard {d}: rel fro {fro:.3e}, max {mx:.3e}"
+    # end to end
+    ref = oracle.attn_rs(Q, K, V, Wo, heads, causal, round_o=True)
+    for d in range(R):
+        fro = float(np.linalg.norm(Y[d] - ref[d]) / np.linalg.norm(ref[d]))
+        assert fro <= O_FRO, f"Y shard {d} end to end: rel fro {fro:.3e}"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("R,T,heads,H", [(1, 256, 1, 256), (2, 512, 2, 384), (4, 1024, 1, 512)])
+def test_attn_rs_matches_the_oracle(dev, R, T, heads, H, causal):
+    res = run_attn(dev, R, T, heads, H, causal, seed=R * 10 + heads)
+    _check_all(*res, heads, causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attn_rs_sharp_scores_and_bf16_output(dev, causal):
+    # Queries four times larger: peaked softmax rows; bf16 projection output.
+    res = run_attn(dev, 2, 512, 1, 256, causal, seed=7, out="bf16", q_scale=4.0)
+    _check_all(*res, 1, causal, out="bf16")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attn_rs_growing_maximum_is_rescaled(dev, causal):
+    res = run_attn(dev, 2, 1024, 1, 256, causal, seed=8, growing_keys=True)
+    _check_all(*res, 1, causal)
+
+
+def test_attn_rs_repeats_bit_for_bit(dev):
+    # Two calls in a row on the same buffers give the same bits.
+    R, T, heads, H = 4, 512, 2, 256
+    Q, K, V, Wo = _inputs(R, T, heads, H, seed=3)
+    plan = B.fo_plan("gemm_rs", R, T, H, R * heads * D)
+    ws = torch.zeros(B.fo_workspace_size(plan), dtype=torch.uint8, device=dev)
+    dQ, dK, dV, dW = ([t.to(dev) for t in ts] for ts in (Q, K, V, Wo))
+    outs = []
+    for _ in range(2):
+        O = [torch.empty(T, heads * D, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        Y = [torch.empty(T // R, H, device=dev) for _ in range(R)]
+        B.fo_attn_rs(plan, dQ, dK, dV, dW, O, Y, heads, True, ws)
+        assert B.fo_status_query(plan, ws)[0] == 0
+        outs.append(([o.clone() for o in O], [y.clone() for y in Y]))
+    for r in range(R):
+        assert torch.equal(outs[0][0][r], outs[1][0][r])
+
+
+def test_attn_rs_llama_shape_sampled(dev):
+    # The layer's attention shape: 8192 tokens over R = 8, 4 heads of 128
+    # per rank (32 heads), H = 4096, causal; O checked on sampled query rows
+    # of every head, Y on sampled rows of every shard.
+    R, T, heads, H = 8, 8192, 4, 4096
+    Q, K, V, Wo, O, Y = run_attn(dev, R, T, heads, H, True, seed=11)
+    rng = np.random.default_rng(0)
+    rows = np.sort(np.concatenate([[0, 127, 128, T - 1], rng.choice(T, 12, replace=False)]))
+    for r in (0, R - 1):
+        Qr = Q[r]
+        ref_rows = np.empty((len(rows), heads * D))
+        for h in range(heads):
+            cols = slice(h * D, (h + 1) * D)
+            for i, t in enumerate(rows):
+                s = (Qr[t, cols] @ K[r][: t + 1, cols].T) / np.sqrt(D)
+                w = np.exp(s - s.max())
+                ref_rows[i, cols] = (w / w.sum()) @ V[r][: t + 1, cols]
+        _check_o(O[r][rows], oracle.round_bf16(ref_rows), f"O rank {r}")
+    srows = np.array([0, 1, 511, 1023])
+    for d in range(R):
+        want = oracle.gemm_rs_rows(O, Wo, d, srows)
+        fro, mx, _ = oracle.rel_errors(Y[d][srows], want)
+        assert fro <= FRO_TOL and mx <= MAX_TOL, f"Y shard {d}: rel fro {fro:.3e}, max {mx:.3e}"
