@@ -31,8 +31,8 @@
 //              rescale of the TMEM output row when the maximum grows by more
 //              than 8 in log2 units (a smaller growth keeps the old maximum:
 //              the weights then stay below 2^8 and the final division by the
-//              sum cancels the choice); the sum takes the weights as rounded
-//              to bf16; at the item's end O / sum, bf16, TMA store.
+//              sum cancels the choice); at the item's end O / sum, bf16, TMA
+//              store.
 // Every wait is bounded; a wait that runs out raises the CTA's abort flag and
 // records FO_ERR_TIMEOUT in the workspace status word.
 #include <cudaTypedefs.h>
@@ -114,6 +114,14 @@ __device__ __forceinline__ void store_row_half(uint32_t half_base, int row, cons
                  "r"(w[w0 + 4 * j + 2]), "r"(w[w0 + 4 * j + 3])
                  : "memory");
   }
+}
+
+// 2^x by the multi-function unit's approximate base-2 exponential
+// (PTX ex2.approx.ftz.f32; 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -285,29 +293,34 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
           break;
         }
         tc_fence_after();
-        float x[128];
+        // The row's 128 scores: four TMEM loads, one wait.
+        uint32_t v[4][32];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + (uint32_t)b * 128u + (uint32_t)cc * 32u, v);
-          tmem_ld_wait();
-          reg_fence(v);
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_off + (uint32_t)b * 128u + (uint32_t)cc * 32u, v[cc]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) x[cc * 32 + t] = __uint_as_float(v[t]) * p.scale_log2;
-        }
+        for (int cc = 0; cc < 4; ++cc) reg_fence(v[cc]);
         // The scores are in registers: the buffer may take the next block.
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free(b));
-        const bool diag = p.causal && j == it.nkb - 1;   // the block holding this tile's own keys
+        if (p.causal && j == it.nkb - 1) {
+          // The block holding this tile's own keys: key t of the block is
+          // query t of the tile, so the row sees keys 0..row.
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+              if (cc * 32 + t > row) v[cc][t] = __float_as_uint(-INFINITY);
+        }
         float mx = -INFINITY;
 #pragma unroll
-        for (int t = 0; t < 128; ++t) {
-          if (diag && t > row) x[t] = -INFINITY;
-          mx = fmaxf(mx, x[t]);
-        }
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(v[cc][t]));
+        mx *= p.scale_log2;   // log2 units (the scale is positive, so the maximum commutes)
         const float m_use = (j == 0 || mx > m + kRescaleLog2) ? fmaxf(m, mx) : m;
-        const float alpha = j == 0 ? 0.f : exp2f(m - m_use);
+        const float alpha = j == 0 ? 0.f : ex2_approx(m - m_use);
         // P in bf16 into buffer b once the weighted sum two blocks back has
         // read it (and this warp's last output store has read it).
         if (!mbar_wait(pv_done(b), ph ^ 1u, abort_flag, kWaitNs)) {
@@ -318,17 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         __syncwarp();
         float sum = 0.f;
         const uint32_t pb = sP + (uint32_t)b * kTileBytes;
+        const float scl = p.scale_log2, neg = -m_use;
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh) {
           uint32_t w[32];
 #pragma unroll
           for (int t = 0; t < 32; ++t) {
-            const float e0 = exp2f(x[kh * 64 + 2 * t] - m_use), e1 = exp2f(x[kh * 64 + 2 * t + 1] - m_use);
-            __nv_bfloat162 h = __floats2bfloat162_rn(e0, e1);
-            // The sum takes the rounded weights the weighted sum uses, so the
-            // output stays a convex combination of the rows of V.
-            sum += __low2float(h) + __high2float(h);
-            w[t] = *reinterpret_cast<uint32_t*>(&h);
+            const int c0 = kh * 64 + 2 * t;
+            const float e0 = ex2_approx(fmaf(__uint_as_float(v[c0 >> 5][c0 & 31]), scl, neg));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(v[(c0 + 1) >> 5][(c0 + 1) & 31]), scl, neg));
+            sum += e0 + e1;
+            w[t] = pack_bf16(e0, e1);
           }
           store_row_half(pb + (uint32_t)kh * kHalf, row, w, 0);
         }

@@ -14,7 +14,8 @@ resident in HBM; together they exceed L2, so no L2 flush runs between steps.
 The JSON line reports whole-job TFLOP/s, the roofline fraction of the fused
 kernel against the measured bf16 dense peak, short timed loops of the other
 fused ops (all-gather QKV projection, DP gradient, all-to-all projection,
-the TP-SP layer's forward and backward) on the same device, the same metric end to end with
+query-split attention with its projection, the TP-SP layer's forward and
+backward) on the same device, the same metric end to end with
 host buffers (host->device inputs and device->host outputs inside the timed
 region), the CPU oracle timed on a bounded sample, and, next to them, the
 pure-GEMM control, the unfused baseline (our GEMM + a separate reduce kernel),
@@ -434,6 +435,8 @@ def run_ours(args):
 
     if args.workload == LAYER_WORKLOAD:
         return run_layer(args, dev, world, rank)
+    if args.workload == ATTN_WORKLOAD:
+        return run_attn(args, dev, world, rank)
     w = WORKLOADS[args.workload]
     if w.op != "gemm_rs":
         return run_other_op(args, w, dev, world, rank)
@@ -576,6 +579,38 @@ def _op_setup(B, w, dev):
     return inp, A, Bm, Y, plan, ws, launch
 
 
+ATTN_WORKLOAD = "attn_rs_causal_r8_t8192_heads32_h4096"
+
+
+def _attn_setup(B, dev, R=8, T=8192, heads=4, H=4096, causal=True, seed=12):
+    """Query-split attention + output projection at the Llama-like layer's
+    attention shape: 8192 tokens over R = 8 ranks, 4 heads of 128 per rank
+    (32 heads), H = 4096; Q, K, V ~ N(0, 1), Wo ~ N(0, 0.02), bf16."""
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    w = heads * 128
+
+    def draw(shape, std):
+        return (torch.randn(shape, generator=g) * std).to(torch.bfloat16).to(dev)
+
+    Q = [draw((T, w), 1.0) for _ in range(R)]
+    K = [draw((T, w), 1.0) for _ in range(R)]
+    V = [draw((T, w), 1.0) for _ in range(R)]
+    Wo = [draw((w, H), 0.02) for _ in range(R)]
+    O = [torch.empty(T, w, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    Y = [torch.empty(T // R, H, dtype=torch.float32, device=dev) for _ in range(R)]
+    plan = B.fo_plan("gemm_rs", R, T, H, R * w)
+    ws = torch.zeros(B.fo_workspace_size(plan), dtype=torch.uint8, device=dev)
+    pplan = B.fo_plan("gemm_rs", R, T, H, R * w)
+    pws = torch.zeros(B.fo_workspace_size(pplan), dtype=torch.uint8, device=dev)
+    attn_flops = R * heads * 2.0 * 2.0 * T * T * 128 * (0.5 if causal else 1.0)
+    proj_flops = 2.0 * T * H * R * w
+    return {"plan": plan, "ws": ws, "attn_flops": attn_flops, "proj_flops": proj_flops,
+            "flops": attn_flops + proj_flops,
+            "call": lambda s: B.fo_attn_rs(plan, Q, K, V, Wo, O, Y, heads, causal, ws, s),
+            "proj": lambda s: B.fo_gemm_rs(pplan, O, Wo, Y, pws, s)}
+
+
 def measure_other_workloads(B, dev, stream, iters=20):
     """Short timed loops of the all-gather GEMM (QKV, R = 4), the DP
     gradient (R = 8) and the TP-SP layer (R = 8, forward + backward), on the
@@ -616,6 +651,27 @@ def measure_other_workloads(B, dev, stream, iters=20):
             out[name].update(a2a_baselines(B, plan, A, Bm, Y, stream, dev, w.flops(), ms))
         del inp, A, Bm, Y, ws
         torch.cuda.empty_cache()
+    # Query-split attention with its output projection (causal, the layer's
+    # attention shape): the whole call, and the projection alone, so the
+    # attention launch's time is their difference.
+    a = _attn_setup(B, dev)
+    for _ in range(3):
+        a["call"](stream)
+    t_all = _time(lambda: a["call"](stream), stream, iters=10)
+    t_proj = _time(lambda: a["proj"](stream), stream, iters=10)
+    code, info = B.fo_status_query(a["plan"], a["ws"], stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} {info} (attention)")
+    t_attn = t_all - t_proj
+    out[ATTN_WORKLOAD] = {"ms": t_all, "tflops": a["flops"] / t_all / 1e9,
+                          "frac_of_burst_peak": a["flops"] / t_all / 1e9 / burst,
+                          "attention_ms": t_attn, "attention_tflops": a["attn_flops"] / t_attn / 1e9,
+                          "attention_frac_of_burst_peak": a["attn_flops"] / t_attn / 1e9 / burst,
+                          "projection_ms": t_proj, "projection_tflops": a["proj_flops"] / t_proj / 1e9,
+                          "launches": 2, "flops": a["flops"],
+                          "flops_note": "causal attention counts the lower triangle: 2 x 2 x T x T x 128 / 2 per head"}
+    del a
+    torch.cuda.empty_cache()
     shape = LayerShape(R=8, T=8192, H=4096, F=14336)
     L = TpspLayerProjections(shape, device=dev, seed=4)
     for _ in range(3):
@@ -746,6 +802,60 @@ def run_other_op(args, w, dev, world, rank):
         tf, desc = oracle_sample(w, oracle_inputs(w))
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                                 "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+def run_attn(args, dev, world, rank):
+    """One step = one fo_attn_rs call: query-split causal attention of 32
+    heads over 8192 tokens (R = 8), then the fused output projection +
+    reduce-scatter (two launches)."""
+    import torch
+    import torch.distributed as dist
+
+    from ag_gemm_gb300 import binding as B
+    a = _attn_setup(B, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        a["call"](stream)
+    steps = max(1, min(args.steps, 500))
+    with ClockSampler(_smi_id(dev)) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        clk.mark("t0")
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            a["call"](stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark("t1")
+    code, info = B.fo_status_query(a["plan"], a["ws"], stream)
+    if code != 0:
+        raise RuntimeError(f"device status {code} {info}")
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev) / steps
+    peaks, peak_src = load_peaks()
+    sustained = ms * steps >= 250.0
+    peak = float(peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"])
+    value = world * a["flops"] / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": ATTN_WORKLOAD, "R": 8, "tokens": 8192, "heads": 32, "head_dim": 128,
+                   "hidden": 4096, "causal": True,
+                   "step": "query-split attention + fused output projection and reduce-scatter (2 launches)",
+                   "l2": "no flush: 470 MB of operands and outputs per step"},
+        "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / world / peak, "traffic": None,
+                     "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)") + ", " + peak_src},
+        "gpu_launches": 2 * steps,
+        "clocks": clk.summary(),
+        "flops_per_step": a["flops"],
+    }
     if rank == 0:
         print(json.dumps(line))
     return 0
