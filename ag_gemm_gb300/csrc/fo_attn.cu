@@ -21,7 +21,7 @@
 //
 // fo_attn_kernel, one CTA per SM, persistent over work items:
 //   warp 0     TMA producer: the item's Q tile (128 x 128) once, then K and
-//              V blocks of 128 keys into a two-stage ring;
+//              V blocks of 128 keys into two-stage rings, K one block ahead;
 //   warp 1     TMEM allocation; MMA issue: S_j = Q K_j^T into one of two
 //              TMEM score buffers, then O += P_{j-1} V_{j-1} once the softmax
 //              warps have written P_{j-1}, so S_j overlaps softmax(j-1);
@@ -137,8 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
   const uint32_t sQ = base + kOffQ, sKV = base + kOffKV, sP = base + kOffP, sBar = base + kOffBar;
   auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
   const uint32_t q_full = bar(0), q_empty = bar(1), o_free = bar(2);
-  auto kv_full = [&](int st) { return bar(3 + st); };
-  auto kv_empty = [&](int st) { return bar(5 + st); };
+  auto k_full = [&](int st) { return bar(3 + st); };
+  auto k_empty = [&](int st) { return bar(5 + st); };
+  auto v_full = [&](int st) { return bar(17 + st); };
+  auto v_empty = [&](int st) { return bar(19 + st); };
   auto s_full = [&](int b) { return bar(7 + b); };
   auto s_free = [&](int b) { return bar(9 + b); };
   auto p_full = [&](int b) { return bar(11 + b); };
@@ -155,8 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
     mbar_init(q_empty, 1);
     mbar_init(o_free, 4);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(kv_full(i), 1);
-      mbar_init(kv_empty(i), 1);
+      mbar_init(k_full(i), 1);
+      mbar_init(k_empty(i), 1);
+      mbar_init(v_full(i), 1);
+      mbar_init(v_empty(i), 1);
       mbar_init(s_full(i), 1);
       mbar_init(s_free(i), 4);
       mbar_init(p_full(i), 4);
@@ -180,39 +184,57 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t g = 0;
+      // K blocks run one ahead of V blocks: K_j is free again once the
+      // scores S_j are computed, V_j only once P_j V_j is, so each K load
+      // gets a whole block of lead.
+      uint32_t gk = 0, gv = 0;   // K and V blocks loaded so far (both number the CTA's blocks)
       int n = 0;
       bool ok = true;
+      auto load_k = [&](const Item& it, int j) -> bool {
+        const int st = (int)(gk & 1u);
+        if (!mbar_wait(k_empty(st), ((gk >> 1) & 1u) ^ 1u, abort_flag, kWaitNs)) return false;
+        const uint32_t sk = sKV + (uint32_t)st * 2u * kTileBytes;
+        mbar_arrive_expect_tx(k_full(st), kTileBytes);
+        tma_load_2d(sk, &p.tmK[it.r], k_full(st), it.h * kHeadDim, j * kTile);
+        tma_load_2d(sk + kHalf, &p.tmK[it.r], k_full(st), it.h * kHeadDim + 64, j * kTile);
+        ++gk;
+        return true;
+      };
+      auto load_v = [&](const Item& it, int j) -> bool {
+        const int st = (int)(gv & 1u);
+        if (!mbar_wait(v_empty(st), ((gv >> 1) & 1u) ^ 1u, abort_flag, kWaitNs)) return false;
+        const uint32_t sv = sKV + (uint32_t)st * 2u * kTileBytes + kTileBytes;
+        mbar_arrive_expect_tx(v_full(st), kTileBytes);
+        // V as the MN-major B operand: per 64 keys, two 64-column boxes.
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+          for (int dh = 0; dh < 2; ++dh)
+            tma_load_2d(sv + (uint32_t)kh * kHalf + (uint32_t)dh * (kHalf / 2), &p.tmV[it.r], v_full(st),
+                        it.h * kHeadDim + dh * 64, j * kTile + kh * 64);
+        ++gv;
+        return true;
+      };
       for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++n) {
         const Item it = decode(p, L);
-        const int col = it.h * kHeadDim;
         if (!mbar_wait(q_empty, (uint32_t)(n & 1) ^ 1u, abort_flag, kWaitNs)) break;
         mbar_arrive_expect_tx(q_full, kTileBytes);
-        tma_load_2d(sQ, &p.tmQ[it.r], q_full, col, it.q0);
-        tma_load_2d(sQ + kHalf, &p.tmQ[it.r], q_full, col + 64, it.q0);
-        for (int j = 0; j < it.nkb; ++j, ++g) {
-          const int st = (int)(g & 1u);
-          if (!mbar_wait(kv_empty(st), ((g >> 1) & 1u) ^ 1u, abort_flag, kWaitNs)) {
+        tma_load_2d(sQ, &p.tmQ[it.r], q_full, it.h * kHeadDim, it.q0);
+        tma_load_2d(sQ + kHalf, &p.tmQ[it.r], q_full, it.h * kHeadDim + 64, it.q0);
+        if (!load_k(it, 0)) break;
+        for (int j = 0; j < it.nkb; ++j) {
+          if ((j + 1 < it.nkb && !load_k(it, j + 1)) || !load_v(it, j)) {
             ok = false;
             break;
           }
-          const uint32_t sk = sKV + (uint32_t)st * 2u * kTileBytes, sv = sk + kTileBytes;
-          mbar_arrive_expect_tx(kv_full(st), 2u * kTileBytes);
-          tma_load_2d(sk, &p.tmK[it.r], kv_full(st), col, j * kTile);
-          tma_load_2d(sk + kHalf, &p.tmK[it.r], kv_full(st), col + 64, j * kTile);
-          // V as the MN-major B operand: per 64 keys, two 64-column boxes.
-#pragma unroll
-          for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-            for (int dh = 0; dh < 2; ++dh)
-              tma_load_2d(sv + (uint32_t)kh * kHalf + (uint32_t)dh * (kHalf / 2), &p.tmV[it.r], kv_full(st),
-                          col + dh * 64, j * kTile + kh * 64);
         }
       }
       // Loads still in flight land before the CTA may exit.
       volatile int never = 0;
-      const uint32_t first = g > 2u ? g - 2u : 0u;
-      for (uint32_t k = first; k < g; ++k) mbar_wait(kv_full((int)(k & 1u)), (k >> 1) & 1u, &never, 100000000ull);
+      for (uint32_t k = gk > 2u ? gk - 2u : 0u; k < gk; ++k)
+        mbar_wait(k_full((int)(k & 1u)), (k >> 1) & 1u, &never, 100000000ull);
+      for (uint32_t k = gv > 2u ? gv - 2u : 0u; k < gv; ++k)
+        mbar_wait(v_full((int)(k & 1u)), (k >> 1) & 1u, &never, 100000000ull);
       if (n > 0) mbar_wait(q_full, (uint32_t)((n - 1) & 1), &never, 100000000ull);
       if (*abort_flag) record_error(p.status, FO_ERR_TIMEOUT, -1, -1, 0);
     }
@@ -224,7 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       bool ok = true;
       auto pv = [&](uint32_t gp, bool first) -> bool {
         const int b = (int)(gp & 1u);
-        if (!mbar_wait(p_full(b), (gp >> 1) & 1u, abort_flag, kWaitNs)) return false;
+        if (!mbar_wait(p_full(b), (gp >> 1) & 1u, abort_flag, kWaitNs) ||
+            !mbar_wait(v_full(b), (gp >> 1) & 1u, abort_flag, kWaitNs))
+          return false;
         if (first && !mbar_wait(o_free, (uint32_t)(n & 1) ^ 1u, abort_flag, kWaitNs)) return false;
         tc_fence_after();
         const uint32_t pa = sP + (uint32_t)b * kTileBytes;
@@ -237,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
           tc_mma<1, false>(tmem + 256u, ad, bd, idesc(true), (!first || k > 0) ? 1u : 0u);
         }
         tc_commit<1>(pv_done(b));
-        tc_commit<1>(kv_empty(b));
+        tc_commit<1>(v_empty(b));
         return true;
       };
       for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++n) {
@@ -247,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         for (int j = 0; j < it.nkb; ++j, ++g) {
           const int st = (int)(g & 1u);
           const uint32_t ph = (g >> 1) & 1u;
-          if (!mbar_wait(kv_full(st), ph, abort_flag, kWaitNs) || !mbar_wait(s_free(st), ph ^ 1u, abort_flag, kWaitNs)) {
+          if (!mbar_wait(k_full(st), ph, abort_flag, kWaitNs) || !mbar_wait(s_free(st), ph ^ 1u, abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
@@ -261,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
             tc_mma<1, false>(tmem + (uint32_t)st * 128u, ad, bd, idesc(false), k > 0 ? 1u : 0u);
           }
           tc_commit<1>(s_full(st));
+          tc_commit<1>(k_empty(st));
           if (j == it.nkb - 1) tc_commit<1>(q_empty);
           if (j > 0 && !pv(g - 1, j == 1)) {
             ok = false;
@@ -313,11 +338,17 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
             for (int t = 0; t < 32; ++t)
               if (cc * 32 + t > row) v[cc][t] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // Maximum and (below) sum over eight independent partial chains: one
+        // warp per scheduler has nothing else to hide a serial chain's latency.
+        float mxs[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mxs[a] = -INFINITY;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
-          for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(v[cc][t]));
+          for (int t = 0; t < 32; ++t) mxs[t & 7] = fmaxf(mxs[t & 7], __uint_as_float(v[cc][t]));
+        float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                         fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
         mx *= p.scale_log2;   // log2 units (the scale is positive, so the maximum commutes)
         const float m_use = (j == 0 || mx > m + kRescaleLog2) ? fmaxf(m, mx) : m;
         const float alpha = j == 0 ? 0.f : ex2_approx(m - m_use);
@@ -329,7 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         }
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        float sum = 0.f;
+        float sums[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) sums[a] = 0.f;
         const uint32_t pb = sP + (uint32_t)b * kTileBytes;
         const float scl = p.scale_log2, neg = -m_use;
 #pragma unroll
@@ -340,11 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
             const int c0 = kh * 64 + 2 * t;
             const float e0 = ex2_approx(fmaf(__uint_as_float(v[c0 >> 5][c0 & 31]), scl, neg));
             const float e1 = ex2_approx(fmaf(__uint_as_float(v[(c0 + 1) >> 5][(c0 + 1) & 31]), scl, neg));
-            sum += e0 + e1;
+            sums[t & 7] += e0 + e1;
             w[t] = pack_bf16(e0, e1);
           }
           store_row_half(pb + (uint32_t)kh * kHalf, row, w, 0);
         }
+        const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
         l = l * alpha + sum;
         m = m_use;
         fence_proxy_async_smem();
