@@ -52,13 +52,16 @@ constexpr int kTile = 128;                       // query rows per item, keys pe
 constexpr int kThreads = 192;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;   // 32 KB of bf16
 constexpr uint32_t kHalf = kTileBytes / 2;              // one 64-column half: 128 rows x 128 B
-constexpr int kStages = 2;
-// Shared memory, from a 1024-byte aligned base: Q, two K/V stages, two P
-// buffers, barriers.
+constexpr int kKStages = 3;   // K blocks in flight (each is free again once its scores are computed)
+constexpr int kVStages = 2;   // V blocks in flight (free once their weighted sum is computed)
+// Shared memory, from a 1024-byte aligned base: Q, the K and V rings, one P
+// buffer (P_j is written once the weighted sum of P_{j-1} has completed),
+// barriers.
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + kTileBytes;
-constexpr uint32_t kOffP = kOffKV + kStages * 2 * kTileBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
+constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+constexpr uint32_t kOffP = kOffV + kVStages * kTileBytes;
+constexpr uint32_t kOffBar = kOffP + kTileBytes;
 constexpr int kSmemBytes = 1024 + (int)kOffBar + 256;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -105,7 +108,8 @@ __device__ __forceinline__ Item decode(const AttnParams& p, int L) {
 
 // Row `row` (one per thread) of a 128-row, 64-column bf16 half in the
 // 128B-swizzle layout: 16-byte chunk j of the row sits at chunk j ^ (row % 8).
-__device__ __forceinline__ void store_row_half(uint32_t half_base, int row, const uint32_t (&w)[32], int w0) {
+template <int NW>
+__device__ __forceinline__ void store_row_half(uint32_t half_base, int row, const uint32_t (&w)[NW], int w0) {
   const uint32_t rb = half_base + (uint32_t)row * 128u;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -134,11 +138,11 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + kOffQ, sKV = base + kOffKV, sP = base + kOffP, sBar = base + kOffBar;
+  const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP, sBar = base + kOffBar;
   auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
   const uint32_t q_full = bar(0), q_empty = bar(1), o_free = bar(2);
-  auto k_full = [&](int st) { return bar(3 + st); };
-  auto k_empty = [&](int st) { return bar(5 + st); };
+  auto k_full = [&](int st) { return bar(21 + st); };
+  auto k_empty = [&](int st) { return bar(24 + st); };
   auto v_full = [&](int st) { return bar(17 + st); };
   auto v_empty = [&](int st) { return bar(19 + st); };
   auto s_full = [&](int b) { return bar(7 + b); };
@@ -156,9 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(o_free, 4);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(k_full(i), 1);
       mbar_init(k_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(v_full(i), 1);
       mbar_init(v_empty(i), 1);
       mbar_init(s_full(i), 1);
@@ -191,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       int n = 0;
       bool ok = true;
       auto load_k = [&](const Item& it, int j) -> bool {
-        const int st = (int)(gk & 1u);
-        if (!mbar_wait(k_empty(st), ((gk >> 1) & 1u) ^ 1u, abort_flag, kWaitNs)) return false;
-        const uint32_t sk = sKV + (uint32_t)st * 2u * kTileBytes;
+        const int st = (int)(gk % kKStages);
+        if (!mbar_wait(k_empty(st), ((gk / kKStages) & 1u) ^ 1u, abort_flag, kWaitNs)) return false;
+        const uint32_t sk = sK + (uint32_t)st * kTileBytes;
         mbar_arrive_expect_tx(k_full(st), kTileBytes);
         tma_load_2d(sk, &p.tmK[it.r], k_full(st), it.h * kHeadDim, j * kTile);
         tma_load_2d(sk + kHalf, &p.tmK[it.r], k_full(st), it.h * kHeadDim + 64, j * kTile);
@@ -203,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       auto load_v = [&](const Item& it, int j) -> bool {
         const int st = (int)(gv & 1u);
         if (!mbar_wait(v_empty(st), ((gv >> 1) & 1u) ^ 1u, abort_flag, kWaitNs)) return false;
-        const uint32_t sv = sKV + (uint32_t)st * 2u * kTileBytes + kTileBytes;
+        const uint32_t sv = sV + (uint32_t)st * kTileBytes;
         mbar_arrive_expect_tx(v_full(st), kTileBytes);
         // V as the MN-major B operand: per 64 keys, two 64-column boxes.
 #pragma unroll
@@ -231,8 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       }
       // Loads still in flight land before the CTA may exit.
       volatile int never = 0;
-      for (uint32_t k = gk > 2u ? gk - 2u : 0u; k < gk; ++k)
-        mbar_wait(k_full((int)(k & 1u)), (k >> 1) & 1u, &never, 100000000ull);
+      for (uint32_t k = gk > (uint32_t)kKStages ? gk - kKStages : 0u; k < gk; ++k)
+        mbar_wait(k_full((int)(k % kKStages)), (k / kKStages) & 1u, &never, 100000000ull);
       for (uint32_t k = gv > 2u ? gv - 2u : 0u; k < gv; ++k)
         mbar_wait(v_full((int)(k & 1u)), (k >> 1) & 1u, &never, 100000000ull);
       if (n > 0) mbar_wait(q_full, (uint32_t)((n - 1) & 1), &never, 100000000ull);
@@ -251,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
           return false;
         if (first && !mbar_wait(o_free, (uint32_t)(n & 1) ^ 1u, abort_flag, kWaitNs)) return false;
         tc_fence_after();
-        const uint32_t pa = sP + (uint32_t)b * kTileBytes;
-        const uint32_t vb = sKV + (uint32_t)b * 2u * kTileBytes + kTileBytes;
+        const uint32_t pa = sP;
+        const uint32_t vb = sV + (uint32_t)b * kTileBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
@@ -271,12 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         for (int j = 0; j < it.nkb; ++j, ++g) {
           const int st = (int)(g & 1u);
           const uint32_t ph = (g >> 1) & 1u;
-          if (!mbar_wait(k_full(st), ph, abort_flag, kWaitNs) || !mbar_wait(s_free(st), ph ^ 1u, abort_flag, kWaitNs)) {
+          const int ks = (int)(g % kKStages);
+          if (!mbar_wait(k_full(ks), (g / kKStages) & 1u, abort_flag, kWaitNs) ||
+              !mbar_wait(s_free(st), ph ^ 1u, abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t kb = sKV + (uint32_t)st * 2u * kTileBytes;
+          const uint32_t kb = sK + (uint32_t)ks * kTileBytes;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
             tc_mma<1, false>(tmem + (uint32_t)st * 128u, ad, bd, idesc(false), k > 0 ? 1u : 0u);
           }
           tc_commit<1>(s_full(st));
-          tc_commit<1>(k_empty(st));
+          tc_commit<1>(k_empty(ks));
           if (j == it.nkb - 1) tc_commit<1>(q_empty);
           if (j > 0 && !pv(g - 1, j == 1)) {
             ok = false;
@@ -352,33 +360,34 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         mx *= p.scale_log2;   // log2 units (the scale is positive, so the maximum commutes)
         const float m_use = (j == 0 || mx > m + kRescaleLog2) ? fmaxf(m, mx) : m;
         const float alpha = j == 0 ? 0.f : ex2_approx(m - m_use);
-        // P in bf16 into buffer b once the weighted sum two blocks back has
-        // read it (and this warp's last output store has read it).
-        if (!mbar_wait(pv_done(b), ph ^ 1u, abort_flag, kWaitNs)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
         float sums[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) sums[a] = 0.f;
-        const uint32_t pb = sP + (uint32_t)b * kTileBytes;
         const float scl = p.scale_log2, neg = -m_use;
+        uint32_t w[64];
 #pragma unroll
-        for (int kh = 0; kh < 2; ++kh) {
-          uint32_t w[32];
-#pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const int c0 = kh * 64 + 2 * t;
-            const float e0 = ex2_approx(fmaf(__uint_as_float(v[c0 >> 5][c0 & 31]), scl, neg));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(v[(c0 + 1) >> 5][(c0 + 1) & 31]), scl, neg));
-            sums[t & 7] += e0 + e1;
-            w[t] = pack_bf16(e0, e1);
-          }
-          store_row_half(pb + (uint32_t)kh * kHalf, row, w, 0);
+        for (int t = 0; t < 64; ++t) {
+          const int c0 = 2 * t;
+          const float e0 = ex2_approx(fmaf(__uint_as_float(v[c0 >> 5][c0 & 31]), scl, neg));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(v[(c0 + 1) >> 5][(c0 + 1) & 31]), scl, neg));
+          sums[t & 7] += e0 + e1;
+          w[t] = pack_bf16(e0, e1);
         }
         const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
+        // P_j goes where P_{j-1} was: wait until that weighted sum has
+        // completed (it also settles O for a rescale below), and until this
+        // warp's last output store has read the buffer.
+        if (j > 0) {
+          const uint32_t gq = g - 1u;
+          if (!mbar_wait(pv_done((int)(gq & 1u)), (gq >> 1) & 1u, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+        }
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh) store_row_half(sP + (uint32_t)kh * kHalf, row, w, kh * 32);
         l = l * alpha + sum;
         m = m_use;
         fence_proxy_async_smem();
@@ -386,11 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         // sum of the previous block has completed).
         const bool need = j > 0 && alpha < 1.f;
         if (__any_sync(0xffffffffu, need)) {
-          const uint32_t gq = g - 1u;
-          if (!mbar_wait(pv_done((int)(gq & 1u)), (gq >> 1) & 1u, abort_flag, kWaitNs)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
           const float a = need ? alpha : 1.f;
 #pragma unroll
@@ -417,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       if (!mbar_wait(pv_done((int)(gl & 1u)), (gl >> 1) & 1u, abort_flag, kWaitNs)) break;
       tc_fence_after();
       const float inv = 1.f / l;
-      const uint32_t stage = sP + (uint32_t)(gl & 1u) * kTileBytes + (uint32_t)q * 4096u;
+      const uint32_t stage = sP + (uint32_t)q * 4096u;
 #pragma unroll
       for (int dh = 0; dh < 2; ++dh) {
         uint32_t w[32];
