@@ -62,7 +62,7 @@ constexpr uint32_t kOffK = kOffQ + kTileBytes;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
 constexpr uint32_t kOffP = kOffV + kVStages * kTileBytes;
 constexpr uint32_t kOffBar = kOffP + kTileBytes;
-constexpr int kSmemBytes = 1024 + (int)kOffBar + 256;
+constexpr int kSmemBytes = 1024 + (int)kOffBar + 512;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kRescaleLog2 = 8.0f;
@@ -145,8 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
   auto k_empty = [&](int st) { return bar(24 + st); };
   auto v_full = [&](int st) { return bar(17 + st); };
   auto v_empty = [&](int st) { return bar(19 + st); };
-  auto s_full = [&](int b) { return bar(7 + b); };
-  auto s_free = [&](int b) { return bar(9 + b); };
+  auto s_full = [&](int b) { return bar(27 + b); };   // three TMEM score buffers
+  auto s_free = [&](int b) { return bar(30 + b); };
   auto p_full = [&](int b) { return bar(11 + b); };
   auto pv_done = [&](int b) { return bar(13 + b); };
   const uint32_t sSlot = bar(15);
@@ -169,6 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       mbar_init(v_empty(i), 1);
       mbar_init(s_full(i), 1);
       mbar_init(s_free(i), 4);
+      if (i == 1) {
+        mbar_init(s_full(2), 1);
+        mbar_init(s_free(2), 4);
+      }
       mbar_init(p_full(i), 4);
       mbar_init(pv_done(i), 1);
     }
@@ -185,14 +189,14 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;   // S buffers at columns 0 and 128, O at 256
+  const uint32_t tmem = *tmem_slot;   // S buffers at columns 0, 128 and 256, O at 384
+  constexpr uint32_t kOCol = 384;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // K blocks run one ahead of V blocks: K_j is free again once the
-      // scores S_j are computed, V_j only once P_j V_j is, so each K load
-      // gets a whole block of lead.
+      // K blocks run two ahead of V blocks, as the scores do: K_j is free
+      // again once S_j is computed, V_j only once P_j V_j is.
       uint32_t gk = 0, gv = 0;   // K and V blocks loaded so far (both number the CTA's blocks)
       int n = 0;
       bool ok = true;
@@ -227,9 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         mbar_arrive_expect_tx(q_full, kTileBytes);
         tma_load_2d(sQ, &p.tmQ[it.r], q_full, it.h * kHeadDim, it.q0);
         tma_load_2d(sQ + kHalf, &p.tmQ[it.r], q_full, it.h * kHeadDim + 64, it.q0);
-        if (!load_k(it, 0)) break;
+        if (!load_k(it, 0) || (it.nkb > 1 && !load_k(it, 1))) break;
         for (int j = 0; j < it.nkb; ++j) {
-          if ((j + 1 < it.nkb && !load_k(it, j + 1)) || !load_v(it, j)) {
+          if ((j + 2 < it.nkb && !load_k(it, j + 2)) || !load_v(it, j)) {
             ok = false;
             break;
           }
@@ -264,43 +268,48 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
           const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
           const uint64_t ad = smem_desc_sw128(pa + kh * kHalf + kk * 32u, 16, 1024);
           const uint64_t bd = smem_desc_sw128(vb + kh * kHalf + kk * 2048u, kHalf / 2, 1024);
-          tc_mma<1, false>(tmem + 256u, ad, bd, idesc(true), (!first || k > 0) ? 1u : 0u);
+          tc_mma<1, false>(tmem + kOCol, ad, bd, idesc(true), (!first || k > 0) ? 1u : 0u);
         }
         tc_commit<1>(pv_done(b));
         tc_commit<1>(v_empty(b));
+        return true;
+      };
+      // S_{j+2} is issued before P_j V_j, so two score blocks wait in the
+      // pipe while the softmax warps work on block j.
+      auto issue_s = [&](uint32_t gs) -> bool {
+        const int sb = (int)(gs % 3u);   // score buffer and K stage
+        const uint32_t ph = (gs / 3u) & 1u;
+        if (!mbar_wait(k_full(sb), ph, abort_flag, kWaitNs) || !mbar_wait(s_free(sb), ph ^ 1u, abort_flag, kWaitNs))
+          return false;
+        tc_fence_after();
+        const uint32_t kb = sK + (uint32_t)sb * kTileBytes;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+          const uint64_t ad = smem_desc_sw128(sQ + kh * kHalf + kk * 32u, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(kb + kh * kHalf + kk * 32u, 16, 1024);
+          tc_mma<1, false>(tmem + (uint32_t)sb * 128u, ad, bd, idesc(false), k > 0 ? 1u : 0u);
+        }
+        tc_commit<1>(s_full(sb));
+        tc_commit<1>(k_empty(sb));
         return true;
       };
       for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++n) {
         const Item it = decode(p, L);
         if (!mbar_wait(q_full, (uint32_t)(n & 1), abort_flag, kWaitNs)) break;
         tc_fence_after();
-        for (int j = 0; j < it.nkb; ++j, ++g) {
-          const int st = (int)(g & 1u);
-          const uint32_t ph = (g >> 1) & 1u;
-          const int ks = (int)(g % kKStages);
-          if (!mbar_wait(k_full(ks), (g / kKStages) & 1u, abort_flag, kWaitNs) ||
-              !mbar_wait(s_free(st), ph ^ 1u, abort_flag, kWaitNs)) {
-            ok = false;
-            break;
+        const uint32_t g0 = g;
+        const int ahead = it.nkb < 2 ? it.nkb : 2;
+        for (int j = 0; j < ahead && ok; ++j) ok = issue_s(g0 + (uint32_t)j);
+        if (ok && it.nkb <= 2) tc_commit<1>(q_empty);   // every score block of the item issued
+        for (int j = 0; j < it.nkb && ok; ++j) {
+          if (j + 2 < it.nkb) {
+            ok = issue_s(g0 + (uint32_t)j + 2u);
+            if (ok && j + 3 == it.nkb) tc_commit<1>(q_empty);
           }
-          tc_fence_after();
-          const uint32_t kb = sK + (uint32_t)ks * kTileBytes;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
-            const uint64_t ad = smem_desc_sw128(sQ + kh * kHalf + kk * 32u, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kb + kh * kHalf + kk * 32u, 16, 1024);
-            tc_mma<1, false>(tmem + (uint32_t)st * 128u, ad, bd, idesc(false), k > 0 ? 1u : 0u);
-          }
-          tc_commit<1>(s_full(st));
-          tc_commit<1>(k_empty(ks));
-          if (j == it.nkb - 1) tc_commit<1>(q_empty);
-          if (j > 0 && !pv(g - 1, j == 1)) {
-            ok = false;
-            break;
-          }
+          if (ok) ok = pv(g0 + (uint32_t)j, j == 0);
         }
-        if (ok && !pv(g - 1, it.nkb == 1)) ok = false;
+        g = g0 + (uint32_t)it.nkb;
       }
       // Every issued MMA completes before TMEM is released.
       tc_commit<1>(bar(16));
@@ -319,9 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < it.nkb; ++j, ++g) {
-        const int b = (int)(g & 1u);
-        const uint32_t ph = (g >> 1) & 1u;
-        if (!mbar_wait(s_full(b), ph, abort_flag, kWaitNs)) {
+        const int b = (int)(g & 1u);      // P / weighted-sum barriers
+        const int sb = (int)(g % 3u);     // score buffer
+        if (!mbar_wait(s_full(sb), (g / 3u) & 1u, abort_flag, kWaitNs)) {
           ok = false;
           break;
         }
@@ -329,14 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         // The row's 128 scores: four TMEM loads, one wait.
         uint32_t v[4][32];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_off + (uint32_t)b * 128u + (uint32_t)cc * 32u, v[cc]);
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_off + (uint32_t)sb * 128u + (uint32_t)cc * 32u, v[cc]);
         tmem_ld_wait();
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) reg_fence(v[cc]);
         // The scores are in registers: the buffer may take the next block.
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(s_free(b));
+        if (lane == 0) mbar_arrive(s_free(sb));
         if (p.causal && j == it.nkb - 1) {
           // The block holding this tile's own keys: key t of the block is
           // query t of the tile, so the row sees keys 0..row.
@@ -400,12 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t v[32];
-            tmem_ld32(tmem + lane_off + 256u + (uint32_t)cc * 32u, v);
+            tmem_ld32(tmem + lane_off + kOCol + (uint32_t)cc * 32u, v);
             tmem_ld_wait();
             reg_fence(v);
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a);
-            tmem_st32(tmem + lane_off + 256u + (uint32_t)cc * 32u, v);
+            tmem_st32(tmem + lane_off + kOCol + (uint32_t)cc * 32u, v);
           }
           tmem_st_wait();
         }
@@ -428,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_off + 256u + (uint32_t)(dh * 64 + cc * 32), v);
+          tmem_ld32(tmem + lane_off + kOCol + (uint32_t)(dh * 64 + cc * 32), v);
           tmem_ld_wait();
           reg_fence(v);
 #pragma unroll
