@@ -128,6 +128,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// D[tmem] (+)= A[tmem] x B[smem]: the A operand read from tensor memory
+// (128 lanes = 128 rows, two 16-bit elements per 32-bit column).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -168,10 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       mbar_init(v_full(i), 1);
       mbar_init(v_empty(i), 1);
       mbar_init(s_full(i), 1);
-      mbar_init(s_free(i), 4);
+      mbar_init(s_free(i), 1);
       if (i == 1) {
         mbar_init(s_full(2), 1);
-        mbar_init(s_free(2), 4);
+        mbar_init(s_free(2), 1);
       }
       mbar_init(p_full(i), 4);
       mbar_init(pv_done(i), 1);
@@ -261,21 +272,24 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
           return false;
         if (first && !mbar_wait(o_free, (uint32_t)(n & 1) ^ 1u, abort_flag, kWaitNs)) return false;
         tc_fence_after();
-        const uint32_t pa = sP;
+        // A = P_j from TMEM: the first 64 columns of its score buffer, row i
+        // in lane i, two bf16 weights per column; 8 columns per 16 keys.
+        const uint32_t pa = tmem + (gp % 3u) * 128u;
         const uint32_t vb = sV + (uint32_t)b * kTileBytes;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
-          const uint64_t ad = smem_desc_sw128(pa + kh * kHalf + kk * 32u, 16, 1024);
           const uint64_t bd = smem_desc_sw128(vb + kh * kHalf + kk * 2048u, kHalf / 2, 1024);
-          tc_mma<1, false>(tmem + kOCol, ad, bd, idesc(true), (!first || k > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + kOCol, pa + (uint32_t)k * 8u, bd, idesc(true), (!first || k > 0) ? 1u : 0u);
         }
         tc_commit<1>(pv_done(b));
         tc_commit<1>(v_empty(b));
+        tc_commit<1>(s_free(gp % 3u));   // P_j read: the buffer may take scores again
         return true;
       };
-      // S_{j+2} is issued before P_j V_j, so two score blocks wait in the
-      // pipe while the softmax warps work on block j.
+      // S_{j+1} is issued before P_j V_j, so a score block waits in the pipe
+      // while the softmax warps work on block j. Its buffer last held P_{j-2},
+      // whose weighted sum completed before P_{j-1} could be written.
       auto issue_s = [&](uint32_t gs) -> bool {
         const int sb = (int)(gs % 3u);   // score buffer and K stage
         const uint32_t ph = (gs / 3u) & 1u;
@@ -299,13 +313,12 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         if (!mbar_wait(q_full, (uint32_t)(n & 1), abort_flag, kWaitNs)) break;
         tc_fence_after();
         const uint32_t g0 = g;
-        const int ahead = it.nkb < 2 ? it.nkb : 2;
-        for (int j = 0; j < ahead && ok; ++j) ok = issue_s(g0 + (uint32_t)j);
-        if (ok && it.nkb <= 2) tc_commit<1>(q_empty);   // every score block of the item issued
+        ok = issue_s(g0);
+        if (ok && it.nkb == 1) tc_commit<1>(q_empty);   // every score block of the item issued
         for (int j = 0; j < it.nkb && ok; ++j) {
-          if (j + 2 < it.nkb) {
-            ok = issue_s(g0 + (uint32_t)j + 2u);
-            if (ok && j + 3 == it.nkb) tc_commit<1>(q_empty);
+          if (j + 1 < it.nkb) {
+            ok = issue_s(g0 + (uint32_t)j + 1u);
+            if (ok && j + 2 == it.nkb) tc_commit<1>(q_empty);
           }
           if (ok) ok = pv(g0 + (uint32_t)j, j == 0);
         }
@@ -342,10 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         tmem_ld_wait();
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) reg_fence(v[cc]);
-        // The scores are in registers: the buffer may take the next block.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free(sb));
         if (p.causal && j == it.nkb - 1) {
           // The block holding this tile's own keys: key t of the block is
           // query t of the tile, so the row sees keys 0..row.
@@ -373,37 +382,31 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
 #pragma unroll
         for (int a = 0; a < 8; ++a) sums[a] = 0.f;
         const float scl = p.scale_log2, neg = -m_use;
-        uint32_t w[64];
+        uint32_t w[2][32];
 #pragma unroll
         for (int t = 0; t < 64; ++t) {
           const int c0 = 2 * t;
           const float e0 = ex2_approx(fmaf(__uint_as_float(v[c0 >> 5][c0 & 31]), scl, neg));
           const float e1 = ex2_approx(fmaf(__uint_as_float(v[(c0 + 1) >> 5][(c0 + 1) & 31]), scl, neg));
           sums[t & 7] += e0 + e1;
-          w[t] = pack_bf16(e0, e1);
+          w[t >> 5][t & 31] = pack_bf16(e0, e1);
         }
         const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
-        // P_j goes where P_{j-1} was: wait until that weighted sum has
-        // completed (it also settles O for a rescale below), and until this
-        // warp's last output store has read the buffer.
-        if (j > 0) {
+        // P_j in bf16 over the first 64 columns of its own score buffer
+        // (the scores are in registers now), the A operand of P_j V_j.
+        tmem_st32(tmem + lane_off + (uint32_t)sb * 128u, w[0]);
+        tmem_st32(tmem + lane_off + (uint32_t)sb * 128u + 32u, w[1]);
+        l = l * alpha + sum;
+        m = m_use;
+        // Rescale this row of O when its maximum moved (after the weighted
+        // sum of the previous block has completed).
+        const bool need = j > 0 && alpha < 1.f;
+        if (__any_sync(0xffffffffu, need)) {
           const uint32_t gq = g - 1u;
           if (!mbar_wait(pv_done((int)(gq & 1u)), (gq >> 1) & 1u, abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
-        }
-        if (lane == 0) bulk_wait_read<0>();
-        __syncwarp();
-#pragma unroll
-        for (int kh = 0; kh < 2; ++kh) store_row_half(sP + (uint32_t)kh * kHalf, row, w, kh * 32);
-        l = l * alpha + sum;
-        m = m_use;
-        fence_proxy_async_smem();
-        // Rescale this row of O when its maximum moved (after the weighted
-        // sum of the previous block has completed).
-        const bool need = j > 0 && alpha < 1.f;
-        if (__any_sync(0xffffffffu, need)) {
           tc_fence_after();
           const float a = need ? alpha : 1.f;
 #pragma unroll
@@ -416,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
             for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a);
             tmem_st32(tmem + lane_off + kOCol + (uint32_t)cc * 32u, v);
           }
-          tmem_st_wait();
         }
+        tmem_st_wait();   // P (and a rescaled O) are in TMEM before the weighted sum may read them
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full(b));
@@ -429,6 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       const uint32_t gl = g - 1u;
       if (!mbar_wait(pv_done((int)(gl & 1u)), (gl >> 1) & 1u, abort_flag, kWaitNs)) break;
       tc_fence_after();
+      if (lane == 0) bulk_wait_read<0>();   // the previous item's output store has read the staging rows
+      __syncwarp();
       const float inv = 1.f / l;
       const uint32_t stage = sP + (uint32_t)q * 4096u;
 #pragma unroll
