@@ -563,10 +563,11 @@ extern "C" fo_status fo_attn_rs(fo_plan_t p, const void* const* Q, const void* c
     return FO_ERR_CUDA;
   }
   kern<<<grid, fo_attn::kThreads, fo_attn::kSmemBytes, (cudaStream_t)stream>>>(k);
-  if (cudaGetLastError() != cudaSuccess) return FO_ERR_CUDA;
+  const cudaError_t e = cudaGetLastError();
   if (fo_log_enabled())
-    fprintf(stderr, "[flashoverlap] attention R=%d T=%lld heads=%d causal=%d: %d items on %d CTAs\n", R,
-            (long long)T, heads, causal, total, grid);
+    fprintf(stderr, "[flashoverlap] attention R=%d T=%lld heads=%d causal=%d: %d items on %d CTAs: %s\n", R,
+            (long long)T, heads, causal, total, grid, cudaGetErrorString(e));
+  if (e != cudaSuccess) return FO_ERR_CUDA;
   // The projection's fused GEMM + reduce-scatter of O_r . Wo_r.
   if ((st = fo_gemm_rs(p, (const void* const*)O, Wo, Y, ws, stream))) return st;
   p->last_launches = 2;
