@@ -19,7 +19,9 @@
 // reduce-adds, already overlapped with its own math; the first launch
 // computes the attention in the same query-block order.
 //
-// fo_attn_kernel, one CTA per SM, persistent over work items:
+// fo_attn_kernel, one CTA per SM, persistent over work items, which CTAs
+// take dynamically (the costlier query tiles of a block first, since under
+// the causal mask a tile's cost grows with its position):
 //   warp 0     TMA producer: the item's Q tile (128 x 128) once, then K and
 //              V blocks of 128 keys into two-stage rings, K one block ahead;
 //   warp 1     TMEM allocation; MMA issue: S_j = Q K_j^T into one of two
@@ -100,7 +102,7 @@ __device__ __forceinline__ Item decode(const AttnParams& p, int L) {
   it.s = p.task_s[task];
   it.c = p.table[it.r][it.s];
   it.h = rem / p.qtiles;
-  const int qt = rem - it.h * p.qtiles;
+  const int qt = p.qtiles - 1 - (rem - it.h * p.qtiles);   // the costlier (later) query tiles first
   it.q0 = it.c * (p.T / p.R) + qt * kTile;
   it.nkb = p.causal ? it.q0 / kTile + 1 : p.T / kTile;
   return it;
@@ -150,17 +152,41 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP, sBar = base + kOffBar;
+  // Barrier slots (8 bytes each) in the barrier area.
+  enum : int {
+    kBarQFull = 0, kBarQEmpty, kBarOFree, kBarMmaDone, kBarSlot,   // kBarSlot: TMEM address, abort flag
+    kBarPFull = 5,       // two: the softmax warps wrote P_j (and a rescaled O)
+    kBarPvDone = 7,      // two: P_j V_j completed
+    kBarVFull = 9,       // kVStages
+    kBarVEmpty = 11,     // kVStages
+    kBarKFull = 13,      // kKStages
+    kBarKEmpty = 16,     // kKStages
+    kBarSFull = 19,      // three score buffers
+    kBarSFree = 22,      // three
+    kBarItemFull = 25,   // two item slots
+    kBarItemFree = 27,   // two
+    kBarItemSlot = 29,   // the two item indices
+    kBarCount = 30
+  };
+  static_assert(kBarCount * 8 <= 512, "barrier area");
   auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
-  const uint32_t q_full = bar(0), q_empty = bar(1), o_free = bar(2);
-  auto k_full = [&](int st) { return bar(21 + st); };
-  auto k_empty = [&](int st) { return bar(24 + st); };
-  auto v_full = [&](int st) { return bar(17 + st); };
-  auto v_empty = [&](int st) { return bar(19 + st); };
-  auto s_full = [&](int b) { return bar(27 + b); };   // three TMEM score buffers
-  auto s_free = [&](int b) { return bar(30 + b); };
-  auto p_full = [&](int b) { return bar(11 + b); };
-  auto pv_done = [&](int b) { return bar(13 + b); };
-  const uint32_t sSlot = bar(15);
+  const uint32_t q_full = bar(kBarQFull), q_empty = bar(kBarQEmpty), o_free = bar(kBarOFree);
+  auto k_full = [&](int st) { return bar(kBarKFull + st); };
+  auto k_empty = [&](int st) { return bar(kBarKEmpty + st); };
+  auto v_full = [&](int st) { return bar(kBarVFull + st); };
+  auto v_empty = [&](int st) { return bar(kBarVEmpty + st); };
+  auto s_full = [&](int b) { return bar(kBarSFull + b); };
+  auto s_free = [&](int b) { return bar(kBarSFree + b); };
+  auto p_full = [&](int b) { return bar(kBarPFull + b); };
+  auto pv_done = [&](int b) { return bar(kBarPvDone + b); };
+  const uint32_t sSlot = bar(kBarSlot);
+  // Work items are dealt dynamically: the producer takes the next item index
+  // from a counter in the workspace header and passes it to the MMA and
+  // softmax warps through a two-slot ring.
+  auto item_full = [&](int sl) { return bar(kBarItemFull + sl); };
+  auto item_free = [&](int sl) { return bar(kBarItemFree + sl); };
+  volatile int32_t* item_slot = reinterpret_cast<volatile int32_t*>(gbase + (bar(kBarItemSlot) - base));
+  uint32_t* const ctr = reinterpret_cast<uint32_t*>(p.status) + 6;   // header pad words: next item, CTAs done
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + (sSlot - base));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (sSlot - base) + 4);
 
@@ -187,7 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       mbar_init(p_full(i), 4);
       mbar_init(pv_done(i), 1);
     }
-    mbar_init(bar(16), 1);   // every MMA issued has completed (before TMEM is freed)
+    mbar_init(bar(kBarMmaDone), 1);   // every MMA issued has completed (before TMEM is freed)
+    for (int sl = 0; sl < 2; ++sl) {
+      mbar_init(item_full(sl), 1);
+      mbar_init(item_free(sl), 5);   // the MMA thread and the four softmax warps
+    }
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -209,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       // K blocks run two ahead of V blocks, as the scores do: K_j is free
       // again once S_j is computed, V_j only once P_j V_j is.
       uint32_t gk = 0, gv = 0;   // K and V blocks loaded so far (both number the CTA's blocks)
-      int n = 0;
+      int n = 0, nq = 0;         // items taken, Q tiles loaded
       bool ok = true;
       auto load_k = [&](const Item& it, int j) -> bool {
         const int st = (int)(gk % kKStages);
@@ -236,12 +266,19 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         ++gv;
         return true;
       };
-      for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++n) {
+      for (;; ++n) {
+        const int sl = n & 1;
+        if (!mbar_wait(item_free(sl), ((uint32_t)(n >> 1) & 1u) ^ 1u, abort_flag, kWaitNs)) break;
+        const int L = (int)atomicAdd(ctr, 1u);
+        item_slot[sl] = L;
+        mbar_arrive(item_full(sl));
+        if (L >= total) break;
         const Item it = decode(p, L);
         if (!mbar_wait(q_empty, (uint32_t)(n & 1) ^ 1u, abort_flag, kWaitNs)) break;
         mbar_arrive_expect_tx(q_full, kTileBytes);
         tma_load_2d(sQ, &p.tmQ[it.r], q_full, it.h * kHeadDim, it.q0);
         tma_load_2d(sQ + kHalf, &p.tmQ[it.r], q_full, it.h * kHeadDim + 64, it.q0);
+        ++nq;
         if (!load_k(it, 0) || (it.nkb > 1 && !load_k(it, 1))) break;
         for (int j = 0; j < it.nkb; ++j) {
           if ((j + 2 < it.nkb && !load_k(it, j + 2)) || !load_v(it, j)) {
@@ -249,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
             break;
           }
         }
+        if (!ok) break;
       }
       // Loads still in flight land before the CTA may exit.
       volatile int never = 0;
@@ -256,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         mbar_wait(k_full((int)(k % kKStages)), (k / kKStages) & 1u, &never, 100000000ull);
       for (uint32_t k = gv > 2u ? gv - 2u : 0u; k < gv; ++k)
         mbar_wait(v_full((int)(k & 1u)), (k >> 1) & 1u, &never, 100000000ull);
-      if (n > 0) mbar_wait(q_full, (uint32_t)((n - 1) & 1), &never, 100000000ull);
+      if (nq > 0) mbar_wait(q_full, (uint32_t)((nq - 1) & 1), &never, 100000000ull);
       if (*abort_flag) record_error(p.status, FO_ERR_TIMEOUT, -1, -1, 0);
     }
   } else if (warp == 1) {
@@ -308,7 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         tc_commit<1>(k_empty(sb));
         return true;
       };
-      for (int L = blockIdx.x; L < total && ok; L += gridDim.x, ++n) {
+      for (; ok; ++n) {
+        const int sl = n & 1;
+        if (!mbar_wait(item_full(sl), (uint32_t)(n >> 1) & 1u, abort_flag, kWaitNs)) break;
+        const int L = item_slot[sl];
+        mbar_arrive(item_free(sl));
+        if (L >= total) break;
         const Item it = decode(p, L);
         if (!mbar_wait(q_full, (uint32_t)(n & 1), abort_flag, kWaitNs)) break;
         tc_fence_after();
@@ -325,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
         g = g0 + (uint32_t)it.nkb;
       }
       // Every issued MMA completes before TMEM is released.
-      tc_commit<1>(bar(16));
+      tc_commit<1>(bar(kBarMmaDone));
       volatile int never = 0;
-      mbar_wait(bar(16), 0, &never, 100000000ull);
+      mbar_wait(bar(kBarMmaDone), 0, &never, 100000000ull);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -336,7 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     uint32_t g = 0;
     int n = 0;
-    for (int L = blockIdx.x; L < total; L += gridDim.x, ++n) {
+    for (;; ++n) {
+      const int sl = n & 1;
+      if (!mbar_wait(item_full(sl), (uint32_t)(n >> 1) & 1u, abort_flag, kWaitNs)) break;
+      const int L = item_slot[sl];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(item_free(sl));
+      if (L >= total) break;
       const Item it = decode(p, L);
       float m = -INFINITY, l = 0.f;
       bool ok = true;
@@ -479,6 +528,16 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
     tc_fence_after();
     __syncwarp();
     tmem_dealloc<1>(tmem, 512);
+  }
+  // The last CTA to finish resets the item counter for the next launch
+  // (every CTA has stopped taking items by then).
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
+      atomicExch(ctr, 0u);
+      atomicExch(ctr + 1, 0u);
+      __threadfence();
+    }
   }
 }
 
