@@ -40,7 +40,7 @@ EXPORTED = [
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
     "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc", "fo_plan_task_order",
     "fo_gemm_ar", "fo_trace_query", "fo_plan_last_split_tiles", "fo_check_device_pointers",
-    "fo_gemm_a2a", "fo_all_to_all_copy", "fo_attn_rs",
+    "fo_gemm_a2a", "fo_all_to_all_copy", "fo_attn_rs", "fo_attention",
 ]
 
 
@@ -97,6 +97,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_gemm_a2a": ([P, PP, PP, PP, P, P], c_int32),
         "fo_all_to_all_copy": ([P, PP, PP, P], c_int32),
         "fo_attn_rs": ([P, PP, PP, PP, PP, PP, PP, c_int32, c_int32, P, P], c_int32),
+        "fo_attention": ([P, PP, PP, PP, PP, c_int32, c_int32, P, P], c_int32),
         "fo_status_query": ([P, P, P, POINTER(c_int32)], c_int32),
         "fo_trace_query": ([P, P, P, POINTER(ctypes.c_uint64), c_int32, POINTER(c_int32)], c_int32),
         "fo_gemm_partials": ([P, PP, PP, PP, P, P], c_int32),
@@ -279,6 +280,12 @@ def fo_attn_rs(plan: Plan, Q, K, V, Wo, O, Y, heads: int, causal: bool, ws, stre
     _check(load().fo_attn_rs(plan, _ptr_array(Q), _ptr_array(K), _ptr_array(V), _ptr_array(Wo), _ptr_array(O),
                              _ptr_array(Y), int(heads), 1 if causal else 0, _ptr(ws), _stream(stream)),
            "fo_attn_rs")
+
+
+def fo_attention(plan: Plan, Q, K, V, O, heads: int, causal: bool, ws, stream=None) -> None:
+    _check(load().fo_attention(plan, _ptr_array(Q), _ptr_array(K), _ptr_array(V), _ptr_array(O), int(heads),
+                               1 if causal else 0, _ptr(ws), _stream(stream)),
+           "fo_attention")
 
 
 def fo_ag_gemm(plan: Plan, X, W, Y, G=None, ws=None, stream=None) -> None:

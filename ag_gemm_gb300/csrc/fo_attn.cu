@@ -566,9 +566,11 @@ bool enc(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t
 
 }  // namespace
 
-extern "C" fo_status fo_attn_rs(fo_plan_t p, const void* const* Q, const void* const* K, const void* const* V,
-                                const void* const* Wo, void* const* O, void* const* Y, int32_t heads,
-                                int32_t causal, void* ws, fo_stream_t stream) {
+namespace {
+
+// Checks the arguments of the attention launch and launches it.
+fo_status launch_attention(fo_plan_t p, const void* const* Q, const void* const* K, const void* const* V,
+                           void* const* O, int32_t heads, int32_t causal, void* ws, fo_stream_t stream) {
   if (!p || !ws) return FO_ERR_INVALID_ARG;
   if (p->d.op != FO_OP_GEMM_RS || p->elem_bytes != 2) return FO_ERR_INVALID_ARG;
   if (heads < 1 || (causal != 0 && causal != 1)) return FO_ERR_INVALID_ARG;
@@ -578,8 +580,7 @@ extern "C" fo_status fo_attn_rs(fo_plan_t p, const void* const* Q, const void* c
   if ((T / R) % fo_attn::kTile) return FO_ERR_SHAPE;      // whole 128-row query tiles per block
   fo_status st;
   if ((st = fo_internal_check_ptrs(R, Q)) || (st = fo_internal_check_ptrs(R, K)) ||
-      (st = fo_internal_check_ptrs(R, V)) || (st = fo_internal_check_ptrs(R, Wo)) ||
-      (st = fo_internal_check_ptrs(R, (const void* const*)O)) || (st = fo_internal_check_ptrs(R, (const void* const*)Y)))
+      (st = fo_internal_check_ptrs(R, V)) || (st = fo_internal_check_ptrs(R, (const void* const*)O)))
     return st;
   if ((st = fo_internal_check_device_ptrs(R, Q, stream)) || (st = fo_internal_check_device_ptrs(R, K, stream)) ||
       (st = fo_internal_check_device_ptrs(R, V, stream)) ||
@@ -627,6 +628,24 @@ extern "C" fo_status fo_attn_rs(fo_plan_t p, const void* const* Q, const void* c
     fprintf(stderr, "[flashoverlap] attention R=%d T=%lld heads=%d causal=%d: %d items on %d CTAs: %s\n", R,
             (long long)T, heads, causal, total, grid, cudaGetErrorString(e));
   if (e != cudaSuccess) return FO_ERR_CUDA;
+  p->last_launches = 1;
+  return FO_OK;
+}
+
+}  // namespace
+
+extern "C" fo_status fo_attention(fo_plan_t p, const void* const* Q, const void* const* K, const void* const* V,
+                                  void* const* O, int32_t heads, int32_t causal, void* ws, fo_stream_t stream) {
+  return launch_attention(p, Q, K, V, O, heads, causal, ws, stream);
+}
+
+extern "C" fo_status fo_attn_rs(fo_plan_t p, const void* const* Q, const void* const* K, const void* const* V,
+                                const void* const* Wo, void* const* O, void* const* Y, int32_t heads,
+                                int32_t causal, void* ws, fo_stream_t stream) {
+  fo_status st;
+  if (p && ((st = fo_internal_check_ptrs(p->R, Wo)) || (st = fo_internal_check_ptrs(p->R, (const void* const*)Y))))
+    return st;
+  if ((st = launch_attention(p, Q, K, V, O, heads, causal, ws, stream))) return st;
   // The projection's fused GEMM + reduce-scatter of O_r . Wo_r.
   if ((st = fo_gemm_rs(p, (const void* const*)O, Wo, Y, ws, stream))) return st;
   p->last_launches = 2;

@@ -93,14 +93,18 @@ def hbm_summary(w, kernel_ms, traffic, peaks):
     return out
 
 
-def kernel_source_sha256() -> str:
+GEMM_SOURCES = ("fo_device.cuh", "fo_kernel.cuh", "fo_plan.cpp")
+ATTN_SOURCES = ("fo_device.cuh", "fo_attn.cu")
+
+
+def kernel_source_sha256(sources=GEMM_SOURCES) -> str:
     """sha256 of the kernel and plan sources with comments and blank lines
     removed, so that a profile stays tied to the code it measured and not to
     its comments."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for f in ("fo_device.cuh", "fo_kernel.cuh", "fo_plan.cpp"):
+    for f in sources:
         with open(os.path.join(ROOT, "ag_gemm_gb300", "csrc", f), encoding="utf-8") as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
@@ -110,11 +114,11 @@ def kernel_source_sha256() -> str:
     return h.hexdigest()
 
 
-def profiled_traffic(workload_name: str):
-    """DRAM bytes per launch of the fused kernel from the committed ncu
-    summary of this workload, or None when that capture was taken on other
+def profiled_traffic(workload_name: str, sources=GEMM_SOURCES, prefix="fused"):
+    """DRAM bytes per launch of the workload's dominant kernel from its
+    committed ncu summary, or None when that capture was taken on other
     kernel source than the one built now."""
-    path = os.path.join(ROOT, "profiles", f"fused_{workload_name}.md")
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload_name}.md")
     if not os.path.exists(path):
         return None
     sha = traffic = None
@@ -124,7 +128,7 @@ def profiled_traffic(workload_name: str):
                 sha = line.split(":", 1)[1].strip()
             elif line.startswith("traffic_bytes_per_launch:"):
                 traffic = float(line.split(":", 1)[1].strip())
-    if sha and traffic and sha == kernel_source_sha256():
+    if sha and traffic and sha == kernel_source_sha256(sources):
         return traffic
     return None
 
@@ -606,8 +610,11 @@ def _attn_setup(B, dev, R=8, T=8192, heads=4, H=4096, causal=True, seed=12):
     attn_flops = R * heads * 2.0 * 2.0 * T * T * 128 * (0.5 if causal else 1.0)
     proj_flops = 2.0 * T * H * R * w
     return {"plan": plan, "ws": ws, "attn_flops": attn_flops, "proj_flops": proj_flops,
-            "flops": attn_flops + proj_flops,
+            "flops": attn_flops + proj_flops, "heads": heads, "causal": causal,
+            "Q": Q, "K": K, "V": V, "Wo": Wo, "O": O, "Y": Y,
+            "mk_plan": lambda: B.fo_plan("gemm_rs", R, T, H, R * w),
             "call": lambda s: B.fo_attn_rs(plan, Q, K, V, Wo, O, Y, heads, causal, ws, s),
+            "attn": lambda s: B.fo_attention(plan, Q, K, V, O, heads, causal, ws, s),
             "proj": lambda s: B.fo_gemm_rs(pplan, O, Wo, Y, pws, s)}
 
 
@@ -807,10 +814,27 @@ def run_other_op(args, w, dev, world, rank):
     return 0
 
 
+def _loop_ms(fn, stream, dev, iters):
+    """Mean CUDA-event time of one fn(stream) call over `iters` back-to-back
+    calls, after three untimed ones."""
+    import torch
+    for _ in range(3):
+        fn(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    torch.cuda.synchronize(dev)
+    for a, b in ev:
+        a.record(stream)
+        fn(stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in ev) / iters
+
+
 def run_attn(args, dev, world, rank):
     """One step = one fo_attn_rs call: query-split causal attention of 32
     heads over 8192 tokens (R = 8), then the fused output projection +
-    reduce-scatter (two launches)."""
+    reduce-scatter (two launches). The roofline is the attention kernel's,
+    timed alone through fo_attention; the projection is timed alone too."""
     import torch
     import torch.distributed as dist
 
@@ -833,6 +857,8 @@ def run_attn(args, dev, world, rank):
         t1.record(stream)
         torch.cuda.synchronize(dev)
         clk.mark("t1")
+        attn_ms = _loop_ms(a["attn"], stream, dev, steps)
+        proj_ms = _loop_ms(a["proj"], stream, dev, steps)
     code, info = B.fo_status_query(a["plan"], a["ws"], stream)
     if code != 0:
         raise RuntimeError(f"device status {code} {info}")
@@ -840,7 +866,17 @@ def run_attn(args, dev, world, rank):
     peaks, peak_src = load_peaks()
     sustained = ms * steps >= 250.0
     peak = float(peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"])
+    burst = float(peaks["bf16_tflops"])
     value = world * a["flops"] / (ms * 1e-3) / 1e12
+    attn_tf = a["attn_flops"] / (attn_ms * 1e-3) / 1e12
+    proj_tf = a["proj_flops"] / (proj_ms * 1e-3) / 1e12
+    heads, causal, O = a["heads"], a["causal"], a["O"]
+    e2e = measure_e2e(B, a["mk_plan"],
+                      lambda p, din, dout, ws_, s_: B.fo_attn_rs(p, din[0], din[1], din[2], din[3], O, dout,
+                                                                 heads, causal, ws_, s_),
+                      [[t.cpu() for t in a[n]] for n in ("Q", "K", "V", "Wo")],
+                      [a["Q"], a["K"], a["V"], a["Wo"]], a["Y"], dev, stream, world, a["flops"],
+                      max(4, min(args.steps, 12)))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -849,9 +885,19 @@ def run_attn(args, dev, world, rank):
                    "hidden": 4096, "causal": True,
                    "step": "query-split attention + fused output projection and reduce-scatter (2 launches)",
                    "l2": "no flush: 470 MB of operands and outputs per step"},
-        "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
-                     "frac": value / world / peak, "traffic": None,
-                     "peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)") + ", " + peak_src},
+        # The dominant kernel: the attention launch, timed alone (burst
+        # peak: one loop of `steps` launches lasts well under a second).
+        "roofline": {"bound": "tensor", "achieved": attn_tf, "peak": burst, "unit": "TFLOP/s",
+                     "frac": attn_tf / burst, "traffic": profiled_traffic(ATTN_WORKLOAD, ATTN_SOURCES, "attention"),
+                     "kernel": "fo_attn_kernel", "ms": attn_ms,
+                     "peak_source": "bf16_tflops (burst), " + peak_src},
+        "kernels": {"attention": {"ms": attn_ms, "tflops": attn_tf, "frac_of_burst_peak": attn_tf / burst,
+                                  "flops": a["attn_flops"]},
+                    "projection_rs": {"ms": proj_ms, "tflops": proj_tf, "frac_of_burst_peak": proj_tf / burst,
+                                      "flops": a["proj_flops"]},
+                    "step_frac_of_peak": value / world / peak,
+                    "step_peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)")},
+        "e2e": e2e,
         "gpu_launches": 2 * steps,
         "clocks": clk.summary(),
         "flops_per_step": a["flops"],

@@ -328,8 +328,7 @@ fo_status fo_gemm_a2a(fo_plan_t plan, const void* const* X, const void* const* W
  * causal = 1 key j is masked for query i when j > i, with 0 nothing is.
  * The queries split into R blocks of T/R rows; rank r's step s takes block
  * (r - 1 - s) mod R, so the block that stays on the rank comes last.
- * Two launches on `stream`: the attention of every (rank, step, head,
- * 128-query tile) in the plan's task order, then fo_gemm_rs of O_r . Wo_r.
+ * Two launches on `stream`: fo_attention, then fo_gemm_rs of O_r . Wo_r.
  * The softmax weights are rounded to bf16 for the tensor cores' weighted
  * sum, and O once to bf16. Requires heads >= 1 and T/R a multiple of 128;
  * FO_ERR_SHAPE when K != R * heads * 128 or T/R is not; FO_ERR_INVALID_ARG
@@ -338,6 +337,16 @@ fo_status fo_gemm_a2a(fo_plan_t plan, const void* const* X, const void* const* W
 fo_status fo_attn_rs(fo_plan_t plan, const void* const* Q, const void* const* K, const void* const* V,
                      const void* const* Wo, void* const* O, void* const* Y, int32_t heads, int32_t causal,
                      void* ws, fo_stream_t stream);
+
+/* The attention half of fo_attn_rs alone, one launch: O_r for every rank,
+ * same arguments, layouts, checks and rounding (Wo and Y are not taken).
+ * The work items, one (rank, step, head, 128-query tile) each, follow the
+ * plan's task order, within a task the costlier (later) query tiles first;
+ * the kernel's CTAs take them one at a time from a counter in the
+ * workspace header, which the last CTA of the launch sets back to zero
+ * (fo_workspace_init zeroes it; fo_status_query does after a failure). */
+fo_status fo_attention(fo_plan_t plan, const void* const* Q, const void* const* K, const void* const* V,
+                       void* const* O, int32_t heads, int32_t causal, void* ws, fo_stream_t stream);
 
 /* Data-parallel weight gradient fused with its reduce-scatter:
  * dW_d = sum_r (X_r^T . dY_r)[rows of d], fp32 (gist.science "Technical

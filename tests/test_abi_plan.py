@@ -478,3 +478,23 @@ def test_attn_rs_rejects_bad_arguments_on_the_host():
     with pytest.raises(B.FlashOverlapError) as e:
         B.fo_attn_rs(ag, fake, fake, fake, fake, fake, fake, 1, False, 4096, stream=0)
     assert e.value.code == B.FO_ERR_INVALID_ARG
+
+
+def test_attention_alone_rejects_bad_arguments_on_the_host():
+    fake = [16 * (i + 1) for i in range(2)]
+
+    def call(plan, heads, causal, V=fake):
+        B._check(B.load().fo_attention(plan, B._ptr_array(fake), B._ptr_array(fake), B._ptr_array(V),
+                                       B._ptr_array(fake), heads, causal, 4096, 0), "fo_attention")
+
+    p = B.fo_plan("gemm_rs", 2, 512, 256, 2 * 2 * 128)
+    f32 = B.fo_plan("gemm_rs", 2, 512, 256, 2 * 2 * 128, in_dtype="f32")
+    for plan, heads, causal, V, code in ((p, 0, 0, fake, B.FO_ERR_INVALID_ARG),
+                                         (p, 2, 2, fake, B.FO_ERR_INVALID_ARG),
+                                         (p, 3, 0, fake, B.FO_ERR_SHAPE),          # K != R * heads * 128
+                                         (p, 2, 1, [16, 0], B.FO_ERR_INVALID_ARG),  # a null V pointer
+                                         (p, 2, 1, [16, 24], B.FO_ERR_ALIGN),       # V not 16-byte aligned
+                                         (f32, 2, 1, fake, B.FO_ERR_INVALID_ARG)):  # fp32 inputs
+        with pytest.raises(B.FlashOverlapError) as e:
+            call(plan, heads, causal, V)
+        assert e.value.code == code

@@ -1,15 +1,19 @@
 """GPU parity of query-split attention with its row-parallel output
-projection (fo_attn_rs) against the CPU oracle, through the C ABI.
+projection (fo_attn_rs, and its attention launch alone, fo_attention)
+against the CPU oracle, through the C ABI.
 
-Tolerances. The tensor cores take the softmax weights in bf16 (unit
-roundoff 2^-9) and the attention output O is rounded once to bf16, so O
-differs from the fp64 oracle by about 1e-3 of its rms from the weights and
-up to one bf16 step on elements whose two values round apart. O is held to
-a relative Frobenius error of 4e-3 and, elementwise, to 2e-2 of max(|ref|,
-rms(ref)). The projection is checked separately at the stated GEMM
-tolerances (relative Frobenius 1e-3, elementwise 2e-2) against the oracle's
-reduce-scatter of the O the GPU produced; end to end, Y is held to the same
-4e-3 Frobenius bound as O.
+Tolerances. The tensor cores take the softmax weights in bf16 (8
+significant bits, unit roundoff u = 2^-8), each weight e_k / l with a
+relative error of at most u, so element (i, j) of O moves by at most
+u * sum_k p_ik |v_kj|: the attention of |V|, which the oracle computes.
+O is then rounded once to bf16 on both sides; values that round apart
+differ by at most one bf16 step, 2^-7 |O_ij|. Elementwise, O is held to
+1.25 (u * attention(|V|) + 2^-7 |O|); the fp32 score, exponent and sum
+errors fit in the quarter of slack. In Frobenius norm O is held to 4e-3
+of the reference. The projection is checked separately at the stated GEMM
+tolerances (relative Frobenius 1e-3, elementwise 2e-2) against the
+oracle's reduce-scatter of the O the GPU produced; end to end, Y is held
+to the same 4e-3 Frobenius bound as O.
 """
 import numpy as np
 import pytest
@@ -20,7 +24,10 @@ from ag_gemm_gb300 import binding as B
 
 pytestmark = pytest.mark.gpu
 
-O_FRO, O_MAX = 4e-3, 2e-2
+O_FRO = 4e-3
+U_BF16 = 2.0 ** -8       # unit roundoff of bf16
+ULP_BF16 = 2.0 ** -7     # one bf16 step, relative to the value
+O_SLACK = 1.25
 FRO_TOL, MAX_TOL = 1e-3, 2e-2
 D = 128
 
@@ -71,18 +78,21 @@ def run_attn(dev, R, T, heads, H, causal, seed=0, out="f32", **kw):
         [_np(o) for o in O], [_np(y) for y in Y]
 
 
-def _check_o(got, ref, what):
-    rms = float(np.sqrt(np.mean(ref * ref)))
+def _check_o(got, ref, absw, what):
+    """got: the kernel's O; ref: the oracle's O rounded to bf16; absw: the
+    oracle's attention of |V| (the per-element weight-rounding bound)."""
     fro = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
-    mx = float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), rms)))
-    assert fro <= O_FRO and mx <= O_MAX, f"{what}: rel fro {fro:.3e}, max {mx:.3e}"
+    bound = O_SLACK * (U_BF16 * absw + ULP_BF16 * np.abs(ref))
+    ratio = float(np.max(np.abs(got - ref) / bound))
+    assert fro <= O_FRO and ratio <= 1.0, f"{what}: rel fro {fro:.3e}, worst element at {ratio:.2f} of its bound"
 
 
 def _check_all(Q, K, V, Wo, O, Y, heads, causal, out="f32"):
     R = len(Q)
     for r in range(R):
         ref_o = oracle.round_bf16(oracle.attention(Q[r], K[r], V[r], heads, causal))
-        _check_o(O[r], ref_o, f"O rank {r}")
+        absw = oracle.attention(Q[r], K[r], np.abs(V[r]), heads, causal)
+        _check_o(O[r], ref_o, absw, f"O rank {r}")
     # the projection on the O the GPU produced: the GEMM-RS tolerances
     proj = oracle.gemm_rs(O, Wo)
     for d in range(R):
@@ -145,15 +155,44 @@ def test_attn_rs_llama_shape_sampled(dev):
     for r in (0, R - 1):
         Qr = Q[r]
         ref_rows = np.empty((len(rows), heads * D))
+        absw = np.empty((len(rows), heads * D))
         for h in range(heads):
             cols = slice(h * D, (h + 1) * D)
             for i, t in enumerate(rows):
                 s = (Qr[t, cols] @ K[r][: t + 1, cols].T) / np.sqrt(D)
                 w = np.exp(s - s.max())
                 ref_rows[i, cols] = (w / w.sum()) @ V[r][: t + 1, cols]
-        _check_o(O[r][rows], oracle.round_bf16(ref_rows), f"O rank {r}")
+                absw[i, cols] = (w / w.sum()) @ np.abs(V[r][: t + 1, cols])
+        _check_o(O[r][rows], oracle.round_bf16(ref_rows), absw, f"O rank {r}")
     srows = np.array([0, 1, 511, 1023])
     for d in range(R):
         want = oracle.gemm_rs_rows(O, Wo, d, srows)
         fro, mx, _ = oracle.rel_errors(Y[d][srows], want)
         assert fro <= FRO_TOL and mx <= MAX_TOL, f"Y shard {d}: rel fro {fro:.3e}, max {mx:.3e}"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_alone_matches_attn_rs_and_resets_its_counter(dev, causal):
+    # fo_attention is the first launch of fo_attn_rs: same O bits, one
+    # launch, and the item counter in the workspace header (words 6 and 7)
+    # is back at zero when the launch ends, ready for the next one.
+    R, T, heads, H = 2, 1024, 2, 256
+    Q, K, V, Wo = _inputs(R, T, heads, H, seed=21)
+    plan = B.fo_plan("gemm_rs", R, T, H, R * heads * D)
+    ws = torch.zeros(B.fo_workspace_size(plan), dtype=torch.uint8, device=dev)
+    dQ, dK, dV, dW = ([t.to(dev) for t in ts] for ts in (Q, K, V, Wo))
+    O1 = [torch.full((T, heads * D), float("nan"), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    O2 = [torch.full((T, heads * D), float("nan"), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    Y = [torch.empty(T // R, H, device=dev) for _ in range(R)]
+    for _ in range(3):
+        B.fo_attention(plan, dQ, dK, dV, O1, heads, causal, ws)
+        assert B.fo_plan_last_launches(plan) == 1
+        assert B.fo_status_query(plan, ws)[0] == 0
+        assert ws[24:32].view(torch.int32).tolist() == [0, 0]
+    B.fo_attn_rs(plan, dQ, dK, dV, dW, O2, Y, heads, causal, ws)
+    assert B.fo_status_query(plan, ws)[0] == 0
+    for r in range(R):
+        assert torch.equal(O1[r], O2[r])
+        q, k, v = _np(Q[r]), _np(K[r]), _np(V[r])
+        ref = oracle.round_bf16(oracle.attention(q, k, v, heads, causal))
+        _check_o(_np(O1[r]), ref, oracle.attention(q, k, np.abs(v), heads, causal), f"O rank {r}")
