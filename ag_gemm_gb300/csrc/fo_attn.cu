@@ -19,22 +19,32 @@
 // reduce-adds, already overlapped with its own math; the first launch
 // computes the attention in the same query-block order.
 //
-// fo_attn_kernel, one CTA per SM, persistent over work items, which CTAs
-// take dynamically (the costlier query tiles of a block first, since under
-// the causal mask a tile's cost grows with its position):
-//   warp 0     TMA producer: the item's Q tile (128 x 128) once, then K and
-//              V blocks of 128 keys into two-stage rings, K one block ahead;
-//   warp 1     TMEM allocation; MMA issue: S_j = Q K_j^T into one of two
-//              TMEM score buffers, then O += P_{j-1} V_{j-1} once the softmax
-//              warps have written P_{j-1}, so S_j overlaps softmax(j-1);
-//   warps 2-5  softmax, one query row per thread: the row's 128 scores from
-//              TMEM, the running maximum and sum (online softmax), P in bf16
-//              into shared memory as the next MMA's A operand, and the
-//              rescale of the TMEM output row when the maximum grows by more
-//              than 8 in log2 units (a smaller growth keeps the old maximum:
-//              the weights then stay below 2^8 and the final division by the
-//              sum cancels the choice); at the item's end O / sum, bf16, TMA
-//              store.
+// fo_attn_kernel, one CTA per SM, persistent over work items (one item =
+// one rank, step, head and 128-query tile), which CTAs take one at a time
+// from a counter in the workspace header, the costlier query tiles of a
+// block first (under the causal mask a tile's cost grows with its
+// position):
+//   warp 0      TMA producer: the item's Q tile (128 x 128) once, then K
+//               blocks of 128 keys into a three-stage ring and V blocks into
+//               a two-stage ring, K two blocks ahead of V;
+//   warp 1      TMEM allocation; S_j = Q K_j^T into score buffer j mod 3
+//               (of three), up to two blocks ahead of the softmax;
+//   warp 2      O += P_j V_j, with P_j read from TMEM (the "A in tensor
+//               memory" form), once the softmax warps have written it. The
+//               two MMA streams come from two warps because a thread that
+//               issues tcgen05.mma runs only a few instructions ahead of the
+//               tensor pipe: one issuer would hold the score MMAs back while
+//               it waits for the softmax;
+//   warps 3-10  softmax: two warps per 32-row quarter of the tile, each over
+//               64 of a block's 128 keys. A thread takes its row's 64 scores
+//               from TMEM, the two warps swap partial row maxima, and each
+//               writes its bf16 weights over its own score columns. The
+//               running maximum only moves when it grows by more than 8 in
+//               log2 units (a smaller growth keeps the old one: the weights
+//               then stay below 2^8 and the final division by the sum
+//               cancels the choice); when it moves, each warp rescales its 64
+//               columns of the TMEM output row. At the item's end the partial
+//               sums are swapped and O / sum is stored in bf16 from registers.
 // Every wait is bounded; a wait that runs out raises the CTA's abort flag and
 // records FO_ERR_TIMEOUT in the workspace status word.
 #include <cudaTypedefs.h>
@@ -51,19 +61,27 @@ using namespace fo;
 
 constexpr int kHeadDim = 128;
 constexpr int kTile = 128;                       // query rows per item, keys per block
-constexpr int kThreads = 192;
+// Warps: 0 TMA producer, 1 score MMAs (and TMEM allocation), 2 weighted-sum
+// MMAs, 3-10 softmax.
+constexpr int kThreads = 352;
+constexpr int kSoftWarp0 = 3;
+// Registers are capped as for 384 threads (168 a thread): three of the
+// eleven warps share each of schedulers 0-2, and a scheduler's register file
+// holds three warps of at most 170 registers.
+constexpr int kRegBoundThreads = 384;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;   // 32 KB of bf16
 constexpr uint32_t kHalf = kTileBytes / 2;              // one 64-column half: 128 rows x 128 B
 constexpr int kKStages = 3;   // K blocks in flight (each is free again once its scores are computed)
 constexpr int kVStages = 2;   // V blocks in flight (free once their weighted sum is computed)
-// Shared memory, from a 1024-byte aligned base: Q, the K and V rings, one P
-// buffer (P_j is written once the weighted sum of P_{j-1} has completed),
+// Shared memory, from a 1024-byte aligned base: Q, the K and V rings, the
+// softmax warps' mailboxes (8 warps x 2 parities x 32 lanes x 8 bytes),
 // barriers.
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kVStages * kTileBytes;
-constexpr uint32_t kOffBar = kOffP + kTileBytes;
+constexpr uint32_t kOffX = kOffV + kVStages * kTileBytes;
+constexpr uint32_t kMailboxWords = 8 * 2 * 32;
+constexpr uint32_t kOffBar = kOffX + kMailboxWords * 8;
 constexpr int kSmemBytes = 1024 + (int)kOffBar + 512;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -80,11 +98,12 @@ struct AttnParams {
   CUtensorMap tmQ[FO_MAX_R];   // Q_r [T x heads*128], box 64 x 128
   CUtensorMap tmK[FO_MAX_R];   // K_r, box 64 x 128
   CUtensorMap tmV[FO_MAX_R];   // V_r, box 64 x 64
-  CUtensorMap tmO[FO_MAX_R];   // O_r, box 64 x 32 (stores)
+  uint16_t* O[FO_MAX_R];       // O_r [T x heads*128] bf16, row stride ld elements
   int32_t table[FO_MAX_R][FO_MAX_R];
   int32_t task_r[FO_MAX_R * FO_MAX_R];
   int32_t task_s[FO_MAX_R * FO_MAX_R];
   int32_t R, T, heads, causal, qtiles;   // qtiles: 128-row query tiles per block of T/R rows
+  int32_t ld;                            // heads * 128
   float scale_log2;                      // log2(e) / sqrt(128)
   int32_t* status;
 };
@@ -106,20 +125,6 @@ __device__ __forceinline__ Item decode(const AttnParams& p, int L) {
   it.q0 = it.c * (p.T / p.R) + qt * kTile;
   it.nkb = p.causal ? it.q0 / kTile + 1 : p.T / kTile;
   return it;
-}
-
-// Row `row` (one per thread) of a 128-row, 64-column bf16 half in the
-// 128B-swizzle layout: 16-byte chunk j of the row sits at chunk j ^ (row % 8).
-template <int NW>
-__device__ __forceinline__ void store_row_half(uint32_t half_base, int row, const uint32_t (&w)[NW], int w0) {
-  const uint32_t rb = half_base + (uint32_t)row * 128u;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t a = rb + ((uint32_t)(j ^ (row & 7)) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[w0 + 4 * j]), "r"(w[w0 + 4 * j + 1]),
-                 "r"(w[w0 + 4 * j + 2]), "r"(w[w0 + 4 * j + 3])
-                 : "memory");
-  }
 }
 
 // 2^x by the multi-function unit's approximate base-2 exponential
@@ -146,43 +151,43 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sP = base + kOffP, sBar = base + kOffBar;
-  // Barrier slots (8 bytes each) in the barrier area.
+  const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV, sBar = base + kOffBar;
+  // Barrier slots (8 bytes each). Per-block barriers have three slots,
+  // indexed by the block's number mod 3, so that a slot's next phase always
+  // depends on the waiter's own progress and a parity wait is never
+  // ambiguous.
   enum : int {
-    kBarQFull = 0, kBarQEmpty, kBarOFree, kBarMmaDone, kBarSlot,   // kBarSlot: TMEM address, abort flag
-    kBarPFull = 5,       // two: the softmax warps wrote P_j (and a rescaled O)
-    kBarPvDone = 7,      // two: P_j V_j completed
-    kBarVFull = 9,       // kVStages
-    kBarVEmpty = 11,     // kVStages
-    kBarKFull = 13,      // kKStages
-    kBarKEmpty = 16,     // kKStages
-    kBarSFull = 19,      // three score buffers
-    kBarSFree = 22,      // three
-    kBarItemFull = 25,   // two item slots
-    kBarItemFree = 27,   // two
-    kBarItemSlot = 29,   // the two item indices
-    kBarCount = 30
+    kBarQFull = 0, kBarQEmpty, kBarOFree, kBarSlot,   // kBarSlot: TMEM address, abort flag
+    kBarSDone, kBarPvDoneAll,                         // every score / weighted-sum MMA issued has completed
+    kBarKFull = 6,      // kKStages: K block loaded
+    kBarVFull = 9,      // kVStages: V block loaded
+    kBarSFull = 11,     // 3: S_j computed (also: K stage j mod 3 free again)
+    kBarPFull = 14,     // 3: the softmax warps wrote P_j (and a rescaled O)
+    kBarPvDone = 17,    // 3: P_j V_j computed (also: V stage free, score buffer free)
+    kBarItemFull = 20,  // 2 item slots
+    kBarItemFree = 22,  // 2
+    kBarItemSlot = 24,  // the two item indices
+    kBarCount = 25
   };
   static_assert(kBarCount * 8 <= 512, "barrier area");
   auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
   const uint32_t q_full = bar(kBarQFull), q_empty = bar(kBarQEmpty), o_free = bar(kBarOFree);
-  auto k_full = [&](int st) { return bar(kBarKFull + st); };
-  auto k_empty = [&](int st) { return bar(kBarKEmpty + st); };
-  auto v_full = [&](int st) { return bar(kBarVFull + st); };
-  auto v_empty = [&](int st) { return bar(kBarVEmpty + st); };
-  auto s_full = [&](int b) { return bar(kBarSFull + b); };
-  auto s_free = [&](int b) { return bar(kBarSFree + b); };
-  auto p_full = [&](int b) { return bar(kBarPFull + b); };
-  auto pv_done = [&](int b) { return bar(kBarPvDone + b); };
+  auto k_full = [&](uint32_t gk) { return bar(kBarKFull + (int)(gk % 3u)); };
+  auto v_full = [&](uint32_t gv) { return bar(kBarVFull + (int)(gv & 1u)); };
+  auto s_full = [&](uint32_t g) { return bar(kBarSFull + (int)(g % 3u)); };
+  auto p_full = [&](uint32_t g) { return bar(kBarPFull + (int)(g % 3u)); };
+  auto pv_done = [&](uint32_t g) { return bar(kBarPvDone + (int)(g % 3u)); };
+  // Parity of block g's phase on its mod-3 slot.
+  auto ph3 = [](uint32_t g) { return (g / 3u) & 1u; };
   const uint32_t sSlot = bar(kBarSlot);
   // Work items are dealt dynamically: the producer takes the next item index
-  // from a counter in the workspace header and passes it to the MMA and
-  // softmax warps through a two-slot ring.
+  // from a counter in the workspace header and passes it to the other warps
+  // through a two-slot ring.
   auto item_full = [&](int sl) { return bar(kBarItemFull + sl); };
   auto item_free = [&](int sl) { return bar(kBarItemFree + sl); };
   volatile int32_t* item_slot = reinterpret_cast<volatile int32_t*>(gbase + (bar(kBarItemSlot) - base));
@@ -196,31 +201,27 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(o_free, 4);
-    for (int i = 0; i < kKStages; ++i) {
-      mbar_init(k_full(i), 1);
-      mbar_init(k_empty(i), 1);
+    mbar_init(o_free, 8);   // every softmax warp has read its O columns
+    mbar_init(bar(kBarSDone), 1);
+    mbar_init(bar(kBarPvDoneAll), 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(bar(kBarKFull + i), 1);
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarPFull + i), 8);
+      mbar_init(bar(kBarPvDone + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(v_full(i), 1);
-      mbar_init(v_empty(i), 1);
-      mbar_init(s_full(i), 1);
-      mbar_init(s_free(i), 1);
-      if (i == 1) {
-        mbar_init(s_full(2), 1);
-        mbar_init(s_free(2), 1);
-      }
-      mbar_init(p_full(i), 4);
-      mbar_init(pv_done(i), 1);
-    }
-    mbar_init(bar(kBarMmaDone), 1);   // every MMA issued has completed (before TMEM is freed)
-    for (int sl = 0; sl < 2; ++sl) {
-      mbar_init(item_full(sl), 1);
-      mbar_init(item_free(sl), 5);   // the MMA thread and the four softmax warps
+      mbar_init(bar(kBarVFull + i), 1);
+      mbar_init(item_full(i), 1);
+      mbar_init(item_free(i), 10);   // both MMA issuers and the eight softmax warps
     }
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
+  }
+  {
+    volatile unsigned long long* mb = reinterpret_cast<volatile unsigned long long*>(gbase + kOffX);
+    for (uint32_t i = threadIdx.x; i < kMailboxWords; i += kThreads) mb[i] = 0ull;
   }
   if (warp == 1) {
     __syncwarp();
@@ -233,35 +234,41 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;   // S buffers at columns 0, 128 and 256, O at 384
   constexpr uint32_t kOCol = 384;
 
+  // Takes item n from its ring slot (every consumer role, one arrival each).
+  auto take_item = [&](int n, int& L) -> bool {
+    const int sl = n & 1;
+    if (!mbar_wait(item_full(sl), (uint32_t)(n >> 1) & 1u, abort_flag, kWaitNs)) return false;
+    L = item_slot[sl];
+    return true;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // K blocks run two ahead of V blocks, as the scores do: K_j is free
-      // again once S_j is computed, V_j only once P_j V_j is.
+      // K blocks run two ahead of V blocks: K_j's stage is free again once
+      // S_j is computed, V_j's once P_j V_j is.
       uint32_t gk = 0, gv = 0;   // K and V blocks loaded so far (both number the CTA's blocks)
       int n = 0, nq = 0;         // items taken, Q tiles loaded
       bool ok = true;
       auto load_k = [&](const Item& it, int j) -> bool {
-        const int st = (int)(gk % kKStages);
-        if (!mbar_wait(k_empty(st), ((gk / kKStages) & 1u) ^ 1u, abort_flag, kWaitNs)) return false;
-        const uint32_t sk = sK + (uint32_t)st * kTileBytes;
-        mbar_arrive_expect_tx(k_full(st), kTileBytes);
-        tma_load_2d(sk, &p.tmK[it.r], k_full(st), it.h * kHeadDim, j * kTile);
-        tma_load_2d(sk + kHalf, &p.tmK[it.r], k_full(st), it.h * kHeadDim + 64, j * kTile);
+        if (gk >= 3u && !mbar_wait(s_full(gk - 3u), ph3(gk - 3u), abort_flag, kWaitNs)) return false;
+        const uint32_t sk = sK + (gk % 3u) * kTileBytes;
+        mbar_arrive_expect_tx(k_full(gk), kTileBytes);
+        tma_load_2d(sk, &p.tmK[it.r], k_full(gk), it.h * kHeadDim, j * kTile);
+        tma_load_2d(sk + kHalf, &p.tmK[it.r], k_full(gk), it.h * kHeadDim + 64, j * kTile);
         ++gk;
         return true;
       };
       auto load_v = [&](const Item& it, int j) -> bool {
-        const int st = (int)(gv & 1u);
-        if (!mbar_wait(v_empty(st), ((gv >> 1) & 1u) ^ 1u, abort_flag, kWaitNs)) return false;
-        const uint32_t sv = sV + (uint32_t)st * kTileBytes;
-        mbar_arrive_expect_tx(v_full(st), kTileBytes);
+        if (gv >= 2u && !mbar_wait(pv_done(gv - 2u), ph3(gv - 2u), abort_flag, kWaitNs)) return false;
+        const uint32_t sv = sV + (gv & 1u) * kTileBytes;
+        mbar_arrive_expect_tx(v_full(gv), kTileBytes);
         // V as the MN-major B operand: per 64 keys, two 64-column boxes.
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh)
 #pragma unroll
           for (int dh = 0; dh < 2; ++dh)
-            tma_load_2d(sv + (uint32_t)kh * kHalf + (uint32_t)dh * (kHalf / 2), &p.tmV[it.r], v_full(st),
+            tma_load_2d(sv + (uint32_t)kh * kHalf + (uint32_t)dh * (kHalf / 2), &p.tmV[it.r], v_full(gv),
                         it.h * kHeadDim + dh * 64, j * kTile + kh * 64);
         ++gv;
         return true;
@@ -290,236 +297,264 @@ __global__ void __launch_bounds__(kThreads, 1) fo_attn_kernel(const __grid_const
       }
       // Loads still in flight land before the CTA may exit.
       volatile int never = 0;
-      for (uint32_t k = gk > (uint32_t)kKStages ? gk - kKStages : 0u; k < gk; ++k)
-        mbar_wait(k_full((int)(k % kKStages)), (k / kKStages) & 1u, &never, 100000000ull);
+      for (uint32_t k = gk > 3u ? gk - 3u : 0u; k < gk; ++k) mbar_wait(k_full(k), ph3(k), &never, 100000000ull);
       for (uint32_t k = gv > 2u ? gv - 2u : 0u; k < gv; ++k)
-        mbar_wait(v_full((int)(k & 1u)), (k >> 1) & 1u, &never, 100000000ull);
+        mbar_wait(v_full(k), (k >> 1) & 1u, &never, 100000000ull);
       if (nq > 0) mbar_wait(q_full, (uint32_t)((nq - 1) & 1), &never, 100000000ull);
       if (*abort_flag) record_error(p.status, FO_ERR_TIMEOUT, -1, -1, 0);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ score MMAs
+    // S_j = Q K_j^T into score buffer j mod 3, as soon as K_j has landed and
+    // the weighted sum of P_{j-3} (the buffer's previous contents) is done:
+    // up to two blocks ahead of the softmax. A thread that issues
+    // tcgen05.mma runs at most a few instructions ahead of the tensor pipe,
+    // so the score and weighted-sum streams come from two warps: neither
+    // stream's waits hold up the other.
     if (lane == 0) {
       uint32_t g = 0;
       int n = 0;
-      bool ok = true;
-      auto pv = [&](uint32_t gp, bool first) -> bool {
-        const int b = (int)(gp & 1u);
-        if (!mbar_wait(p_full(b), (gp >> 1) & 1u, abort_flag, kWaitNs) ||
-            !mbar_wait(v_full(b), (gp >> 1) & 1u, abort_flag, kWaitNs))
-          return false;
-        if (first && !mbar_wait(o_free, (uint32_t)(n & 1) ^ 1u, abort_flag, kWaitNs)) return false;
-        tc_fence_after();
-        // A = P_j from TMEM: the first 64 columns of its score buffer, row i
-        // in lane i, two bf16 weights per column; 8 columns per 16 keys.
-        const uint32_t pa = tmem + (gp % 3u) * 128u;
-        const uint32_t vb = sV + (uint32_t)b * kTileBytes;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
-          const uint64_t bd = smem_desc_sw128(vb + kh * kHalf + kk * 2048u, kHalf / 2, 1024);
-          tc_mma_ts(tmem + kOCol, pa + (uint32_t)k * 8u, bd, idesc(true), (!first || k > 0) ? 1u : 0u);
-        }
-        tc_commit<1>(pv_done(b));
-        tc_commit<1>(v_empty(b));
-        tc_commit<1>(s_free(gp % 3u));   // P_j read: the buffer may take scores again
-        return true;
-      };
-      // S_{j+1} is issued before P_j V_j, so a score block waits in the pipe
-      // while the softmax warps work on block j. Its buffer last held P_{j-2},
-      // whose weighted sum completed before P_{j-1} could be written.
-      auto issue_s = [&](uint32_t gs) -> bool {
-        const int sb = (int)(gs % 3u);   // score buffer and K stage
-        const uint32_t ph = (gs / 3u) & 1u;
-        if (!mbar_wait(k_full(sb), ph, abort_flag, kWaitNs) || !mbar_wait(s_free(sb), ph ^ 1u, abort_flag, kWaitNs))
-          return false;
-        tc_fence_after();
-        const uint32_t kb = sK + (uint32_t)sb * kTileBytes;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
-          const uint64_t ad = smem_desc_sw128(sQ + kh * kHalf + kk * 32u, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(kb + kh * kHalf + kk * 32u, 16, 1024);
-          tc_mma<1, false>(tmem + (uint32_t)sb * 128u, ad, bd, idesc(false), k > 0 ? 1u : 0u);
-        }
-        tc_commit<1>(s_full(sb));
-        tc_commit<1>(k_empty(sb));
-        return true;
-      };
-      for (; ok; ++n) {
-        const int sl = n & 1;
-        if (!mbar_wait(item_full(sl), (uint32_t)(n >> 1) & 1u, abort_flag, kWaitNs)) break;
-        const int L = item_slot[sl];
-        mbar_arrive(item_free(sl));
+      for (;; ++n) {
+        int L;
+        if (!take_item(n, L)) break;
+        mbar_arrive(item_free(n & 1));
         if (L >= total) break;
         const Item it = decode(p, L);
         if (!mbar_wait(q_full, (uint32_t)(n & 1), abort_flag, kWaitNs)) break;
-        tc_fence_after();
-        const uint32_t g0 = g;
-        ok = issue_s(g0);
-        if (ok && it.nkb == 1) tc_commit<1>(q_empty);   // every score block of the item issued
-        for (int j = 0; j < it.nkb && ok; ++j) {
-          if (j + 1 < it.nkb) {
-            ok = issue_s(g0 + (uint32_t)j + 1u);
-            if (ok && j + 2 == it.nkb) tc_commit<1>(q_empty);
+        bool ok = true;
+        for (int j = 0; j < it.nkb; ++j, ++g) {
+          if (!mbar_wait(k_full(g), ph3(g), abort_flag, kWaitNs) ||
+              (g >= 3u && !mbar_wait(pv_done(g - 3u), ph3(g - 3u), abort_flag, kWaitNs))) {
+            ok = false;
+            break;
           }
-          if (ok) ok = pv(g0 + (uint32_t)j, j == 0);
+          tc_fence_after();
+          const uint32_t sb = g % 3u;
+          const uint32_t kb = sK + sb * kTileBytes;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+            const uint64_t ad = smem_desc_sw128(sQ + kh * kHalf + kk * 32u, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(kb + kh * kHalf + kk * 32u, 16, 1024);
+            tc_mma<1, false>(tmem + sb * 128u, ad, bd, idesc(false), k > 0 ? 1u : 0u);
+          }
+          tc_commit<1>(s_full(g));
         }
-        g = g0 + (uint32_t)it.nkb;
+        if (!ok) break;
+        tc_commit<1>(q_empty);   // every score block of the item issued
       }
       // Every issued MMA completes before TMEM is released.
-      tc_commit<1>(bar(kBarMmaDone));
+      tc_commit<1>(bar(kBarSDone));
       volatile int never = 0;
-      mbar_wait(bar(kBarMmaDone), 0, &never, 100000000ull);
+      mbar_wait(bar(kBarSDone), 0, &never, 100000000ull);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ weighted-sum MMAs
+    if (lane == 0) {
+      uint32_t g = 0;
+      int n = 0;
+      for (;; ++n) {
+        int L;
+        if (!take_item(n, L)) break;
+        mbar_arrive(item_free(n & 1));
+        if (L >= total) break;
+        const Item it = decode(p, L);
+        bool ok = true;
+        for (int j = 0; j < it.nkb; ++j, ++g) {
+          if (!mbar_wait(p_full(g), ph3(g), abort_flag, kWaitNs) ||
+              !mbar_wait(v_full(g), (g >> 1) & 1u, abort_flag, kWaitNs) ||
+              (j == 0 && !mbar_wait(o_free, (uint32_t)(n & 1) ^ 1u, abort_flag, kWaitNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // A = P_j from TMEM, in its score buffer: row i in lane i, two
+          // bf16 weights per column, 8 columns per 16 keys; keys 0-63 in
+          // columns 0-31, keys 64-127 in columns 64-95 (each softmax warp
+          // writes its weights over the first half of its own 64 score
+          // columns).
+          const uint32_t pa = tmem + (g % 3u) * 128u;
+          const uint32_t vb = sV + (g & 1u) * kTileBytes;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t kh = (uint32_t)(k >> 2), kk = (uint32_t)(k & 3);
+            const uint64_t bd = smem_desc_sw128(vb + kh * kHalf + kk * 2048u, kHalf / 2, 1024);
+            tc_mma_ts(tmem + kOCol, pa + kh * 64u + kk * 8u, bd, idesc(true), (j > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit<1>(pv_done(g));
+        }
+        if (!ok) break;
+      }
+      tc_commit<1>(bar(kBarPvDoneAll));
+      volatile int never = 0;
+      mbar_wait(bar(kBarPvDoneAll), 0, &never, 100000000ull);
     }
   } else {
     // ------------------------------------------------------------ softmax
+    // Warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, its quarter of
+    // the query rows. Warps 3-6 take keys 0-63 of every block and columns
+    // 0-63 of O, warps 7-10 keys 64-127 and columns 64-127. The two warps of
+    // a quarter swap their partial row maxima every block, and their partial
+    // row sums at the item's end, through mailboxes in shared memory: one
+    // 64-bit word per lane holds the exchange's sequence number and value,
+    // and the reader waits (bounded) for the number it expects.
     const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int sw = warp - kSoftWarp0;       // softmax warp 0..7
+    const int half = sw >> 2;               // which 64 keys / O columns
     const int row = q * 32 + lane;          // query row within the tile
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    volatile unsigned long long* const mbox = reinterpret_cast<volatile unsigned long long*>(gbase + kOffX);
+    uint32_t x = 0;                         // exchanges so far
+    // Two mailboxes a lane, by the exchange's parity: exchange x + 2
+    // overwrites exchange x's word only after this warp has read the
+    // partner's x + 1, which the partner writes after reading x.
+    auto swap = [&](float mine, float& theirs) -> bool {
+      ++x;
+      const int par = (int)(x & 1u);
+      mbox[(sw * 2 + par) * 32 + lane] = ((unsigned long long)x << 32) | __float_as_uint(mine);
+      volatile unsigned long long* const t = mbox + (((sw ^ 4) * 2 + par) * 32 + lane);
+      unsigned long long w = *t;
+      if ((uint32_t)(w >> 32) != x) {
+        const uint64_t t0 = globaltimer();
+        uint32_t n = 0;
+        while ((uint32_t)((w = *t) >> 32) != x) {
+          if ((++n & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+              *abort_flag = 1;
+              return false;
+            }
+          }
+        }
+      }
+      theirs = __uint_as_float((uint32_t)w);
+      return true;
+    };
     uint32_t g = 0;
-    int n = 0;
-    for (;; ++n) {
-      const int sl = n & 1;
-      if (!mbar_wait(item_full(sl), (uint32_t)(n >> 1) & 1u, abort_flag, kWaitNs)) break;
-      const int L = item_slot[sl];
+    for (int n = 0;; ++n) {
+      int L;
+      if (!take_item(n, L)) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(item_free(sl));
+      if (lane == 0) mbar_arrive(item_free(n & 1));
       if (L >= total) break;
       const Item it = decode(p, L);
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < it.nkb; ++j, ++g) {
-        const int b = (int)(g & 1u);      // P / weighted-sum barriers
-        const int sb = (int)(g % 3u);     // score buffer
-        if (!mbar_wait(s_full(sb), (g / 3u) & 1u, abort_flag, kWaitNs)) {
+        if (!mbar_wait(s_full(g), ph3(g), abort_flag, kWaitNs)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // The row's 128 scores: four TMEM loads, one wait.
-        uint32_t v[4][32];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lane_off + (uint32_t)sb * 128u + (uint32_t)cc * 32u, v[cc]);
+        // This warp's 64 scores of the row: two TMEM loads, one wait.
+        const uint32_t scol = tmem + lane_off + (g % 3u) * 128u + (uint32_t)half * 64u;
+        uint32_t v[2][32];
+        tmem_ld32(scol, v[0]);
+        tmem_ld32(scol + 32u, v[1]);
         tmem_ld_wait();
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) reg_fence(v[cc]);
+        reg_fence(v[0]);
+        reg_fence(v[1]);
         if (p.causal && j == it.nkb - 1) {
           // The block holding this tile's own keys: key t of the block is
           // query t of the tile, so the row sees keys 0..row.
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
+          for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
             for (int t = 0; t < 32; ++t)
-              if (cc * 32 + t > row) v[cc][t] = __float_as_uint(-INFINITY);
+              if (half * 64 + cc * 32 + t > row) v[cc][t] = __float_as_uint(-INFINITY);
         }
-        // Maximum and (below) sum over eight independent partial chains: one
-        // warp per scheduler has nothing else to hide a serial chain's latency.
+        // Maximum and (below) sum over eight independent partial chains.
         float mxs[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mxs[a] = -INFINITY;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
           for (int t = 0; t < 32; ++t) mxs[t & 7] = fmaxf(mxs[t & 7], __uint_as_float(v[cc][t]));
         float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
                          fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
-        mx *= p.scale_log2;   // log2 units (the scale is positive, so the maximum commutes)
+        float mx_other;
+        if (!__all_sync(0xffffffffu, swap(mx, mx_other))) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, mx_other) * p.scale_log2;   // log2 units (the scale is positive)
         const float m_use = (j == 0 || mx > m + kRescaleLog2) ? fmaxf(m, mx) : m;
         const float alpha = j == 0 ? 0.f : ex2_approx(m - m_use);
         float sums[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) sums[a] = 0.f;
         const float scl = p.scale_log2, neg = -m_use;
-        uint32_t w[2][32];
+        uint32_t w[32];
 #pragma unroll
-        for (int t = 0; t < 64; ++t) {
-          const int c0 = 2 * t;
-          const float e0 = ex2_approx(fmaf(__uint_as_float(v[c0 >> 5][c0 & 31]), scl, neg));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(v[(c0 + 1) >> 5][(c0 + 1) & 31]), scl, neg));
+        for (int t = 0; t < 32; ++t) {
+          const float e0 = ex2_approx(fmaf(__uint_as_float(v[t >> 4][(2 * t) & 31]), scl, neg));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(v[t >> 4][(2 * t + 1) & 31]), scl, neg));
           sums[t & 7] += e0 + e1;
-          w[t >> 5][t & 31] = pack_bf16(e0, e1);
+          w[t] = pack_bf16(e0, e1);
         }
         const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
-        // P_j in bf16 over the first 64 columns of its own score buffer
-        // (the scores are in registers now), the A operand of P_j V_j.
-        tmem_st32(tmem + lane_off + (uint32_t)sb * 128u, w[0]);
-        tmem_st32(tmem + lane_off + (uint32_t)sb * 128u + 32u, w[1]);
+        // P_j in bf16 over the first 32 of this warp's score columns (the
+        // scores are in registers now), the A operand of P_j V_j.
+        tmem_st32(scol, w);
         l = l * alpha + sum;
         m = m_use;
-        // Rescale this row of O when its maximum moved (after the weighted
-        // sum of the previous block has completed).
+        // Rescale this warp's half of the O row when the maximum moved
+        // (after the weighted sum of the previous block has completed).
         const bool need = j > 0 && alpha < 1.f;
         if (__any_sync(0xffffffffu, need)) {
-          const uint32_t gq = g - 1u;
-          if (!mbar_wait(pv_done((int)(gq & 1u)), (gq >> 1) & 1u, abort_flag, kWaitNs)) {
+          if (!mbar_wait(pv_done(g - 1u), ph3(g - 1u), abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const float a = need ? alpha : 1.f;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + kOCol + (uint32_t)cc * 32u, v);
+          for (int cc = 0; cc < 2; ++cc) {
+            const uint32_t oc = tmem + lane_off + kOCol + (uint32_t)(half * 64 + cc * 32);
+            uint32_t o[32];
+            tmem_ld32(oc, o);
             tmem_ld_wait();
-            reg_fence(v);
+            reg_fence(o);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * a);
-            tmem_st32(tmem + lane_off + kOCol + (uint32_t)cc * 32u, v);
+            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * a);
+            tmem_st32(oc, o);
           }
         }
         tmem_st_wait();   // P (and a rescaled O) are in TMEM before the weighted sum may read them
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full(b));
+        if (lane == 0) mbar_arrive(p_full(g));
       }
       if (!ok) break;
-      // The item's output: O / l in bf16, staged in this warp's own rows of
-      // the P buffer the last weighted sum read (the rows this warp alone
-      // writes), then TMA-stored, 64 columns x 32 rows per op.
-      const uint32_t gl = g - 1u;
-      if (!mbar_wait(pv_done((int)(gl & 1u)), (gl >> 1) & 1u, abort_flag, kWaitNs)) break;
+      // The row's sum over all 128 keys of every block, then the item's
+      // output: this warp's 64 columns of O / sum in bf16, stored straight
+      // from registers (128 contiguous bytes a row).
+      float l_other;
+      if (!__all_sync(0xffffffffu, swap(l, l_other))) break;
+      const float inv = 1.f / (l + l_other);
+      if (!mbar_wait(pv_done(g - 1u), ph3(g - 1u), abort_flag, kWaitNs)) break;
       tc_fence_after();
-      if (lane == 0) bulk_wait_read<0>();   // the previous item's output store has read the staging rows
-      __syncwarp();
-      const float inv = 1.f / l;
-      const uint32_t stage = sP + (uint32_t)q * 4096u;
-#pragma unroll
-      for (int dh = 0; dh < 2; ++dh) {
-        uint32_t w[32];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + kOCol + (uint32_t)(dh * 64 + cc * 32), v);
-          tmem_ld_wait();
-          reg_fence(v);
-#pragma unroll
-          for (int t = 0; t < 16; ++t)
-            w[cc * 16 + t] = pack_bf16(__uint_as_float(v[2 * t]) * inv, __uint_as_float(v[2 * t + 1]) * inv);
-        }
-        // 32 rows x 128 B per box, rows indexed by lane: the half dh of the
-        // P buffer, this warp's 32 rows.
-        const uint32_t rb = stage + (uint32_t)dh * kHalf + (uint32_t)lane * 128u;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(rb + ((uint32_t)(j ^ (lane & 7)) << 4)),
-                       "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
-                       : "memory");
-      }
+      uint32_t o[2][32];
+      tmem_ld32(tmem + lane_off + kOCol + (uint32_t)half * 64u, o[0]);
+      tmem_ld32(tmem + lane_off + kOCol + (uint32_t)half * 64u + 32u, o[1]);
+      tmem_ld_wait();
+      reg_fence(o[0]);
+      reg_fence(o[1]);
       tc_fence_before();
-      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(o_free);
-        tma_store_2d(&p.tmO[it.r], stage, it.h * kHeadDim, it.q0 + q * 32);
-        tma_store_2d(&p.tmO[it.r], stage + kHalf, it.h * kHeadDim + 64, it.q0 + q * 32);
-        bulk_commit();
+      if (lane == 0) mbar_arrive(o_free);   // the next item's first weighted sum may overwrite O
+      uint4* dst = reinterpret_cast<uint4*>(p.O[it.r] + (size_t)(it.q0 + row) * (size_t)p.ld +
+                                            (size_t)(it.h * kHeadDim + half * 64));
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t* s8 = &o[c >> 2][(c & 3) * 8];
+        dst[c] = make_uint4(pack_bf16(__uint_as_float(s8[0]) * inv, __uint_as_float(s8[1]) * inv),
+                            pack_bf16(__uint_as_float(s8[2]) * inv, __uint_as_float(s8[3]) * inv),
+                            pack_bf16(__uint_as_float(s8[4]) * inv, __uint_as_float(s8[5]) * inv),
+                            pack_bf16(__uint_as_float(s8[6]) * inv, __uint_as_float(s8[7]) * inv));
       }
-      __syncwarp();
     }
-    if (lane == 0) bulk_wait<0>();
-    __syncwarp();
   }
 
   tc_fence_before();
@@ -602,7 +637,7 @@ fo_status launch_attention(fo_plan_t p, const void* const* Q, const void* const*
     ok &= enc(&k.tmQ[r], Q[r], (uint64_t)width, (uint64_t)T, 64, 128);
     ok &= enc(&k.tmK[r], K[r], (uint64_t)width, (uint64_t)T, 64, 128);
     ok &= enc(&k.tmV[r], V[r], (uint64_t)width, (uint64_t)T, 64, 64);
-    ok &= enc(&k.tmO[r], O[r], (uint64_t)width, (uint64_t)T, 64, 32);
+    k.O[r] = static_cast<uint16_t*>(O[r]);
   }
   if (!ok) return FO_ERR_CUDA;
   memcpy(k.table, p->table, sizeof(k.table));
@@ -613,6 +648,7 @@ fo_status launch_attention(fo_plan_t p, const void* const* Q, const void* const*
   k.heads = heads;
   k.causal = causal;
   k.qtiles = (int32_t)(T / R / fo_attn::kTile);
+  k.ld = (int32_t)width;
   k.scale_log2 = (float)(1.4426950408889634 / sqrt((double)fo_attn::kHeadDim));
   k.status = static_cast<int32_t*>(ws);
   const int total = R * R * heads * k.qtiles;
