@@ -659,21 +659,22 @@ def measure_other_workloads(B, dev, stream, iters=20):
         del inp, A, Bm, Y, ws
         torch.cuda.empty_cache()
     # Query-split attention with its output projection (causal, the layer's
-    # attention shape): the whole call, and the projection alone, so the
-    # attention launch's time is their difference.
+    # attention shape): the whole call, the attention launch alone
+    # (fo_attention) and the projection alone.
     a = _attn_setup(B, dev)
     for _ in range(3):
         a["call"](stream)
     t_all = _time(lambda: a["call"](stream), stream, iters=10)
+    t_attn = _time(lambda: a["attn"](stream), stream, iters=10)
     t_proj = _time(lambda: a["proj"](stream), stream, iters=10)
     code, info = B.fo_status_query(a["plan"], a["ws"], stream)
     if code != 0:
         raise RuntimeError(f"device status {code} {info} (attention)")
-    t_attn = t_all - t_proj
     out[ATTN_WORKLOAD] = {"ms": t_all, "tflops": a["flops"] / t_all / 1e9,
                           "frac_of_burst_peak": a["flops"] / t_all / 1e9 / burst,
                           "attention_ms": t_attn, "attention_tflops": a["attn_flops"] / t_attn / 1e9,
                           "attention_frac_of_burst_peak": a["attn_flops"] / t_attn / 1e9 / burst,
+                          "attention_traffic": profiled_traffic(ATTN_WORKLOAD, ATTN_SOURCES, "attention"),
                           "projection_ms": t_proj, "projection_tflops": a["proj_flops"] / t_proj / 1e9,
                           "launches": 2, "flops": a["flops"],
                           "flops_note": "causal attention counts the lower triangle: 2 x 2 x T x T x 128 / 2 per head"}
