@@ -151,6 +151,39 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Packed fp32 pairs (PTX .f32x2 arithmetic, sm_100 and later): each lane of
+// the pair is rounded exactly as the scalar instruction would round it.
+using f32x2 = unsigned long long;
+__device__ __forceinline__ f32x2 f2(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(f32x2 r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Maximum of three (one instruction).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -408,11 +441,12 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __gr
     // Two mailboxes a lane, by the exchange's parity: exchange x + 2
     // overwrites exchange x's word only after this warp has read the
     // partner's x + 1, which the partner writes after reading x.
-    auto swap = [&](float mine, float& theirs) -> bool {
+    auto post = [&](float mine) {
       ++x;
-      const int par = (int)(x & 1u);
-      mbox[(sw * 2 + par) * 32 + lane] = ((unsigned long long)x << 32) | __float_as_uint(mine);
-      volatile unsigned long long* const t = mbox + (((sw ^ 4) * 2 + par) * 32 + lane);
+      mbox[(sw * 2 + (int)(x & 1u)) * 32 + lane] = ((unsigned long long)x << 32) | __float_as_uint(mine);
+    };
+    auto fetch = [&](float& theirs) -> bool {
+      volatile unsigned long long* const t = mbox + (((sw ^ 4) * 2 + (int)(x & 1u)) * 32 + lane);
       unsigned long long w = *t;
       if ((uint32_t)(w >> 32) != x) {
         const uint64_t t0 = globaltimer();
@@ -463,37 +497,57 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __gr
             for (int t = 0; t < 32; ++t)
               if (half * 64 + cc * 32 + t > row) v[cc][t] = __float_as_uint(-INFINITY);
         }
-        // Maximum and (below) sum over eight independent partial chains.
+        // This half's row maximum (raw scores): three-input maxima over eight
+        // independent chains.
         float mxs[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mxs[a] = -INFINITY;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc)
+        for (int t = 0; t < 32; ++t)
+          mxs[t & 7] = max3(mxs[t & 7], __uint_as_float(v[t >> 4][(2 * t) & 31]),
+                            __uint_as_float(v[t >> 4][(2 * t + 1) & 31]));
+        const float mxl = max3(max3(mxs[0], mxs[1], mxs[2]), max3(mxs[3], mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])) *
+                          p.scale_log2;   // log2 units (the scale is positive)
+        post(mxl);
+        // 2^(s * scale - m) for the row's 64 keys: the argument by packed
+        // FMAs, the power on the MUFU, the row sum over four packed chains,
+        // the weights packed to bf16.
+        float sum = 0.f;
+        uint32_t w[32];
+        auto exps = [&](float mm) {
+          const f32x2 scl2 = f2(p.scale_log2, p.scale_log2), neg2 = f2(-mm, -mm);
+          f32x2 acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-          for (int t = 0; t < 32; ++t) mxs[t & 7] = fmaxf(mxs[t & 7], __uint_as_float(v[cc][t]));
-        float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                         fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+          for (int t = 0; t < 32; ++t) {
+            float x0, x1;
+            f2_split(fma2(f2(__uint_as_float(v[t >> 4][(2 * t) & 31]), __uint_as_float(v[t >> 4][(2 * t + 1) & 31])),
+                          scl2, neg2),
+                     x0, x1);
+            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            acc[t & 3] = add2(acc[t & 3], f2(e0, e1));
+            w[t] = pack_bf16(e0, e1);
+          }
+          float s0, s1, s2, s3;
+          f2_split(add2(acc[0], acc[1]), s0, s1);
+          f2_split(add2(acc[2], acc[3]), s2, s3);
+          sum = (s0 + s1) + (s2 + s3);
+        };
+        // While the partner's maximum is on its way, compute the weights with
+        // the running maximum: they are final unless the maximum moves (by
+        // more than 8), which a half whose own maximum stays below m + 8
+        // learns from the partner's value. Weights computed this way are at
+        // most 2^8.
+        const bool spec = j > 0 && mxl <= m + kRescaleLog2;
+        if (spec) exps(m);
         float mx_other;
-        if (!__all_sync(0xffffffffu, swap(mx, mx_other))) {
+        if (!__all_sync(0xffffffffu, fetch(mx_other))) {
           ok = false;
           break;
         }
-        mx = fmaxf(mx, mx_other) * p.scale_log2;   // log2 units (the scale is positive)
+        const float mx = fmaxf(mxl, mx_other);
         const float m_use = (j == 0 || mx > m + kRescaleLog2) ? fmaxf(m, mx) : m;
         const float alpha = j == 0 ? 0.f : ex2_approx(m - m_use);
-        float sums[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) sums[a] = 0.f;
-        const float scl = p.scale_log2, neg = -m_use;
-        uint32_t w[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const float e0 = ex2_approx(fmaf(__uint_as_float(v[t >> 4][(2 * t) & 31]), scl, neg));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(v[t >> 4][(2 * t + 1) & 31]), scl, neg));
-          sums[t & 7] += e0 + e1;
-          w[t] = pack_bf16(e0, e1);
-        }
-        const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
+        if (!spec || m_use != m) exps(m_use);
         // P_j in bf16 over the first 32 of this warp's score columns (the
         // scores are in registers now), the A operand of P_j V_j.
         tmem_st32(scol, w);
@@ -516,8 +570,14 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __gr
             tmem_ld32(oc, o);
             tmem_ld_wait();
             reg_fence(o);
+            const f32x2 a2 = f2(a, a);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * a);
+            for (int t = 0; t < 32; t += 2) {
+              float r0, r1;
+              f2_split(mul2(f2(__uint_as_float(o[t]), __uint_as_float(o[t + 1])), a2), r0, r1);
+              o[t] = __float_as_uint(r0);
+              o[t + 1] = __float_as_uint(r1);
+            }
             tmem_st32(oc, o);
           }
         }
@@ -531,7 +591,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __gr
       // output: this warp's 64 columns of O / sum in bf16, stored straight
       // from registers (128 contiguous bytes a row).
       float l_other;
-      if (!__all_sync(0xffffffffu, swap(l, l_other))) break;
+      post(l);
+      if (!__all_sync(0xffffffffu, fetch(l_other))) break;
       const float inv = 1.f / (l + l_other);
       if (!mbar_wait(pv_done(g - 1u), ph3(g - 1u), abort_flag, kWaitNs)) break;
       tc_fence_after();
@@ -546,13 +607,16 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __gr
       if (lane == 0) mbar_arrive(o_free);   // the next item's first weighted sum may overwrite O
       uint4* dst = reinterpret_cast<uint4*>(p.O[it.r] + (size_t)(it.q0 + row) * (size_t)p.ld +
                                             (size_t)(it.h * kHeadDim + half * 64));
+      const f32x2 inv2 = f2(inv, inv);
+      auto scaled = [&](uint32_t a, uint32_t b) {
+        float r0, r1;
+        f2_split(mul2(f2(__uint_as_float(a), __uint_as_float(b)), inv2), r0, r1);
+        return pack_bf16(r0, r1);
+      };
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint32_t* s8 = &o[c >> 2][(c & 3) * 8];
-        dst[c] = make_uint4(pack_bf16(__uint_as_float(s8[0]) * inv, __uint_as_float(s8[1]) * inv),
-                            pack_bf16(__uint_as_float(s8[2]) * inv, __uint_as_float(s8[3]) * inv),
-                            pack_bf16(__uint_as_float(s8[4]) * inv, __uint_as_float(s8[5]) * inv),
-                            pack_bf16(__uint_as_float(s8[6]) * inv, __uint_as_float(s8[7]) * inv));
+        dst[c] = make_uint4(scaled(s8[0], s8[1]), scaled(s8[2], s8[3]), scaled(s8[4], s8[5]), scaled(s8[6], s8[7]));
       }
     }
   }
