@@ -106,8 +106,11 @@ def _check_all(Q, K, V, Wo, O, Y, heads, causal, out="f32"):
         assert fro <= O_FRO, f"Y shard {d} end to end: rel fro {fro:.3e}"
 
 
+# Query blocks of T/R rows hold (T/R)/128 tiles: one, two, three and four
+# tiles per block, R = 1 to 4.
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("R,T,heads,H", [(1, 256, 1, 256), (2, 512, 2, 384), (4, 1024, 1, 512)])
+@pytest.mark.parametrize("R,T,heads,H", [(1, 256, 1, 256), (2, 512, 2, 384), (4, 1024, 1, 512),
+                                         (2, 256, 1, 256), (2, 768, 2, 256), (3, 1152, 1, 384)])
 def test_attn_rs_matches_the_oracle(dev, R, T, heads, H, causal):
     res = run_attn(dev, R, T, heads, H, causal, seed=R * 10 + heads)
     _check_all(*res, heads, causal)
@@ -120,9 +123,10 @@ def test_attn_rs_sharp_scores_and_bf16_output(dev, causal):
     _check_all(*res, 1, causal, out="bf16")
 
 
+@pytest.mark.parametrize("T", [768, 1024])
 @pytest.mark.parametrize("causal", [False, True])
-def test_attn_rs_growing_maximum_is_rescaled(dev, causal):
-    res = run_attn(dev, 2, 1024, 1, 256, causal, seed=8, growing_keys=True)
+def test_attn_rs_growing_maximum_is_rescaled(dev, causal, T):
+    res = run_attn(dev, 2, T, 1, 256, causal, seed=8, growing_keys=True)
     _check_all(*res, 1, causal)
 
 
