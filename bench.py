@@ -466,7 +466,10 @@ def run_ours(args):
     if code != 0:
         raise RuntimeError(f"device status {code} {info}")
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # The timed region holds nothing but the fused kernel's launches, back
+    # to back on one stream: its average launch duration is the region's
+    # CUDA-event time over the launch count (events between the launches
+    # would add their own gaps).
     launches = 0
     with ClockSampler(_smi_id(dev)) as clk:
         if world > 1:
@@ -477,9 +480,7 @@ def run_ours(args):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for i in range(args.steps):
-            ev[i][0].record(stream)
             step()
-            ev[i][1].record(stream)
             launches += B.fo_plan_last_launches(plan)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
@@ -490,7 +491,7 @@ def run_ours(args):
     code, info = B.fo_status_query(plan, ws, stream)
     if code != 0:
         raise RuntimeError(f"device status {code} {info}")
-    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    kernel_ms = elapsed_ms / args.steps   # one launch a step
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
     ms_per_step = elapsed_ms / args.steps
@@ -754,22 +755,25 @@ def run_other_op(args, w, dev, world, rank):
 
     for _ in range(max(args.warmup, 3)):
         step()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # Only this op's launches, back to back: the region's event time over
+    # the step count is the average launch duration.
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(_smi_id(dev)) as clk:
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
         clk.mark("t0")
+        t0.record(stream)
         for i in range(args.steps):
-            ev[i][0].record(stream)
             step()
-            ev[i][1].record(stream)
+        t1.record(stream)
         torch.cuda.synchronize(dev)
         clk.mark("t1")
     code, info = B.fo_status_query(plan, ws, stream)
     if code != 0:
         raise RuntimeError(f"device status {code} {info}")
-    elapsed_ms = ev[0][0].elapsed_time(ev[-1][1])
+    elapsed_ms = t0.elapsed_time(t1)
     if w.op == "gemm_a2a":
         e2e = measure_e2e(B, lambda: B.fo_plan("gemm_a2a", R, M, Nr, K),
                           lambda p, din, dout, ws_, s_: B.fo_gemm_a2a(p, din[0], din[1], dout, ws_, s_),
@@ -785,7 +789,7 @@ def run_other_op(args, w, dev, world, rank):
                           lambda p, din, dout, ws_, s_: B.fo_dp_grad_rs(p, din[0], din[1], dout, ws_, s_),
                           [inp["X"], inp["dY"]], [A, Bm], Y, dev, stream, world, w.flops(),
                           max(4, min(args.steps, 12)))
-    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    kernel_ms = elapsed_ms / args.steps
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     flops = w.flops()
     peaks, peak_src = load_peaks()
