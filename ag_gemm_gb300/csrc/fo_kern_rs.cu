@@ -8,6 +8,7 @@ cudaError_t fo_variant_rs(int v, bool pair, const fo::FoParams* p, int grid, cud
     case FO_V_RS_BF16_KN: return FO_DISPATCH_PAIR(fo::EPI_RS, false, true, false);
     case FO_V_RS_BF16_NK: return FO_DISPATCH_PAIR(fo::EPI_RS, false, false, false);
     case FO_V_RS_TF32_NK: return FO_DISPATCH_SINGLE(fo::EPI_RS, false, false, true);
+    case FO_V_RS_BF16_KN_SK: return FO_DISPATCH_PAIR_SK(fo::EPI_RS, false, true, false);
   }
   return cudaErrorInvalidValue;
 }

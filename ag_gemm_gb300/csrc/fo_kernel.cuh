@@ -67,7 +67,10 @@ namespace fo {
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBuf = 32 * 128;              // 32 rows x 128 bytes
 // Staging buffers per epilogue warp and pipeline depths (overridable at
-// build time; the defaults fill the 227 KB of shared memory).
+// build time; the defaults fill the 227 KB of shared memory). The short-
+// reduction variant (SK) of the CTA-pair kernel trades a pipeline stage for
+// two more staging buffers per warp: with few k-blocks per tile the
+// epilogue, not the operand stream, sets the pace.
 #ifndef FO_EPI_BUFS
 #define FO_EPI_BUFS 2
 #endif
@@ -77,7 +80,12 @@ constexpr int kEpiBuf = 32 * 128;              // 32 rows x 128 bytes
 #ifndef FO_SINGLE_STAGES
 #define FO_SINGLE_STAGES 4
 #endif
-constexpr int kEpiBufs = FO_EPI_BUFS;
+#ifndef FO_SK_EPI_BUFS
+#define FO_SK_EPI_BUFS 4
+#endif
+#ifndef FO_SK_PAIR_STAGES
+#define FO_SK_PAIR_STAGES 5
+#endif
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 // AG variants that also move X shards into the gather buffers G_r carry four
 // more warps; a piece is 32 rows of one shard.
@@ -88,9 +96,11 @@ constexpr int kBarBytes = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kMbarLimitNs = 2000000000ull;
 
-template <bool PAIR>
+template <bool PAIR, bool SK = false>
 struct Cfg {
-  static constexpr int kStages = PAIR ? FO_PAIR_STAGES : FO_SINGLE_STAGES;
+  static_assert(!SK || PAIR, "the short-reduction variant has CTA-pair tiles");
+  static constexpr int kStages = PAIR ? (SK ? FO_SK_PAIR_STAGES : FO_PAIR_STAGES) : FO_SINGLE_STAGES;
+  static constexpr int kEpiBufs = SK ? FO_SK_EPI_BUFS : FO_EPI_BUFS;
   static constexpr int kAStage = FO_BM * FO_BK_BYTES;                       // 16 KB
   static constexpr int kBRows = PAIR ? FO_BN / 2 : FO_BN;                   // B rows (N) in this CTA
   static constexpr int kBStage = kBRows * FO_BK_BYTES;                      // 16 or 32 KB
@@ -347,11 +357,12 @@ __device__ __forceinline__ void read_row_sw128(uint32_t buf, int lane, float (&f
 // GST: peer-read all-gather with a gather buffer and narrow outputs: the
 // producer writes every A stage it loaded for a tile of the first column
 // block back out to G_r, instead of mover warps copying the shards.
-template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false, bool GST = false>
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false, bool GST = false, bool SK = false>
 __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(const __grid_constant__ FoParams p) {
   static_assert(!MOV || EPI == EPI_AG, "movers belong to the all-gather kernel");
   static_assert(!GST || (EPI == EPI_AG && !MOV), "gather stores replace the movers of the all-gather kernel");
-  using C = Cfg<PAIR>;
+  using C = Cfg<PAIR, SK>;
+  constexpr int kEpiBufs = C::kEpiBufs;
   constexpr int CG = PAIR ? 2 : 1;
   constexpr int kStages = C::kStages;
   constexpr int kEsz = TF32 ? 4 : 2;
@@ -1147,6 +1158,7 @@ enum fo_variant {
   FO_V_AG_BF16_NK_MOV,
   FO_V_AG_BF16_KN_GST,
   FO_V_AG_BF16_NK_GST,
+  FO_V_RS_BF16_KN_SK,   // GEMM-RS with few k-blocks a task (CTA pairs only)
   FO_V_COUNT
 };
 

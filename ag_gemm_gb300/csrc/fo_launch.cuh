@@ -3,10 +3,10 @@
 
 #include "fo_kernel.cuh"
 
-template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false, bool GST = false>
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false, bool GST = false, bool SK = false>
 cudaError_t fo_launch_one(const fo::FoParams& p, int grid, cudaStream_t stream) {
-  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV, GST>;
-  constexpr int smem = fo::Cfg<PAIR>::kSmemBytes;
+  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV, GST, SK>;
+  constexpr int smem = fo::Cfg<PAIR, SK>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -34,10 +34,10 @@ cudaError_t fo_launch_one(const fo::FoParams& p, int grid, cudaStream_t stream) 
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false, bool GST = false>
+template <int EPI, bool A_MN, bool B_MN, bool TF32, bool PAIR, bool MOV = false, bool GST = false, bool SK = false>
 cudaError_t fo_max_ctas_one(int* ctas) {
-  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV, GST>;
-  constexpr int smem = fo::Cfg<PAIR>::kSmemBytes;
+  auto kern = fo::fo_chunk_gemm_kernel<EPI, A_MN, B_MN, TF32, PAIR, MOV, GST, SK>;
+  constexpr int smem = fo::Cfg<PAIR, SK>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -73,6 +73,11 @@ cudaError_t fo_max_ctas_one(int* ctas) {
                 : fo_launch_one<EPI, A_MN, B_MN, TF32, true>(*p, grid, s))                     \
         : (ctas ? fo_max_ctas_one<EPI, A_MN, B_MN, TF32, false>(ctas)                         \
                 : fo_launch_one<EPI, A_MN, B_MN, TF32, false>(*p, grid, s)))
+// The short-reduction variant: CTA pairs only.
+#define FO_DISPATCH_PAIR_SK(EPI, A_MN, B_MN, TF32)                                           \
+  (pair ? (ctas ? fo_max_ctas_one<EPI, A_MN, B_MN, TF32, true, false, false, true>(ctas)      \
+                : fo_launch_one<EPI, A_MN, B_MN, TF32, true, false, false, true>(*p, grid, s)) \
+        : cudaErrorInvalidValue)
 #define FO_DISPATCH_SINGLE(EPI, A_MN, B_MN, TF32)                                            \
   (pair ? cudaErrorInvalidValue                                                               \
         : (ctas ? fo_max_ctas_one<EPI, A_MN, B_MN, TF32, false>(ctas)                         \
