@@ -616,6 +616,8 @@ def _attn_setup(B, dev, R=8, T=8192, heads=4, H=4096, causal=True, seed=12):
             "mk_plan": lambda: B.fo_plan("gemm_rs", R, T, H, R * w),
             "call": lambda s: B.fo_attn_rs(plan, Q, K, V, Wo, O, Y, heads, causal, ws, s),
             "attn": lambda s: B.fo_attention(plan, Q, K, V, O, heads, causal, ws, s),
+            "attn_noncausal": lambda s: B.fo_attention(plan, Q, K, V, O, heads, False, ws, s),
+            "attn_noncausal_flops": attn_flops / (0.5 if causal else 1.0),
             "proj": lambda s: B.fo_gemm_rs(pplan, O, Wo, Y, pws, s)}
 
 
@@ -864,6 +866,7 @@ def run_attn(args, dev, world, rank):
         clk.mark("t1")
         attn_ms = _loop_ms(a["attn"], stream, dev, steps)
         proj_ms = _loop_ms(a["proj"], stream, dev, steps)
+        full_ms = _loop_ms(a["attn_noncausal"], stream, dev, steps)
     code, info = B.fo_status_query(a["plan"], a["ws"], stream)
     if code != 0:
         raise RuntimeError(f"device status {code} {info}")
@@ -900,6 +903,12 @@ def run_attn(args, dev, world, rank):
                                   "flops": a["attn_flops"]},
                     "projection_rs": {"ms": proj_ms, "tflops": proj_tf, "frac_of_burst_peak": proj_tf / burst,
                                       "flops": a["proj_flops"]},
+                    # The same launch without the causal mask (every query
+                    # sees every key): uniform items, twice the work.
+                    "attention_noncausal": {"ms": full_ms,
+                                            "tflops": a["attn_noncausal_flops"] / (full_ms * 1e-3) / 1e12,
+                                            "frac_of_burst_peak": a["attn_noncausal_flops"] / (full_ms * 1e-3) / 1e12 / burst,
+                                            "flops": a["attn_noncausal_flops"]},
                     "step_frac_of_peak": value / world / peak,
                     "step_peak_source": ("bf16_tflops_sustained" if sustained else "bf16_tflops (burst)")},
         "e2e": e2e,
