@@ -84,7 +84,7 @@ constexpr uint32_t kMailboxWords = 8 * 2 * 32;
 constexpr uint32_t kOffBar = kOffX + kMailboxWords * 8;
 constexpr int kSmemBytes = 1024 + (int)kOffBar + 512;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kWaitNs = 2000000000ull;   // every wait's bound
 constexpr float kRescaleLog2 = 8.0f;
 
 // kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, A
@@ -106,6 +106,10 @@ struct AttnParams {
   int32_t ld;                            // heads * 128
   float scale_log2;                      // log2(e) / sqrt(128)
   int32_t* status;
+  // Test hook (the plan's FO_INJECT_SKIP_SIGNAL): the first softmax warp of
+  // CTA 0 does not report its first weights, so that CTA's weighted-sum
+  // wait runs out and the launch reports FO_ERR_TIMEOUT.
+  int32_t skip_signal;
 };
 
 struct Item {
@@ -334,7 +338,6 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __gr
       for (uint32_t k = gv > 2u ? gv - 2u : 0u; k < gv; ++k)
         mbar_wait(v_full(k), (k >> 1) & 1u, &never, 100000000ull);
       if (nq > 0) mbar_wait(q_full, (uint32_t)((nq - 1) & 1), &never, 100000000ull);
-      if (*abort_flag) record_error(p.status, FO_ERR_TIMEOUT, -1, -1, 0);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ score MMAs
@@ -438,6 +441,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __gr
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     volatile unsigned long long* const mbox = reinterpret_cast<volatile unsigned long long*>(gbase + kOffX);
     uint32_t x = 0;                         // exchanges so far
+    const bool skip_first = p.skip_signal != 0 && blockIdx.x == 0 && sw == 0;   // test hook
     // Two mailboxes a lane, by the exchange's parity: exchange x + 2
     // overwrites exchange x's word only after this warp has read the
     // partner's x + 1, which the partner writes after reading x.
@@ -584,7 +588,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __gr
         tmem_st_wait();   // P (and a rescaled O) are in TMEM before the weighted sum may read them
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full(g));
+        if (lane == 0 && !(skip_first && g == 0)) mbar_arrive(p_full(g));
       }
       if (!ok) break;
       // The row's sum over all 128 keys of every block, then the item's
@@ -628,9 +632,12 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) fo_attn_kernel(const __gr
     __syncwarp();
     tmem_dealloc<1>(tmem, 512);
   }
-  // The last CTA to finish resets the item counter for the next launch
-  // (every CTA has stopped taking items by then).
+  // A wait that ran out anywhere in the CTA (every role has left its loops
+  // by now) is reported in the workspace status word. The last CTA to
+  // finish resets the item counter for the next launch (every CTA has
+  // stopped taking items by then).
   if (threadIdx.x == 0) {
+    if (*abort_flag) record_error(p.status, FO_ERR_TIMEOUT, -1, -1, 0);
     __threadfence();
     if (atomicAdd(ctr + 1, 1u) == gridDim.x - 1) {
       atomicExch(ctr, 0u);
@@ -715,6 +722,7 @@ fo_status launch_attention(fo_plan_t p, const void* const* Q, const void* const*
   k.ld = (int32_t)width;
   k.scale_log2 = (float)(1.4426950408889634 / sqrt((double)fo_attn::kHeadDim));
   k.status = static_cast<int32_t*>(ws);
+  k.skip_signal = p->d.fault_inject == FO_INJECT_SKIP_SIGNAL ? 1 : 0;
   const int total = R * R * heads * k.qtiles;
   const int grid = total < sms ? total : sms;
   auto kern = fo_attn::fo_attn_kernel;

@@ -332,8 +332,12 @@ fo_status fo_gemm_a2a(fo_plan_t plan, const void* const* X, const void* const* W
  * The softmax weights are rounded to bf16 for the tensor cores' weighted
  * sum, and O once to bf16. Requires heads >= 1 and T/R a multiple of 128;
  * FO_ERR_SHAPE when K != R * heads * 128 or T/R is not; FO_ERR_INVALID_ARG
- * for another op, fp32 inputs, heads < 1 or causal not 0 or 1. Device-side
- * waits are bounded and report through fo_status_query like fo_gemm_rs. */
+ * for another op, fp32 inputs, heads < 1 or causal not 0 or 1. Every
+ * device-side wait of the attention launch gives up after 2 s (the plan's
+ * timeout_ns bounds the projection's waits) and reports through
+ * fo_status_query like fo_gemm_rs; a plan with FO_INJECT_SKIP_SIGNAL (tests)
+ * makes one softmax signal of the attention launch go missing, so that a
+ * wait runs out and the call reports FO_ERR_TIMEOUT. */
 fo_status fo_attn_rs(fo_plan_t plan, const void* const* Q, const void* const* K, const void* const* V,
                      const void* const* Wo, void* const* O, void* const* Y, int32_t heads, int32_t causal,
                      void* ws, fo_stream_t stream);

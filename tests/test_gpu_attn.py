@@ -200,3 +200,30 @@ def test_attention_alone_matches_attn_rs_and_resets_its_counter(dev, causal):
         q, k, v = _np(Q[r]), _np(K[r]), _np(V[r])
         ref = oracle.round_bf16(oracle.attention(q, k, v, heads, causal))
         _check_o(_np(O1[r]), ref, oracle.attention(q, k, np.abs(v), heads, causal), f"O rank {r}")
+
+
+def test_attention_wait_that_runs_out_reports_and_the_next_call_is_exact(dev):
+    # One softmax warp of CTA 0 withholds its first "weights written" signal
+    # (the plan's skip_signal hook): that CTA's weighted-sum wait runs out
+    # (the attention launch's waits give up after 2 s), every role leaves
+    # its loops, and the call reports FO_ERR_TIMEOUT. fo_status_query then zeroes the workspace, and
+    # a clean call on the same buffers is exact, with the item counter back
+    # at zero.
+    R, T, heads, H = 2, 1024, 2, 256
+    Q, K, V, Wo = _inputs(R, T, heads, H, seed=31)
+    bad = B.fo_plan("gemm_rs", R, T, H, R * heads * D, fault_inject="skip_signal")
+    good = B.fo_plan("gemm_rs", R, T, H, R * heads * D)
+    ws = torch.zeros(max(B.fo_workspace_size(bad), B.fo_workspace_size(good)), dtype=torch.uint8, device=dev)
+    dQ, dK, dV = ([t.to(dev) for t in ts] for ts in (Q, K, V))
+    O = [torch.empty(T, heads * D, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    B.fo_attention(bad, dQ, dK, dV, O, heads, True, ws)
+    code, info = B.fo_status_query(bad, ws)
+    assert code == B.FO_ERR_TIMEOUT, (code, info)
+    assert ws[24:32].view(torch.int32).tolist() == [0, 0]
+    B.fo_attention(good, dQ, dK, dV, O, heads, True, ws)
+    assert B.fo_status_query(good, ws)[0] == 0
+    assert ws[24:32].view(torch.int32).tolist() == [0, 0]
+    for r in range(R):
+        q, k, v = _np(Q[r]), _np(K[r]), _np(V[r])
+        ref = oracle.round_bf16(oracle.attention(q, k, v, heads, True))
+        _check_o(_np(O[r]), ref, oracle.attention(q, k, np.abs(v), heads, True), f"O rank {r}")
