@@ -87,15 +87,14 @@ bool enc3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t d0,
 // Kernel variant of a GEMM-RS / GEMM-AR plan: bf16 operands with W as
 // [K x N] (B MN-major) or [N x K] (B K-major); tf32 operands always with B
 // K-major (a W given as [K x N] is first transposed into the workspace).
-// A direct fp32 reduce-scatter over CTA pairs with at most 12 k-blocks a
-// task (K_r <= 768) runs the short-reduction variant: one pipeline stage
-// fewer, twice the epilogue's staging buffers. On the attention
-// projection (K_r = 512) that took 0.351 ms to 0.320 ms; on the
+// A direct reduce-scatter over CTA pairs with at most 12 k-blocks a task
+// (K_r <= 768) runs the short-reduction variant: one pipeline stage fewer,
+// twice the epilogue's staging buffers. On the attention projection
+// (K_r = 512, fp32 out) that took 0.351 ms to 0.320 ms; on the
 // 8192 x 1792 x 4096 reduce-scatter (28 k-blocks) the same split cost 6%.
 int rs_variant(fo_plan_t p) {
   if (p->elem_bytes == 4) return FO_V_RS_TF32_NK;
-  if (p->d.w_layout == FO_W_KN && p->pair && p->num_kb <= 12 && p->d.op == FO_OP_GEMM_RS && !p->ring &&
-      p->d.out_dtype == FO_F32)
+  if (p->d.w_layout == FO_W_KN && p->pair && p->num_kb <= 12 && p->d.op == FO_OP_GEMM_RS && !p->ring)
     return FO_V_RS_BF16_KN_SK;
   return p->d.w_layout == FO_W_KN ? FO_V_RS_BF16_KN : FO_V_RS_BF16_NK;
 }
