@@ -227,3 +227,12 @@ def test_attention_wait_that_runs_out_reports_and_the_next_call_is_exact(dev):
         q, k, v = _np(Q[r]), _np(K[r]), _np(V[r])
         ref = oracle.round_bf16(oracle.attention(q, k, v, heads, True))
         _check_o(_np(O[r]), ref, oracle.attention(q, k, np.abs(v), heads, True), f"O rank {r}")
+
+
+@pytest.mark.parametrize("R,T,heads,H,causal", [(16, 2048, 1, 256, True), (16, 4096, 1, 256, False),
+                                                (2, 512, 8, 256, True), (8, 2048, 4, 512, False)])
+def test_attn_rs_more_ranks_and_heads(dev, R, T, heads, H, causal):
+    # The largest rank count (16 query blocks of one tile each, or two),
+    # eight heads per rank, and R = 8 without the mask.
+    res = run_attn(dev, R, T, heads, H, causal, seed=R + heads)
+    _check_all(*res, heads, causal)
