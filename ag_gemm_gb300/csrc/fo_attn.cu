@@ -15,7 +15,7 @@
 //      tile) in the plan's task order, O_r = softmax(Q K^T / sqrt(128) +
 //      mask) V, written bf16 into the caller's O_r;
 //   2. the fused GEMM + reduce-scatter (fo_gemm_rs) of O_r . Wo_r.
-// On one GPU the reduce-scatter's transfers are the second launch's L2
+// fo_attention runs the first launch alone. On one GPU the reduce-scatter's transfers are the second launch's L2
 // reduce-adds, already overlapped with its own math; the first launch
 // computes the attention in the same query-block order.
 //
@@ -37,16 +37,20 @@
 //               it waits for the softmax;
 //   warps 3-10  softmax: two warps per 32-row quarter of the tile, each over
 //               64 of a block's 128 keys. A thread takes its row's 64 scores
-//               from TMEM, the two warps swap partial row maxima, and each
-//               writes its bf16 weights over its own score columns. The
+//               from TMEM, the two warps swap partial row maxima (each
+//               computes its weights with the running maximum while the
+//               partner's value is in flight, and again only if the
+//               maximum moved), and each writes its bf16 weights over its
+//               own score columns. The
 //               running maximum only moves when it grows by more than 8 in
 //               log2 units (a smaller growth keeps the old one: the weights
 //               then stay below 2^8 and the final division by the sum
 //               cancels the choice); when it moves, each warp rescales its 64
 //               columns of the TMEM output row. At the item's end the partial
 //               sums are swapped and O / sum is stored in bf16 from registers.
-// Every wait is bounded; a wait that runs out raises the CTA's abort flag and
-// records FO_ERR_TIMEOUT in the workspace status word.
+// Every wait gives up after 2 s; a wait that runs out raises the CTA's abort
+// flag, every role leaves its loops, and the CTA records FO_ERR_TIMEOUT in
+// the workspace status word.
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdio.h>
