@@ -40,7 +40,7 @@ EXPORTED = [
     "fo_status_query", "fo_gemm_partials", "fo_reduce_scatter_f32", "fo_all_gather_copy",
     "fo_plan_last_launches", "fo_status_string", "fo_version", "fo_gemm_rs_noalloc", "fo_plan_task_order",
     "fo_gemm_ar", "fo_trace_query", "fo_plan_last_split_tiles", "fo_check_device_pointers",
-    "fo_gemm_a2a", "fo_all_to_all_copy", "fo_attn_rs", "fo_attention",
+    "fo_gemm_a2a", "fo_all_to_all_copy", "fo_attn_rs", "fo_attention", "fo_gemm_partials_sharded",
 ]
 
 
@@ -98,6 +98,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "fo_all_to_all_copy": ([P, PP, PP, P], c_int32),
         "fo_attn_rs": ([P, PP, PP, PP, PP, PP, PP, c_int32, c_int32, P, P], c_int32),
         "fo_attention": ([P, PP, PP, PP, PP, c_int32, c_int32, P, P], c_int32),
+        "fo_gemm_partials_sharded": ([P, PP, PP, PP, P, P], c_int32),
         "fo_status_query": ([P, P, P, POINTER(c_int32)], c_int32),
         "fo_trace_query": ([P, P, P, POINTER(ctypes.c_uint64), c_int32, POINTER(c_int32)], c_int32),
         "fo_gemm_partials": ([P, PP, PP, PP, P, P], c_int32),
@@ -307,6 +308,11 @@ def fo_dp_grad_rs(plan: Plan, X, dY, dW, ws, stream=None) -> None:
 def fo_gemm_partials(plan: Plan, A, B, P, ws, stream=None) -> None:
     _check(load().fo_gemm_partials(plan, _ptr_array(A), _ptr_array(B), _ptr_array(P), _ptr(ws),
                                    _stream(stream)), "fo_gemm_partials")
+
+
+def fo_gemm_partials_sharded(plan: Plan, A_shards, B, P, ws, stream=None) -> None:
+    _check(load().fo_gemm_partials_sharded(plan, _ptr_array(A_shards), _ptr_array(B), _ptr_array(P), _ptr(ws),
+                                           _stream(stream)), "fo_gemm_partials_sharded")
 
 
 def fo_check_device_pointers(ptrs, stream=None) -> int:

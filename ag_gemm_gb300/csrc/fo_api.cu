@@ -106,7 +106,7 @@ float* wt_copy(fo_plan_t p, void* ws, int r) {
   return reinterpret_cast<float*>(static_cast<char*>(ws) + p->ws_wt_off + (size_t)r * p->ws_wt_stride);
 }
 
-enum CallKind { KIND_NONE = 0, KIND_RS = 1, KIND_DP = 2, KIND_AG = 3, KIND_PART = 4, KIND_A2A = 5 };
+enum CallKind { KIND_NONE = 0, KIND_RS = 1, KIND_DP = 2, KIND_AG = 3, KIND_PART = 4, KIND_A2A = 5, KIND_PART_SHARDED = 6 };
 
 // Returns the cached parameter block when the same call kind is made with
 // the same pointers again, else nullptr.
@@ -731,6 +731,50 @@ fo_status fo_gemm_a2a(fo_plan_t p, const void* const* X, const void* const* W, v
   if ((st = build_a2a(p, X, W, Y, ws, (cudaStream_t)stream, &k))) return st;
   return run_chunk_gemm(p, p->d.w_layout == FO_W_KN ? FO_V_AG_BF16_KN : FO_V_AG_BF16_NK, k, di,
                         (cudaStream_t)stream);
+}
+
+fo_status fo_gemm_partials_sharded(fo_plan_t p, const void* const* A, const void* const* B, void* const* P,
+                                   void* ws, fo_stream_t stream) {
+  if (!p || !ws) return FO_ERR_INVALID_ARG;
+  if (p->d.op != FO_OP_DP_GRAD_RS || p->elem_bytes != 2) return FO_ERR_INVALID_ARG;
+  const int R = p->R;
+  const uint64_t kr = (uint64_t)p->k_red;                  // T: the reduction, split into R shards of rows
+  const uint32_t bk = FO_BK_BYTES / 2;
+  if (kr % (uint64_t)R || (kr / (uint64_t)R) % bk) return FO_ERR_SHAPE;   // a k-block never straddles two shards
+  fo_status st;
+  if ((st = check_ptrs(R, A)) || (st = check_ptrs(R, B)) || (st = check_ptrs(R, (const void* const*)P))) return st;
+  DevInfo di;
+  if ((st = preflight(p, &di))) return st;
+  const uint64_t M = (uint64_t)p->d.M, N = (uint64_t)p->n_out, rpc = (uint64_t)p->rows_per_chunk;
+  // Shards that lie back to back in rank order already form the gathered
+  // A: one tensor map over all of it, the same for every rank. Otherwise
+  // one map per shard, picked per k-block (measured on GB300 at the
+  // layer's 8192 x 4096 shapes: 20-35% slower than one map).
+  const uint64_t shard_bytes = kr / (uint64_t)R * M * 2;
+  bool adjacent = true;
+  for (int s = 1; s < R; ++s)
+    adjacent &= static_cast<const char*>(A[s]) == static_cast<const char*>(A[0]) + s * shard_bytes;
+  fo::FoParams* k = cached_params(p, KIND_PART_SHARDED, A, B, (const void* const*)P);
+  if (!k) {
+    if ((st = check_call_ptrs(R, A, B, (const void* const*)P, nullptr, ws, (cudaStream_t)stream))) return st;
+    k = fresh_params(p);
+    if (!k) return FO_ERR_INVALID_ARG;
+    bool ok = true;
+    for (int r = 0; r < R && ok; ++r) {
+      if (adjacent) ok &= enc2d(&k->tmA[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A[0], M, kr, M * 2, bk, bk);
+      else ok &= enc2d(&k->tmA[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A[r], M, kr / (uint64_t)R, M * 2, bk, bk);
+      ok &= enc2d(&k->tmB[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B[r], N, kr, N * 2, bk, bk);
+      ok &= enc3d(&k->tmD[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, P[r], N, rpc, R, N * 4, rpc * N * 4, 32, 32);
+    }
+    if (!ok) return FO_ERR_CUDA;
+    remember(p, KIND_PART_SHARDED, A, B, (const void* const*)P);
+    p->param_cache_ws = ws;
+  }
+  fill_common(p, k, ws);
+  k->completion = fo::FO_COMPLETE_NONE;
+  k->ring = 0;
+  k->a_shard_rows = adjacent ? 0 : (int32_t)(kr / (uint64_t)R);
+  return run_chunk_gemm(p, FO_V_PART_DP, k, di, (cudaStream_t)stream);
 }
 
 fo_status fo_gemm_partials(fo_plan_t p, const void* const* A, const void* const* B, void* const* P, void* ws,

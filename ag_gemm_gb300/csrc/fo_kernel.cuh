@@ -175,6 +175,11 @@ struct alignas(128) FoParams {
   float* sk_buf;
   uint32_t* sk_ctr;
   CUtensorMap tmSK;
+  // MN-major A given as R row shards of a_shard_rows rows each (0: one A per
+  // rank): the rows of k-block kb come from shard kb * kBK / a_shard_rows,
+  // whose map is tmA[shard]. Every task reads the same A, in place: the
+  // all-gather of the shards, without a gathered copy.
+  int32_t a_shard_rows;
 };
 
 enum Completion : int { FO_COMPLETE_NONE = 0, FO_COMPLETE_BF16 = 1, FO_COMPLETE_ALLREDUCE = 2 };
@@ -517,12 +522,22 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
               g_r[stage] = ti.r, g_c[stage] = ti.c, g_row[stage] = a_mn0, g_k[stage] = k0, g_it[stage] = it;
             }
           }
+          // A given as row shards: this k-block's rows are in one shard.
+          const CUtensorMap* mAk = mA;
+          int kA = k0;
+          if constexpr (A_MN) {
+            if (p.a_shard_rows) {
+              const int src = k0 / p.a_shard_rows;
+              mAk = &p.tmA[src];
+              kA = k0 - src * p.a_shard_rows;
+            }
+          }
           if constexpr (PAIR) {
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
             if (leader) mbar_arrive_expect_tx(full_bar(stage), kTxBytes);
             if constexpr (A_MN) {
 #pragma unroll
-              for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d_pair(sa + j * kBoxBytes, mA, fb, a_mn0 + j * kBK, k0);
+              for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d_pair(sa + j * kBoxBytes, mAk, fb, a_mn0 + j * kBK, kA);
             } else {
               tma_load_2d_pair(sa, mA, fb, k0, a_mn0);
             }
@@ -538,7 +553,7 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
             mbar_arrive_expect_tx(fb, kTxBytes);
             if constexpr (A_MN) {
 #pragma unroll
-              for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d(sa + j * kBoxBytes, mA, fb, a_mn0 + j * kBK, k0);
+              for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d(sa + j * kBoxBytes, mAk, fb, a_mn0 + j * kBK, kA);
             } else {
               tma_load_2d(sa, mA, fb, k0, a_mn0);
             }

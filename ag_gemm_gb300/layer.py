@@ -24,6 +24,10 @@ transposed, as AllGather(dY)^T . X_r, i.e. in the nn.Linear layout
 [out x in] = [H x H/R] and [H x F/R]: the per-rank GEMM then splits H rows
 into R chunks of H/R rows instead of H/R or F/R rows into R chunks (64 or
 224 rows for the default shape, which fill 128- and 256-row tiles poorly).
+Each weight gradient contracts over all T tokens of an all-gathered
+operand; it reads the R token shards where they lie, so no gathered copy
+of x, h, dy or dh is written. Those shards are allocated back to back in
+rank order, which the weight-gradient call reads as one tensor.
 
 The attention core, the SwiGLU and the norms are not part of the path: their
 outputs (attn_r, act_r) and upstream gradients are fixed synthetic tensors.
@@ -67,9 +71,18 @@ class TpspLayerProjections:
     """Buffers, plans and launches for one layer's projections (R virtual ranks
     on one GPU). `mode="randn"` draws weights ~N(0, 0.02) and activations /
     gradients ~N(0, 1); `mode="int"` draws integers in [-4, 4] so every sum
-    is exact in fp32."""
+    is exact in fp32.
 
-    def __init__(self, shape: LayerShape = LayerShape(), *, device="cuda", seed=4, mode="randn"):
+    The weight gradients after an all-gather GEMM (dWqkv, dWug, dWd, dWo)
+    contract over the gathered tokens. By default they read the R row shards
+    where they lie (fo_gemm_partials_sharded) and the all-gather GEMMs keep
+    no gathered copy; `keep_gathered=True` has the all-gather GEMMs write the
+    gathered inputs (Gx, Gh, G_dy, G_dh) and the weight gradients read those,
+    as a framework that saves the gathered activation for its backward
+    would."""
+
+    def __init__(self, shape: LayerShape = LayerShape(), *, device="cuda", seed=4, mode="randn",
+                 keep_gathered=False):
         self.s = s = shape
         R, T, H, F = s.R, s.T, s.H, s.F
         if T % R or H % R or F % R:
@@ -83,26 +96,35 @@ class TpspLayerProjections:
         def per_rank(shp, dtype=bf):
             return [torch.empty(shp, dtype=dtype, device=dev) for _ in range(R)]
 
+        def token_shards(draw, shp):
+            # The R token shards of a sequence-parallel tensor, back to back
+            # in rank order: their all-gather is the whole buffer.
+            whole = torch.cat([draw(shp) for _ in range(R)]) if draw else torch.empty((R * shp[0], shp[1]),
+                                                                                      dtype=bf, device=dev)
+            return list(whole.split(shp[0]))
+
         # weights (each rank's slice)
         self.Wqkv = [w((H, 3 * H // R)) for _ in range(R)]
         self.Wo = [w((H // R, H)) for _ in range(R)]
         self.Wug = [w((H, 2 * F // R)) for _ in range(R)]
         self.Wd = [w((F // R, H)) for _ in range(R)]
         # forward inputs and the synthetic outputs of the skipped parts
-        self.x = [a((T // R, H)) for _ in range(R)]
+        self.x = token_shards(a, (T // R, H))
         self.attn = [a((T, H // R)) for _ in range(R)]
         self.act = [a((T, F // R)) for _ in range(R)]
         # upstream gradients
-        self.dy = [a((T // R, H)) for _ in range(R)]        # into the down projection's output
-        self.dh = [a((T // R, H)) for _ in range(R)]        # into the o projection's output
+        self.dy = token_shards(a, (T // R, H))              # into the down projection's output
+        self.dh = token_shards(a, (T // R, H))              # into the o projection's output
         self.dug = [a((T, 2 * F // R)) for _ in range(R)]   # into up|gate's output (through SwiGLU)
         self.dqkv = [a((T, 3 * H // R)) for _ in range(R)]  # into QKV's output (through attention)
-        # forward outputs (and the gathered inputs kept for the weight gradients)
-        self.Gx, self.Gh = per_rank((T, H)), per_rank((T, H))
+        # forward outputs (and, if kept, the gathered inputs for the weight gradients)
+        self.keep_gathered = keep_gathered
+        gathered = per_rank if keep_gathered else (lambda shp: None)
+        self.Gx, self.Gh = gathered((T, H)), gathered((T, H))
         self.y_qkv, self.y_ug = per_rank((T, 3 * H // R)), per_rank((T, 2 * F // R))
-        self.h, self.y = per_rank((T // R, H)), per_rank((T // R, H))
+        self.h, self.y = token_shards(None, (T // R, H)), per_rank((T // R, H))
         # backward outputs
-        self.G_dy, self.G_dh = per_rank((T, H)), per_rank((T, H))
+        self.G_dy, self.G_dh = gathered((T, H)), gathered((T, H))
         self.d_act, self.d_attn = per_rank((T, F // R)), per_rank((T, H // R))
         self.d_h_from_ug, self.d_x = per_rank((T // R, H)), per_rank((T // R, H))
         self.dWd, self.dWo = per_rank((H, F // R), f32), per_rank((H, H // R), f32)   # [out x in]
@@ -139,20 +161,28 @@ class TpspLayerProjections:
         B.fo_gemm_rs(P["down"], self.act, self.Wd, self.y, ws["down"], stream)
         self.launches += 4
 
+    def _weight_grad(self, key, G, shards, dY, dW, stream):
+        """dW_r = AllGather(shards)^T . dY_r for every rank: from the
+        gathered copy G when it was kept, else from the shards in place."""
+        if G is not None:
+            B.fo_gemm_partials(self.plans[key], G, dY, dW, self.ws[key], stream)
+        else:
+            B.fo_gemm_partials_sharded(self.plans[key], shards, dY, dW, self.ws[key], stream)
+
     def backward(self, stream=None):
         P, ws = self.plans, self.ws
         # down (row-parallel): dAct = AG(dy) . Wd^T, dWd^T = AG(dy)^T . act
         B.fo_ag_gemm(P["down_dx"], self.dy, self.Wd, self.d_act, self.G_dy, ws["down_dx"], stream)
-        B.fo_gemm_partials(P["down_dw"], self.G_dy, self.act, self.dWd, ws["down_dw"], stream)
-        # up|gate (column-parallel): dh = RS(dug . Wug^T), dWug = Gh^T . dug
+        self._weight_grad("down_dw", self.G_dy, self.dy, self.act, self.dWd, stream)
+        # up|gate (column-parallel): dh = RS(dug . Wug^T), dWug = AG(h)^T . dug
         B.fo_gemm_rs(P["ug_dx"], self.dug, self.Wug, self.d_h_from_ug, ws["ug_dx"], stream)
-        B.fo_gemm_partials(P["ug_dw"], self.Gh, self.dug, self.dWug, ws["ug_dw"], stream)
+        self._weight_grad("ug_dw", self.Gh, self.h, self.dug, self.dWug, stream)
         # o (row-parallel): dAttn = AG(dh) . Wo^T, dWo^T = AG(dh)^T . attn
         B.fo_ag_gemm(P["o_dx"], self.dh, self.Wo, self.d_attn, self.G_dh, ws["o_dx"], stream)
-        B.fo_gemm_partials(P["o_dw"], self.G_dh, self.attn, self.dWo, ws["o_dw"], stream)
-        # QKV (column-parallel): dx = RS(dqkv . Wqkv^T), dWqkv = Gx^T . dqkv
+        self._weight_grad("o_dw", self.G_dh, self.dh, self.attn, self.dWo, stream)
+        # QKV (column-parallel): dx = RS(dqkv . Wqkv^T), dWqkv = AG(x)^T . dqkv
         B.fo_gemm_rs(P["qkv_dx"], self.dqkv, self.Wqkv, self.d_x, ws["qkv_dx"], stream)
-        B.fo_gemm_partials(P["qkv_dw"], self.Gx, self.dqkv, self.dWqkv, ws["qkv_dw"], stream)
+        self._weight_grad("qkv_dw", self.Gx, self.x, self.dqkv, self.dWqkv, stream)
         self.launches += 8
 
     def status(self) -> List[int]:

@@ -338,6 +338,21 @@ fo_status fo_gemm_a2a(fo_plan_t plan, const void* const* X, const void* const* W
  * fo_status_query like fo_gemm_rs; a plan with FO_INJECT_SKIP_SIGNAL (tests)
  * makes one softmax signal of the attention launch go missing, so that a
  * wait runs out and the call reports FO_ERR_TIMEOUT. */
+/* fo_gemm_partials for a DP_GRAD_RS plan whose A operand is the all-gather
+ * of R row shards, read where they are: A_shards[s] is shard s [K/R x M]
+ * bf16 (rows s*K/R .. of the gathered A [K x M], K the plan's reduction,
+ * i.e. tokens), and every rank r computes P_r = A^T . B_r, B_r [K x N]
+ * bf16, into P_r [R x M/R x N] fp32 like fo_gemm_partials. This is the
+ * weight gradient that follows an all-gather GEMM (dW_r = AllGather(X)^T .
+ * dY_r) without a gathered copy of X: the gather buffers of fo_ag_gemm can
+ * be left out. Shards that lie back to back in rank order (A_shards[s] =
+ * A_shards[0] + s*K/R*M elements) are read as one [K x M] tensor; others
+ * through one tensor map per shard, which ran 20-35% slower on GB300.
+ * Requires K/R to be a multiple of 64; FO_ERR_SHAPE otherwise,
+ * FO_ERR_INVALID_ARG for another op or fp32 inputs. One launch. */
+fo_status fo_gemm_partials_sharded(fo_plan_t plan, const void* const* A_shards, const void* const* B,
+                                   void* const* P, void* ws, fo_stream_t stream);
+
 fo_status fo_attn_rs(fo_plan_t plan, const void* const* Q, const void* const* K, const void* const* V,
                      const void* const* Wo, void* const* O, void* const* Y, int32_t heads, int32_t causal,
                      void* ws, fo_stream_t stream);

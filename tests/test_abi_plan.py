@@ -498,3 +498,17 @@ def test_attention_alone_rejects_bad_arguments_on_the_host():
         with pytest.raises(B.FlashOverlapError) as e:
             call(plan, heads, causal, V)
         assert e.value.code == code
+
+
+def test_partials_sharded_rejects_bad_arguments_on_the_host():
+    fake = [16 * (i + 1) for i in range(4)]
+    dp = B.fo_plan("dp_grad_rs", 4, 512, 256, 1024)
+    for plan, A, code in ((B.fo_plan("gemm_rs", 4, 512, 256, 1024), fake, B.FO_ERR_INVALID_ARG),
+                          (B.fo_plan("ag_gemm", 4, 512, 256, 1024), fake, B.FO_ERR_INVALID_ARG),
+                          (B.fo_plan("dp_grad_rs", 4, 512, 256, 1026), fake, B.FO_ERR_SHAPE),  # T % R
+                          (B.fo_plan("dp_grad_rs", 4, 512, 256, 1040), fake, B.FO_ERR_SHAPE),  # T/R % 64
+                          (dp, [16, 32, 0, 64], B.FO_ERR_INVALID_ARG),              # a null shard
+                          (dp, [16, 32, 40, 64], B.FO_ERR_ALIGN)):                  # a shard off 16 bytes
+        with pytest.raises(B.FlashOverlapError) as e:
+            B.fo_gemm_partials_sharded(plan, A, fake, fake, 4096, stream=0)
+        assert e.value.code == code

@@ -427,6 +427,46 @@ def test_partials_control_stores_each_ranks_gemm(dev):
         assert np.array_equal(_np(Y[d]), ref[d])
 
 
+
+@pytest.mark.parametrize("placement", ["separate", "back_to_back"])
+@pytest.mark.parametrize("R,T,M,N", [(2, 128, 256, 64), (4, 768, 800, 328), (8, 1024, 512, 136)])
+def test_partials_sharded_reads_the_gather_in_place(dev, R, T, M, N, placement):
+    """fo_gemm_partials_sharded: A = AllGather of R row shards of [T/R x M],
+    read where the shards lie (separate allocations: one tensor map per
+    shard; back to back: one map); P_r = A^T . dY_r for every rank, bit for
+    bit (integer inputs make the fp32 sums exact)."""
+    inp = dp_grad_inputs(R, T, M, N, mode="int", seed=11)
+    shards = list(inp["X"][0].split(T // R))
+    if placement == "separate":
+        A = [a.to(dev) for a in shards]
+    else:
+        A = list(inp["X"][0].to(dev).split(T // R))
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T)
+    P = Guarded(R, (M, N), torch.float32, dev)
+    ws = _ws(plan, dev)
+    B.fo_gemm_partials_sharded(plan, A, [y.to(dev) for y in inp["dY"]], P.views, ws)
+    _status_ok(plan, ws)
+    P.check()
+    G = oracle.all_gather_rows([_np(a) for a in shards])
+    ref = oracle.weight_grads([G] * R, [_np(y) for y in inp["dY"]])
+    for r in range(R):
+        assert np.array_equal(_np(P.views[r]), ref[r]), f"rank {r}"
+
+
+def test_partials_sharded_random_bf16_within_tolerance(dev):
+    R, T, M, N = 4, 2048, 1024, 512
+    inp = dp_grad_inputs(R, T, M, N, mode="randn", seed=12)
+    shards = list(inp["X"][0].split(T // R))
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T)
+    P = [torch.empty(M, N, device=dev) for _ in range(R)]
+    ws = _ws(plan, dev)
+    B.fo_gemm_partials_sharded(plan, [a.to(dev) for a in shards], [y.to(dev) for y in inp["dY"]], P, ws)
+    _status_ok(plan, ws)
+    G = oracle.all_gather_rows([_np(a) for a in shards])
+    ref = oracle.weight_grads([G] * R, [_np(y) for y in inp["dY"]])
+    for r in range(R):
+        _assert_close(_np(P[r]), ref[r])
+
 def test_all_gather_copy(dev):
     R, M, K, N = 4, 512, 256, 512
     inp = ag_gemm_inputs(R, M, K, N // R, mode="randn", seed=4)
