@@ -70,8 +70,8 @@ def test_backward_projections(layer):
     d_x = oracle.gemm_rs(dqkv, _T(Wqkv))
     dWd = oracle.weight_grads(act, [G_dy] * R)
     dWo = oracle.weight_grads(attn, [G_dh] * R)
-    dWug = oracle.weight_grads(Gh, dug)
-    dWqkv = oracle.weight_grads(Gx, dqkv)
+    dWug = oracle.weight_grads([Gh] * R, dug)
+    dWqkv = oracle.weight_grads([Gx] * R, dqkv)
     for r in range(R):
         assert np.array_equal(_np(L.d_act[r]), oracle.round_bf16(d_act[r]))
         assert np.array_equal(_np(L.d_attn[r]), oracle.round_bf16(d_attn[r]))
