@@ -1,5 +1,6 @@
 """Seeded random shapes for every op (reduce-scatter with bf16 and fp32
-inputs, all-gather, DP gradient, all-reduce, all-to-all): R from 1 to 16, ragged rows, K and N,
+inputs, all-gather, DP gradient, the weight gradient over token shards,
+all-reduce, all-to-all): R from 1 to 16, ragged rows, K and N,
 either tile configuration, any interleave, both weight layouts and output
 dtypes, with the tail split forced on in about half the draws. Integer inputs, so every result must equal the oracle bit for bit
 (bf16 outputs: the oracle rounded once); guard bands around every output.
@@ -118,6 +119,33 @@ def test_random_dp_grad_rs(dev, seed):
         want = ref[d] if out == "f32" else oracle.round_bf16(ref[d])
         assert np.array_equal(_np(dW.views[d]), want), f"R={R} T={T} M={M} N={N} {tile} {il} {out} {split} shard {d}"
 
+
+
+@pytest.mark.parametrize("seed", range(CASES))
+def test_random_partials_sharded(dev, seed):
+    # The gathered A given as R token shards (64-row multiples), either
+    # separate allocations or back to back; P_r = AllGather(A)^T . dY_r.
+    g, R, rows, _, N = _draw(9000 + seed)
+    M = R * rows
+    T = R * 64 * int(g.integers(1, 5))
+    tile = ["auto", "single"][int(g.integers(2))]
+    il = INTERLEAVES[int(g.integers(len(INTERLEAVES)))]
+    split = SPLITS[int(g.integers(2))]
+    adjacent = bool(g.integers(2))
+    inp = dp_grad_inputs(R, T, M, N, mode="int", seed=seed)
+    whole = inp["X"][0]
+    A = list(whole.to(dev).split(T // R)) if adjacent else [a.to(dev) for a in whole.split(T // R)]
+    plan = B.fo_plan("dp_grad_rs", R, M, N, T, tile_config=tile, interleave=il, tail_split=split)
+    P = Guarded(R, (M, N), torch.float32, dev)
+    ws = _ws(plan, dev)
+    B.fo_gemm_partials_sharded(plan, A, [y.to(dev) for y in inp["dY"]], P.views, ws)
+    _status_ok(plan, ws)
+    P.check()
+    ref = oracle.weight_grads([oracle.all_gather_rows([_np(a) for a in whole.split(T // R)])] * R,
+                              [_np(y) for y in inp["dY"]])
+    for r in range(R):
+        assert np.array_equal(_np(P.views[r]), ref[r]), \
+            f"R={R} T={T} M={M} N={N} {tile} {il} {split} adjacent={adjacent} rank {r}"
 
 @pytest.mark.parametrize("seed", range(CASES))
 def test_random_gemm_ar(dev, seed):
