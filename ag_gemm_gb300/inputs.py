@@ -69,7 +69,7 @@ def dp_grad_inputs(R: int, T: int, M: int, N: int, *, dtype="bf16", mode="randn"
 class Workload:
     """One named workload: the op, the virtual rank count and the global sizes."""
     name: str
-    op: str            # "gemm_rs" | "ag_gemm" | "dp_grad_rs" | "gemm_a2a"
+    op: str            # "gemm_rs" | "gemm_ar" | "ag_gemm" | "dp_grad_rs" | "gemm_a2a"
     R: int
     dims: Dict[str, int] = field(default_factory=dict)
     dtype: str = "bf16"
@@ -78,7 +78,7 @@ class Workload:
 
     def flops(self) -> float:
         d = self.dims
-        if self.op == "gemm_rs":
+        if self.op in ("gemm_rs", "gemm_ar"):
             return 2.0 * self.R * d["M"] * d["N"] * d["K"]
         if self.op == "ag_gemm":
             return 2.0 * self.R * d["M"] * d["N"] * d["K"]
@@ -90,7 +90,7 @@ class Workload:
 
     def make(self, **kw):
         d = self.dims
-        if self.op == "gemm_rs":
+        if self.op in ("gemm_rs", "gemm_ar"):
             return gemm_rs_inputs(self.R, d["M"], d["K"], d["N"], dtype=self.dtype,
                                   mode=self.mode, seed=self.seed, **kw)
         if self.op in ("ag_gemm", "gemm_a2a"):
@@ -102,10 +102,10 @@ class Workload:
         raise ValueError(self.op)
 
 
-# The named workloads. Sizes are global: M rows of the RS output / gathered
-# sequence, K the per-rank reduction size (RS) or hidden size (AG, A2A), N the
-# output width per rank (AG) or total (RS, A2A: all R head groups), T tokens
-# (DP grad). The all-to-all draws its inputs like the all-gather: X_r
+# The named workloads. Sizes are global: M rows of the RS / AR output /
+# gathered sequence, K the per-rank reduction size (RS, AR) or hidden size
+# (AG, A2A), N the output width per rank (AG) or total (RS, AR, A2A: all R
+# head groups), T tokens (DP grad). The all-to-all draws its inputs like the all-gather: X_r
 # [M/R x K], then W_r [K x N] (the whole projection on every rank).
 WORKLOADS = {
     "gemm_rs_int_r2_256x512x512": Workload("gemm_rs_int_r2_256x512x512", "gemm_rs", 2,
@@ -114,6 +114,10 @@ WORKLOADS = {
                                                  {"M": 4096, "K": 4096, "N": 3072}, "bf16", "randn", 1),
     "gemm_rs_down_r8_t8192_k1792_n4096": Workload("gemm_rs_down_r8_t8192_k1792_n4096", "gemm_rs", 8,
                                                   {"M": 8192, "K": 1792, "N": 4096}, "bf16", "randn", 2),
+    # The fused all-reduce (reduce-scatter, then every finished tile copied
+    # into every rank's full output) on the down projection's shape.
+    "gemm_ar_r8_t8192_k1792_n4096": Workload("gemm_ar_r8_t8192_k1792_n4096", "gemm_ar", 8,
+                                             {"M": 8192, "K": 1792, "N": 4096}, "bf16", "randn", 2),
     "dp_grad_rs_r8_t4096_4096x4096": Workload("dp_grad_rs_r8_t4096_4096x4096", "dp_grad_rs", 8,
                                               {"T": 4096, "M": 4096, "N": 4096}, "bf16", "randn", 3),
     # Ulysses QKV projection of the Llama-like layer's shape: 8192 tokens

@@ -67,6 +67,11 @@ def algorithmic_bytes(w) -> float:
         M, K, N = d["M"], d["K"], d["N"]
         eb = 4 if w.dtype == "f32" else 2
         return R * (M * K + K * N) * eb + 2.0 * (R - 1) * M * N * 4 + M * N * 4
+    if w.op == "gemm_ar":
+        # The reduce-scatter's bytes, with the fp32 result written into all
+        # R ranks' full outputs instead of once.
+        M, K, N = d["M"], d["K"], d["N"]
+        return R * (M * K + K * N) * 2 + 2.0 * (R - 1) * M * N * 4 + R * M * N * 4
     if w.op == "dp_grad_rs":
         T, M, N = d["T"], d["M"], d["N"]
         return R * (T * M + T * N) * 2 + 2.0 * (R - 1) * M * N * 4 + M * N * 4
@@ -242,7 +247,9 @@ def oracle_pass(workload, arrays, rows: int):
     A, Bn = arrays
     idx = np.arange(rows)
     t0 = time.perf_counter()
-    if workload.op == "gemm_rs":
+    if workload.op in ("gemm_rs", "gemm_ar"):
+        # (The all-reduce's rows of shard sh are the reduce-scatter's, the
+        # same in every rank's output.)
         for sh in range(R):
             oracle.gemm_rs_rows(A, Bn, sh, idx)
         flops = 2.0 * R * rows * R * d["K"] * d["N"]
@@ -306,9 +313,9 @@ def cpu_cores() -> int:
 def workload_config(w, world: int) -> dict:
     """The `config` object of a bench line, the same for both arms."""
     dims = dict(w.dims)
-    if w.op == "gemm_rs":
+    if w.op in ("gemm_rs", "gemm_ar"):
         dims = {"M": dims["M"], "K_per_rank": dims["K"], "N": dims["N"]}
-        l2 = "no flush: inputs (352 MB) and output (134 MB) of a step exceed the 129 MB L2"
+        l2 = "no flush: inputs (352 MB) and output (134 MB or more) of a step exceed the 129 MB L2"
     else:
         l2 = "no flush: a step's operands exceed the 129 MB L2"
     return {"workload": w.name, "R": w.R, **dims, "l2": l2,
@@ -547,7 +554,7 @@ LAYER_WORKLOAD = "tpsp_layer_r8_t8192_h4096_f14336"
 
 
 def _op_setup(B, w, dev):
-    """Device inputs, outputs, plan and workspace of an AG-GEMM, A2A or
+    """Device inputs, outputs, plan and workspace of an AG-GEMM, A2A, AR or
     DP-grad-RS workload: (inp, A, Bm, Y, plan, ws, launch(stream))."""
     import torch
     d = w.dims
@@ -558,6 +565,12 @@ def _op_setup(B, w, dev):
         Bm = [x.to(dev) for x in inp["W"]]
         Y = [torch.empty(M, N // R, dtype=torch.bfloat16, device=dev) for _ in range(R)]
         plan = B.fo_plan("gemm_a2a", R, M, N, K)
+    elif w.op == "gemm_ar":
+        R, M, K, N = w.R, d["M"], d["K"], d["N"]
+        A = [x.to(dev) for x in inp["X"]]
+        Bm = [x.to(dev) for x in inp["W"]]
+        Y = [torch.empty(M, N, dtype=torch.float32, device=dev) for _ in range(R)]
+        plan = B.fo_plan("gemm_ar", R, M, N, K * R)
     elif w.op == "ag_gemm":
         R, M, K, Nr = w.R, d["M"], d["K"], d["N"]
         A = [x.to(dev) for x in inp["X"]]
@@ -576,6 +589,8 @@ def _op_setup(B, w, dev):
     def launch(stream):
         if w.op == "gemm_a2a":
             B.fo_gemm_a2a(plan, A, Bm, Y, ws, stream)
+        elif w.op == "gemm_ar":
+            B.fo_gemm_ar(plan, A, Bm, Y, ws, stream)
         elif w.op == "ag_gemm":
             B.fo_ag_gemm(plan, A, Bm, Y, None, ws, stream)
         else:
@@ -623,7 +638,9 @@ def _attn_setup(B, dev, R=8, T=8192, heads=4, H=4096, causal=True, seed=12):
 
 def measure_other_workloads(B, dev, stream, iters=20):
     """Short timed loops of the all-gather GEMM (QKV, R = 4), the DP
-    gradient (R = 8) and the TP-SP layer (R = 8, forward + backward), on the
+    gradient (R = 8), the all-to-all projection (R = 8), the fused
+    all-reduce (R = 8), the query-split attention with its projection and
+    the TP-SP layer (R = 8, forward + backward), on the
     device that times the default line: per workload the mean CUDA-event
     time per launch (per step for the layer), TFLOP/s, the fraction of the
     measured burst bf16 peak (each loop lasts well under a quarter second),
@@ -637,7 +654,7 @@ def measure_other_workloads(B, dev, stream, iters=20):
     burst = float(peaks["bf16_tflops"])
     out = {}
     for name in ("ag_gemm_qkv_r4_s4096_h4096_n3072", "dp_grad_rs_r8_t4096_4096x4096",
-                 "gemm_a2a_qkv_r8_t8192_h4096_n12288"):
+                 "gemm_a2a_qkv_r8_t8192_h4096_n12288", "gemm_ar_r8_t8192_k1792_n4096"):
         w = WORKLOADS[name]
         inp, A, Bm, Y, plan, ws, launch = _op_setup(B, w, dev)
         for _ in range(5):
@@ -738,8 +755,8 @@ def a2a_baselines(B, plan, X, W, Y, stream, dev, flops, fused_ms):
 
 
 def run_other_op(args, w, dev, world, rank):
-    """Timed loop of the AG-GEMM, A2A or DP-grad-RS workloads (same timing
-    rules as the default line; no comparison legs)."""
+    """Timed loop of the AG-GEMM, A2A, AR or DP-grad-RS workloads (same
+    timing rules as the default line; no comparison legs)."""
     import torch
     import torch.distributed as dist
 
@@ -747,7 +764,7 @@ def run_other_op(args, w, dev, world, rank):
     d = w.dims
     stream = torch.cuda.current_stream(dev)
     inp, A, Bm, Y, plan, ws, launch = _op_setup(B, w, dev)
-    if w.op in ("ag_gemm", "gemm_a2a"):
+    if w.op in ("ag_gemm", "gemm_a2a", "gemm_ar"):
         R, M, K, Nr = w.R, d["M"], d["K"], d["N"]
     else:
         R, T, M, N = w.R, d["T"], d["M"], d["N"]
@@ -779,6 +796,11 @@ def run_other_op(args, w, dev, world, rank):
     if w.op == "gemm_a2a":
         e2e = measure_e2e(B, lambda: B.fo_plan("gemm_a2a", R, M, Nr, K),
                           lambda p, din, dout, ws_, s_: B.fo_gemm_a2a(p, din[0], din[1], dout, ws_, s_),
+                          [inp["X"], inp["W"]], [A, Bm], Y, dev, stream, world, w.flops(),
+                          max(4, min(args.steps, 12)))
+    elif w.op == "gemm_ar":
+        e2e = measure_e2e(B, lambda: B.fo_plan("gemm_ar", R, M, Nr, K * R),
+                          lambda p, din, dout, ws_, s_: B.fo_gemm_ar(p, din[0], din[1], dout, ws_, s_),
                           [inp["X"], inp["W"]], [A, Bm], Y, dev, stream, world, w.flops(),
                           max(4, min(args.steps, 12)))
     elif w.op == "ag_gemm":
