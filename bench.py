@@ -315,7 +315,13 @@ def workload_config(w, world: int) -> dict:
     dims = dict(w.dims)
     if w.op in ("gemm_rs", "gemm_ar"):
         dims = {"M": dims["M"], "K_per_rank": dims["K"], "N": dims["N"]}
-        l2 = "no flush: inputs (352 MB) and output (134 MB or more) of a step exceed the 129 MB L2"
+        out_mb = (w.R if w.op == "gemm_ar" else 1) * dims["M"] * dims["N"] * 4 / 1e6
+        in_mb = w.R * (dims["M"] * dims["K_per_rank"] + dims["K_per_rank"] * dims["N"]) * \
+            (4 if w.dtype == "f32" else 2) / 1e6
+        if in_mb + out_mb > 129:
+            l2 = f"no flush: inputs ({in_mb:.0f} MB) and output ({out_mb:.0f} MB) of a step exceed the 129 MB L2"
+        else:
+            l2 = f"inputs ({in_mb:.1f} MB) and output ({out_mb:.1f} MB) fit in the 129 MB L2: a parity case"
     else:
         l2 = "no flush: a step's operands exceed the 129 MB L2"
     return {"workload": w.name, "R": w.R, **dims, "l2": l2,
