@@ -2,10 +2,11 @@
 sampled output rows the oracle computes one by one.
 
 * Integer mode (entries uniform in [-4, 4]): every fp32 partial sum is an
-  exact integer below 2^24 at these sizes (the 8192 x 1792 x 4096 RS sums stay
-  below 8 x 1792 x 16 = 229,376; the DP sums below 8 x 4096 x 16 = 524,288),
-  so the sampled rows must match the oracle bit for bit; bf16 outputs match
-  the oracle's value rounded once to bf16.
+  exact integer below 2^24 at these sizes (the 8192 x 1792 x 4096 RS and AR
+  sums stay below 8 x 1792 x 16 = 229,376; the DP sums below 8 x 4096 x 16 =
+  524,288), so the sampled rows must match the oracle bit for bit (for the
+  all-reduce, in every rank's output); bf16 outputs match the oracle's value
+  rounded once to bf16.
 * The TP-SP layer (R = 8, T = 8192, H = 4096, F = 14336), forward and
   backward, in the normal-distributed mode the bench uses: every output of
   the 12 launches on sampled rows, within the stated tolerances (relative
@@ -100,6 +101,31 @@ def test_full_size_gemm_rs_down_proj_integer_bit_exact(dev):
         got = _np(Y[d][torch.as_tensor(rows, device=dev)])
         assert np.array_equal(got, oracle.gemm_rs_rows(Xn, Wn, d, rows)), f"shard {d}"
 
+
+
+def test_full_size_gemm_ar_integer_bit_exact(dev):
+    # The fused all-reduce on the bench's all-reduce workload: every rank's
+    # full output holds every shard's sums, bit for bit.
+    w = _int_workload("gemm_ar_r8_t8192_k1792_n4096")
+    R, M, K, N = w.R, w.dims["M"], w.dims["K"], w.dims["N"]
+    inp = w.make()
+    plan = B.fo_plan("gemm_ar", R, M, N, K * R)
+    X = [x.to(dev) for x in inp["X"]]
+    W = [x.to(dev) for x in inp["W"]]
+    Y = [torch.full((M, N), float("nan"), device=dev) for _ in range(R)]
+    ws = _ws(plan, dev)
+    B.fo_gemm_ar(plan, X, W, Y, ws)
+    _status_ok(plan, ws)
+    Xn = [_np(x) for x in inp["X"]]
+    Wn = [_np(x) for x in inp["W"]]
+    rng = np.random.default_rng(23)
+    rpc = M // R
+    for d in range(R):
+        rows = _rows_in_shard(rng, rpc, 4)
+        want = oracle.gemm_rs_rows(Xn, Wn, d, rows)
+        for q in range(R):
+            got = _np(Y[q][torch.as_tensor(d * rpc + rows, device=dev)])
+            assert np.array_equal(got, want), f"shard {d} in rank {q}'s output"
 
 def test_full_size_ag_gemm_qkv_integer_bit_exact(dev):
     w = _int_workload("ag_gemm_qkv_r4_s4096_h4096_n3072")
