@@ -1236,7 +1236,8 @@ def slicing_sweep(B, X, W, Y, stream, dev, fused, pure, unfused, counts=(1, 2, 4
 
 def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
     """Same-GPU comparisons: pure-GEMM control (no transfer), unfused
-    (GEMM to per-rank partials, then a separate reduce kernel), cuBLAS."""
+    (GEMM to per-rank partials, then a separate reduce kernel), cuBLAS with
+    bf16 and with fp32 output."""
     import torch
     R = len(X)
     M, N = X[0].shape[0], W[0].shape[1]
@@ -1256,6 +1257,17 @@ def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
             torch.matmul(X[r], W[r])
 
     cub = _time(cublas, stream)
+
+    # The same GEMMs by cuBLAS with fp32 output (bf16 inputs, fp32
+    # accumulate): the output bytes the fused kernel's partials carry.
+    def cublas_f32():
+        for r in range(R):
+            torch.mm(X[r], W[r], out_dtype=torch.float32, out=P[r])
+
+    try:
+        cub32 = _time(cublas_f32, stream)
+    except (TypeError, RuntimeError):   # a torch without mm's out_dtype
+        cub32 = None
     del P
     torch.cuda.empty_cache()
     # Schedule ablation: the data-slicing order (every rank on slice s at
@@ -1296,6 +1308,9 @@ def measure_extras(B, plan, X, W, Y, ws, stream, flops, dev):
         "exposed_move_pct": 100.0 * (fused - pure) / pure,
         "unfused_ms": unf, "unfused_tflops": flops / unf / 1e9, "unfused_reduce_kernel_ms": red,
         "cublas_matmul_bf16_out_ms": cub, "cublas_matmul_tflops": flops / cub / 1e9,
+        "cublas_matmul_fp32_out_ms": cub32,
+        "cublas_matmul_fp32_out_tflops": flops / cub32 / 1e9 if cub32 else None,
+        "fused_over_cublas_fp32_out": fused / cub32 if cub32 else None,
     }
 
 
