@@ -506,6 +506,15 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           }
         }
         bool ok = true;
+        // Sharded A: the shard of the task's first k-block, then stepped
+        // along with the k-blocks (no division in the loop).
+        int a_src = 0, a_base = 0;
+        if constexpr (A_MN) {
+          if (p.a_shard_rows) {
+            a_src = (w.kb0 * kBK) / p.a_shard_rows;
+            a_base = a_src * p.a_shard_rows;
+          }
+        }
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
           const int stage = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
@@ -527,9 +536,12 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           int kA = k0;
           if constexpr (A_MN) {
             if (p.a_shard_rows) {
-              const int src = k0 / p.a_shard_rows;
-              mAk = &p.tmA[src];
-              kA = k0 - src * p.a_shard_rows;
+              if (k0 - a_base >= p.a_shard_rows) {
+                ++a_src;
+                a_base += p.a_shard_rows;
+              }
+              kA = k0 - a_base;
+              mAk = &p.tmA[a_src];
             }
           }
           if constexpr (PAIR) {

@@ -347,7 +347,7 @@ fo_status fo_gemm_a2a(fo_plan_t plan, const void* const* X, const void* const* W
  * dY_r) without a gathered copy of X: the gather buffers of fo_ag_gemm can
  * be left out. Shards that lie back to back in rank order (A_shards[s] =
  * A_shards[0] + s*K/R*M elements) are read as one [K x M] tensor; others
- * through one tensor map per shard, which ran 20-35% slower on GB300.
+ * through one tensor map per shard, which ran about 4% slower on GB300.
  * Requires K/R to be a multiple of 64; FO_ERR_SHAPE otherwise,
  * FO_ERR_INVALID_ARG for another op or fp32 inputs. One launch. */
 fo_status fo_gemm_partials_sharded(fo_plan_t plan, const void* const* A_shards, const void* const* B,

@@ -139,14 +139,14 @@ def test_attn_rs_replays_from_a_cuda_graph(dev, causal):
             assert fro <= 1e-3 and mx <= 2e-2, f"seed {seed} shard {d}: {fro:.2e} {mx:.2e}"
 
 
-@pytest.mark.parametrize("adjacent", [False, True])
-def test_partials_sharded_replays_from_a_cuda_graph(dev, adjacent):
+@pytest.mark.parametrize("placement", ["separate", "back_to_back", "spaced"])
+def test_partials_sharded_replays_from_a_cuda_graph(dev, placement):
+    from test_gpu_parity import _place_shards
     R, T, M, N = 4, 512, 256, 192
     plan = B.fo_plan("dp_grad_rs", R, M, N, T)
     ws = _ws(plan, dev)
     bf = torch.bfloat16
-    whole = torch.zeros(T, M, dtype=bf, device=dev)
-    A = list(whole.split(T // R)) if adjacent else [torch.zeros(T // R, M, dtype=bf, device=dev) for _ in range(R)]
+    A = _place_shards([torch.zeros(T // R, M, dtype=bf) for _ in range(R)], placement, dev)
     dY = [torch.zeros(T, N, dtype=bf, device=dev) for _ in range(R)]
     P = [torch.empty(M, N, device=dev) for _ in range(R)]
     B.fo_gemm_partials_sharded(plan, A, dY, P, ws)

@@ -428,19 +428,32 @@ def test_partials_control_stores_each_ranks_gemm(dev):
 
 
 
-@pytest.mark.parametrize("placement", ["separate", "back_to_back"])
+def _place_shards(shards, placement, dev):
+    """The shards on the device: separate allocations, back to back in one
+    buffer, or one buffer with a 64-row gap after each shard."""
+    if placement == "separate":
+        return [a.to(dev) for a in shards]
+    if placement == "back_to_back":
+        return list(torch.cat(shards).to(dev).split(shards[0].shape[0]))
+    rows, gap = shards[0].shape[0], 64
+    buf = torch.zeros(len(shards) * (rows + gap), shards[0].shape[1], dtype=shards[0].dtype, device=dev)
+    views = [buf[s * (rows + gap):s * (rows + gap) + rows] for s in range(len(shards))]
+    for v, a in zip(views, shards):
+        v.copy_(a)
+    return views
+
+
+@pytest.mark.parametrize("placement", ["separate", "back_to_back", "spaced"])
 @pytest.mark.parametrize("R,T,M,N", [(2, 128, 256, 64), (4, 768, 800, 328), (8, 1024, 512, 136)])
 def test_partials_sharded_reads_the_gather_in_place(dev, R, T, M, N, placement):
     """fo_gemm_partials_sharded: A = AllGather of R row shards of [T/R x M],
     read where the shards lie (separate allocations: one tensor map per
-    shard; back to back: one map); P_r = A^T . dY_r for every rank, bit for
-    bit (integer inputs make the fp32 sums exact)."""
+    shard; back to back: one map; one stride apart: one 3-D map); P_r =
+    A^T . dY_r for every rank, bit for bit (integer inputs make the fp32
+    sums exact)."""
     inp = dp_grad_inputs(R, T, M, N, mode="int", seed=11)
     shards = list(inp["X"][0].split(T // R))
-    if placement == "separate":
-        A = [a.to(dev) for a in shards]
-    else:
-        A = list(inp["X"][0].to(dev).split(T // R))
+    A = _place_shards(shards, placement, dev)
     plan = B.fo_plan("dp_grad_rs", R, M, N, T)
     P = Guarded(R, (M, N), torch.float32, dev)
     ws = _ws(plan, dev)

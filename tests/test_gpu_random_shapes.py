@@ -14,7 +14,7 @@ import torch
 import oracle
 from ag_gemm_gb300 import binding as B
 from ag_gemm_gb300.inputs import ag_gemm_inputs, dp_grad_inputs, gemm_rs_inputs
-from test_gpu_parity import Guarded, _np, _status_ok, _ws
+from test_gpu_parity import Guarded, _np, _place_shards, _status_ok, _ws
 
 pytestmark = pytest.mark.gpu
 
@@ -123,18 +123,18 @@ def test_random_dp_grad_rs(dev, seed):
 
 @pytest.mark.parametrize("seed", range(CASES))
 def test_random_partials_sharded(dev, seed):
-    # The gathered A given as R token shards (64-row multiples), either
-    # separate allocations or back to back; P_r = AllGather(A)^T . dY_r.
+    # The gathered A given as R token shards (64-row multiples): separate
+    # allocations, back to back, or one stride apart; P_r = AllGather(A)^T . dY_r.
     g, R, rows, _, N = _draw(9000 + seed)
     M = R * rows
     T = R * 64 * int(g.integers(1, 5))
     tile = ["auto", "single"][int(g.integers(2))]
     il = INTERLEAVES[int(g.integers(len(INTERLEAVES)))]
     split = SPLITS[int(g.integers(2))]
-    adjacent = bool(g.integers(2))
+    placement = ["separate", "back_to_back", "spaced"][int(g.integers(3))]
     inp = dp_grad_inputs(R, T, M, N, mode="int", seed=seed)
     whole = inp["X"][0]
-    A = list(whole.to(dev).split(T // R)) if adjacent else [a.to(dev) for a in whole.split(T // R)]
+    A = _place_shards(list(whole.split(T // R)), placement, dev)
     plan = B.fo_plan("dp_grad_rs", R, M, N, T, tile_config=tile, interleave=il, tail_split=split)
     P = Guarded(R, (M, N), torch.float32, dev)
     ws = _ws(plan, dev)
@@ -145,7 +145,7 @@ def test_random_partials_sharded(dev, seed):
                               [_np(y) for y in inp["dY"]])
     for r in range(R):
         assert np.array_equal(_np(P.views[r]), ref[r]), \
-            f"R={R} T={T} M={M} N={N} {tile} {il} {split} adjacent={adjacent} rank {r}"
+            f"R={R} T={T} M={M} N={N} {tile} {il} {split} {placement} rank {r}"
 
 @pytest.mark.parametrize("seed", range(CASES))
 def test_random_gemm_ar(dev, seed):
