@@ -444,6 +444,11 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
+      // The ring position of k-block `it`, stepped along with it: the
+      // producer's path from a freed stage to its next loads is the MMA's
+      // critical path, so it carries no division.
+      int pst = 0;
+      uint32_t pph = 0;
       // Gather stores still owed per stage: the A block a stage holds goes to
       // G_r once the MMA has read it and before the stage is refilled.
       constexpr int kG = GST ? kStages : 1;
@@ -516,8 +521,12 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
           }
         }
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int stage = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
+          const int stage = pst;
+          const uint32_t ph = pph;
+          if (++pst == kStages) {
+            pst = 0;
+            pph ^= 1u;
+          }
           if (!mbar_wait(empty_bar(stage), ph ^ 1u, abort_flag, kMbarLimitNs)) {
             ok = false;
             break;
@@ -609,6 +618,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       uint32_t it = 0, tcount = 0;
+      int mst = 0;   // ring position of k-block `it`, stepped along with it
+      uint32_t mph = 0;
       Work w;
       for (int wi = 0; get_work(p, total, unit, units, wi, w); ++wi, ++tcount) {
         if (*abort_flag) break;
@@ -619,8 +630,12 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
         const uint32_t d = tmem_base + (uint32_t)(acc * FO_BN);
         bool ok = true;
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-          const int stage = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
+          const int stage = mst;
+          const uint32_t ph = mph;
+          if (++mst == kStages) {
+            mst = 0;
+            mph ^= 1u;
+          }
           if (!mbar_wait(full_bar(stage), ph, abort_flag, kMbarLimitNs)) {
             ok = false;
             break;
