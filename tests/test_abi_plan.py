@@ -89,7 +89,15 @@ def test_dropped_transfer_is_rejected():
     (dict(op="gemm_rs", R=2, M=8, N=8, K=9), B.FO_ERR_SHAPE),           # K % R
     (dict(op="gemm_rs", R=2, M=8, N=6, K=32), B.FO_ERR_ALIGN),          # rows of W not 16 B
     (dict(op="gemm_rs", R=2, M=8, N=8, K=12), B.FO_ERR_ALIGN),          # rows of X_r not 16 B
-    (dict(op="gemm_rs", R=2, M=0, N=8, K=16), B.FO_ERR_SHAPE),
+    (dict(op="gemm_rs", R=2, M=0, N=8, K=16), B.FO_ERR_SHAPE),         # empty: no rows
+    (dict(op="gemm_rs", R=2, M=8, N=0, K=16), B.FO_ERR_SHAPE),         # no columns
+    (dict(op="gemm_rs", R=2, M=8, N=8, K=0), B.FO_ERR_SHAPE),          # no reduction
+    (dict(op="ag_gemm", R=2, M=8, N=0, K=16), B.FO_ERR_SHAPE),
+    (dict(op="ag_gemm", R=2, M=8, N=16, K=0), B.FO_ERR_SHAPE),
+    (dict(op="dp_grad_rs", R=2, M=0, N=8, K=16), B.FO_ERR_SHAPE),
+    (dict(op="dp_grad_rs", R=2, M=16, N=8, K=0), B.FO_ERR_SHAPE),      # no tokens
+    (dict(op="gemm_a2a", R=2, M=8, N=0, K=16), B.FO_ERR_SHAPE),
+    (dict(op="gemm_ar", R=2, M=8, N=8, K=0), B.FO_ERR_SHAPE),
     (dict(op="ag_gemm", R=2, M=8, N=10, K=16), B.FO_ERR_ALIGN),         # N/R = 5
     (dict(op="ag_gemm", R=3, M=9, N=8, K=16), B.FO_ERR_SHAPE),          # N % R
     (dict(op="dp_grad_rs", R=2, M=8, N=8, K=16), B.FO_ERR_ALIGN),       # M/R = 4 columns
