@@ -449,6 +449,9 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
       // critical path, so it carries no division.
       int pst = 0;
       uint32_t pph = 0;
+      // All-gather: the X shards, which every rank's tasks read again, stay
+      // in L2 ahead of the streamed outputs.
+      const uint64_t pol_x = l2_policy_evict_last();
       // Gather stores still owed per stage: the A block a stage holds goes to
       // G_r once the MMA has read it and before the stage is refilled.
       constexpr int kG = GST ? kStages : 1;
@@ -560,7 +563,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
 #pragma unroll
               for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d_pair(sa + j * kBoxBytes, mAk, fb, a_mn0 + j * kBK, kA);
             } else {
-              tma_load_2d_pair(sa, mA, fb, k0, a_mn0);
+              if (EPI == EPI_AG) tma_load_2d_pair_hint(sa, mA, fb, k0, a_mn0, pol_x);
+              else tma_load_2d_pair(sa, mA, fb, k0, a_mn0);
             }
             if constexpr (B_MN) {
 #pragma unroll
@@ -576,7 +580,8 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
 #pragma unroll
               for (int j = 0; j < FO_BM / kBK; ++j) tma_load_2d(sa + j * kBoxBytes, mAk, fb, a_mn0 + j * kBK, kA);
             } else {
-              tma_load_2d(sa, mA, fb, k0, a_mn0);
+              if (EPI == EPI_AG) tma_load_2d_hint(sa, mA, fb, k0, a_mn0, pol_x);
+              else tma_load_2d(sa, mA, fb, k0, a_mn0);
             }
             if constexpr (B_MN) {
 #pragma unroll
@@ -1033,8 +1038,10 @@ __global__ void __launch_bounds__(threads_for(MOV), 1) fo_chunk_gemm_kernel(cons
             if (lane == 0) {
               for (int jj = j - (j % kB); jj <= j; ++jj) {
                 const uint32_t bb = sEpi + (uint32_t)((e * kEpiBufs + (jj % kB)) * kEpiBuf);
-                if (p.a2a) tma_store_3d(&p.tmD[ti.c], bb, n0 + jj * 64, row0, ti.r);
-                else tma_store_3d(&p.tmD[ti.r], bb, n0 + jj * 64, row0, ti.c);
+                // Y is written once and never read here: its lines leave L2 first.
+                const uint64_t pol = l2_policy_evict_first();
+                if (p.a2a) tma_store_3d_hint(&p.tmD[ti.c], bb, n0 + jj * 64, row0, ti.r, pol);
+                else tma_store_3d_hint(&p.tmD[ti.r], bb, n0 + jj * 64, row0, ti.c, pol);
                 bulk_commit();
               }
             }
